@@ -1,0 +1,204 @@
+/*
+ * fp8lin.h — C ABI of the GB300 (sm_103a) FP8 linear-layer library.
+ *
+ * The operations follow the recipes of the Megatron Core developer guide page
+ * "Low-Precision Training Guide": section "Hardware and Recipe Compatibility" (the recipe
+ * names delayed / tensorwise / mxfp8 / blockwise and the --fp8-format values), section
+ * "Recipe Reference" (what each recipe scales by), section "Numerical Stability Knobs"
+ * (--fp8-margin, --fp8-amax-history-len, --fp8-amax-compute-algo, --fp8-wgrad), and the
+ * TransformerEngine issue "How to reduce cuda memory usage of fp8?" (the backward pass runs
+ * from cached FP8 copies of the layer input instead of a bf16 copy). The MegaDLMs summary
+ * "Benefits of Using FP8 Precision with MegaDLMs and Required Hardware" (section "Python API
+ * Configuration") is the source of the MLP entry points that keep the GeLU input in FP8.
+ *
+ * Numerics (readings where the pages are silent):
+ *   E4M3 is OCP E4M3FN (max 448, min subnormal 2^-9, no Inf). A code is
+ *   encode(fp32(x * s)): round to nearest even, +-Inf and finite overflow saturate to
+ *   +-448, NaN -> 0x7F with the input's sign bit.
+ *   Per-tensor / per-block scale: s = fp32(448 / amax) * 2^-margin (IEEE division), s = 1
+ *   when amax is 0, Inf or NaN, an infinite s becomes FLT_MAX; s_inv = fp32(1 / s).
+ *   MXFP8 E8M0 exponent of a 1x32 block: the smallest e with amax <= 448 * 2^e, clamped to
+ *   [-127, 127], -127 when amax < 2^-126; byte e + 127; codes encode(x * 2^-e). A block
+ *   holding Inf or NaN gets byte 0xFF and codes encode(x).
+ *   GEMMs accumulate in fp32 and round once to bf16 (round to nearest even).
+ *
+ * Layouts (all tensors row-major, all pointers device pointers unless stated):
+ *   X[M,K] activations, W[N,K] weights (the layer computes Y = X W^T), dY[M,N] gradients.
+ *   A quantised tensor of source shape [R,C] has a row-wise copy row[R][C] (blocks along C)
+ *   and a column-wise copy col[C][R] = the quantised transpose (blocks along R).
+ *   Scale storage per recipe:
+ *     DELAYED, TENSORWISE: fp32 scalars amax, scale, scale_inv (one for the tensor).
+ *     MXFP8: uint8 E8M0, R*C/32 bytes per copy, in the tiled order that the tensor core's
+ *       block-scale path reads: the byte of row r, 32-block kb of a copy with C columns is
+ *         ((r/128) * (C/128) + kb/4) * 512 + (r%32) * 16 + ((r%128)/32) * 4 + kb%4.
+ *     BLOCKWISE, role ACTIVATION or GRAD (1x128 blocks): fp32 s_inv, R*C/128 floats per
+ *       copy, block-major: s_inv of row r, 128-block kb at kb * R + r.
+ *     BLOCKWISE, role WEIGHT (128x128 blocks): fp32 s_inv, row copy [R/128][C/128],
+ *       column copy [C/128][R/128] (the transposed grid). col = byte transpose of row.
+ *
+ * Ownership and ordering: the caller owns every buffer. No entry point allocates or frees
+ * device memory, synchronises the device or the stream, or keeps state between calls; all
+ * work is enqueued on the caller's stream in stream order. Every entry point is safe to call
+ * from several host threads on different streams.
+ *
+ * Errors: argument errors are found on the host before anything is enqueued and returned as
+ * a status (nothing is launched then). Conditions seen on the device (a pipeline wait that
+ * ran out of its time budget) are written to *dev_status (int32, caller-zeroed; may be NULL)
+ * and the kernel returns early; the caller reads it after its own synchronisation.
+ */
+#ifndef FP8LIN_H
+#define FP8LIN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FP8_OK = 0,
+  FP8_ERR_NULL = 1,         /* a required pointer is NULL */
+  FP8_ERR_ALIGN = 2,        /* a pointer is not 16-byte aligned */
+  FP8_ERR_SHAPE = 3,        /* sizes negative, not multiples of the required block, or
+                               inconsistent between operands */
+  FP8_ERR_UNSUPPORTED = 4,  /* a recipe option this build does not implement */
+  FP8_ERR_CUDA = 5,         /* a CUDA launch or query failed */
+  FP8_ERR_TIMEOUT = 6,      /* device-side only: a pipeline wait exceeded its budget */
+  FP8_ERR_WORKSPACE = 7     /* workspace missing or smaller than fp8_workspace_bytes() */
+} fp8_status;
+
+/* --fp8-recipe values (section "Hardware and Recipe Compatibility"). */
+typedef enum {
+  FP8_RECIPE_DELAYED = 0,
+  FP8_RECIPE_TENSORWISE = 1,
+  FP8_RECIPE_MXFP8 = 2,
+  FP8_RECIPE_BLOCKWISE = 3
+} fp8_recipe_kind;
+
+/* --fp8-format values. HYBRID is accepted by the recipe table but never defined on the
+ * pages; this build returns FP8_ERR_UNSUPPORTED for it. MXFP8 takes E4M3 only. */
+typedef enum { FP8_FORMAT_E4M3 = 0, FP8_FORMAT_HYBRID = 1 } fp8_format;
+
+/* Which block shape the blockwise recipe uses for a tensor: 1x128 for activations and
+ * gradients, 128x128 for weights (recipe entry "blockwise"). Ignored by other recipes. */
+typedef enum { FP8_ROLE_ACTIVATION = 0, FP8_ROLE_WEIGHT = 1, FP8_ROLE_GRAD = 2 } fp8_role;
+
+/* The recipe statement, one field per flag. */
+typedef struct {
+  int32_t kind;               /* fp8_recipe_kind (--fp8-recipe) */
+  int32_t format;             /* fp8_format (--fp8-format) */
+  int32_t margin;             /* --fp8-margin, in [-64, 64]; s is multiplied by 2^-margin */
+  int32_t amax_history_len;   /* --fp8-amax-history-len (DELAYED), >= 1 */
+  int32_t amax_compute_algo;  /* --fp8-amax-compute-algo: 0 = max (the only one built) */
+  int32_t fp8_wgrad;          /* --fp8-wgrad: 1 = wgrad GEMM in FP8, 0 = in bf16 */
+} fp8_recipe;
+
+/* A quantised tensor: codes and scales of both copies, all device memory owned by the
+ * caller. row / col may be NULL when that copy is not wanted. */
+typedef struct {
+  uint8_t *row;          /* [rows][cols] E4M3 codes */
+  uint8_t *col;          /* [cols][rows] E4M3 codes */
+  void *row_scale;       /* MXFP8: uint8 E8M0; BLOCKWISE: float s_inv; else unused */
+  void *col_scale;       /* same for the column-wise copy */
+  float *amax;           /* DELAYED/TENSORWISE: amax of this tensor (written) */
+  float *scale;          /* TENSORWISE: written. DELAYED: read (the scale from history) */
+  float *scale_inv;      /* TENSORWISE: written. DELAYED: read */
+  int64_t rows, cols;    /* source shape [R, C] */
+  int32_t kind;          /* recipe the codes were made with (set by fp8_quantize) */
+  int32_t role;          /* fp8_role */
+} fp8_tensor;
+
+/* Delayed-scaling state: a rolling window of the last `len` amax values. */
+typedef struct {
+  float *history;        /* [len] fp32, start as zeros */
+  int32_t *head;         /* next slot to write, starts at 0 */
+  int32_t len;           /* --fp8-amax-history-len */
+} fp8_amax_history;
+
+/* Bytes of scratch memory fp8_quantize needs for this recipe and shape (0 if none). The
+ * tensorwise and delayed recipes reduce the amax through per-tile partial maxima. */
+size_t fp8_workspace_bytes(const fp8_recipe *recipe, int64_t rows, int64_t cols);
+
+/*
+ * fp8_quantize — bf16 tensor -> E4M3 codes plus scales, row-wise and/or column-wise copy.
+ *
+ * Recipe entries "tensorwise" (scale from this tensor's own amax), "delayed" (scale read from
+ * out->scale / out->scale_inv, which fp8_amax_update derived from earlier steps; this call
+ * writes this tensor's amax to out->amax for the next update), "mxfp8" (E8M0 per 1x32 block)
+ * and "blockwise" (1x128 or 128x128 by role).
+ *   x_bf16     [rows][cols] bf16, 16-byte aligned, read only.
+ *   rows, cols >= 0. MXFP8 and BLOCKWISE need both to be multiples of 128; TENSORWISE and
+ *              DELAYED need multiples of 16. An empty tensor writes amax 0, scale 1.
+ *   want_row / want_col: which copies to write (at least one).
+ *   out        codes/scales destinations (see the layouts above); out->rows/cols/role/kind
+ *              are set by this call.
+ *   workspace  device scratch of at least fp8_workspace_bytes() (may be NULL when that is 0).
+ * Returns FP8_OK or a host-detected error (nothing launched on error).
+ */
+fp8_status fp8_quantize(const fp8_recipe *recipe, const void *x_bf16, int64_t rows,
+                        int64_t cols, int32_t role, int32_t want_row, int32_t want_col,
+                        fp8_tensor *out, void *workspace, size_t ws_bytes,
+                        int32_t *dev_status, cudaStream_t stream);
+
+/*
+ * fp8_amax_update — delayed scaling: push *amax_new into the history (the oldest of `len`
+ * entries drops out) and write scale = f(max(history)), scale_inv = 1/scale with f the
+ * per-tensor rule above (--fp8-amax-history-len, --fp8-amax-compute-algo max, --fp8-margin).
+ * One CTA; reads and writes device memory only.
+ */
+fp8_status fp8_amax_update(const fp8_recipe *recipe, fp8_amax_history *hist,
+                           const float *amax_new, float *scale, float *scale_inv,
+                           cudaStream_t stream);
+
+/*
+ * fp8_linear_fwd — fprop Y[M,N] = deq(X)[M,K] . deq(W)[N,K]^T (fp32 accumulation).
+ * Uses x->row and w->row. x and w must come from the same recipe. Tensor scales are applied
+ * after accumulation, MXFP8 block scales by the tensor core during accumulation, blockwise
+ * scales per 128-wide K chunk. y is bf16 [M][N] (y_fp32 = 0) or fp32 [M][N] (y_fp32 = 1,
+ * for accumulation checks). M, N multiples of 16 (128 for MXFP8/BLOCKWISE), K multiple of
+ * 128 (16 for DELAYED/TENSORWISE).
+ */
+fp8_status fp8_linear_fwd(const fp8_recipe *recipe, const fp8_tensor *x, const fp8_tensor *w,
+                          void *y, int32_t y_fp32, int32_t *dev_status, cudaStream_t stream);
+
+/*
+ * fp8_linear_bwd — dgrad dX[M,K] = deq(dY)[M,N] . deq(W^T)[K,N]^T from dy->row and w->col,
+ * and wgrad dW[N,K] = deq(dY^T)[N,M] . deq(X^T)[K,M]^T from dy->col and x_saved->col (the
+ * FP8 copies cached in the forward pass). With recipe->fp8_wgrad == 0 the wgrad GEMM runs on
+ * the bf16 dy_bf16 [M][N] and x_bf16 [M][K] instead. dx or dw may be NULL to skip that GEMM.
+ * Outputs are bf16 (out_fp32 = 0) or fp32 (out_fp32 = 1).
+ */
+fp8_status fp8_linear_bwd(const fp8_recipe *recipe, const fp8_tensor *dy,
+                          const fp8_tensor *x_saved, const fp8_tensor *w,
+                          const void *x_bf16, const void *dy_bf16, void *dx, void *dw,
+                          int32_t out_fp32, int32_t *dev_status, cudaStream_t stream);
+
+/*
+ * fp8_gelu_quantize — MLP activation with its input kept in FP8 for the backward pass
+ * (activation_func_fp8_input_store): a = bf16(gelu(h)) with gelu(h) = h * Phi(h) in fp32,
+ * quantised (row and column copies) into a_q, and h itself quantised (row copy) into h_q.
+ * a_bf16 may be NULL (only needed for bf16 wgrad or inspection). MXFP8 recipe only.
+ */
+fp8_status fp8_gelu_quantize(const fp8_recipe *recipe, const void *h_bf16, int64_t rows,
+                             int64_t cols, void *a_bf16, fp8_tensor *a_q, fp8_tensor *h_q,
+                             int32_t *dev_status, cudaStream_t stream);
+
+/*
+ * fp8_dgelu_quantize — dh = bf16(da * gelu'(deq(h_q))) in fp32, gelu'(h) = Phi(h) + h phi(h),
+ * reading h back from its FP8 row copy, then quantised (row and column copies) into dh_q.
+ * dh_bf16 may be NULL. MXFP8 recipe only.
+ */
+fp8_status fp8_dgelu_quantize(const fp8_recipe *recipe, const void *da_bf16,
+                              const fp8_tensor *h_q, void *dh_bf16, fp8_tensor *dh_q,
+                              int32_t *dev_status, cudaStream_t stream);
+
+/* Human-readable name of a status. */
+const char *fp8_status_str(fp8_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8LIN_H */

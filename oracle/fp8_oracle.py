@@ -22,7 +22,8 @@ where they are silent the readings below are the plainest ones the rest supports
   * A code is encode(fp32(x * s)): the product is rounded to fp32 first, then to E4M3.
   * MXFP8: per 1x32 block the E8M0 exponent is the smallest e with amax <= 448 * 2^e,
     clamped to [-127, 127]; blocks with amax below 2^-126 (zero, or subnormal) get -127.
-    The stored byte is e + 127. Codes are encode(x * 2^-e), an exact product.
+    The stored byte is e + 127. Codes are encode(x * 2^-e), an exact product. A block
+    holding an Inf or a NaN gets the E8M0 NaN byte 0xFF and codes encode(x) (e = 0).
   * Delayed: the history starts as L zeros and s = 1; a step quantises with the scale from
     the history of the previous steps only, then pushes its own amax (evicting the oldest
     entry once L are held) and derives the next scale from max(history).
@@ -254,21 +255,26 @@ def _mx_quantize_lastdim(x_f32):
     R, C = x_f32.shape
     blocks = x_f32.reshape(R, C // MX_BLOCK, MX_BLOCK)
     amax = np.max(np.abs(blocks), axis=2)
-    e = mx_exponent(amax)
+    bad = ~np.isfinite(amax)                      # the block holds an Inf or a NaN
+    e = np.where(bad, 0, mx_exponent(np.where(bad, 0.0, amax)))
     scaled = blocks.astype(np.float64) * np.ldexp(1.0, -e)[:, :, None]   # exact
     codes = e4m3_encode(scaled.astype(np.float32)).reshape(R, C)
-    return codes, (e + 127).astype(np.uint8)
+    return codes, np.where(bad, 255, e + 127).astype(np.uint8)
 
 
-def quantize_mxfp8(x_bf16):
+def quantize_mxfp8(x_bf16, want_col=True):
     """Row-wise copy with 1x32 blocks along C, column-wise copy of X^T with blocks along R.
 
-    Returns dict(row=[R,C], row_scale=[R,C/32], col=[C,R], col_scale=[C,R/32]).
+    Returns dict(row=[R,C], row_scale=[R,C/32], col=[C,R], col_scale=[C,R/32]); the column
+    entries are omitted when want_col is False (the row copy of any subset of rows is then
+    the same as that subset of the full tensor's row copy).
     """
     x = bf16_to_f32(x_bf16)
     row, row_scale = _mx_quantize_lastdim(x)
-    col, col_scale = _mx_quantize_lastdim(np.ascontiguousarray(x.T))
-    return dict(row=row, row_scale=row_scale, col=col, col_scale=col_scale)
+    out = dict(row=row, row_scale=row_scale)
+    if want_col:
+        out["col"], out["col_scale"] = _mx_quantize_lastdim(np.ascontiguousarray(x.T))
+    return out
 
 
 def e8m0_decode(bytes_):

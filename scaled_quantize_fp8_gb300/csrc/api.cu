@@ -1,0 +1,295 @@
+// extern "C" entry points of the FP8 linear-layer library (declared in include/fp8lin.h).
+// Arguments are checked on the host before anything is enqueued; every launch goes to the
+// caller's stream; no entry point allocates, frees or synchronises.
+#include <cstdint>
+#include <cstring>
+
+#include "internal.cuh"
+
+
+using namespace fp8lin;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+fp8_status check_ptr(const void* p) {
+  if (p == nullptr) return FP8_ERR_NULL;
+  if (!aligned16(p)) return FP8_ERR_ALIGN;
+  return FP8_OK;
+}
+
+#define FP8_TRY(expr)                    \
+  do {                                   \
+    const fp8_status _s = (expr);        \
+    if (_s != FP8_OK) return _s;         \
+  } while (0)
+
+fp8_status check_recipe(const fp8_recipe* r) {
+  if (r == nullptr) return FP8_ERR_NULL;
+  if (r->kind < FP8_RECIPE_DELAYED || r->kind > FP8_RECIPE_BLOCKWISE) return FP8_ERR_UNSUPPORTED;
+  if (r->format != FP8_FORMAT_E4M3) return FP8_ERR_UNSUPPORTED;   // hybrid: not defined
+  if (r->margin < -64 || r->margin > 64) return FP8_ERR_UNSUPPORTED;
+  if (r->amax_compute_algo != 0) return FP8_ERR_UNSUPPORTED;      // only `max`
+  if (r->kind == FP8_RECIPE_DELAYED && r->amax_history_len < 1) return FP8_ERR_SHAPE;
+  return FP8_OK;
+}
+
+// Row/column multiple a recipe needs: 128 for the block recipes, 16 for per-tensor scales.
+int64_t shape_quantum(int kind) {
+  return (kind == FP8_RECIPE_MXFP8 || kind == FP8_RECIPE_BLOCKWISE) ? 128 : 16;
+}
+
+fp8_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA; }
+
+// Scale pointers a recipe needs for one copy.
+fp8_status check_copy(int kind, const uint8_t* codes, const void* scale) {
+  FP8_TRY(check_ptr(codes));
+  if (kind == FP8_RECIPE_MXFP8 || kind == FP8_RECIPE_BLOCKWISE) FP8_TRY(check_ptr(scale));
+  return FP8_OK;
+}
+
+fp8_status check_scalars(int kind, const fp8_tensor* t) {
+  if (kind == FP8_RECIPE_TENSORWISE || kind == FP8_RECIPE_DELAYED) {
+    if (t->amax == nullptr || t->scale == nullptr || t->scale_inv == nullptr) return FP8_ERR_NULL;
+  }
+  return FP8_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fp8_status_str(fp8_status s) {
+  switch (s) {
+    case FP8_OK: return "ok";
+    case FP8_ERR_NULL: return "null pointer";
+    case FP8_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case FP8_ERR_SHAPE: return "bad shape";
+    case FP8_ERR_UNSUPPORTED: return "unsupported recipe option";
+    case FP8_ERR_CUDA: return "CUDA launch failed";
+    case FP8_ERR_TIMEOUT: return "device wait timed out";
+    case FP8_ERR_WORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+size_t fp8_workspace_bytes(const fp8_recipe* recipe, int64_t rows, int64_t cols) {
+  if (recipe == nullptr) return 0;
+  return quantize_workspace_bytes(recipe->kind, rows, cols);
+}
+
+fp8_status fp8_quantize(const fp8_recipe* recipe, const void* x_bf16, int64_t rows, int64_t cols,
+                        int32_t role, int32_t want_row, int32_t want_col, fp8_tensor* out,
+                        void* workspace, size_t ws_bytes, int32_t* dev_status,
+                        cudaStream_t stream) {
+  (void)dev_status;
+  FP8_TRY(check_recipe(recipe));
+  if (out == nullptr) return FP8_ERR_NULL;
+  if (role < FP8_ROLE_ACTIVATION || role > FP8_ROLE_GRAD) return FP8_ERR_UNSUPPORTED;
+  if (!want_row && !want_col) return FP8_ERR_SHAPE;
+  const int kind = recipe->kind;
+  const int64_t q = shape_quantum(kind);
+  if (rows < 0 || cols < 0 || rows % q != 0 || cols % q != 0) return FP8_ERR_SHAPE;
+  if (rows > (int64_t(1) << 31) || cols > (int64_t(1) << 31)) return FP8_ERR_SHAPE;
+  FP8_TRY(check_scalars(kind, out));
+  const bool empty = rows == 0 || cols == 0;
+  if (!empty) {
+    FP8_TRY(check_ptr(x_bf16));
+    if (want_row) FP8_TRY(check_copy(kind, out->row, out->row_scale));
+    if (want_col) FP8_TRY(check_copy(kind, out->col, out->col_scale));
+    const size_t need = quantize_workspace_bytes(kind, rows, cols);
+    if (need > 0 && (workspace == nullptr || ws_bytes < need)) return FP8_ERR_WORKSPACE;
+    if (need > 0 && !aligned16(workspace)) return FP8_ERR_ALIGN;
+  }
+  out->rows = rows;
+  out->cols = cols;
+  out->role = role;
+  out->kind = kind;
+  return cuda_status(quantize_launch(kind, role, recipe->margin,
+                                     reinterpret_cast<const uint16_t*>(x_bf16), rows, cols,
+                                     want_row != 0, want_col != 0, out, workspace, stream));
+}
+
+fp8_status fp8_amax_update(const fp8_recipe* recipe, fp8_amax_history* hist,
+                           const float* amax_new, float* scale, float* scale_inv,
+                           cudaStream_t stream) {
+  FP8_TRY(check_recipe(recipe));
+  if (recipe->kind != FP8_RECIPE_DELAYED) return FP8_ERR_UNSUPPORTED;
+  if (hist == nullptr || hist->history == nullptr || hist->head == nullptr || amax_new == nullptr ||
+      scale == nullptr || scale_inv == nullptr)
+    return FP8_ERR_NULL;
+  if (hist->len < 1 || hist->len != recipe->amax_history_len) return FP8_ERR_SHAPE;
+  return cuda_status(amax_update_launch(hist->history, hist->head, hist->len, amax_new, scale,
+                                        scale_inv, recipe->margin, stream));
+}
+
+}  // extern "C"
+
+namespace {
+
+// One TN GEMM D[M][N] = A[M][Kr] . B[N][Kr]^T for the recipe, from two quantised copies.
+struct Operand {
+  const uint8_t* codes;
+  const void* scale;        // per recipe (see fp8lin.h)
+  const float* scale_inv;   // per-tensor recipes
+  int role;
+};
+
+fp8_status run_gemm(int kind, const Operand& a, const Operand& b, int64_t M, int64_t N,
+                    int64_t Kr, void* D, int fp32_out, int32_t* status, cudaStream_t st) {
+  FP8_TRY(check_ptr(a.codes));
+  FP8_TRY(check_ptr(b.codes));
+  FP8_TRY(check_ptr(D));
+  const int64_t q = shape_quantum(kind);
+  if (M % q || N % q || Kr % q) return FP8_ERR_SHAPE;
+  if (M > (int64_t(1) << 30) || N > (int64_t(1) << 30) || Kr > (int64_t(1) << 30))
+    return FP8_ERR_SHAPE;
+  if (M == 0 || N == 0) return FP8_OK;
+  if (Kr == 0) {
+    return cuda_status(cudaMemsetAsync(D, 0, size_t(M) * N * (fp32_out ? 4 : 2), st));
+  }
+  GemmLaunch g{};
+  g.A = a.codes;
+  g.B = b.codes;
+  g.p.M = int(M);
+  g.p.N = int(N);
+  g.p.K = int(Kr);
+  g.p.D = D;
+  g.p.ldd = N;
+  g.p.d_fp32 = fp32_out;
+  g.p.status = status;
+  switch (kind) {
+    case FP8_RECIPE_TENSORWISE:
+    case FP8_RECIPE_DELAYED:
+      if (a.scale_inv == nullptr || b.scale_inv == nullptr) return FP8_ERR_NULL;
+      g.mode = G_TENSOR;
+      g.p.a_sinv = a.scale_inv;
+      g.p.b_sinv = b.scale_inv;
+      break;
+    case FP8_RECIPE_MXFP8:
+      FP8_TRY(check_ptr(a.scale));
+      FP8_TRY(check_ptr(b.scale));
+      g.mode = G_MX;
+      g.p.sfa = reinterpret_cast<const uint8_t*>(a.scale);
+      g.p.sfb = reinterpret_cast<const uint8_t*>(b.scale);
+      break;
+    case FP8_RECIPE_BLOCKWISE:
+      FP8_TRY(check_ptr(a.scale));
+      FP8_TRY(check_ptr(b.scale));
+      if (a.role == FP8_ROLE_WEIGHT) return FP8_ERR_UNSUPPORTED;   // A is always 1x128
+      g.mode = G_BLOCK;
+      g.p.a_bs = reinterpret_cast<const float*>(a.scale);
+      g.p.b_bs = reinterpret_cast<const float*>(b.scale);
+      g.p.b_is_128 = b.role == FP8_ROLE_WEIGHT;
+      break;
+    default:
+      return FP8_ERR_UNSUPPORTED;
+  }
+  return cuda_status(gemm_launch(g, st));
+}
+
+fp8_status check_tensor(const fp8_recipe* r, const fp8_tensor* t) {
+  if (t == nullptr) return FP8_ERR_NULL;
+  if (t->kind != r->kind) return FP8_ERR_UNSUPPORTED;
+  return FP8_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fp8_status fp8_linear_fwd(const fp8_recipe* recipe, const fp8_tensor* x, const fp8_tensor* w,
+                          void* y, int32_t y_fp32, int32_t* dev_status, cudaStream_t stream) {
+  FP8_TRY(check_recipe(recipe));
+  FP8_TRY(check_tensor(recipe, x));
+  FP8_TRY(check_tensor(recipe, w));
+  if (x->cols != w->cols) return FP8_ERR_SHAPE;
+  const Operand a{x->row, x->row_scale, x->scale_inv, x->role};
+  const Operand b{w->row, w->row_scale, w->scale_inv, w->role};
+  return run_gemm(recipe->kind, a, b, x->rows, w->rows, x->cols, y, y_fp32, dev_status, stream);
+}
+
+fp8_status fp8_linear_bwd(const fp8_recipe* recipe, const fp8_tensor* dy,
+                          const fp8_tensor* x_saved, const fp8_tensor* w, const void* x_bf16,
+                          const void* dy_bf16, void* dx, void* dw, int32_t out_fp32,
+                          int32_t* dev_status, cudaStream_t stream) {
+  FP8_TRY(check_recipe(recipe));
+  FP8_TRY(check_tensor(recipe, dy));
+  (void)x_bf16;
+  (void)dy_bf16;
+  const int64_t M = dy->rows, N = dy->cols;
+  if (dx != nullptr) {
+    FP8_TRY(check_tensor(recipe, w));
+    if (w->rows != N) return FP8_ERR_SHAPE;
+    const int64_t K = w->cols;
+    // dgrad: dX[M][K] = dY[M][N] . (W^T)[K][N]^T
+    const Operand a{dy->row, dy->row_scale, dy->scale_inv, dy->role};
+    const Operand b{w->col, w->col_scale, w->scale_inv, w->role};
+    FP8_TRY(run_gemm(recipe->kind, a, b, M, K, N, dx, out_fp32, dev_status, stream));
+  }
+  if (dw != nullptr) {
+    if (!recipe->fp8_wgrad) return FP8_ERR_UNSUPPORTED;
+    FP8_TRY(check_tensor(recipe, x_saved));
+    if (x_saved->rows != M) return FP8_ERR_SHAPE;
+    const int64_t K = x_saved->cols;
+    // wgrad: dW[N][K] = (dY^T)[N][M] . (X^T)[K][M]^T
+    const Operand a{dy->col, dy->col_scale, dy->scale_inv, dy->role};
+    const Operand b{x_saved->col, x_saved->col_scale, x_saved->scale_inv, x_saved->role};
+    FP8_TRY(run_gemm(recipe->kind, a, b, N, K, M, dw, out_fp32, dev_status, stream));
+  }
+  return FP8_OK;
+}
+
+fp8_status fp8_gelu_quantize(const fp8_recipe* recipe, const void* h_bf16, int64_t rows,
+                             int64_t cols, void* a_bf16, fp8_tensor* a_q, fp8_tensor* h_q,
+                             int32_t* dev_status, cudaStream_t stream) {
+  (void)dev_status;
+  FP8_TRY(check_recipe(recipe));
+  if (recipe->kind != FP8_RECIPE_MXFP8) return FP8_ERR_UNSUPPORTED;
+  if (a_q == nullptr || h_q == nullptr) return FP8_ERR_NULL;
+  if (rows < 0 || cols < 0 || rows % 128 || cols % 128) return FP8_ERR_SHAPE;
+  if (rows > 0 && cols > 0) {
+    FP8_TRY(check_ptr(h_bf16));
+    FP8_TRY(check_copy(FP8_RECIPE_MXFP8, a_q->row, a_q->row_scale));
+    FP8_TRY(check_copy(FP8_RECIPE_MXFP8, a_q->col, a_q->col_scale));
+    FP8_TRY(check_copy(FP8_RECIPE_MXFP8, h_q->row, h_q->row_scale));
+    if (a_bf16 != nullptr && !aligned16(a_bf16)) return FP8_ERR_ALIGN;
+  }
+  for (fp8_tensor* t : {a_q, h_q}) {
+    t->rows = rows;
+    t->cols = cols;
+    t->kind = FP8_RECIPE_MXFP8;
+    t->role = FP8_ROLE_ACTIVATION;
+  }
+  return cuda_status(gelu_quantize_launch(reinterpret_cast<const uint16_t*>(h_bf16), rows, cols,
+                                          reinterpret_cast<uint16_t*>(a_bf16), a_q, h_q, stream));
+}
+
+fp8_status fp8_dgelu_quantize(const fp8_recipe* recipe, const void* da_bf16,
+                              const fp8_tensor* h_q, void* dh_bf16, fp8_tensor* dh_q,
+                              int32_t* dev_status, cudaStream_t stream) {
+  (void)dev_status;
+  FP8_TRY(check_recipe(recipe));
+  if (recipe->kind != FP8_RECIPE_MXFP8) return FP8_ERR_UNSUPPORTED;
+  if (h_q == nullptr || dh_q == nullptr) return FP8_ERR_NULL;
+  if (h_q->kind != FP8_RECIPE_MXFP8) return FP8_ERR_UNSUPPORTED;
+  const int64_t rows = h_q->rows, cols = h_q->cols;
+  if (rows < 0 || cols < 0 || rows % 128 || cols % 128) return FP8_ERR_SHAPE;
+  if (rows > 0 && cols > 0) {
+    FP8_TRY(check_ptr(da_bf16));
+    FP8_TRY(check_copy(FP8_RECIPE_MXFP8, h_q->row, h_q->row_scale));
+    FP8_TRY(check_copy(FP8_RECIPE_MXFP8, dh_q->row, dh_q->row_scale));
+    FP8_TRY(check_copy(FP8_RECIPE_MXFP8, dh_q->col, dh_q->col_scale));
+    if (dh_bf16 != nullptr && !aligned16(dh_bf16)) return FP8_ERR_ALIGN;
+  }
+  dh_q->rows = rows;
+  dh_q->cols = cols;
+  dh_q->kind = FP8_RECIPE_MXFP8;
+  dh_q->role = FP8_ROLE_GRAD;
+  return cuda_status(dgelu_quantize_launch(reinterpret_cast<const uint16_t*>(da_bf16), h_q, rows,
+                                           cols, reinterpret_cast<uint16_t*>(dh_bf16), dh_q,
+                                           stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,443 @@
+// Scaled FP8 GEMMs of the FP8 linear layer on the sm_103a tensor core (tcgen05 + TMEM + TMA).
+//
+// Every GEMM of the layer is "TN": D[M][N] = sum_k A[M][K] * B[N][K] with both operands
+// K-major, because the column-wise FP8 copies are physically transposed (fprop X.W^T from
+// the row copies, dgrad dY.(W^T)^T from dY's row copy and W's column copy, wgrad
+// (dY^T).(X^T)^T from the two column copies). Scaling, per recipe of the Megatron Core
+// "Low-Precision Training Guide" (Recipe Reference):
+//   G_TENSOR  delayed / tensorwise: fp32 accumulation of the raw codes, times
+//             s_inv(A) * s_inv(B) in the epilogue.
+//   G_MX      mxfp8: the tensor core applies the E8M0 scale of every 32-wide K block of A
+//             and B during accumulation (tcgen05.mma kind::mxf8f6f4.block_scale).
+//   G_BLOCK   blockwise: each 128-wide K chunk is accumulated alone into TMEM; epilogue
+//             warps promote it into fp32 registers times s_inv(A row, chunk) * s_inv(B, chunk)
+//             (B: 128x128 tile scale, or per-row 1x128 scale for wgrad).
+//   G_BF16    bf16 x bf16 (wgrad with --fp8-wgrad off).
+//
+// Structure: a persistent kernel, one CTA per SM, 128 x 256 output tiles handed out
+// round-robin. Warp 0 streams A/B (and MX scale) tiles with TMA into a 4-stage shared-memory
+// ring; warp 1 allocates TMEM and issues the MMAs (one thread); warps 2..9 drain TMEM,
+// scale, round to bf16 and store. Accumulators are double-buffered in TMEM (512 columns) so
+// a tile's epilogue overlaps the next tile's main loop (MX keeps one accumulator buffer and
+// uses the remaining columns for the scale factors; its epilogue frees TMEM as soon as it
+// has read it). Every barrier wait has a clock budget; on expiry the kernel records
+// FP8_ERR_TIMEOUT in the caller's status word, lets in-flight copies land, frees TMEM and
+// returns.
+#include <algorithm>
+#include <cstdio>
+
+#include "common.cuh"
+#include "sm100_ptx.cuh"
+#include "internal.cuh"
+
+namespace fp8lin {
+
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBKBytes = 128;                 // one 128-byte swizzle row of K per stage
+constexpr int kStages = 4;
+constexpr int kEpiWarps = 8;
+constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
+constexpr uint32_t kTileABytes = kBM * kBKBytes;      // 16 KiB
+constexpr uint32_t kTileBBytes = kBN * kBKBytes;      // 32 KiB
+constexpr uint32_t kSfStageBytes = 2048;              // SFA 512 B at 0, SFB 2 x 512 B at 512
+constexpr uint32_t kStageBytes = kTileABytes + kTileBBytes + kSfStageBytes;
+constexpr uint32_t kGemmSmemBytes = 1024 + kStages * kStageBytes + 256;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint64_t kWaitBudgetCycles = 4000000000ull;   // ~2 s at 2 GHz
+
+
+struct SharedCtl {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t accf[2];
+  uint64_t acce[2];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, SharedCtl* ctl,
+                                         int32_t* status) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::clock64_();
+  while (true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*reinterpret_cast<volatile int*>(&ctl->abort_flag)) return false;
+    if (ptx::clock64_() - t0 > kWaitBudgetCycles) {
+      *reinterpret_cast<volatile int*>(&ctl->abort_flag) = 1;
+      report_status(status, FP8_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+template <int MODE>
+__device__ __forceinline__ uint32_t instr_desc() {
+  // [4,6) D format (1 = f32) | [7,10) A fmt | [10,13) B fmt | [15] A major | [16] B major
+  // | [17,23) N >> 3 | [24,29) M >> 4. E4M3 = 0, bf16 = 1.
+  uint32_t d = (uint32_t(kBN >> 3) << 17) | (uint32_t(kBM >> 4) << 24);
+  if constexpr (MODE == G_MX) {
+    d |= (1u << 23);                          // scale factors are E8M0
+  } else if constexpr (MODE == G_BF16) {
+    d |= (1u << 4) | (1u << 7) | (1u << 10);
+  } else {
+    d |= (1u << 4);
+  }
+  return d;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Store one thread's row segment of 128 fp32 values (columns n .. n+127 of row m).
+__device__ __forceinline__ void store_row128(const GemmParams& p, int m, int n, const float* v) {
+  if (m >= p.M) return;
+  if (p.d_fp32) {
+    float* dst = reinterpret_cast<float*>(p.D) + int64_t(m) * p.ldd + n;
+#pragma unroll
+    for (int j = 0; j < 128; j += 8) {
+      if (n + j < p.N) {
+        reinterpret_cast<float4*>(dst + j)[0] = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+        reinterpret_cast<float4*>(dst + j)[1] =
+            make_float4(v[j + 4], v[j + 5], v[j + 6], v[j + 7]);
+      }
+    }
+  } else {
+    uint16_t* dst = reinterpret_cast<uint16_t*>(p.D) + int64_t(m) * p.ldd + n;
+#pragma unroll
+    for (int j = 0; j < 128; j += 8) {
+      if (n + j < p.N) {
+        *reinterpret_cast<uint4*>(dst + j) =
+            make_uint4(pack_bf16x2(v[j], v[j + 1]), pack_bf16x2(v[j + 2], v[j + 3]),
+                       pack_bf16x2(v[j + 4], v[j + 5]), pack_bf16x2(v[j + 6], v[j + 7]));
+      }
+    }
+  }
+}
+
+// Read 128 consecutive accumulator columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_load128(uint32_t taddr, float* out) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t r[32];
+    ptx::tmem_ld_32x32b_x32(taddr + 32 * c, r);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) out[32 * c + j] = __uint_as_float(r[j]);
+  }
+}
+
+template <int MODE>
+__global__ void __maxnreg__(200)
+    gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA,
+                   const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * kTileABytes;
+  uint8_t* sSF = sB + kStages * kTileBBytes;
+  SharedCtl* ctl = reinterpret_cast<SharedCtl*>(sSF + kStages * kSfStageBytes);
+
+  constexpr int kNumAcc = (MODE == G_MX) ? 1 : 2;
+  constexpr int kElem = (MODE == G_BF16) ? 2 : 1;
+  constexpr int kBKElems = kBKBytes / kElem;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tiles_m = (p.M + kBM - 1) / kBM;
+  const int tiles_n = (p.N + kBN - 1) / kBN;
+  const int n_tiles = tiles_m * tiles_n;
+  const int nk = (p.K + kBKElems - 1) / kBKElems;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(&ctl->full[s], 1);
+      ptx::mbar_init(&ctl->empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&ctl->accf[b], 1);
+      ptx::mbar_init(&ctl->acce[b], kEpiWarps);
+    }
+    ctl->abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&ctl->tmem_base, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tmA);
+      ptx::prefetch_tmap(&tmB);
+      int s = 0;
+      uint32_t ph = 0;
+      const int kblocks128 = p.K / 128;       // MX scale atoms per operand row tile
+      for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+        const int m0 = (tile % tiles_m) * kBM, n0 = (tile / tiles_m) * kBN;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!wait_bar(&ctl->empty[s], ph ^ 1u, ctl, p.status)) goto producer_done;
+          uint32_t bytes = kTileABytes + kTileBBytes;
+          const bool sfb_hi = (n0 + 128) < p.N;
+          if constexpr (MODE == G_MX) bytes += 512u + (sfb_hi ? 1024u : 512u);
+          ptx::mbar_arrive_expect_tx(&ctl->full[s], bytes);
+          ptx::tma_load_2d(sA + s * kTileABytes, &tmA, kb * kBKElems, m0, &ctl->full[s]);
+          ptx::tma_load_2d(sB + s * kTileBBytes, &tmB, kb * kBKElems, n0, &ctl->full[s]);
+          if constexpr (MODE == G_MX) {
+            uint8_t* sf = sSF + s * kSfStageBytes;
+            ptx::bulk_load(sf, p.sfa + (int64_t(m0 >> 7) * kblocks128 + kb) * 512, 512,
+                           &ctl->full[s]);
+            ptx::bulk_load(sf + 512, p.sfb + (int64_t(n0 >> 7) * kblocks128 + kb) * 512, 512,
+                           &ctl->full[s]);
+            if (sfb_hi)
+              ptx::bulk_load(sf + 1024, p.sfb + (int64_t((n0 >> 7) + 1) * kblocks128 + kb) * 512,
+                             512, &ctl->full[s]);
+          }
+          if (++s == kStages) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+    producer_done:;
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = instr_desc<MODE>();
+      const uint32_t sfa_t = tmem + 256, sfb_t = tmem + 260;   // MX scale-factor columns
+      int s = 0;
+      uint32_t ph = 0;
+      uint32_t u = 0;
+      for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+        uint32_t d_t = tmem;
+        if constexpr (MODE != G_BLOCK) {
+          const uint32_t b = u % kNumAcc;
+          if (!wait_bar(&ctl->acce[b], ((u / kNumAcc) & 1u) ^ 1u, ctl, p.status)) goto mma_done;
+          ptx::tc_fence_after();
+          d_t = tmem + b * kBN;
+        }
+        for (int kb = 0; kb < nk; ++kb) {
+          uint32_t b = 0;
+          if constexpr (MODE == G_BLOCK) {
+            b = u & 1u;
+            if (!wait_bar(&ctl->acce[b], ((u >> 1) & 1u) ^ 1u, ctl, p.status)) goto mma_done;
+            ptx::tc_fence_after();
+            d_t = tmem + b * kBN;
+          }
+          if (!wait_bar(&ctl->full[s], ph, ctl, p.status)) goto mma_done;
+          ptx::tc_fence_after();
+          const uint32_t a_addr = ptx::smem_u32(sA + s * kTileABytes);
+          const uint32_t b_addr = ptx::smem_u32(sB + s * kTileBBytes);
+          if constexpr (MODE == G_MX) {
+            const uint32_t sf = ptx::smem_u32(sSF + s * kSfStageBytes);
+            ptx::tmem_cp_32x128b_warpx4(sfa_t, ptx::smem_desc(sf, 0, 128, ptx::kSwizzleNone));
+            ptx::tmem_cp_32x128b_warpx4(sfb_t,
+                                        ptx::smem_desc(sf + 512, 0, 128, ptx::kSwizzleNone));
+            ptx::tmem_cp_32x128b_warpx4(sfb_t + 4,
+                                        ptx::smem_desc(sf + 1024, 0, 128, ptx::kSwizzleNone));
+          }
+#pragma unroll
+          for (int k = 0; k < kBKBytes / 32; ++k) {
+            const uint64_t ad = ptx::smem_desc(a_addr + 32 * k, 16, 1024, ptx::kSwizzle128B);
+            const uint64_t bd = ptx::smem_desc(b_addr + 32 * k, 16, 1024, ptx::kSwizzle128B);
+            if constexpr (MODE == G_MX) {
+              const uint32_t id = idesc | (uint32_t(k) << 29) | (uint32_t(k) << 4);
+              ptx::mma_mxf8f6f4(d_t, ad, bd, id, sfa_t, sfb_t, (kb | k) != 0);
+            } else if constexpr (MODE == G_BF16) {
+              ptx::mma_f16(d_t, ad, bd, idesc, (kb | k) != 0);
+            } else if constexpr (MODE == G_BLOCK) {
+              ptx::mma_f8f6f4(d_t, ad, bd, idesc, k != 0);
+            } else {
+              ptx::mma_f8f6f4(d_t, ad, bd, idesc, (kb | k) != 0);
+            }
+          }
+          ptx::mma_commit(&ctl->empty[s]);
+          if constexpr (MODE == G_BLOCK) {
+            ptx::mma_commit(&ctl->accf[b]);
+            ++u;
+          }
+          if (++s == kStages) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if constexpr (MODE != G_BLOCK) {
+          ptx::mma_commit(&ctl->accf[u % kNumAcc]);
+          ++u;
+        }
+      }
+    mma_done:;
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue warps
+    const int ew = warp - 2;
+    const int quad = warp & 3;            // TMEM lane quadrant this warp may access
+    const int half = ew >> 2;             // which 128 columns of the 256-wide tile
+    const int row = 32 * quad + lane;
+    const uint32_t t_lane = tmem + (uint32_t(32 * quad) << 16) + uint32_t(half * 128);
+    float alpha = 1.0f;
+    if constexpr (MODE == G_TENSOR) alpha = __fmul_rn(*p.a_sinv, *p.b_sinv);
+    uint32_t u = 0;
+    float acc[128];
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+      const int m0 = (tile % tiles_m) * kBM, n0 = (tile / tiles_m) * kBN;
+      const int m = m0 + row, n = n0 + half * 128;
+      if constexpr (MODE != G_BLOCK) {
+        const uint32_t b = u % kNumAcc;
+        if (!wait_bar(&ctl->accf[b], (u / kNumAcc) & 1u, ctl, p.status)) break;
+        ptx::tc_fence_after();
+        tmem_load128(t_lane + b * kBN, acc);
+        ptx::tmem_wait_ld();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&ctl->acce[b]);
+        ++u;
+        if constexpr (MODE == G_TENSOR) {
+#pragma unroll
+          for (int j = 0; j < 128; ++j) acc[j] = __fmul_rn(acc[j], alpha);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+        const int kblocks = p.K / 128;
+        bool ok = true;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          const float sa = (m < p.M) ? p.a_bs[int64_t(kb) * p.M + m] : 0.0f;
+          float sb = 0.0f;
+          if (p.b_is_128 && n < p.N) sb = p.b_bs[int64_t(n >> 7) * kblocks + kb];
+          const uint32_t b = u & 1u;
+          if (!wait_bar(&ctl->accf[b], (u >> 1) & 1u, ctl, p.status)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          // Promote the chunk 32 columns at a time (keeps the partials out of registers).
+          const float f = __fmul_rn(sa, sb);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t r[32];
+            ptx::tmem_ld_32x32b_x32(t_lane + b * kBN + 32 * c, r);
+            ptx::tmem_wait_ld();
+            if (p.b_is_128) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                acc[32 * c + j] = __fmaf_rn(__uint_as_float(r[j]), f, acc[32 * c + j]);
+            } else {
+              const float* sbv = p.b_bs + int64_t(kb) * p.N + n + 32 * c;
+#pragma unroll
+              for (int j = 0; j < 32; j += 4) {
+                float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (n + 32 * c + j < p.N) q = *reinterpret_cast<const float4*>(sbv + j);
+                const int i = 32 * c + j;
+                acc[i] = __fmaf_rn(__uint_as_float(r[j]), __fmul_rn(sa, q.x), acc[i]);
+                acc[i + 1] = __fmaf_rn(__uint_as_float(r[j + 1]), __fmul_rn(sa, q.y), acc[i + 1]);
+                acc[i + 2] = __fmaf_rn(__uint_as_float(r[j + 2]), __fmul_rn(sa, q.z), acc[i + 2]);
+                acc[i + 3] = __fmaf_rn(__uint_as_float(r[j + 3]), __fmul_rn(sa, q.w), acc[i + 3]);
+              }
+            }
+          }
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&ctl->acce[b]);
+          ++u;
+        }
+        if (!ok) break;
+      }
+      store_row128(p, m, n, acc);
+    }
+  }
+
+  __syncthreads();
+  if (*reinterpret_cast<volatile int*>(&ctl->abort_flag)) {
+    // Let copies and MMAs already in flight land before the CTA's memory is released.
+    const uint64_t t0 = ptx::clock64_();
+    while (ptx::clock64_() - t0 < 20000000ull) {
+    }
+  }
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------------------------
+// Host side: tensor maps and launch
+// ------------------------------------------------------------------------------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// 2D K-major operand [rows][k] (elements of elem_bytes), box = 128 bytes of K x box_rows.
+static bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t k,
+                             int elem_bytes, int box_rows) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {cuuint64_t(k), cuuint64_t(rows)};
+  const cuuint64_t strides[1] = {cuuint64_t(k) * elem_bytes};
+  const cuuint32_t box[2] = {cuuint32_t(kBKBytes / elem_bytes), cuuint32_t(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r =
+      enc(map, elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+          2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+
+template <int MODE>
+static cudaError_t launch_mode(const GemmLaunch& g, cudaStream_t st) {
+  CUtensorMap ma, mb;
+  const int eb = MODE == G_BF16 ? 2 : 1;
+  if (!make_operand_map(&ma, g.A, g.p.M, g.p.K, eb, kBM)) return cudaErrorInvalidValue;
+  if (!make_operand_map(&mb, g.B, g.p.N, g.p.K, eb, kBN)) return cudaErrorInvalidValue;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tn_kernel<MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(kGemmSmemBytes));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int tiles = ((g.p.M + kBM - 1) / kBM) * ((g.p.N + kBN - 1) / kBN);
+  const int grid = std::max(1, std::min(tiles, sms));
+  gemm_tn_kernel<MODE><<<grid, kGemmThreads, kGemmSmemBytes, st>>>(ma, mb, g.p);
+  return cudaGetLastError();
+}
+
+cudaError_t gemm_launch(const GemmLaunch& g, cudaStream_t st) {
+  if (g.p.M == 0 || g.p.N == 0) return cudaSuccess;
+  switch (g.mode) {
+    case G_TENSOR: return launch_mode<G_TENSOR>(g, st);
+    case G_MX: return launch_mode<G_MX>(g, st);
+    case G_BLOCK: return launch_mode<G_BLOCK>(g, st);
+    case G_BF16: return launch_mode<G_BF16>(g, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fp8lin

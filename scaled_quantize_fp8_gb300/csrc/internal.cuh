@@ -1,0 +1,52 @@
+// Host-side interfaces between the C ABI (api.cu) and the kernel files.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "fp8lin.h"
+
+namespace fp8lin {
+
+// ---- quantize.cu
+size_t quantize_workspace_bytes(int kind, int64_t R, int64_t C);
+cudaError_t quantize_launch(int kind, int role, int margin, const uint16_t* x, int64_t R,
+                            int64_t C, bool want_row, bool want_col, fp8_tensor* out,
+                            void* workspace, cudaStream_t st);
+cudaError_t gelu_quantize_launch(const uint16_t* h, int64_t R, int64_t C, uint16_t* a_bf16,
+                                 fp8_tensor* a_q, fp8_tensor* h_q, cudaStream_t st);
+cudaError_t dgelu_quantize_launch(const uint16_t* da, const fp8_tensor* h_q, int64_t R,
+                                  int64_t C, uint16_t* dh_bf16, fp8_tensor* dh_q,
+                                  cudaStream_t st);
+cudaError_t amax_update_launch(float* hist, int32_t* head, int len, const float* amax_new,
+                               float* scale, float* scale_inv, int margin, cudaStream_t st);
+
+// ---- gemm.cu
+enum GMode : int { G_TENSOR = 0, G_MX = 1, G_BLOCK = 2, G_BF16 = 3 };
+
+struct GemmParams {
+  int M, N, K;              // D[M][N] = sum_k A[M][K] B[N][K]; K in elements
+  void* D;
+  int64_t ldd;
+  int d_fp32;
+  const float* a_sinv;      // G_TENSOR: per-tensor dequantisation factors
+  const float* b_sinv;
+  const uint8_t* sfa;       // G_MX: E8M0 scales in the tiled atom order
+  const uint8_t* sfb;
+  const float* a_bs;        // G_BLOCK: A 1x128 s_inv, [K/128][M]
+  const float* b_bs;        // G_BLOCK: B 128x128 grid [N/128][K/128] or 1x128 [K/128][N]
+  int b_is_128;
+  int32_t* status;          // device status word (may be null)
+};
+
+struct GemmLaunch {
+  int mode;                 // GMode
+  const void* A;            // [M][K] codes (bf16 for G_BF16)
+  const void* B;            // [N][K]
+  GemmParams p;
+};
+
+cudaError_t gemm_launch(const GemmLaunch& g, cudaStream_t st);
+
+}  // namespace fp8lin

@@ -211,3 +211,15 @@ def test_blockwise_each_block_max_hits_448():
             blk = xf[r, 128*j:128*j+128]
             c = np.argmax(np.abs(blk))
             assert q["row"][r, 128*j + c] in (0x7E, 0xFE)
+
+
+def test_mx_nonfinite_block_gets_nan_scale():
+    blk = np.ones((32, 64), np.float32)
+    blk[3, 40] = np.inf
+    blk[7, 2] = np.nan
+    q = O.quantize_mxfp8(bf16_bits_from_f32(blk))
+    assert q["row_scale"][3, 1] == 255 and q["row_scale"][7, 0] == 255
+    assert q["row_scale"][3, 0] == 119 and q["row_scale"][0, 1] == 119     # e = -8 for amax 1
+    assert q["row"][3, 40] == 0x7E and (q["row"][7, 2] & 0x7F) == 0x7F
+    assert q["row"][3, 41] == O.e4m3_encode(np.float32(1.0))                 # e = 0 in the NaN block
+    assert np.isnan(O.e8m0_decode(np.uint8(255)))
