@@ -197,6 +197,10 @@ fp8_status fp8_dgelu_quantize(const fp8_recipe *recipe, const void *da_bf16,
 /* Human-readable name of a status. */
 const char *fp8_status_str(fp8_status status);
 
+/* Text of the CUDA error behind the calling thread's most recent FP8_ERR_CUDA ("" if none).
+ * The string is owned by the library and stays valid until the thread's next failing call. */
+const char *fp8_last_cuda_error(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -58,6 +58,7 @@ _SIG = {
     "fp8_dgelu_quantize": (_I32, [ctypes.POINTER(Recipe), _P, ctypes.POINTER(Tensor), _P,
                                   ctypes.POINTER(Tensor), _P, _P]),
     "fp8_status_str": (ctypes.c_char_p, [_I32]),
+    "fp8_last_cuda_error": (ctypes.c_char_p, []),
 }
 
 _lib = None
@@ -94,4 +95,6 @@ class Fp8Error(RuntimeError):
 
 def check(status, where):
     if status != FP8_OK:
+        if status == 5 and _lib is not None:
+            where = f"{where} ({_lib.fp8_last_cuda_error().decode()})"
         raise Fp8Error(status, where)

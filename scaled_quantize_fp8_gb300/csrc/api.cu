@@ -40,7 +40,13 @@ int64_t shape_quantum(int kind) {
   return (kind == FP8_RECIPE_MXFP8 || kind == FP8_RECIPE_BLOCKWISE) ? 128 : 16;
 }
 
-fp8_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA; }
+thread_local const char* g_last_cuda_error = "";
+
+fp8_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return FP8_OK;
+  g_last_cuda_error = cudaGetErrorString(e);
+  return FP8_ERR_CUDA;
+}
 
 // Scale pointers a recipe needs for one copy.
 fp8_status check_copy(int kind, const uint8_t* codes, const void* scale) {
@@ -73,6 +79,8 @@ const char* fp8_status_str(fp8_status s) {
   }
   return "unknown status";
 }
+
+const char* fp8_last_cuda_error(void) { return g_last_cuda_error; }
 
 size_t fp8_workspace_bytes(const fp8_recipe* recipe, int64_t rows, int64_t cols) {
   if (recipe == nullptr) return 0;

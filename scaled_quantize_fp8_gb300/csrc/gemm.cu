@@ -128,8 +128,8 @@ __device__ __forceinline__ void tmem_load128(uint32_t taddr, float* out) {
   }
 }
 
-template <int MODE>
-__global__ void __maxnreg__(200)
+template <int MODE, int B128 = 1>
+__global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -310,7 +310,7 @@ __global__ void __maxnreg__(200)
         for (int kb = 0; kb < kblocks; ++kb) {
           const float sa = (m < p.M) ? p.a_bs[int64_t(kb) * p.M + m] : 0.0f;
           float sb = 0.0f;
-          if (p.b_is_128 && n < p.N) sb = p.b_bs[int64_t(n >> 7) * kblocks + kb];
+          if (B128 && n < p.N) sb = p.b_bs[int64_t(n >> 7) * kblocks + kb];
           const uint32_t b = u & 1u;
           if (!wait_bar(&ctl->accf[b], (u >> 1) & 1u, ctl, p.status)) {
             ok = false;
@@ -324,7 +324,7 @@ __global__ void __maxnreg__(200)
             uint32_t r[32];
             ptx::tmem_ld_32x32b_x32(t_lane + b * kBN + 32 * c, r);
             ptx::tmem_wait_ld();
-            if (p.b_is_128) {
+            if constexpr (B128 != 0) {
 #pragma unroll
               for (int j = 0; j < 32; ++j)
                 acc[32 * c + j] = __fmaf_rn(__uint_as_float(r[j]), f, acc[32 * c + j]);
@@ -406,7 +406,7 @@ static bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, i
 }
 
 
-template <int MODE>
+template <int MODE, int B128 = 1>
 static cudaError_t launch_mode(const GemmLaunch& g, cudaStream_t st) {
   CUtensorMap ma, mb;
   const int eb = MODE == G_BF16 ? 2 : 1;
@@ -414,7 +414,7 @@ static cudaError_t launch_mode(const GemmLaunch& g, cudaStream_t st) {
   if (!make_operand_map(&mb, g.B, g.p.N, g.p.K, eb, kBN)) return cudaErrorInvalidValue;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tn_kernel<MODE>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_tn_kernel<MODE, B128>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(kGemmSmemBytes));
     if (e != cudaSuccess) return e;
@@ -425,7 +425,7 @@ static cudaError_t launch_mode(const GemmLaunch& g, cudaStream_t st) {
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int tiles = ((g.p.M + kBM - 1) / kBM) * ((g.p.N + kBN - 1) / kBN);
   const int grid = std::max(1, std::min(tiles, sms));
-  gemm_tn_kernel<MODE><<<grid, kGemmThreads, kGemmSmemBytes, st>>>(ma, mb, g.p);
+  gemm_tn_kernel<MODE, B128><<<grid, kGemmThreads, kGemmSmemBytes, st>>>(ma, mb, g.p);
   return cudaGetLastError();
 }
 
@@ -434,7 +434,8 @@ cudaError_t gemm_launch(const GemmLaunch& g, cudaStream_t st) {
   switch (g.mode) {
     case G_TENSOR: return launch_mode<G_TENSOR>(g, st);
     case G_MX: return launch_mode<G_MX>(g, st);
-    case G_BLOCK: return launch_mode<G_BLOCK>(g, st);
+    case G_BLOCK:
+      return g.p.b_is_128 ? launch_mode<G_BLOCK, 1>(g, st) : launch_mode<G_BLOCK, 0>(g, st);
     case G_BF16: return launch_mode<G_BF16>(g, st);
   }
   return cudaErrorInvalidValue;
