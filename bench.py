@@ -1,0 +1,409 @@
+"""Benchmark of the FP8 linear-layer hot path on GB300.
+
+One step = one forward + backward pass of an MXFP8 transformer MLP block (8192 tokens,
+hidden 4096, ffn 16384), everything through the library's C ABI:
+    quantize X, W1, W2 (row + column copies) -> fc1 GEMM -> GeLU with its input kept in FP8
+    (fused with the MXFP8 quantize of the activation) -> fc2 GEMM -> quantize dY ->
+    fc2 dgrad + wgrad -> dGeLU (fused with the quantize of dh) -> fc1 dgrad + wgrad.
+Metric: GEMM TFLOP/s of the whole step (quantize time included), plus the quantize kernels'
+algorithmic HBM GB/s. Inputs are seeded synthetic bf16 tensors resident in HBM (about 2 GB
+touched per step, far above the 129 MB L2). `e2e` repeats the step with the inputs copied
+from pinned host memory and every result copied back inside the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+`--impl reference` times the CPU oracle (a deliberately slow, plain implementation) on a
+bounded sample of the same workload and reports the same metric.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "FP8 linear fwd+bwd TFLOPS (incl. quantize) vs FP8 peak; quantize HBM GB/s"
+TOKENS, HIDDEN, FFN = 8192, 4096, 16384
+GEMM_FLOPS = 6 * 2.0 * TOKENS * HIDDEN * FFN          # fc1, fc2 fwd; dgrad + wgrad of both
+WORKLOAD = "mxfp8_mlp_fwd_bwd tokens=8192 hidden=4096 ffn=16384"
+KERNELS_PER_STEP = 12                                 # 4 quantize, gelu, dgelu, 6 GEMMs
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FP8_OVER_BF16 = 2.0                                   # nominal dense fp8 / bf16 rate
+
+
+def peaks():
+    """(hbm GB/s, fp8 TFLOP/s, source). Measured peaks if the file exists, else fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        hbm = float(d.get("hbm_gbs"))
+        bf16 = float(d.get("bf16_tflops"))
+        return hbm, bf16 * FP8_OVER_BF16, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS * FP8_OVER_BF16, "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 200 ms while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- GPU step
+
+class MlpStep:
+    """Preallocated device buffers and the step itself (device-resident inputs)."""
+
+    def __init__(self, torch, F, dev):
+        self.torch, self.F, self.dev = torch, F, dev
+        from workloads import bf16_bits_normal
+        self.rec = F.Recipe(kind="mxfp8")
+        M, H, Fd = TOKENS, HIDDEN, FFN
+        host = {
+            "x": bf16_bits_normal(M, H, seed=0, stream=0),
+            "w1": bf16_bits_normal(Fd, H, seed=0, stream=1, sigma=0.02),
+            "w2": bf16_bits_normal(H, Fd, seed=0, stream=3, sigma=0.02),
+            "dy": bf16_bits_normal(M, H, seed=0, stream=2, sigma=1e-3),
+        }
+        # pinned host copies (for the end-to-end leg) and device copies
+        self.h = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory()
+                  for k, v in host.items()}
+        self.d = {k: v.to(dev) for k, v in self.h.items()}
+        e = F.empty_qtensor
+        self.xq = e(self.rec, M, H, "activation", device=dev)
+        self.w1q = e(self.rec, Fd, H, "weight", device=dev)
+        self.w2q = e(self.rec, H, Fd, "weight", device=dev)
+        self.dyq = e(self.rec, M, H, "grad", device=dev)
+        self.aq = e(self.rec, M, Fd, "activation", device=dev)
+        self.hq = e(self.rec, M, Fd, "activation", want_col=False, device=dev)
+        self.dhq = e(self.rec, M, Fd, "grad", device=dev)
+        bf = torch.bfloat16
+        self.hbuf = torch.empty((M, Fd), dtype=bf, device=dev)
+        self.y = torch.empty((M, H), dtype=bf, device=dev)
+        self.da = torch.empty((M, Fd), dtype=bf, device=dev)
+        self.dw2 = torch.empty((H, Fd), dtype=bf, device=dev)
+        self.dx = torch.empty((M, H), dtype=bf, device=dev)
+        self.dw1 = torch.empty((Fd, H), dtype=bf, device=dev)
+        self.outs = {"y": self.y, "dx": self.dx, "dw1": self.dw1, "dw2": self.dw2}
+        self.h_out = {k: torch.empty(v.shape, dtype=bf).pin_memory() for k, v in self.outs.items()}
+        # algorithmic bytes of the quantize kernels per step
+        mx = lambda r, c, copies: r * c * (2 + copies + copies / 32.0)  # noqa: E731
+        self.quant_bytes = (mx(M, H, 2) + mx(Fd, H, 2) + mx(H, Fd, 2) + mx(M, H, 2)
+                            + M * Fd * (2 + 3 + 3 / 32.0)                # gelu: h in, a x2 + h x1
+                            + M * Fd * (2 + 1 + 1 / 32.0 + 2 + 2 / 32.0))  # dgelu: da, h_q in
+        self.stream = torch.cuda.current_stream(dev)
+        self.events = []
+
+    def _timed(self, kind, fn):
+        if self.events is None:
+            return fn()
+        s = self.torch.cuda.Event(enable_timing=True)
+        e = self.torch.cuda.Event(enable_timing=True)
+        s.record(self.stream)
+        r = fn()
+        e.record(self.stream)
+        self.events.append((kind, s, e))
+        return r
+
+    def run(self, src=None):
+        F, rec, T = self.F, self.rec, self._timed
+        d = src or self.d
+        T("quant", lambda: F.quantize(rec, d["x"], "activation", out=self.xq))
+        T("quant", lambda: F.quantize(rec, d["w1"], "weight", out=self.w1q))
+        T("quant", lambda: F.quantize(rec, d["w2"], "weight", out=self.w2q))
+        T("gemm", lambda: F.linear_fwd(rec, self.xq, self.w1q, y=self.hbuf))
+        T("quant", lambda: F.gelu_quantize(rec, self.hbuf, a_q=self.aq, h_q=self.hq))
+        T("gemm", lambda: F.linear_fwd(rec, self.aq, self.w2q, y=self.y))
+        T("quant", lambda: F.quantize(rec, d["dy"], "grad", out=self.dyq))
+        T("gemm", lambda: F.linear_bwd(rec, self.dyq, self.aq, self.w2q, want_dw=False,
+                                       dx=self.da))
+        T("gemm", lambda: F.linear_bwd(rec, self.dyq, self.aq, self.w2q, want_dx=False,
+                                       dw=self.dw2))
+        T("quant", lambda: F.dgelu_quantize(rec, self.da, self.hq, dh_q=self.dhq))
+        T("gemm", lambda: F.linear_bwd(rec, self.dhq, self.xq, self.w1q, want_dw=False,
+                                       dx=self.dx))
+        T("gemm", lambda: F.linear_bwd(rec, self.dhq, self.xq, self.w1q, want_dx=False,
+                                       dw=self.dw1))
+
+    def run_e2e(self):
+        """Inputs copied from pinned host memory, all results copied back, inside the step."""
+        d = {k: self.d[k].copy_(v, non_blocking=True) for k, v in self.h.items()}
+        self.run(d)
+        for k, v in self.outs.items():
+            self.h_out[k].copy_(v, non_blocking=True)
+
+    def h2d_bytes(self):
+        return sum(v.numel() * 2 for v in self.h.values())
+
+    def d2h_bytes(self):
+        return sum(v.numel() * 2 for v in self.outs.values())
+
+    def kernel_stats(self):
+        ms = {"gemm": [], "quant": []}
+        for kind, s, e in self.events:
+            ms[kind].append(s.elapsed_time(e))
+        return ms
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from scaled_quantize_fp8_gb300 import build as B
+    B.build()
+    import scaled_quantize_fp8_gb300 as F
+
+    st = MlpStep(torch, F, dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    def max_over_ranks(v):
+        if world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    # ---- device-resident leg
+    st.events = None
+    for _ in range(args.warmup):
+        st.run()
+    barrier()
+    st.events = []
+    clocks = ClockSampler(local)
+    clocks.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(st.stream)
+    for _ in range(args.steps):
+        st.run()
+    t1.record(st.stream)
+    barrier()
+    clk = clocks.stop()
+    ms_total = max_over_ranks(t0.elapsed_time(t1))
+    ks = st.kernel_stats()
+
+    # ---- end-to-end leg (host buffers, copies inside the timed region)
+    st.events = None
+    for _ in range(max(1, args.warmup // 2)):
+        st.run_e2e()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(st.stream)
+    for _ in range(args.steps):
+        st.run_e2e()
+    e1.record(st.stream)
+    barrier()
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1))
+
+    ms_step = ms_total / args.steps
+    value = world * GEMM_FLOPS / (ms_step * 1e-3) / 1e12
+    e2e_value = world * GEMM_FLOPS / (ms_e2e / args.steps * 1e-3) / 1e12
+    hbm, fp8_peak, src = peaks()
+    gemm_ms = statistics.mean(ks["gemm"])
+    gemm_flops_launch = GEMM_FLOPS / 6
+    achieved = gemm_flops_launch / (gemm_ms * 1e-3) / 1e12
+    quant_ms_step = sum(ks["quant"]) / args.steps
+    quant_gbs = st.quant_bytes / (quant_ms_step * 1e-3) / 1e9
+
+    if rank == 0:
+        cpu = cpu_baseline()
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3 (fp32 accumulate)", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "recipe": "mxfp8",
+                       "parallelism": "replicas" if world > 1 else "single",
+                       "l2": "inputs larger than L2 (~2 GB touched per step)",
+                       "gemm_flops_per_step": GEMM_FLOPS},
+            "roofline": {"bound": "tensor", "kernel": "gemm_tn_kernel<G_MX>",
+                         "achieved": round(achieved, 1), "peak": fp8_peak, "unit": "TFLOP/s",
+                         "frac": round(achieved / fp8_peak, 4), "traffic": None,
+                         "peak_source": f"{src}: bf16 x {FP8_OVER_BF16} (nominal fp8/bf16)",
+                         "avg_launch_ms": round(gemm_ms, 4)},
+            "quantize": {"gbs": round(quant_gbs, 1), "peak_gbs": hbm,
+                         "frac": round(quant_gbs / hbm, 4), "ms_per_step": round(quant_ms_step, 4),
+                         "algorithmic_bytes_per_step": st.quant_bytes, "peak_source": src},
+            "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": st.h2d_bytes(), "d2h_bytes_per_step": st.d2h_bytes()},
+            "gpu_launches": KERNELS_PER_STEP * args.steps,
+            "clocks": clk,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+_ORACLE_SETUP = {}
+
+
+def _oracle_setup():
+    """Untimed: seeded inputs and the dequantised full weights the sampled GEMMs read."""
+    if not _ORACLE_SETUP:
+        from oracle import fp8_oracle as O
+        from workloads import bf16_bits_normal
+        w1 = bf16_bits_normal(FFN, HIDDEN, seed=0, stream=1, sigma=0.02)
+        w2 = bf16_bits_normal(HIDDEN, FFN, seed=0, stream=3, sigma=0.02)
+        qw1, qw2 = O.quantize_mxfp8(w1), O.quantize_mxfp8(w2)
+        dq = lambda q, c: O.dequant_mx(q[c], q[c + "_scale"])  # noqa: E731
+        _ORACLE_SETUP.update(
+            w1=w1, w2=w2, w1r=dq(qw1, "row"), w1c=dq(qw1, "col"), w2r=dq(qw2, "row"),
+            w2c=dq(qw2, "col"),
+            x=bf16_bits_normal(TOKENS, HIDDEN, seed=0, stream=0),
+            dy=bf16_bits_normal(TOKENS, HIDDEN, seed=0, stream=2, sigma=1e-3))
+    return _ORACLE_SETUP
+
+
+def cpu_baseline(m_sample=128, w_frac=16):
+    """The oracle, as it stands, on a bounded sample of the same step: the token-proportional
+    work on m_sample of the 8192 tokens (scaled up by 8192/m_sample) plus the per-step weight
+    quantisation on 1/w_frac of the weight rows (scaled up by w_frac)."""
+    from oracle import fp8_oracle as O
+    S = _oracle_setup()
+    dq = lambda q, c: O.dequant_mx(q[c], q[c + "_scale"])  # noqa: E731
+    x, dy = S["x"][:m_sample], S["dy"][:m_sample]
+    t0 = time.perf_counter()
+    O.quantize_mxfp8(S["w1"][: FFN // w_frac])
+    O.quantize_mxfp8(S["w2"][: HIDDEN // w_frac])
+    t_w = (time.perf_counter() - t0) * w_frac
+    t0 = time.perf_counter()
+    qx = O.quantize_mxfp8(x)
+    h = O.f64_to_bf16(O.gemm_tn_f64(dq(qx, "row"), S["w1r"]))
+    qh = O.quantize_mxfp8(h, want_col=False)
+    qa = O.quantize_mxfp8(O.gelu_bf16(h))
+    O.f64_to_bf16(O.gemm_tn_f64(dq(qa, "row"), S["w2r"]))
+    qdy = O.quantize_mxfp8(dy)
+    da = O.f64_to_bf16(O.gemm_tn_f64(dq(qdy, "row"), S["w2c"]))
+    O.gemm_tn_f64(dq(qdy, "col"), dq(qa, "col"))
+    qdh = O.quantize_mxfp8(O.dgelu_bf16(da, qh["row"], qh["row_scale"]))
+    O.gemm_tn_f64(dq(qdh, "row"), S["w1c"])
+    O.gemm_tn_f64(dq(qdh, "col"), dq(qx, "col"))
+    t_tok = (time.perf_counter() - t0) * (TOKENS // m_sample)
+    step_s = t_w + t_tok
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": round(GEMM_FLOPS / step_s / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
+            "kind": "oracle", "step_seconds_estimate": round(step_s, 2),
+            "sample": (f"oracle MLP step on {m_sample} of {TOKENS} tokens (x{TOKENS // m_sample})"
+                       f" plus weight quantisation of 1/{w_frac} of the rows (x{w_frac}); "
+                       "numpy: elementwise work on one core, fp64 matmuls on the BLAS threads")}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1 and rank != 0:
+        return
+    vals = []
+    _oracle_setup()
+    for _ in range(min(args.warmup, 1)):
+        cpu_baseline(m_sample=32, w_frac=64)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        vals.append(cpu_baseline(m_sample=32, w_frac=64))
+    elapsed = time.perf_counter() - t0
+    v = statistics.median(x["value"] for x in vals)
+    c = dict(vals[0])
+    c["value"] = v
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(statistics.median(x["step_seconds_estimate"] for x in vals) * 1e3, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64 (oracle)", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "recipe": "mxfp8", "parallelism": "single"},
+        "cpu_baseline": c, "wall_seconds": round(elapsed, 1),
+        "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

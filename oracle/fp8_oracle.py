@@ -32,7 +32,8 @@ where they are silent the readings below are the plainest ones the rest supports
     weights, whose column-wise copy is the byte transpose with the scale grid transposed.
   * GEMMs: every code is decoded and multiplied by its dequantisation factor in float64, the
     product is summed in float64 (numpy matmul), and the result is rounded once to bf16.
-  * GeLU is the exact erf form; its derivative is Phi(h) + h * phi(h).
+  * GeLU is the exact form h * Phi(h) (Phi evaluated through erfc so the negative tail keeps
+    full relative precision); its derivative is Phi(h) + h * phi(h).
 
 Conventions: X[M,K] activations, W[N,K] weights, Y = X W^T, dY[M,N]. The row-wise copy
 has the source's shape with blocks along its last dimension; the column-wise copy is the
@@ -373,21 +374,26 @@ def bf16_gemm_tn_f64(a_bf16, b_bf16):
 # GeLU with its input stored in FP8 (activation_func_fp8_input_store)
 # --------------------------------------------------------------------------------------
 
-_erf = np.vectorize(math.erf, otypes=[np.float64])
+_erfc = np.vectorize(math.erfc, otypes=[np.float64])
+
+
+def normal_cdf(h):
+    """Phi(h) = 0.5 erfc(-h / sqrt 2): the same function as 0.5 (1 + erf(h / sqrt 2)), but
+    without the cancellation that formula suffers when erf is close to -1 (h below about -5)."""
+    return 0.5 * _erfc(-np.asarray(h, dtype=np.float64) / math.sqrt(2.0))
 
 
 def gelu_f64(h):
-    """gelu(h) = 0.5 h (1 + erf(h / sqrt 2)), float64."""
+    """gelu(h) = h Phi(h) = 0.5 h (1 + erf(h / sqrt 2)), float64."""
     h = np.asarray(h, dtype=np.float64)
-    return 0.5 * h * (1.0 + _erf(h / math.sqrt(2.0)))
+    return h * normal_cdf(h)
 
 
 def gelu_grad_f64(h):
     """gelu'(h) = Phi(h) + h phi(h), float64."""
     h = np.asarray(h, dtype=np.float64)
-    Phi = 0.5 * (1.0 + _erf(h / math.sqrt(2.0)))
     phi = np.exp(-0.5 * h * h) / math.sqrt(2.0 * math.pi)
-    return Phi + h * phi
+    return normal_cdf(h) + h * phi
 
 
 def gelu_bf16(h_bf16):

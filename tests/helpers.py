@@ -56,3 +56,11 @@ def gemm_f32_normwise(got_f32, ref64):
     m = np.max(np.abs(ref64))
     err = float(np.max(np.abs(got_f32.astype(np.float64) - ref64)) / (m if m > 0 else 1.0))
     return err <= GEMM_F32_NORMWISE, err
+
+
+def same_f32(a, b):
+    """Bit-identical float32 scalars, or both NaN (a NaN's payload is not part of the result)."""
+    a, b = np.float32(a), np.float32(b)
+    if np.isnan(a) or np.isnan(b):
+        return bool(np.isnan(a) and np.isnan(b))
+    return a.tobytes() == b.tobytes()

@@ -10,7 +10,7 @@ import numpy as np
 import pytest
 import torch
 
-from helpers import bw_untile, cuda_ok, from_dev_bf16, mx_untile, to_dev_bf16
+from helpers import bw_untile, cuda_ok, mx_untile, same_f32, to_dev_bf16
 from oracle import fp8_oracle as O
 from workloads import bf16_bits_from_f32, bf16_bits_normal
 
@@ -39,9 +39,9 @@ def _np(t):
 def check_tensorwise(x_bits, margin=0):
     q = _q("tensorwise", x_bits, margin=margin)
     ref = O.quantize_tensorwise(x_bits, margin)
-    assert _np(q.amax)[0].tobytes() == np.float32(ref["amax"]).tobytes()
-    assert _np(q.scale)[0].tobytes() == np.float32(ref["scale"]).tobytes()
-    assert _np(q.scale_inv)[0].tobytes() == np.float32(ref["scale_inv"]).tobytes()
+    assert same_f32(_np(q.amax)[0], ref["amax"])
+    assert same_f32(_np(q.scale)[0], ref["scale"])
+    assert same_f32(_np(q.scale_inv)[0], ref["scale_inv"])
     assert np.array_equal(_np(q.row), ref["row"])
     assert np.array_equal(_np(q.col), ref["col"])
 
@@ -53,7 +53,7 @@ def check_delayed(x_bits, scale):
     ref = d.quantize(x_bits)
     assert np.array_equal(_np(q.row), ref["row"])
     assert np.array_equal(_np(q.col), ref["col"])
-    assert _np(q.amax)[0].tobytes() == np.float32(ref["amax"]).tobytes()
+    assert same_f32(_np(q.amax)[0], ref["amax"])
 
 
 def check_mx(x_bits):

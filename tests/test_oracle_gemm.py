@@ -117,6 +117,14 @@ def test_gelu_tabulated_normal_cdf():
     assert abs(O.gelu_grad_f64(1.0) - (0.8413447460685429 + 0.24197072451914337)) < 1e-15
 
 
+def test_gelu_negative_tail_keeps_relative_precision():
+    # Phi(-8) = 6.220960574271784e-16, Phi(-10) = 7.61985302416047e-24 (standard normal tables)
+    assert abs(O.gelu_f64(-8.0) / (-8.0 * 6.220960574271784e-16) - 1) < 1e-12
+    assert abs(O.gelu_f64(-10.0) / (-10.0 * 7.61985302416047e-24) - 1) < 1e-12
+    # phi(-8) = 5.052271083536893e-15: gelu'(-8) = Phi(-8) - 8 phi(-8)
+    assert abs(O.gelu_grad_f64(-8.0) / (6.220960574271784e-16 - 8 * 5.052271083536893e-15) - 1) < 1e-12
+
+
 def test_gelu_grad_matches_finite_difference():
     h = np.linspace(-6, 6, 241)
     eps = 1e-6
@@ -131,6 +139,6 @@ def test_dgelu_reads_h_from_fp8_copy():
     dh = O.dgelu_bf16(da, qh["row"], qh["row_scale"])
     hq = O.dequant_mx(qh["row"], qh["row_scale"])
     ref = O.bf16_to_f32(da).astype(np.float64) * np.array(
-        [0.5 * (1 + math.erf(v / math.sqrt(2))) + v * math.exp(-v * v / 2) / math.sqrt(2 * math.pi)
+        [0.5 * math.erfc(-v / math.sqrt(2)) + v * math.exp(-v * v / 2) / math.sqrt(2 * math.pi)
          for v in hq.ravel()]).reshape(hq.shape)
     assert np.array_equal(dh, O.f64_to_bf16(ref))
