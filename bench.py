@@ -390,8 +390,39 @@ def run_reference(args):
     }), flush=True)
 
 
+def run_profile_case(args):
+    """Launch one kernel kind a few times on its own (for ncu captures; prints no JSON line).
+    quant_mx / quant_tensorwise / quant_blockwise: X 16384 x 8192 bf16 (256 MiB, above L2).
+    gemm_mx / gemm_tensorwise / gemm_blockwise: fprop 8192 x 4096 x 4096."""
+    import torch
+    import scaled_quantize_fp8_gb300 as F
+    from scaled_quantize_fp8_gb300 import build as B
+    B.build()
+    case = args.profile
+    kind = {"mx": "mxfp8"}.get(case.split("_", 1)[1], case.split("_", 1)[1])
+    rec = F.Recipe(kind=kind)
+    g = torch.Generator(device="cuda").manual_seed(0)
+    if case.startswith("quant"):
+        x = torch.randn((16384, 8192), device="cuda", generator=g).to(torch.bfloat16)
+        q = F.empty_qtensor(rec, 16384, 8192, "activation")
+        for _ in range(args.steps):
+            F.quantize(rec, x, "activation", out=q)
+    else:
+        x = torch.randn((8192, 4096), device="cuda", generator=g).to(torch.bfloat16)
+        w = (torch.randn((4096, 4096), device="cuda", generator=g) * 0.02).to(torch.bfloat16)
+        xq, wq = F.quantize(rec, x, "activation"), F.quantize(rec, w, "weight")
+        y = torch.empty((8192, 4096), dtype=torch.bfloat16, device="cuda")
+        for _ in range(args.steps):
+            F.linear_fwd(rec, xq, wq, y=y)
+    torch.cuda.synchronize()
+    print(f"profile case {case}: {args.steps} launches done")
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--profile", default=None,
+                    choices=["quant_mx", "quant_tensorwise", "quant_blockwise", "gemm_mx",
+                             "gemm_tensorwise", "gemm_blockwise"])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
@@ -399,7 +430,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.profile:
+        run_profile_case(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
