@@ -203,6 +203,21 @@ class MlpStep:
         return ms
 
 
+def max_over_ranks(value, dist=None, device=None):
+    """The slowest rank's figure (timings are taken as the max over ranks)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world, ms_total, steps):
+    """All ranks' GEMM flops (each rank runs its own replica step) over the slowest time."""
+    return world * GEMM_FLOPS / (ms_total / steps * 1e-3) / 1e12
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -226,13 +241,6 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    def max_over_ranks(v):
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
     # ---- device-resident leg
     st.events = None
     for _ in range(args.warmup):
@@ -249,7 +257,7 @@ def run_ours(args):
     t1.record(st.stream)
     barrier()
     clk = clocks.stop()
-    ms_total = max_over_ranks(t0.elapsed_time(t1))
+    ms_total = max_over_ranks(t0.elapsed_time(t1), dist if world > 1 else None, dev)
     ks = st.kernel_stats()
 
     # ---- end-to-end leg (host buffers, copies inside the timed region)
@@ -264,11 +272,11 @@ def run_ours(args):
         st.run_e2e()
     e1.record(st.stream)
     barrier()
-    ms_e2e = max_over_ranks(e0.elapsed_time(e1))
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1), dist if world > 1 else None, dev)
 
     ms_step = ms_total / args.steps
-    value = world * GEMM_FLOPS / (ms_step * 1e-3) / 1e12
-    e2e_value = world * GEMM_FLOPS / (ms_e2e / args.steps * 1e-3) / 1e12
+    value = whole_job_tflops(world, ms_total, args.steps)
+    e2e_value = whole_job_tflops(world, ms_e2e, args.steps)
     hbm, fp8_peak, src = peaks()
     gemm_ms = statistics.mean(ks["gemm"])
     gemm_flops_launch = GEMM_FLOPS / 6
