@@ -401,7 +401,8 @@ def run_reference(args):
 def run_profile_case(args):
     """Launch one kernel kind a few times on its own (for ncu captures; prints no JSON line).
     quant_mx / quant_tensorwise / quant_blockwise: X 16384 x 8192 bf16 (256 MiB, above L2).
-    gemm_mx / gemm_tensorwise / gemm_blockwise: fprop 8192 x 4096 x 4096."""
+    gemm_mx / gemm_tensorwise / gemm_blockwise: fprop 8192 x 4096 x 4096.
+    gelu_mx / dgelu_mx: the fused GeLU / dGeLU + MXFP8 quantize on h 8192 x 16384."""
     import torch
     import scaled_quantize_fp8_gb300 as F
     from scaled_quantize_fp8_gb300 import build as B
@@ -410,7 +411,15 @@ def run_profile_case(args):
     kind = {"mx": "mxfp8"}.get(case.split("_", 1)[1], case.split("_", 1)[1])
     rec = F.Recipe(kind=kind)
     g = torch.Generator(device="cuda").manual_seed(0)
-    if case.startswith("quant"):
+    if case in ("gelu_mx", "dgelu_mx"):
+        h = torch.randn((8192, 16384), device="cuda", generator=g).to(torch.bfloat16)
+        a_q, h_q, _ = F.gelu_quantize(rec, h)
+        for _ in range(args.steps):
+            if case == "gelu_mx":
+                F.gelu_quantize(rec, h, a_q=a_q, h_q=h_q)
+            else:
+                F.dgelu_quantize(rec, h, h_q, dh_q=a_q)
+    elif case.startswith("quant"):
         x = torch.randn((16384, 8192), device="cuda", generator=g).to(torch.bfloat16)
         q = F.empty_qtensor(rec, 16384, 8192, "activation")
         for _ in range(args.steps):
@@ -430,9 +439,9 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--profile", default=None,
                     choices=["quant_mx", "quant_tensorwise", "quant_blockwise", "gemm_mx",
-                             "gemm_tensorwise", "gemm_blockwise"])
+                             "gemm_tensorwise", "gemm_blockwise", "gelu_mx", "dgelu_mx"])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     args = ap.parse_args()

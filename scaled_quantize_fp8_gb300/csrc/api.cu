@@ -91,7 +91,6 @@ fp8_status fp8_quantize(const fp8_recipe* recipe, const void* x_bf16, int64_t ro
                         int32_t role, int32_t want_row, int32_t want_col, fp8_tensor* out,
                         void* workspace, size_t ws_bytes, int32_t* dev_status,
                         cudaStream_t stream) {
-  (void)dev_status;
   FP8_TRY(check_recipe(recipe));
   if (out == nullptr) return FP8_ERR_NULL;
   if (role < FP8_ROLE_ACTIVATION || role > FP8_ROLE_GRAD) return FP8_ERR_UNSUPPORTED;
@@ -99,7 +98,7 @@ fp8_status fp8_quantize(const fp8_recipe* recipe, const void* x_bf16, int64_t ro
   const int kind = recipe->kind;
   const int64_t q = shape_quantum(kind);
   if (rows < 0 || cols < 0 || rows % q != 0 || cols % q != 0) return FP8_ERR_SHAPE;
-  if (rows > (int64_t(1) << 31) || cols > (int64_t(1) << 31)) return FP8_ERR_SHAPE;
+  if (rows * cols >= (int64_t(1) << 31)) return FP8_ERR_SHAPE;   // 32-bit element offsets
   FP8_TRY(check_scalars(kind, out));
   const bool empty = rows == 0 || cols == 0;
   if (!empty) {
@@ -116,7 +115,8 @@ fp8_status fp8_quantize(const fp8_recipe* recipe, const void* x_bf16, int64_t ro
   out->kind = kind;
   return cuda_status(quantize_launch(kind, role, recipe->margin,
                                      reinterpret_cast<const uint16_t*>(x_bf16), rows, cols,
-                                     want_row != 0, want_col != 0, out, workspace, stream));
+                                     want_row != 0, want_col != 0, out, workspace, dev_status,
+                                     stream));
 }
 
 fp8_status fp8_amax_update(const fp8_recipe* recipe, fp8_amax_history* hist,
@@ -252,11 +252,11 @@ fp8_status fp8_linear_bwd(const fp8_recipe* recipe, const fp8_tensor* dy,
 fp8_status fp8_gelu_quantize(const fp8_recipe* recipe, const void* h_bf16, int64_t rows,
                              int64_t cols, void* a_bf16, fp8_tensor* a_q, fp8_tensor* h_q,
                              int32_t* dev_status, cudaStream_t stream) {
-  (void)dev_status;
   FP8_TRY(check_recipe(recipe));
   if (recipe->kind != FP8_RECIPE_MXFP8) return FP8_ERR_UNSUPPORTED;
   if (a_q == nullptr || h_q == nullptr) return FP8_ERR_NULL;
   if (rows < 0 || cols < 0 || rows % 128 || cols % 128) return FP8_ERR_SHAPE;
+  if (rows * cols >= (int64_t(1) << 31)) return FP8_ERR_SHAPE;
   if (rows > 0 && cols > 0) {
     FP8_TRY(check_ptr(h_bf16));
     FP8_TRY(check_copy(FP8_RECIPE_MXFP8, a_q->row, a_q->row_scale));
@@ -271,19 +271,20 @@ fp8_status fp8_gelu_quantize(const fp8_recipe* recipe, const void* h_bf16, int64
     t->role = FP8_ROLE_ACTIVATION;
   }
   return cuda_status(gelu_quantize_launch(reinterpret_cast<const uint16_t*>(h_bf16), rows, cols,
-                                          reinterpret_cast<uint16_t*>(a_bf16), a_q, h_q, stream));
+                                          reinterpret_cast<uint16_t*>(a_bf16), a_q, h_q, dev_status,
+                                          stream));
 }
 
 fp8_status fp8_dgelu_quantize(const fp8_recipe* recipe, const void* da_bf16,
                               const fp8_tensor* h_q, void* dh_bf16, fp8_tensor* dh_q,
                               int32_t* dev_status, cudaStream_t stream) {
-  (void)dev_status;
   FP8_TRY(check_recipe(recipe));
   if (recipe->kind != FP8_RECIPE_MXFP8) return FP8_ERR_UNSUPPORTED;
   if (h_q == nullptr || dh_q == nullptr) return FP8_ERR_NULL;
   if (h_q->kind != FP8_RECIPE_MXFP8) return FP8_ERR_UNSUPPORTED;
   const int64_t rows = h_q->rows, cols = h_q->cols;
   if (rows < 0 || cols < 0 || rows % 128 || cols % 128) return FP8_ERR_SHAPE;
+  if (rows * cols >= (int64_t(1) << 31)) return FP8_ERR_SHAPE;
   if (rows > 0 && cols > 0) {
     FP8_TRY(check_ptr(da_bf16));
     FP8_TRY(check_copy(FP8_RECIPE_MXFP8, h_q->row, h_q->row_scale));
@@ -297,7 +298,7 @@ fp8_status fp8_dgelu_quantize(const fp8_recipe* recipe, const void* da_bf16,
   dh_q->role = FP8_ROLE_GRAD;
   return cuda_status(dgelu_quantize_launch(reinterpret_cast<const uint16_t*>(da_bf16), h_q, rows,
                                            cols, reinterpret_cast<uint16_t*>(dh_bf16), dh_q,
-                                           stream));
+                                           dev_status, stream));
 }
 
 }  // extern "C"

@@ -23,12 +23,18 @@ __device__ __forceinline__ void report_status(int32_t* st, int32_t code) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// |x| of two bf16 held in one word, as 16-bit integers: for non-NaN values the magnitude
-// order is the integer order of the low 15 bits; NaN patterns sort above +Inf (0x7F80).
-__device__ __forceinline__ uint32_t bf16x2_abs_bits(uint32_t w) { return w & 0x7FFF7FFFu; }
-__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) { return __vmaxu2(a, b); }
-__device__ __forceinline__ uint32_t hmax_u16x2(uint32_t a) {
-  return max(a & 0xFFFFu, a >> 16);
+// Magnitude maxima of packed bf16 pairs. The packed bf16 max propagates NaN, so a block or
+// tensor holding a NaN reports a NaN magnitude (any bit pattern above +Inf, 0x7F80, once the
+// sign is cleared); otherwise the result is the exact largest |x|.
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t acc, uint32_t w) {
+  __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&acc);
+  __nv_bfloat162 b = __habs2(*reinterpret_cast<__nv_bfloat162*>(&w));
+  __nv_bfloat162 m = __hmax2_nan(a, b);
+  return *reinterpret_cast<uint32_t*>(&m);
+}
+// Fold a packed pair of magnitudes into one 15-bit magnitude pattern.
+__device__ __forceinline__ uint32_t fold_bf16x2(uint32_t m) {
+  return max(m & 0x7FFFu, (m >> 16) & 0x7FFFu);
 }
 // amax (as a float) from the 15-bit bf16 magnitude pattern.
 __device__ __forceinline__ float amax_from_bits(uint32_t m) { return __uint_as_float(m << 16); }

@@ -370,41 +370,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // Host side: tensor maps and launch
 // ------------------------------------------------------------------------------------
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn get_encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (fn == nullptr) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  }
-  return fn;
-}
-
 // 2D K-major operand [rows][k] (elements of elem_bytes), box = 128 bytes of K x box_rows.
 static bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t k,
                              int elem_bytes, int box_rows) {
-  EncodeTiledFn enc = get_encode_fn();
-  if (enc == nullptr) return false;
-  const cuuint64_t dims[2] = {cuuint64_t(k), cuuint64_t(rows)};
-  const cuuint64_t strides[1] = {cuuint64_t(k) * elem_bytes};
-  const cuuint32_t box[2] = {cuuint32_t(kBKBytes / elem_bytes), cuuint32_t(box_rows)};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r =
-      enc(map, elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
-          2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return make_tmap_2d(map, base, elem_bytes, k, rows, kBKBytes / elem_bytes, box_rows, true);
 }
-
 
 template <int MODE, int B128 = 1>
 static cudaError_t launch_mode(const GemmLaunch& g, cudaStream_t st) {
@@ -420,9 +390,7 @@ static cudaError_t launch_mode(const GemmLaunch& g, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int sms = num_sms();
   const int tiles = ((g.p.M + kBM - 1) / kBM) * ((g.p.N + kBN - 1) / kBN);
   const int grid = std::max(1, std::min(tiles, sms));
   gemm_tn_kernel<MODE, B128><<<grid, kGemmThreads, kGemmSmemBytes, st>>>(ma, mb, g.p);

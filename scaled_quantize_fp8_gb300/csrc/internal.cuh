@@ -7,18 +7,28 @@
 
 #include "fp8lin.h"
 
+struct CUtensorMap_st;
+
 namespace fp8lin {
+
+// ---- tma.cu
+// 2-D tensor map over a row-major [rows][inner] array (elements of elem_bytes); box of
+// box_inner x box_rows elements; optional 128-byte swizzle; out-of-bounds reads fill zeros.
+bool make_tmap_2d(CUtensorMap_st* map, const void* base, int elem_bytes, int64_t inner,
+                  int64_t rows, int box_inner, int box_rows, bool swizzle128);
+int num_sms();
 
 // ---- quantize.cu
 size_t quantize_workspace_bytes(int kind, int64_t R, int64_t C);
 cudaError_t quantize_launch(int kind, int role, int margin, const uint16_t* x, int64_t R,
                             int64_t C, bool want_row, bool want_col, fp8_tensor* out,
-                            void* workspace, cudaStream_t st);
+                            void* workspace, int32_t* status, cudaStream_t st);
 cudaError_t gelu_quantize_launch(const uint16_t* h, int64_t R, int64_t C, uint16_t* a_bf16,
-                                 fp8_tensor* a_q, fp8_tensor* h_q, cudaStream_t st);
+                                 fp8_tensor* a_q, fp8_tensor* h_q, int32_t* status,
+                                 cudaStream_t st);
 cudaError_t dgelu_quantize_launch(const uint16_t* da, const fp8_tensor* h_q, int64_t R,
                                   int64_t C, uint16_t* dh_bf16, fp8_tensor* dh_q,
-                                  cudaStream_t st);
+                                  int32_t* status, cudaStream_t st);
 cudaError_t amax_update_launch(float* hist, int32_t* head, int len, const float* amax_new,
                                float* scale, float* scale_inv, int margin, cudaStream_t st);
 

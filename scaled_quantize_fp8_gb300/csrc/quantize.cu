@@ -14,6 +14,7 @@
 
 #include "common.cuh"
 #include "internal.cuh"
+#include "sm100_ptx.cuh"
 
 namespace fp8lin {
 
@@ -38,6 +39,7 @@ struct QuantParams {
   uint32_t* part_out;         // delayed: this tile's amax partial
   int margin;
   // MLP epilogues
+  int32_t* status;            // device status word (may be null)
   uint16_t* y_bf16;           // GELU: a = gelu(h) in bf16; DGELU: dh in bf16 (optional)
   uint8_t* aux_row;           // GELU: h row codes; DGELU: h row codes (read)
   uint8_t* aux_scale;         // GELU: h row E8M0 (written); DGELU: h row E8M0 (read)
@@ -62,9 +64,8 @@ __device__ __forceinline__ float gelu_grad_f32(float h) {
 
 // Max of the 15-bit magnitudes of the eight bf16 in a vector.
 __device__ __forceinline__ uint32_t vec_amax_bits(uint4 v) {
-  uint32_t m = max_u16x2(max_u16x2(bf16x2_abs_bits(v.x), bf16x2_abs_bits(v.y)),
-                         max_u16x2(bf16x2_abs_bits(v.z), bf16x2_abs_bits(v.w)));
-  return hmax_u16x2(m);
+  uint32_t m = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(0u, v.x), v.y), v.z), v.w);
+  return fold_bf16x2(m);
 }
 
 // Block-wide max of a per-thread value (256 threads), result broadcast to all threads.
@@ -101,31 +102,38 @@ __device__ __forceinline__ void encode_col32(const uint32_t* w, bool hi, float s
   out[1] = make_uint4(c[4], c[5], c[6], c[7]);
 }
 
+struct QuantSmem {
+  uint32_t tile[2][128][64];        // double-buffered bf16 tile, [row][col/2] pairs (64 KiB)
+  uint8_t sc_row[512];              // MXFP8 scale atom of the row copy
+  uint8_t sc_col[512];              // ... of the column copy
+  float scf_row[128];               // blockwise 1x128 s_inv staging
+  float scf_col[128];
+  uint32_t red[8];
+  uint32_t red_col[4][128];
+  uint64_t bar[2];                  // TMA completion, one per buffer
+  int abort_flag;
+};
+constexpr uint64_t kQuantWaitBudget = 4000000000ull;   // ~2 s at 2 GHz
+constexpr int kQuantCtasPerSm = 3;                     // 3 x ~69 KiB of shared memory
+
+// Quantise one 128 x 128 tile held in shared memory (see the file comment for the scheme).
 template <int MODE, int EPI>
-__global__ void __launch_bounds__(256) quantize_tile_kernel(const QuantParams p) {
-  __shared__ __align__(16) uint32_t tile[128][64];      // bf16 pairs: [row][col/2]
-  __shared__ __align__(16) uint8_t sc_row[512];
-  __shared__ __align__(16) uint8_t sc_col[512];
-  __shared__ __align__(16) float scf_row[128];
-  __shared__ __align__(16) float scf_col[128];
-  __shared__ uint32_t red[8];
-  __shared__ uint32_t red_col[4][128];
-
+__device__ __forceinline__ void quantize_one_tile(const QuantParams& p, QuantSmem& S,
+                                                  uint32_t (*tile)[64], int tile_id,
+                                                  float s_tensor, bool tensor_nan) {
   const int t = threadIdx.x;
-  const int tr = blockIdx.x / p.tiles_c, tc = blockIdx.x % p.tiles_c;
-  const int64_t r0 = int64_t(tr) * kTile, c0 = int64_t(tc) * kTile;
+  const int tr = tile_id / p.tiles_c, tc = tile_id % p.tiles_c;
+  // 32-bit index arithmetic: the host guarantees R * C < 2^31.
+  const uint32_t r0 = uint32_t(tr) * kTile, c0 = uint32_t(tc) * kTile;
   const int vcol = t & 15, rb = t >> 4;
-  const int64_t R = p.R, C = p.C;
+  const uint32_t R = uint32_t(p.R), C = uint32_t(p.C);
   const bool col_ok = (c0 + 8 * vcol) < C;
+  const uint32_t rowoff0 = (r0 + rb) * C + c0 + 8 * vcol;   // element offset of v[0]
 
-  // ---- load the tile (8 vectors of 8 bf16 per thread, all in flight together)
+  // ---- this thread's eight 16-byte vectors (out-of-range parts of the tile read as zero)
   uint4 v[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int64_t r = r0 + rb + 16 * i;
-    v[i] = make_uint4(0, 0, 0, 0);
-    if (r < R && col_ok) v[i] = ldg_nc_v4(p.x + r * C + c0 + 8 * vcol);
-  }
+  for (int i = 0; i < 8; ++i) v[i] = *reinterpret_cast<const uint4*>(&tile[rb + 16 * i][4 * vcol]);
 
   // ---- MLP epilogues: turn the input into the tensor to quantise
   if constexpr (EPI == EPI_GELU) {
@@ -137,10 +145,10 @@ __global__ void __launch_bounds__(256) quantize_tile_kernel(const QuantParams p)
       m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
       float mult;
       const uint32_t b = mx_scale_byte(m, &mult);
-      const int64_t r = r0 + rb + 16 * i;
+      const uint32_t r = r0 + rb + 16 * i;
+      const uint32_t off = rowoff0 + 16 * i * C;
       if (r < R && col_ok) {
-        *reinterpret_cast<uint2*>(p.aux_row + r * C + c0 + 8 * vcol) =
-            encode8(v[i], mult, m > 0x7F80u);
+        *reinterpret_cast<uint2*>(p.aux_row + off) = encode8(v[i], mult, m > 0x7F80u);
         if ((vcol & 3) == 0) p.aux_scale[mx_scale_offset(r, (c0 + 8 * vcol) >> 5, C)] = uint8_t(b);
       }
       uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
@@ -150,15 +158,17 @@ __global__ void __launch_bounds__(256) quantize_tile_kernel(const QuantParams p)
       }
       v[i] = make_uint4(w[0], w[1], w[2], w[3]);
       if (p.y_bf16 != nullptr && r < R && col_ok)
-        *reinterpret_cast<uint4*>(p.y_bf16 + r * C + c0 + 8 * vcol) = v[i];
+        *reinterpret_cast<uint4*>(p.y_bf16 + off) = v[i];
+      *reinterpret_cast<uint4*>(&tile[rb + 16 * i][4 * vcol]) = v[i];   // for the column pass
     }
   } else if constexpr (EPI == EPI_DGELU) {
     // dh = bf16(da * gelu'(h)) with h decoded from its MXFP8 row copy.
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const int64_t r = r0 + rb + 16 * i;
+      const uint32_t r = r0 + rb + 16 * i;
+      const uint32_t off = rowoff0 + 16 * i * C;
       if (r < R && col_ok) {
-        const uint2 hc = *reinterpret_cast<const uint2*>(p.aux_row + r * C + c0 + 8 * vcol);
+        const uint2 hc = *reinterpret_cast<const uint2*>(p.aux_row + off);
         const uint32_t sb = p.aux_scale[mx_scale_offset(r, (c0 + 8 * vcol) >> 5, C)];
         const float hs = sb == 0xFFu ? __uint_as_float(0x7FC00000u) : exp2i(int(sb) - 127);
         const uint32_t cw[2] = {hc.x, hc.y};
@@ -172,9 +182,9 @@ __global__ void __launch_bounds__(256) quantize_tile_kernel(const QuantParams p)
           w[k] = bf16_rn_bits(d0) | (bf16_rn_bits(d1) << 16);
         }
         v[i] = make_uint4(w[0], w[1], w[2], w[3]);
-        if (p.y_bf16 != nullptr)
-          *reinterpret_cast<uint4*>(p.y_bf16 + r * C + c0 + 8 * vcol) = v[i];
+        if (p.y_bf16 != nullptr) *reinterpret_cast<uint4*>(p.y_bf16 + off) = v[i];
       }
+      *reinterpret_cast<uint4*>(&tile[rb + 16 * i][4 * vcol]) = v[i];
     }
   }
 
@@ -184,28 +194,16 @@ __global__ void __launch_bounds__(256) quantize_tile_kernel(const QuantParams p)
   for (int i = 0; i < 8; ++i) lmax = max(lmax, vec_amax_bits(v[i]));
 
   // ---- the tile-wide scale (per-tensor and 128x128 recipes)
-  float s_tile = 1.0f, sinv_tile = 1.0f;
-  bool tile_nan = false;
+  float s_tile = s_tensor, sinv_tile = 1.0f;
+  bool tile_nan = tensor_nan;
   if constexpr (MODE == Q_TENSOR) {
-    if (p.scale_in != nullptr) {
-      s_tile = *p.scale_in;                                   // delayed: from the history
-      const uint32_t tm = block_max_u32(lmax, red);
+    if (p.part_out != nullptr) {                              // delayed: record this tile's amax
+      const uint32_t tm = block_max_u32(lmax, S.red);
       tile_nan = tm > 0x7F80u;
-      if (t == 0 && p.part_out != nullptr) p.part_out[blockIdx.x] = tm;
-    } else {                                                  // tensorwise: from partials
-      uint32_t m = 0;
-      for (int i = t; i < p.n_part_in; i += 256) m = max(m, p.part_in[i]);
-      m = block_max_u32(m, red);
-      tile_nan = m > 0x7F80u;
-      s_tile = scale_from_amax(amax_from_bits(m), p.margin, &sinv_tile);
-      if (blockIdx.x == 0 && t == 0) {
-        *p.amax_out = amax_from_bits(m);
-        *p.scale_out = s_tile;
-        *p.scale_inv_out = sinv_tile;
-      }
+      if (t == 0) p.part_out[tile_id] = tm;
     }
   } else if constexpr (MODE == Q_BW128) {
-    const uint32_t tm = block_max_u32(lmax, red);
+    const uint32_t tm = block_max_u32(lmax, S.red);
     tile_nan = tm > 0x7F80u;
     s_tile = scale_from_amax(amax_from_bits(tm), p.margin, &sinv_tile);
     if (t == 0) {
@@ -219,7 +217,7 @@ __global__ void __launch_bounds__(256) quantize_tile_kernel(const QuantParams p)
   if (p.row != nullptr) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const int64_t r = r0 + rb + 16 * i;
+      const uint32_t r = r0 + rb + 16 * i;
       const int lr = rb + 16 * i;
       uint2 codes;
       if constexpr (MODE == Q_TENSOR || MODE == Q_BW128) {
@@ -231,7 +229,7 @@ __global__ void __launch_bounds__(256) quantize_tile_kernel(const QuantParams p)
         float mult;
         const uint32_t b = mx_scale_byte(m, &mult);
         codes = encode8(v[i], mult, m > 0x7F80u);
-        if ((vcol & 3) == 0) sc_row[(lr & 31) * 16 + (lr >> 5) * 4 + (vcol >> 2)] = uint8_t(b);
+        if ((vcol & 3) == 0) S.sc_row[(lr & 31) * 16 + (lr >> 5) * 4 + (vcol >> 2)] = uint8_t(b);
       } else {  // Q_BW1x128: the block is the whole 128-wide tile row (16 lanes)
         uint32_t m = vec_amax_bits(v[i]);
 #pragma unroll
@@ -239,108 +237,169 @@ __global__ void __launch_bounds__(256) quantize_tile_kernel(const QuantParams p)
         float sinv;
         const float s = scale_from_amax(amax_from_bits(m), p.margin, &sinv);
         codes = encode8(v[i], s, m > 0x7F80u);
-        if (vcol == 0) scf_row[lr] = sinv;
+        if (vcol == 0) S.scf_row[lr] = sinv;
       }
-      if (r < R && col_ok) *reinterpret_cast<uint2*>(p.row + r * C + c0 + 8 * vcol) = codes;
+      if (r < R && col_ok) *reinterpret_cast<uint2*>(p.row + rowoff0 + 16 * i * C) = codes;
     }
   }
 
-  if (p.col == nullptr) {
-    // still flush the row scales
-    if constexpr (MODE == Q_MX || MODE == Q_BW1x128) {
-      if (p.row != nullptr) {
-        __syncthreads();
-        if constexpr (MODE == Q_MX) {
-          if (t < 32)
-            reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.row_scale) +
-                                     (int64_t(tr) * p.tiles_c + tc) * 512)[t] =
-                reinterpret_cast<const uint4*>(sc_row)[t];
-        } else {
-          if (t < 128) reinterpret_cast<float*>(p.row_scale)[int64_t(tc) * R + r0 + t] = scf_row[t];
-        }
+  if (p.col != nullptr) {
+    if constexpr (EPI != EPI_NONE) __syncthreads();          // transformed tile written back
+
+    // ---- column-wise copy: thread owns source columns 2pp, 2pp+1 and rows 32q .. 32q+31
+    const int pp = t & 63, q = t >> 6;
+    uint32_t w[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) w[j] = tile[32 * q + j][pp];
+    uint32_t mw = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) mw = absmax_bf16x2(mw, w[j]);
+    const uint32_t ma = mw & 0x7FFFu, mb = (mw >> 16) & 0x7FFFu;   // columns 2pp and 2pp+1
+
+    float sa = s_tile, sb = s_tile;
+    bool na = tile_nan, nb = tile_nan;
+    if constexpr (MODE == Q_MX) {
+      float fa, fb;
+      const uint32_t ba = mx_scale_byte(ma, &fa), bb = mx_scale_byte(mb, &fb);
+      sa = fa;
+      sb = fb;
+      na = ma > 0x7F80u;
+      nb = mb > 0x7F80u;
+      const int ca = 2 * pp, cb = 2 * pp + 1;
+      S.sc_col[(ca & 31) * 16 + (ca >> 5) * 4 + q] = uint8_t(ba);
+      S.sc_col[(cb & 31) * 16 + (cb >> 5) * 4 + q] = uint8_t(bb);
+    } else if constexpr (MODE == Q_BW1x128) {
+      S.red_col[q][2 * pp] = ma;
+      S.red_col[q][2 * pp + 1] = mb;
+      __syncthreads();
+      const uint32_t fa = max(max(S.red_col[0][2 * pp], S.red_col[1][2 * pp]),
+                              max(S.red_col[2][2 * pp], S.red_col[3][2 * pp]));
+      const uint32_t fb = max(max(S.red_col[0][2 * pp + 1], S.red_col[1][2 * pp + 1]),
+                              max(S.red_col[2][2 * pp + 1], S.red_col[3][2 * pp + 1]));
+      float ia, ib;
+      sa = scale_from_amax(amax_from_bits(fa), p.margin, &ia);
+      sb = scale_from_amax(amax_from_bits(fb), p.margin, &ib);
+      na = fa > 0x7F80u;
+      nb = fb > 0x7F80u;
+      if (q == 0) {
+        S.scf_col[2 * pp] = ia;
+        S.scf_col[2 * pp + 1] = ib;
       }
     }
-    return;
-  }
 
-  // ---- park the tile in shared memory for the column-wise copy
+    uint4 out[2];
+    const uint32_t rr = r0 + 32 * q;
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
-    *reinterpret_cast<uint4*>(&tile[rb + 16 * i][4 * vcol]) = v[i];
-  __syncthreads();
-
-  // ---- column-wise copy: thread owns source columns 2pp, 2pp+1 and rows 32q .. 32q+31
-  const int pp = t & 63, q = t >> 6;
-  uint32_t w[32];
-#pragma unroll
-  for (int j = 0; j < 32; ++j) w[j] = tile[32 * q + j][pp];
-  uint32_t mw = 0;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) mw = max_u16x2(mw, bf16x2_abs_bits(w[j]));
-  const uint32_t ma = mw & 0xFFFFu, mb = mw >> 16;    // columns 2pp and 2pp+1
-
-  float sa = s_tile, sb = s_tile;
-  bool na = tile_nan, nb = tile_nan;
-  if constexpr (MODE == Q_MX) {
-    float fa, fb;
-    const uint32_t ba = mx_scale_byte(ma, &fa), bb = mx_scale_byte(mb, &fb);
-    sa = fa;
-    sb = fb;
-    na = ma > 0x7F80u;
-    nb = mb > 0x7F80u;
-    const int ca = 2 * pp, cb = 2 * pp + 1;
-    sc_col[(ca & 31) * 16 + (ca >> 5) * 4 + q] = uint8_t(ba);
-    sc_col[(cb & 31) * 16 + (cb >> 5) * 4 + q] = uint8_t(bb);
-  } else if constexpr (MODE == Q_BW1x128) {
-    red_col[q][2 * pp] = ma;
-    red_col[q][2 * pp + 1] = mb;
-    __syncthreads();
-    const uint32_t fa = max(max(red_col[0][2 * pp], red_col[1][2 * pp]),
-                            max(red_col[2][2 * pp], red_col[3][2 * pp]));
-    const uint32_t fb = max(max(red_col[0][2 * pp + 1], red_col[1][2 * pp + 1]),
-                            max(red_col[2][2 * pp + 1], red_col[3][2 * pp + 1]));
-    float ia, ib;
-    sa = scale_from_amax(amax_from_bits(fa), p.margin, &ia);
-    sb = scale_from_amax(amax_from_bits(fb), p.margin, &ib);
-    na = fa > 0x7F80u;
-    nb = fb > 0x7F80u;
-    if (q == 0) {
-      scf_col[2 * pp] = ia;
-      scf_col[2 * pp + 1] = ib;
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t c = c0 + 2 * pp + h;
+      encode_col32(w, h == 1, h == 0 ? sa : sb, h == 0 ? na : nb, out);
+      if (c < C) {
+        uint8_t* dst = p.col + c * R + rr;
+        if (rr < R) *reinterpret_cast<uint4*>(dst) = out[0];
+        if (rr + 16 < R) *reinterpret_cast<uint4*>(dst + 16) = out[1];
+      }
     }
   }
 
-  uint4 out[2];
-  const int64_t rr = r0 + 32 * q;
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int64_t c = c0 + 2 * pp + h;
-    encode_col32(w, h == 1, h == 0 ? sa : sb, h == 0 ? na : nb, out);
-    if (c < C) {
-      uint8_t* dst = p.col + c * R + rr;
-      if (rr < R) *reinterpret_cast<uint4*>(dst) = out[0];
-      if (rr + 16 < R) *reinterpret_cast<uint4*>(dst + 16) = out[1];
-    }
-  }
-
-  // ---- scales of both copies
+  // ---- scales of the copies written from staging
   if constexpr (MODE == Q_MX || MODE == Q_BW1x128) {
     __syncthreads();
     if constexpr (MODE == Q_MX) {
       const int tiles_r = int(R >> 7);
       if (t < 32 && p.row != nullptr)
         reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.row_scale) +
-                                 (int64_t(tr) * p.tiles_c + tc) * 512)[t] =
-            reinterpret_cast<const uint4*>(sc_row)[t];
-      if (t >= 32 && t < 64)
+                                 (uint32_t(tr) * p.tiles_c + tc) * 512)[t] =
+            reinterpret_cast<const uint4*>(S.sc_row)[t];
+      if (t >= 32 && t < 64 && p.col != nullptr)
         reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.col_scale) +
-                                 (int64_t(tc) * tiles_r + tr) * 512)[t - 32] =
-            reinterpret_cast<const uint4*>(sc_col)[t - 32];
+                                 (uint32_t(tc) * tiles_r + tr) * 512)[t - 32] =
+            reinterpret_cast<const uint4*>(S.sc_col)[t - 32];
     } else {
       if (t < 128 && p.row != nullptr)
-        reinterpret_cast<float*>(p.row_scale)[int64_t(tc) * R + r0 + t] = scf_row[t];
-      if (t >= 128)
-        reinterpret_cast<float*>(p.col_scale)[int64_t(tr) * C + c0 + (t - 128)] = scf_col[t - 128];
+        reinterpret_cast<float*>(p.row_scale)[uint32_t(tc) * R + r0 + t] = S.scf_row[t];
+      if (t >= 128 && p.col != nullptr)
+        reinterpret_cast<float*>(p.col_scale)[uint32_t(tr) * C + c0 + (t - 128)] =
+            S.scf_col[t - 128];
+    }
+  }
+}
+
+// Bounded wait on a TMA completion barrier (all threads); false once the budget is spent.
+__device__ __forceinline__ bool quant_wait(QuantSmem& S, int b, uint32_t parity, int32_t* st) {
+  if (ptx::mbar_try_wait(&S.bar[b], parity)) return true;
+  const uint64_t t0 = ptx::clock64_();
+  while (!ptx::mbar_try_wait(&S.bar[b], parity)) {
+    if (*reinterpret_cast<volatile int*>(&S.abort_flag)) return false;
+    if (ptx::clock64_() - t0 > kQuantWaitBudget) {
+      *reinterpret_cast<volatile int*>(&S.abort_flag) = 1;
+      report_status(st, FP8_ERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+// Persistent quantize kernel: each CTA walks tiles blockIdx.x, +gridDim.x, ...; thread 0
+// issues the TMA load of the next tile into the other buffer before the current one is
+// processed, so HBM reads overlap the conversion and the stores.
+template <int MODE, int EPI>
+__global__ void __launch_bounds__(256, kQuantCtasPerSm) quantize_tile_kernel(const __grid_constant__ CUtensorMap tmX,
+                                                            const QuantParams p) {
+  extern __shared__ uint8_t qsm_raw[];
+  QuantSmem& S = *reinterpret_cast<QuantSmem*>(
+      (reinterpret_cast<uintptr_t>(qsm_raw) + 127) & ~uintptr_t(127));
+  const int t = threadIdx.x;
+  const int tiles_r = int((p.R + 127) >> 7);
+  const int n_tiles = tiles_r * p.tiles_c;
+
+  if (t == 0) {
+    ptx::mbar_init(&S.bar[0], 1);
+    ptx::mbar_init(&S.bar[1], 1);
+    S.abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+
+  // per-tensor scale once per CTA: tensorwise from the amax partials, delayed from memory
+  float s_tensor = 1.0f;
+  bool tensor_nan = false;
+  if constexpr (MODE == Q_TENSOR) {
+    if (p.scale_in != nullptr) {
+      s_tensor = *p.scale_in;
+    } else {
+      uint32_t m = 0;
+      for (int i = t; i < p.n_part_in; i += 256) m = max(m, p.part_in[i]);
+      m = block_max_u32(m, S.red);
+      tensor_nan = m > 0x7F80u;
+      float sinv;
+      s_tensor = scale_from_amax(amax_from_bits(m), p.margin, &sinv);
+      if (blockIdx.x == 0 && t == 0) {
+        *p.amax_out = amax_from_bits(m);
+        *p.scale_out = s_tensor;
+        *p.scale_inv_out = sinv;
+      }
+    }
+  }
+
+  auto issue = [&](int tile_id, int b) {
+    const int tr = tile_id / p.tiles_c, tc = tile_id % p.tiles_c;
+    ptx::mbar_arrive_expect_tx(&S.bar[b], 128 * 128 * 2);
+    ptx::tma_load_2d(&S.tile[b][0][0], &tmX, tc * kTile, tr * kTile, &S.bar[b]);
+  };
+
+  int tile = blockIdx.x;
+  if (t == 0 && tile < n_tiles) issue(tile, 0);
+  for (int i = 0; tile < n_tiles; ++i, tile += gridDim.x) {
+    const int b = i & 1;
+    const int next = tile + int(gridDim.x);
+    if (t == 0 && next < n_tiles) issue(next, b ^ 1);
+    if (!quant_wait(S, b, uint32_t(i >> 1) & 1u, p.status)) break;
+    quantize_one_tile<MODE, EPI>(p, S, S.tile[b], tile, s_tensor, tensor_nan);
+    __syncthreads();                                 // buffer b is refilled next iteration
+  }
+  if (*reinterpret_cast<volatile int*>(&S.abort_flag)) {
+    const uint64_t t0 = ptx::clock64_();             // let the outstanding copy land
+    while (ptx::clock64_() - t0 < 20000000ull) {
     }
   }
 }
@@ -437,9 +496,7 @@ __global__ void __launch_bounds__(1024) amax_history_update_kernel(
 // ------------------------------------------------------------------------------------
 
 int amax_partial_ctas(int64_t n_vec) {
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int sms = num_sms();
   int64_t want = (n_vec + 2047) / 2048;                    // >= 4 vectors per thread
   return int(std::max<int64_t>(1, std::min<int64_t>(want, int64_t(sms) * 4)));
 }
@@ -456,14 +513,26 @@ template <int MODE, int EPI>
 static cudaError_t launch_tiles(const QuantParams& p, cudaStream_t st) {
   const int tiles_r = int((p.R + 127) / 128);
   const int n = tiles_r * p.tiles_c;
-  quantize_tile_kernel<MODE, EPI><<<n, 256, 0, st>>>(p);
+  CUtensorMap map;
+  if (!make_tmap_2d(&map, p.x, 2, p.C, p.R, kTile, kTile, false)) return cudaErrorInvalidValue;
+  const int smem = int(sizeof(QuantSmem)) + 128;
+  static bool attr = false;
+  if (!attr) {
+    const cudaError_t e = cudaFuncSetAttribute(quantize_tile_kernel<MODE, EPI>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const int grid = std::max(1, std::min(n, num_sms() * kQuantCtasPerSm));
+  quantize_tile_kernel<MODE, EPI><<<grid, 256, smem, st>>>(map, p);
   return cudaGetLastError();
 }
 
 cudaError_t quantize_launch(int kind, int role, int margin, const uint16_t* x, int64_t R,
                             int64_t C, bool want_row, bool want_col, fp8_tensor* out,
-                            void* workspace, cudaStream_t st) {
+                            void* workspace, int32_t* status, cudaStream_t st) {
   QuantParams p{};
+  p.status = status;
   p.x = x;
   p.R = R;
   p.C = C;
@@ -516,9 +585,11 @@ cudaError_t quantize_launch(int kind, int role, int margin, const uint16_t* x, i
 }
 
 cudaError_t gelu_quantize_launch(const uint16_t* h, int64_t R, int64_t C, uint16_t* a_bf16,
-                                 fp8_tensor* a_q, fp8_tensor* h_q, cudaStream_t st) {
+                                 fp8_tensor* a_q, fp8_tensor* h_q, int32_t* status,
+                                 cudaStream_t st) {
   if (R == 0 || C == 0) return cudaSuccess;
   QuantParams p{};
+  p.status = status;
   p.x = h;
   p.R = R;
   p.C = C;
@@ -535,9 +606,10 @@ cudaError_t gelu_quantize_launch(const uint16_t* h, int64_t R, int64_t C, uint16
 
 cudaError_t dgelu_quantize_launch(const uint16_t* da, const fp8_tensor* h_q, int64_t R,
                                   int64_t C, uint16_t* dh_bf16, fp8_tensor* dh_q,
-                                  cudaStream_t st) {
+                                  int32_t* status, cudaStream_t st) {
   if (R == 0 || C == 0) return cudaSuccess;
   QuantParams p{};
+  p.status = status;
   p.x = da;
   p.R = R;
   p.C = C;
