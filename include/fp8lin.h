@@ -194,6 +194,30 @@ fp8_status fp8_dgelu_quantize(const fp8_recipe *recipe, const void *da_bf16,
                               const fp8_tensor *h_q, void *dh_bf16, fp8_tensor *dh_q,
                               int32_t *dev_status, cudaStream_t stream);
 
+/*
+ * fp8_quantize_static_scratch — fp8_quantize for callers that cannot allocate device memory.
+ * The pages have no counterpart: this is a convenience of this library. Some callers cannot
+ * hand the library a workspace (code inside a host framework whose allocator owns the whole
+ * device pool, or loops that must not pay for cudaMalloc's implicit synchronisation). This
+ * entry point takes the same arguments as fp8_quantize minus the workspace, and reduces the
+ * tensorwise / delayed amax partials in a fixed 256 KiB array inside the library's device
+ * image (held by every GPU that loads the library until the process exits). It allocates
+ * nothing.
+ *   Limit: tensors needing more than 65536 partials (delayed: more than 65536 128x128 tiles)
+ *   return FP8_ERR_WORKSPACE; MXFP8 and blockwise need no scratch.
+ *   Set-up: the first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call before any stream
+ *   capture.
+ *   Sharing: every call on a device uses the same array, which keeps the last call's
+ *   contents (nothing in it needs to start at zero); calls whose work overlaps on the GPU
+ *   (different streams, or several host threads) race on it and must be serialised by the
+ *   caller.
+ */
+fp8_status fp8_quantize_static_scratch(const fp8_recipe *recipe, const void *x_bf16,
+                                       int64_t rows, int64_t cols, int32_t role,
+                                       int32_t want_row, int32_t want_col, fp8_tensor *out,
+                                       int32_t *dev_status, cudaStream_t stream);
+
 /* Human-readable name of a status. */
 const char *fp8_status_str(fp8_status status);
 

@@ -130,6 +130,26 @@ def quantize(recipe: Recipe, x: torch.Tensor, role="activation", want_row=True, 
     return out
 
 
+def quantize_static_scratch(recipe: Recipe, x: torch.Tensor, role="activation", want_row=True,
+                            want_col=True, out: Optional[QTensor] = None, status=None,
+                            stream=None):
+    """fp8_quantize_static_scratch: like quantize(), but the library supplies the amax scratch
+    from a fixed array in its device image, so the call allocates nothing (for callers that
+    cannot allocate device memory). Calls that overlap on the GPU share that array and race."""
+    lib = L.load()
+    rows, cols = x.shape
+    if out is None:
+        out = empty_qtensor(recipe, rows, cols, role, want_row, want_col, device=x.device)
+    rc = recipe.c()
+    ct = out.c()
+    st = lib.fp8_quantize_static_scratch(ctypes.byref(rc), _ptr(x), rows, cols, ROLES[role],
+                                         int(want_row), int(want_col), ctypes.byref(ct),
+                                         _ptr(status), _stream(stream))
+    L.check(st, "fp8_quantize_static_scratch")
+    out.rows, out.cols, out.kind, out.role = ct.rows, ct.cols, ct.kind, ct.role
+    return out
+
+
 class DelayedState:
     """Device-resident delayed-scaling state: amax history, head, scale, scale_inv."""
 
