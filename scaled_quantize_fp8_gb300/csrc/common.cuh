@@ -92,24 +92,47 @@ __device__ __forceinline__ float scale_from_amax(float amax, int margin, float* 
 }
 
 // MXFP8 E8M0 byte from a block amax given as a 15-bit bf16 magnitude pattern: the smallest e
-// with amax <= 448 * 2^e (448 = 1.75 * 2^8), -127 below 2^-126, clamped to [-127, 127];
+// with amax <= 448 * 2^e (448 = 1.75 * 2^8, so e = E - 8, plus one when the mantissa exceeds
+// 1.75), -127 below 2^-126, clamped to [-127, 127] (a finite bf16 amax never exceeds e = 120);
 // 0xFF (NaN) when the block holds Inf/NaN. Also returns the multiplier 2^-e (1 for NaN).
 __device__ __forceinline__ uint32_t mx_scale_byte(uint32_t amax_bits, float* mult) {
-  const uint32_t bexp = (amax_bits >> 7) & 0xFFu;     // biased exponent of the bf16 value
-  if (bexp == 0xFFu) {
-    *mult = 1.0f;
-    return 0xFFu;
+  const int bexp = int((amax_bits >> 7) & 0xFFu);
+  int e = bexp - 135 + int((amax_bits & 0x7Fu) > 0x60u);
+  e = max(e, -127);
+  const bool nan = bexp == 0xFF;
+  *mult = nan ? 1.0f : __uint_as_float(uint32_t(127 - e) << 23);
+  return nan ? 0xFFu : uint32_t(e + 127);
+}
+
+// Four floats -> four E4M3 codes in one word (byte i holds the code of x_i).
+__device__ __forceinline__ uint32_t cvt_e4m3x4(float x0, float x1, float x2, float x3) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "f"(x0), "f"(x1), "f"(x2), "f"(x3));
+  return r;
+}
+
+// Two words of packed bf16 (4 values) times s -> one word of 4 codes.
+__device__ __forceinline__ uint32_t encode4(uint32_t w0, uint32_t w1, float s) {
+  return cvt_e4m3x4(__fmul_rn(bf16_lo(w0), s), __fmul_rn(bf16_hi(w0), s),
+                    __fmul_rn(bf16_lo(w1), s), __fmul_rn(bf16_hi(w1), s));
+}
+
+// Give the codes of NaN inputs the NaN code with the input's sign (rare path).
+__device__ __forceinline__ uint32_t fix_nan4(uint32_t code, uint32_t w0, uint32_t w1) {
+  const uint32_t in[4] = {w0 & 0xFFFFu, w0 >> 16, w1 & 0xFFFFu, w1 >> 16};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    if ((in[k] & 0x7FFFu) > 0x7F80u) {
+      const uint32_t c = 0x7Fu | ((in[k] >> 8) & 0x80u);
+      code = (code & ~(0xFFu << (8 * k))) | (c << (8 * k));
+    }
   }
-  int e;
-  if (bexp == 0u) {
-    e = -127;
-  } else {
-    const int E = int(bexp) - 127;
-    e = E - 8 + (((amax_bits & 0x7Fu) > 0x60u) ? 1 : 0);   // mantissa > 0.75 <=> m > 1.75
-    e = max(-127, min(127, e));
-  }
-  *mult = exp2i(-e);
-  return uint32_t(e + 127);
+  return code;
 }
 
 // Offset of the E8M0 byte of row r, 32-block kb in the tiled order used by the tensor

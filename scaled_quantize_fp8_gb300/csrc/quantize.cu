@@ -57,9 +57,38 @@ __device__ __forceinline__ float2 e4m3x2_to_f2(uint16_t codes) {
   return __half22float2(h);
 }
 
-__device__ __forceinline__ float gelu_f32(float h) { return h * normcdff(h); }
+// Standard normal CDF Phi(h) = 0.5 erfc(-h / sqrt 2) in fp32, and optionally exp(-h^2 / 2).
+// erfc(z), z >= 0, uses the Chebyshev-fitted form of Numerical Recipes ("erfcc", Press et al.,
+// Numerical Recipes in C, 2nd ed., section 6.2): erfc(z) = t exp(-z^2 + P(t)), t = 1/(1 + z/2),
+// with a stated fractional error below 1.2e-7 for all z >= 0. For h >= 0, Phi = 1 - erfc/2.
+// The fast exponential is exact enough here (bf16 output); below h = -13 its result would be
+// flushed, so that rare tail takes the full-range expf.
+__device__ __forceinline__ float phi_cdf(float h, float* gauss) {
+  const float z = fabsf(h) * 0.70710678118654752f;
+  const float t = __fdividef(1.0f, fmaf(0.5f, z, 1.0f));
+  float P = 0.17087277f;
+  P = fmaf(P, t, -0.82215223f);
+  P = fmaf(P, t, 1.48851587f);
+  P = fmaf(P, t, -1.13520398f);
+  P = fmaf(P, t, 0.27886807f);
+  P = fmaf(P, t, -0.18628806f);
+  P = fmaf(P, t, 0.09678418f);
+  P = fmaf(P, t, 0.37409196f);
+  P = fmaf(P, t, 1.00002368f);
+  P = fmaf(P, t, -1.26551223f);
+  const float z2 = z * z;
+  const float arg = P - z2;
+  const float e = z > 9.0f ? expf(arg) : __expf(arg);
+  const float half_erfc = 0.5f * t * e;
+  if (gauss != nullptr) *gauss = 0.3989422804014327f * (z > 9.0f ? expf(-z2) : __expf(-z2));
+  return h >= 0.0f ? 1.0f - half_erfc : half_erfc;
+}
+// gelu(h) = h Phi(h); gelu'(h) = Phi(h) + h phi(h), phi(h) = exp(-h^2/2) / sqrt(2 pi).
+__device__ __forceinline__ float gelu_f32(float h) { return h * phi_cdf(h, nullptr); }
 __device__ __forceinline__ float gelu_grad_f32(float h) {
-  return normcdff(h) + h * (0.3989422804014327f * expf(-0.5f * h * h));
+  float g;
+  const float c = phi_cdf(h, &g);
+  return fmaf(h, g, c);
 }
 
 // Max of the 15-bit magnitudes of the eight bf16 in a vector.
@@ -81,29 +110,15 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t* red) {
   return m;
 }
 
-// 32 column values (low or high halves of 32 words) times s -> 32 codes in two uint4.
-__device__ __forceinline__ void encode_col32(const uint32_t* w, bool hi, float s, bool nan,
-                                             uint4* out) {
-  uint32_t c[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    uint32_t pk = 0;
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const float x0 = hi ? bf16_hi(w[4 * j + 2 * k]) : bf16_lo(w[4 * j + 2 * k]);
-      const float x1 = hi ? bf16_hi(w[4 * j + 2 * k + 1]) : bf16_lo(w[4 * j + 2 * k + 1]);
-      uint32_t p = cvt_e4m3x2(__fmul_rn(x0, s), __fmul_rn(x1, s));
-      if (nan) p = fix_nan_code(p & 0xFFu, x0) | (fix_nan_code(p >> 8, x1) << 8);
-      pk |= p << (16 * k);
-    }
-    c[j] = pk;
-  }
-  out[0] = make_uint4(c[0], c[1], c[2], c[3]);
-  out[1] = make_uint4(c[4], c[5], c[6], c[7]);
-}
 
-struct QuantSmem {
-  uint32_t tile[2][128][64];        // double-buffered bf16 tile, [row][col/2] pairs (64 KiB)
+// Shared-memory layout of the quantize kernel (offsets from a 1024-byte aligned base):
+//   [0, 5120)          control and staging (QuantCtl)
+//   [5120, 70656)      two tile buffers, each two 16 KiB halves (64 columns x 128 rows of
+//                      bf16) written by TMA with the 128-byte swizzle: logical 16-byte chunk
+//                      c of row r sits at physical chunk c ^ (r % 8)
+//   [70656, 87040)     row-wise codes of the tile (per-tensor and 128x128 recipes only), same
+//                      swizzle, read back transposed for the column-wise copy
+struct QuantCtl {
   uint8_t sc_row[512];              // MXFP8 scale atom of the row copy
   uint8_t sc_col[512];              // ... of the column copy
   float scf_row[128];               // blockwise 1x128 s_inv staging
@@ -113,190 +128,282 @@ struct QuantSmem {
   uint64_t bar[2];                  // TMA completion, one per buffer
   int abort_flag;
 };
+constexpr uint32_t kQCtlBytes = 5120;
+constexpr uint32_t kQTileBytes = 32768;
+constexpr uint32_t kQCodesOff = kQCtlBytes + 2 * kQTileBytes;
+constexpr uint32_t kQCodesBytes = 16384;
+static_assert(sizeof(QuantCtl) <= kQCtlBytes, "control block too large");
 constexpr uint64_t kQuantWaitBudget = 4000000000ull;   // ~2 s at 2 GHz
-constexpr int kQuantCtasPerSm = 3;                     // 3 x ~69 KiB of shared memory
 
-// Quantise one 128 x 128 tile held in shared memory (see the file comment for the scheme).
+template <int MODE>
+__host__ __device__ constexpr bool uses_code_tile() { return MODE == Q_TENSOR || MODE == Q_BW128; }
+template <int MODE>
+__host__ __device__ constexpr uint32_t quant_smem_bytes() {
+  return 1024 + kQCodesOff + (uses_code_tile<MODE>() ? kQCodesBytes : 0);
+}
 template <int MODE, int EPI>
-__device__ __forceinline__ void quantize_one_tile(const QuantParams& p, QuantSmem& S,
-                                                  uint32_t (*tile)[64], int tile_id,
+__host__ __device__ constexpr int quant_ctas_per_sm() {
+  return (uses_code_tile<MODE>() || EPI != EPI_NONE) ? 2 : 3;
+}
+
+// Byte offset of logical 16-byte chunk c (0..7) of row r in a 128-byte-swizzled 128-row block.
+__device__ __forceinline__ uint32_t swz(uint32_t r, uint32_t c) {
+  return r * 128u + (((c ^ r) & 7u) << 4);
+}
+
+// Quantise one 128 x 128 tile held in shared memory.
+//   Row pass: warp w, lane = 16 h + 4 rr + cc: row r = 32 i + 4 w + rr (i = 0..3), columns
+//   64 h + 16 cc .. +15 (two 16-byte chunks). A 1x32 MXFP8 block is two lanes, a 1x128 block
+//   eight. Each lane writes 16 codes (one 16-byte store); a warp covers four 128-byte rows.
+//   Column pass: thread (pp = t % 64, q = t / 64) owns source columns 2pp, 2pp+1 over rows
+//   32q .. 32q+31 and writes 32 consecutive bytes of each transposed row (re-quantised for
+//   MXFP8 and 1x128); per-tensor and 128x128 scales transpose the row codes instead.
+template <int MODE, int EPI>
+__device__ __forceinline__ void quantize_one_tile(const QuantParams& p, QuantCtl& S,
+                                                  uint8_t* tile, uint8_t* codes, int tile_id,
                                                   float s_tensor, bool tensor_nan) {
   const int t = threadIdx.x;
+  const int warp = t >> 5, lane = t & 31;
+  const int h = lane >> 4, rr = (lane >> 2) & 3, cc = lane & 3;
   const int tr = tile_id / p.tiles_c, tc = tile_id % p.tiles_c;
   // 32-bit index arithmetic: the host guarantees R * C < 2^31.
   const uint32_t r0 = uint32_t(tr) * kTile, c0 = uint32_t(tc) * kTile;
-  const int vcol = t & 15, rb = t >> 4;
   const uint32_t R = uint32_t(p.R), C = uint32_t(p.C);
-  const bool col_ok = (c0 + 8 * vcol) < C;
-  const uint32_t rowoff0 = (r0 + rb) * C + c0 + 8 * vcol;   // element offset of v[0]
+  const uint32_t ccol = 64u * h + 16u * cc;            // first column of this lane's 16
+  const bool col_ok = (c0 + ccol) < C;
+  uint8_t* half = tile + h * 16384;
 
-  // ---- this thread's eight 16-byte vectors (out-of-range parts of the tile read as zero)
-  uint4 v[8];
+  // ---- this lane's 4 x 16 bf16 (out-of-range parts of the tile read as zero)
+  uint32_t w[4][8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = *reinterpret_cast<const uint4*>(&tile[rb + 16 * i][4 * vcol]);
-
-  // ---- MLP epilogues: turn the input into the tensor to quantise
-  if constexpr (EPI == EPI_GELU) {
-    // h row copy (MXFP8, blocks of 32 along C) first, then a = bf16(gelu(h)).
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      uint32_t m = vec_amax_bits(v[i]);
-      m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-      m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
-      float mult;
-      const uint32_t b = mx_scale_byte(m, &mult);
-      const uint32_t r = r0 + rb + 16 * i;
-      const uint32_t off = rowoff0 + 16 * i * C;
-      if (r < R && col_ok) {
-        *reinterpret_cast<uint2*>(p.aux_row + off) = encode8(v[i], mult, m > 0x7F80u);
-        if ((vcol & 3) == 0) p.aux_scale[mx_scale_offset(r, (c0 + 8 * vcol) >> 5, C)] = uint8_t(b);
-      }
-      uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        w[k] = bf16_rn_bits(gelu_f32(bf16_lo(w[k]))) | (bf16_rn_bits(gelu_f32(bf16_hi(w[k]))) << 16);
-      }
-      v[i] = make_uint4(w[0], w[1], w[2], w[3]);
-      if (p.y_bf16 != nullptr && r < R && col_ok)
-        *reinterpret_cast<uint4*>(p.y_bf16 + off) = v[i];
-      *reinterpret_cast<uint4*>(&tile[rb + 16 * i][4 * vcol]) = v[i];   // for the column pass
-    }
-  } else if constexpr (EPI == EPI_DGELU) {
-    // dh = bf16(da * gelu'(h)) with h decoded from its MXFP8 row copy.
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t r = r0 + rb + 16 * i;
-      const uint32_t off = rowoff0 + 16 * i * C;
-      if (r < R && col_ok) {
-        const uint2 hc = *reinterpret_cast<const uint2*>(p.aux_row + off);
-        const uint32_t sb = p.aux_scale[mx_scale_offset(r, (c0 + 8 * vcol) >> 5, C)];
-        const float hs = sb == 0xFFu ? __uint_as_float(0x7FC00000u) : exp2i(int(sb) - 127);
-        const uint32_t cw[2] = {hc.x, hc.y};
-        uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float2 hv = e4m3x2_to_f2(uint16_t(cw[k >> 1] >> (16 * (k & 1))));
-          const float h0 = __fmul_rn(hv.x, hs), h1 = __fmul_rn(hv.y, hs);
-          const float d0 = __fmul_rn(bf16_lo(w[k]), gelu_grad_f32(h0));
-          const float d1 = __fmul_rn(bf16_hi(w[k]), gelu_grad_f32(h1));
-          w[k] = bf16_rn_bits(d0) | (bf16_rn_bits(d1) << 16);
-        }
-        v[i] = make_uint4(w[0], w[1], w[2], w[3]);
-        if (p.y_bf16 != nullptr) *reinterpret_cast<uint4*>(p.y_bf16 + off) = v[i];
-      }
-      *reinterpret_cast<uint4*>(&tile[rb + 16 * i][4 * vcol]) = v[i];
-    }
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t r = 32u * i + 4u * warp + rr;
+    const uint4 a = *reinterpret_cast<const uint4*>(half + swz(r, 2 * cc));
+    const uint4 b = *reinterpret_cast<const uint4*>(half + swz(r, 2 * cc + 1));
+    w[i][0] = a.x; w[i][1] = a.y; w[i][2] = a.z; w[i][3] = a.w;
+    w[i][4] = b.x; w[i][5] = b.y; w[i][6] = b.z; w[i][7] = b.w;
   }
 
-  // ---- per-thread magnitude max
-  uint32_t lmax = 0;
+  // ---- MLP epilogues: turn the input into the tensor to quantise (and write it back)
+  if constexpr (EPI != EPI_NONE) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) lmax = max(lmax, vec_amax_bits(v[i]));
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t r = 32u * i + 4u * warp + rr;
+      const bool ok = (r0 + r < R) && col_ok;
+      const uint32_t off = (r0 + r) * C + c0 + ccol;
+      if constexpr (EPI == EPI_GELU) {
+        // h's own MXFP8 row copy first (the FP8 input store), then a = bf16(gelu(h))
+        uint32_t m = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m = absmax_bf16x2(m, w[i][k]);
+        m = fold_bf16x2(m);
+        m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        float mult;
+        const uint32_t sb = mx_scale_byte(m, &mult);
+        uint4 hc = make_uint4(encode4(w[i][0], w[i][1], mult), encode4(w[i][2], w[i][3], mult),
+                              encode4(w[i][4], w[i][5], mult), encode4(w[i][6], w[i][7], mult));
+        if (m > 0x7F80u) {
+          hc.x = fix_nan4(hc.x, w[i][0], w[i][1]); hc.y = fix_nan4(hc.y, w[i][2], w[i][3]);
+          hc.z = fix_nan4(hc.z, w[i][4], w[i][5]); hc.w = fix_nan4(hc.w, w[i][6], w[i][7]);
+        }
+        if (ok) {
+          *reinterpret_cast<uint4*>(p.aux_row + off) = hc;
+          if ((cc & 1) == 0) p.aux_scale[mx_scale_offset(r0 + r, (c0 + ccol) >> 5, C)] = uint8_t(sb);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          w[i][k] = bf16_rn_bits(gelu_f32(bf16_lo(w[i][k]))) |
+                    (bf16_rn_bits(gelu_f32(bf16_hi(w[i][k]))) << 16);
+      } else {
+        // dh = bf16(da * gelu'(h)), h decoded from its MXFP8 row copy
+        if (ok) {
+          const uint4 hc = *reinterpret_cast<const uint4*>(p.aux_row + off);
+          const uint32_t sb = p.aux_scale[mx_scale_offset(r0 + r, (c0 + ccol) >> 5, C)];
+          const float hs = sb == 0xFFu ? __uint_as_float(0x7FC00000u) : exp2i(int(sb) - 127);
+          const uint32_t cw[4] = {hc.x, hc.y, hc.z, hc.w};
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const float2 hv = e4m3x2_to_f2(uint16_t(cw[k >> 1] >> (16 * (k & 1))));
+            const float d0 = __fmul_rn(bf16_lo(w[i][k]), gelu_grad_f32(__fmul_rn(hv.x, hs)));
+            const float d1 = __fmul_rn(bf16_hi(w[i][k]), gelu_grad_f32(__fmul_rn(hv.y, hs)));
+            w[i][k] = bf16_rn_bits(d0) | (bf16_rn_bits(d1) << 16);
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) w[i][k] = 0u;
+        }
+      }
+      if (p.y_bf16 != nullptr && ok) {
+        *reinterpret_cast<uint4*>(p.y_bf16 + off) = make_uint4(w[i][0], w[i][1], w[i][2], w[i][3]);
+        *reinterpret_cast<uint4*>(p.y_bf16 + off + 8) = make_uint4(w[i][4], w[i][5], w[i][6], w[i][7]);
+      }
+      if (p.col != nullptr) {
+        *reinterpret_cast<uint4*>(half + swz(r, 2 * cc)) = make_uint4(w[i][0], w[i][1], w[i][2], w[i][3]);
+        *reinterpret_cast<uint4*>(half + swz(r, 2 * cc + 1)) = make_uint4(w[i][4], w[i][5], w[i][6], w[i][7]);
+      }
+    }
+  }
 
   // ---- the tile-wide scale (per-tensor and 128x128 recipes)
   float s_tile = s_tensor, sinv_tile = 1.0f;
   bool tile_nan = tensor_nan;
-  if constexpr (MODE == Q_TENSOR) {
-    if (p.part_out != nullptr) {                              // delayed: record this tile's amax
-      const uint32_t tm = block_max_u32(lmax, S.red);
-      tile_nan = tm > 0x7F80u;
-      if (t == 0) p.part_out[tile_id] = tm;
-    }
-  } else if constexpr (MODE == Q_BW128) {
-    const uint32_t tm = block_max_u32(lmax, S.red);
+  const bool need_tile_amax =
+      MODE == Q_BW128 || (MODE == Q_TENSOR && p.part_out != nullptr);
+  if (need_tile_amax) {
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int k = 0; k < 8; ++k) m = absmax_bf16x2(m, w[i][k]);
+    const uint32_t tm = block_max_u32(fold_bf16x2(m), S.red);
     tile_nan = tm > 0x7F80u;
-    s_tile = scale_from_amax(amax_from_bits(tm), p.margin, &sinv_tile);
-    if (t == 0) {
-      const int tiles_r = int((R + 127) >> 7);
-      if (p.row_scale) reinterpret_cast<float*>(p.row_scale)[tr * p.tiles_c + tc] = sinv_tile;
-      if (p.col_scale) reinterpret_cast<float*>(p.col_scale)[tc * tiles_r + tr] = sinv_tile;
+    if constexpr (MODE == Q_TENSOR) {
+      if (t == 0) p.part_out[tile_id] = tm;               // delayed: record this tile's amax
+    } else {
+      s_tile = scale_from_amax(amax_from_bits(tm), p.margin, &sinv_tile);
+      if (t == 0) {
+        const int tiles_r = int((R + 127) >> 7);
+        if (p.row_scale) reinterpret_cast<float*>(p.row_scale)[tr * p.tiles_c + tc] = sinv_tile;
+        if (p.col_scale) reinterpret_cast<float*>(p.col_scale)[tc * tiles_r + tr] = sinv_tile;
+      }
     }
   }
 
-  // ---- row-wise copy from registers
-  if (p.row != nullptr) {
+  // ---- row-wise copy (and the code tile for the transposed copy)
+  if (p.row != nullptr || uses_code_tile<MODE>()) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t r = r0 + rb + 16 * i;
-      const int lr = rb + 16 * i;
-      uint2 codes;
-      if constexpr (MODE == Q_TENSOR || MODE == Q_BW128) {
-        codes = encode8(v[i], s_tile, tile_nan);
-      } else if constexpr (MODE == Q_MX) {
-        uint32_t m = vec_amax_bits(v[i]);
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t r = 32u * i + 4u * warp + rr;
+      float s = s_tile;
+      bool nan = tile_nan;
+      if constexpr (MODE == Q_MX || MODE == Q_BW1x128) {
+        uint32_t m = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m = absmax_bf16x2(m, w[i][k]);
+        m = fold_bf16x2(m);
         m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-        m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
-        float mult;
-        const uint32_t b = mx_scale_byte(m, &mult);
-        codes = encode8(v[i], mult, m > 0x7F80u);
-        if ((vcol & 3) == 0) S.sc_row[(lr & 31) * 16 + (lr >> 5) * 4 + (vcol >> 2)] = uint8_t(b);
-      } else {  // Q_BW1x128: the block is the whole 128-wide tile row (16 lanes)
-        uint32_t m = vec_amax_bits(v[i]);
-#pragma unroll
-        for (int o = 1; o < 16; o <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-        float sinv;
-        const float s = scale_from_amax(amax_from_bits(m), p.margin, &sinv);
-        codes = encode8(v[i], s, m > 0x7F80u);
-        if (vcol == 0) S.scf_row[lr] = sinv;
+        if constexpr (MODE == Q_MX) {
+          const uint32_t sb = mx_scale_byte(m, &s);
+          if ((cc & 1) == 0) S.sc_row[(r & 31) * 16 + (r >> 5) * 4 + 2 * h + (cc >> 1)] = uint8_t(sb);
+        } else {
+          m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+          m = max(m, __shfl_xor_sync(0xffffffffu, m, 16));
+          float sinv;
+          s = scale_from_amax(amax_from_bits(m), p.margin, &sinv);
+          if (h == 0 && cc == 0) S.scf_row[r] = sinv;
+        }
+        nan = m > 0x7F80u;
       }
-      if (r < R && col_ok) *reinterpret_cast<uint2*>(p.row + rowoff0 + 16 * i * C) = codes;
+      uint4 q4 = make_uint4(encode4(w[i][0], w[i][1], s), encode4(w[i][2], w[i][3], s),
+                            encode4(w[i][4], w[i][5], s), encode4(w[i][6], w[i][7], s));
+      if (nan) {
+        q4.x = fix_nan4(q4.x, w[i][0], w[i][1]); q4.y = fix_nan4(q4.y, w[i][2], w[i][3]);
+        q4.z = fix_nan4(q4.z, w[i][4], w[i][5]); q4.w = fix_nan4(q4.w, w[i][6], w[i][7]);
+      }
+      if (p.row != nullptr && (r0 + r < R) && col_ok)
+        *reinterpret_cast<uint4*>(p.row + (r0 + r) * C + c0 + ccol) = q4;
+      if constexpr (uses_code_tile<MODE>())
+        *reinterpret_cast<uint4*>(codes + swz(r, 4 * h + cc)) = q4;
     }
   }
 
   if (p.col != nullptr) {
-    if constexpr (EPI != EPI_NONE) __syncthreads();          // transformed tile written back
-
-    // ---- column-wise copy: thread owns source columns 2pp, 2pp+1 and rows 32q .. 32q+31
-    const int pp = t & 63, q = t >> 6;
-    uint32_t w[32];
+    __syncthreads();                                   // write-backs / code tile visible
+    if constexpr (uses_code_tile<MODE>()) {
+      // ---- column-wise copy = byte transpose of the row codes. Thread (c4, g): source
+      // columns 4 c4 .. 4 c4 + 3, rows 16 g .. 16 g + 15 (four 4x4 byte transposes).
+      const int c4 = t & 31, g = t >> 5;
+      uint32_t outw[4][4];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) w[j] = tile[32 * q + j][pp];
-    uint32_t mw = 0;
+      for (int blk = 0; blk < 4; ++blk) {
+        uint32_t x[4];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) mw = absmax_bf16x2(mw, w[j]);
-    const uint32_t ma = mw & 0x7FFFu, mb = (mw >> 16) & 0x7FFFu;   // columns 2pp and 2pp+1
-
-    float sa = s_tile, sb = s_tile;
-    bool na = tile_nan, nb = tile_nan;
-    if constexpr (MODE == Q_MX) {
-      float fa, fb;
-      const uint32_t ba = mx_scale_byte(ma, &fa), bb = mx_scale_byte(mb, &fb);
-      sa = fa;
-      sb = fb;
-      na = ma > 0x7F80u;
-      nb = mb > 0x7F80u;
-      const int ca = 2 * pp, cb = 2 * pp + 1;
-      S.sc_col[(ca & 31) * 16 + (ca >> 5) * 4 + q] = uint8_t(ba);
-      S.sc_col[(cb & 31) * 16 + (cb >> 5) * 4 + q] = uint8_t(bb);
-    } else if constexpr (MODE == Q_BW1x128) {
-      S.red_col[q][2 * pp] = ma;
-      S.red_col[q][2 * pp + 1] = mb;
-      __syncthreads();
-      const uint32_t fa = max(max(S.red_col[0][2 * pp], S.red_col[1][2 * pp]),
-                              max(S.red_col[2][2 * pp], S.red_col[3][2 * pp]));
-      const uint32_t fb = max(max(S.red_col[0][2 * pp + 1], S.red_col[1][2 * pp + 1]),
-                              max(S.red_col[2][2 * pp + 1], S.red_col[3][2 * pp + 1]));
-      float ia, ib;
-      sa = scale_from_amax(amax_from_bits(fa), p.margin, &ia);
-      sb = scale_from_amax(amax_from_bits(fb), p.margin, &ib);
-      na = fa > 0x7F80u;
-      nb = fb > 0x7F80u;
-      if (q == 0) {
-        S.scf_col[2 * pp] = ia;
-        S.scf_col[2 * pp + 1] = ib;
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t r = 16u * g + 4u * blk + j;
+          x[j] = *reinterpret_cast<const uint32_t*>(codes + swz(r, c4 >> 2) + 4 * (c4 & 3));
+        }
+        const uint32_t t0 = __byte_perm(x[0], x[1], 0x5140), t1 = __byte_perm(x[0], x[1], 0x7362);
+        const uint32_t t2 = __byte_perm(x[2], x[3], 0x5140), t3 = __byte_perm(x[2], x[3], 0x7362);
+        outw[0][blk] = __byte_perm(t0, t2, 0x5410);
+        outw[1][blk] = __byte_perm(t0, t2, 0x7632);
+        outw[2][blk] = __byte_perm(t1, t3, 0x5410);
+        outw[3][blk] = __byte_perm(t1, t3, 0x7632);
       }
-    }
-
-    uint4 out[2];
-    const uint32_t rr = r0 + 32 * q;
+      const uint32_t rr0 = r0 + 16u * g;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint32_t c = c0 + 2 * pp + h;
-      encode_col32(w, h == 1, h == 0 ? sa : sb, h == 0 ? na : nb, out);
-      if (c < C) {
-        uint8_t* dst = p.col + c * R + rr;
-        if (rr < R) *reinterpret_cast<uint4*>(dst) = out[0];
-        if (rr + 16 < R) *reinterpret_cast<uint4*>(dst + 16) = out[1];
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t c = c0 + 4u * c4 + k;
+        if (c < C && rr0 < R)
+          *reinterpret_cast<uint4*>(p.col + c * R + rr0) =
+              make_uint4(outw[k][0], outw[k][1], outw[k][2], outw[k][3]);
+      }
+    } else {
+      // ---- column-wise copy re-quantised along the rows
+      const int pp = t & 63, q = t >> 6;
+      const uint8_t* hb = tile + (pp >> 5) * 16384;
+      const uint32_t chunk = (pp & 31) >> 2, wofs = 4u * (pp & 3);
+      uint32_t x[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const uint32_t r = 32u * q + j;
+        x[j] = *reinterpret_cast<const uint32_t*>(hb + swz(r, chunk) + wofs);
+      }
+      uint32_t mw = 0;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) mw = absmax_bf16x2(mw, x[j]);
+      const uint32_t ma = mw & 0x7FFFu, mb = (mw >> 16) & 0x7FFFu;   // columns 2pp and 2pp+1
+      float sa, sb;
+      if constexpr (MODE == Q_MX) {
+        const uint32_t ba = mx_scale_byte(ma, &sa), bb = mx_scale_byte(mb, &sb);
+        const int ca = 2 * pp, cb = 2 * pp + 1;
+        S.sc_col[(ca & 31) * 16 + (ca >> 5) * 4 + q] = uint8_t(ba);
+        S.sc_col[(cb & 31) * 16 + (cb >> 5) * 4 + q] = uint8_t(bb);
+      } else {
+        S.red_col[q][2 * pp] = ma;
+        S.red_col[q][2 * pp + 1] = mb;
+        __syncthreads();
+        const uint32_t fa = max(max(S.red_col[0][2 * pp], S.red_col[1][2 * pp]),
+                                max(S.red_col[2][2 * pp], S.red_col[3][2 * pp]));
+        const uint32_t fb = max(max(S.red_col[0][2 * pp + 1], S.red_col[1][2 * pp + 1]),
+                                max(S.red_col[2][2 * pp + 1], S.red_col[3][2 * pp + 1]));
+        float ia, ib;
+        sa = scale_from_amax(amax_from_bits(fa), p.margin, &ia);
+        sb = scale_from_amax(amax_from_bits(fb), p.margin, &ib);
+        if (q == 0) {
+          S.scf_col[2 * pp] = ia;
+          S.scf_col[2 * pp + 1] = ib;
+        }
+      }
+      // codes of column 2pp (low halves) and 2pp+1 (high halves), 32 rows each
+      uint32_t ca[8], cb[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t x0 = x[4 * j], x1 = x[4 * j + 1], x2 = x[4 * j + 2], x3 = x[4 * j + 3];
+        ca[j] = cvt_e4m3x4(__fmul_rn(bf16_lo(x0), sa), __fmul_rn(bf16_lo(x1), sa),
+                           __fmul_rn(bf16_lo(x2), sa), __fmul_rn(bf16_lo(x3), sa));
+        cb[j] = cvt_e4m3x4(__fmul_rn(bf16_hi(x0), sb), __fmul_rn(bf16_hi(x1), sb),
+                           __fmul_rn(bf16_hi(x2), sb), __fmul_rn(bf16_hi(x3), sb));
+      }
+      if ((mw & 0x7FFFu) > 0x7F80u || ((mw >> 16) & 0x7FFFu) > 0x7F80u) {   // NaN present
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t lo01 = (x[4 * j] & 0xFFFFu) | (x[4 * j + 1] << 16);
+          const uint32_t lo23 = (x[4 * j + 2] & 0xFFFFu) | (x[4 * j + 3] << 16);
+          const uint32_t hi01 = (x[4 * j] >> 16) | (x[4 * j + 1] & 0xFFFF0000u);
+          const uint32_t hi23 = (x[4 * j + 2] >> 16) | (x[4 * j + 3] & 0xFFFF0000u);
+          ca[j] = fix_nan4(ca[j], lo01, lo23);
+          cb[j] = fix_nan4(cb[j], hi01, hi23);
+        }
+      }
+      const uint32_t rr0 = r0 + 32u * q;
+      const uint32_t cA = c0 + 2u * pp;
+      if (cA < C) {
+        uint8_t* dst = p.col + cA * R + rr0;
+        if (rr0 < R) *reinterpret_cast<uint4*>(dst) = make_uint4(ca[0], ca[1], ca[2], ca[3]);
+        if (rr0 + 16 < R) *reinterpret_cast<uint4*>(dst + 16) = make_uint4(ca[4], ca[5], ca[6], ca[7]);
+        dst += R;
+        if (rr0 < R) *reinterpret_cast<uint4*>(dst) = make_uint4(cb[0], cb[1], cb[2], cb[3]);
+        if (rr0 + 16 < R) *reinterpret_cast<uint4*>(dst + 16) = make_uint4(cb[4], cb[5], cb[6], cb[7]);
       }
     }
   }
@@ -325,7 +432,7 @@ __device__ __forceinline__ void quantize_one_tile(const QuantParams& p, QuantSme
 }
 
 // Bounded wait on a TMA completion barrier (all threads); false once the budget is spent.
-__device__ __forceinline__ bool quant_wait(QuantSmem& S, int b, uint32_t parity, int32_t* st) {
+__device__ __forceinline__ bool quant_wait(QuantCtl& S, int b, uint32_t parity, int32_t* st) {
   if (ptx::mbar_try_wait(&S.bar[b], parity)) return true;
   const uint64_t t0 = ptx::clock64_();
   while (!ptx::mbar_try_wait(&S.bar[b], parity)) {
@@ -340,14 +447,17 @@ __device__ __forceinline__ bool quant_wait(QuantSmem& S, int b, uint32_t parity,
 }
 
 // Persistent quantize kernel: each CTA walks tiles blockIdx.x, +gridDim.x, ...; thread 0
-// issues the TMA load of the next tile into the other buffer before the current one is
+// issues the TMA loads of the next tile into the other buffer before the current one is
 // processed, so HBM reads overlap the conversion and the stores.
 template <int MODE, int EPI>
-__global__ void __launch_bounds__(256, kQuantCtasPerSm) quantize_tile_kernel(const __grid_constant__ CUtensorMap tmX,
-                                                            const QuantParams p) {
+__global__ void __launch_bounds__(256, quant_ctas_per_sm<MODE, EPI>())
+    quantize_tile_kernel(const __grid_constant__ CUtensorMap tmX, const QuantParams p) {
   extern __shared__ uint8_t qsm_raw[];
-  QuantSmem& S = *reinterpret_cast<QuantSmem*>(
-      (reinterpret_cast<uintptr_t>(qsm_raw) + 127) & ~uintptr_t(127));
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(qsm_raw) + 1023) & ~uintptr_t(1023));
+  QuantCtl& S = *reinterpret_cast<QuantCtl*>(base);
+  uint8_t* tiles = base + kQCtlBytes;
+  uint8_t* codes = base + kQCodesOff;
   const int t = threadIdx.x;
   const int tiles_r = int((p.R + 127) >> 7);
   const int n_tiles = tiles_r * p.tiles_c;
@@ -383,8 +493,10 @@ __global__ void __launch_bounds__(256, kQuantCtasPerSm) quantize_tile_kernel(con
 
   auto issue = [&](int tile_id, int b) {
     const int tr = tile_id / p.tiles_c, tc = tile_id % p.tiles_c;
-    ptx::mbar_arrive_expect_tx(&S.bar[b], 128 * 128 * 2);
-    ptx::tma_load_2d(&S.tile[b][0][0], &tmX, tc * kTile, tr * kTile, &S.bar[b]);
+    uint8_t* dst = tiles + b * kQTileBytes;
+    ptx::mbar_arrive_expect_tx(&S.bar[b], kQTileBytes);
+    ptx::tma_load_2d(dst, &tmX, tc * kTile, tr * kTile, &S.bar[b]);
+    ptx::tma_load_2d(dst + 16384, &tmX, tc * kTile + 64, tr * kTile, &S.bar[b]);
   };
 
   int tile = blockIdx.x;
@@ -394,11 +506,12 @@ __global__ void __launch_bounds__(256, kQuantCtasPerSm) quantize_tile_kernel(con
     const int next = tile + int(gridDim.x);
     if (t == 0 && next < n_tiles) issue(next, b ^ 1);
     if (!quant_wait(S, b, uint32_t(i >> 1) & 1u, p.status)) break;
-    quantize_one_tile<MODE, EPI>(p, S, S.tile[b], tile, s_tensor, tensor_nan);
+    quantize_one_tile<MODE, EPI>(p, S, tiles + b * kQTileBytes, codes, tile, s_tensor,
+                                 tensor_nan);
     __syncthreads();                                 // buffer b is refilled next iteration
   }
   if (*reinterpret_cast<volatile int*>(&S.abort_flag)) {
-    const uint64_t t0 = ptx::clock64_();             // let the outstanding copy land
+    const uint64_t t0 = ptx::clock64_();             // let the outstanding copies land
     while (ptx::clock64_() - t0 < 20000000ull) {
     }
   }
@@ -514,8 +627,8 @@ static cudaError_t launch_tiles(const QuantParams& p, cudaStream_t st) {
   const int tiles_r = int((p.R + 127) / 128);
   const int n = tiles_r * p.tiles_c;
   CUtensorMap map;
-  if (!make_tmap_2d(&map, p.x, 2, p.C, p.R, kTile, kTile, false)) return cudaErrorInvalidValue;
-  const int smem = int(sizeof(QuantSmem)) + 128;
+  if (!make_tmap_2d(&map, p.x, 2, p.C, p.R, 64, kTile, true)) return cudaErrorInvalidValue;
+  constexpr int smem = int(quant_smem_bytes<MODE>());
   static bool attr = false;
   if (!attr) {
     const cudaError_t e = cudaFuncSetAttribute(quantize_tile_kernel<MODE, EPI>,
@@ -523,7 +636,7 @@ static cudaError_t launch_tiles(const QuantParams& p, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  const int grid = std::max(1, std::min(n, num_sms() * kQuantCtasPerSm));
+  const int grid = std::max(1, std::min(n, num_sms() * quant_ctas_per_sm<MODE, EPI>()));
   quantize_tile_kernel<MODE, EPI><<<grid, 256, smem, st>>>(map, p);
   return cudaGetLastError();
 }
