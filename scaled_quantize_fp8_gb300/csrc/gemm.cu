@@ -32,24 +32,31 @@
 
 namespace fp8lin {
 
-constexpr int kBM = 128;
-constexpr int kBN = 256;
+constexpr int kBM = 128;                      // accumulator rows per CTA (TMEM lanes)
+constexpr int kBN = 256;                      // accumulator columns per tile
 constexpr int kBKBytes = 128;                 // one 128-byte swizzle row of K per stage
-constexpr int kStages = 4;
 constexpr int kEpiWarps = 8;
 constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kTileABytes = kBM * kBKBytes;      // 16 KiB
-constexpr uint32_t kTileBBytes = kBN * kBKBytes;      // 32 KiB
 constexpr uint32_t kSfStageBytes = 2048;              // SFA 512 B at 0, SFB 2 x 512 B at 512
-constexpr uint32_t kStageBytes = kTileABytes + kTileBBytes + kSfStageBytes;
-constexpr uint32_t kGemmSmemBytes = 1024 + kStages * kStageBytes + 256;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitBudgetCycles = 4000000000ull;   // ~2 s at 2 GHz
 
+// Per-configuration geometry. A single CTA (CTA2 = 0) owns a 128 x 256 tile and loads the
+// whole 256-row B tile; a CTA pair (CTA2 = 1) owns a 256 x 256 tile, each CTA loading its own
+// 128 rows of A and 128 of the 256 rows of B, so a stage is 32 KiB and six of them fit.
+template <int CTA2>
+struct Geo {
+  static constexpr int kStages = CTA2 ? 6 : 4;
+  static constexpr uint32_t kTileBBytes = (CTA2 ? kBN / 2 : kBN) * kBKBytes;
+  static constexpr uint32_t kStageBytes = kTileABytes + kTileBBytes + kSfStageBytes;
+  static constexpr uint32_t kSmemBytes = 1024 + kStages * kStageBytes + 512;
+  static constexpr int kTileM = CTA2 ? 2 * kBM : kBM;     // output rows per tile
+};
 
 struct SharedCtl {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[6];
+  uint64_t empty[6];
   uint64_t accf[2];
   uint64_t acce[2];
   uint32_t tmem_base;
@@ -71,11 +78,12 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, SharedC
   }
 }
 
-template <int MODE>
+template <int MODE, int CTA2>
 __device__ __forceinline__ uint32_t instr_desc() {
   // [4,6) D format (1 = f32) | [7,10) A fmt | [10,13) B fmt | [15] A major | [16] B major
-  // | [17,23) N >> 3 | [24,29) M >> 4. E4M3 = 0, bf16 = 1.
-  uint32_t d = (uint32_t(kBN >> 3) << 17) | (uint32_t(kBM >> 4) << 24);
+  // | [17,23) N >> 3 | [24,29) M >> 4. E4M3 = 0, bf16 = 1. The pair's MMA has M = 256.
+  const uint32_t M = CTA2 ? 2 * kBM : kBM;
+  uint32_t d = (uint32_t(kBN >> 3) << 17) | ((M >> 4) << 24);
   if constexpr (MODE == G_MX) {
     d |= (1u << 23);                          // scale factors are E8M0
   } else if constexpr (MODE == G_BF16) {
@@ -128,45 +136,57 @@ __device__ __forceinline__ void tmem_load128(uint32_t taddr, float* out) {
   }
 }
 
-template <int MODE, int B128 = 1>
+template <int MODE, int B128, int CTA2>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+  using G = Geo<CTA2>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + kStages * kTileABytes;
-  uint8_t* sSF = sB + kStages * kTileBBytes;
-  SharedCtl* ctl = reinterpret_cast<SharedCtl*>(sSF + kStages * kSfStageBytes);
+  uint8_t* sB = smem + G::kStages * kTileABytes;
+  uint8_t* sSF = sB + G::kStages * G::kTileBBytes;
+  SharedCtl* ctl = reinterpret_cast<SharedCtl*>(sSF + G::kStages * kSfStageBytes);
 
   constexpr int kNumAcc = (MODE == G_MX) ? 1 : 2;
   constexpr int kElem = (MODE == G_BF16) ? 2 : 1;
   constexpr int kBKElems = kBKBytes / kElem;
+  constexpr uint32_t kBRows = CTA2 ? kBN / 2 : kBN;     // B rows this CTA loads per stage
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tiles_m = (p.M + kBM - 1) / kBM;
+  const uint32_t rank = CTA2 ? ptx::cluster_rank() : 0u;
+  const bool leader = rank == 0;
+  const int unit = CTA2 ? int(blockIdx.x >> 1) : int(blockIdx.x);       // CTA or CTA pair
+  const int n_units = CTA2 ? int(gridDim.x >> 1) : int(gridDim.x);
+  const int tiles_m = (p.M + G::kTileM - 1) / G::kTileM;
   const int tiles_n = (p.N + kBN - 1) / kBN;
   const int n_tiles = tiles_m * tiles_n;
   const int nk = (p.K + kBKElems - 1) / kBKElems;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < G::kStages; ++s) {
       ptx::mbar_init(&ctl->full[s], 1);
       ptx::mbar_init(&ctl->empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&ctl->accf[b], 1);
-      ptx::mbar_init(&ctl->acce[b], kEpiWarps);
+      ptx::mbar_init(&ctl->acce[b], CTA2 ? 2 * kEpiWarps : kEpiWarps);
     }
     ctl->abort_flag = 0;
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
-    ptx::tmem_alloc(&ctl->tmem_base, kTmemCols);
-    ptx::tmem_relinquish();
+    if constexpr (CTA2) {
+      ptx::tmem_alloc_pair(&ctl->tmem_base, kTmemCols);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(&ctl->tmem_base, kTmemCols);
+      ptx::tmem_relinquish();
+    }
   }
   __syncthreads();
+  if constexpr (CTA2) ptx::cluster_sync();           // peer barriers initialised
   ptx::tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
 
@@ -178,27 +198,39 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int s = 0;
       uint32_t ph = 0;
       const int kblocks128 = p.K / 128;       // MX scale atoms per operand row tile
-      for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
-        const int m0 = (tile % tiles_m) * kBM, n0 = (tile / tiles_m) * kBN;
+      for (int tile = unit; tile < n_tiles; tile += n_units) {
+        const int m0 = (tile % tiles_m) * G::kTileM + int(rank) * kBM;
+        const int n0 = (tile / tiles_m) * kBN + int(rank) * int(kBRows);
         for (int kb = 0; kb < nk; ++kb) {
           if (!wait_bar(&ctl->empty[s], ph ^ 1u, ctl, p.status)) goto producer_done;
-          uint32_t bytes = kTileABytes + kTileBBytes;
-          const bool sfb_hi = (n0 + 128) < p.N;
-          if constexpr (MODE == G_MX) bytes += 512u + (sfb_hi ? 1024u : 512u);
-          ptx::mbar_arrive_expect_tx(&ctl->full[s], bytes);
-          ptx::tma_load_2d(sA + s * kTileABytes, &tmA, kb * kBKElems, m0, &ctl->full[s]);
-          ptx::tma_load_2d(sB + s * kTileBBytes, &tmB, kb * kBKElems, n0, &ctl->full[s]);
-          if constexpr (MODE == G_MX) {
-            uint8_t* sf = sSF + s * kSfStageBytes;
-            ptx::bulk_load(sf, p.sfa + (int64_t(m0 >> 7) * kblocks128 + kb) * 512, 512,
-                           &ctl->full[s]);
-            ptx::bulk_load(sf + 512, p.sfb + (int64_t(n0 >> 7) * kblocks128 + kb) * 512, 512,
-                           &ctl->full[s]);
-            if (sfb_hi)
-              ptx::bulk_load(sf + 1024, p.sfb + (int64_t((n0 >> 7) + 1) * kblocks128 + kb) * 512,
-                             512, &ctl->full[s]);
+          uint8_t* a_dst = sA + s * kTileABytes;
+          uint8_t* b_dst = sB + s * G::kTileBBytes;
+          if constexpr (CTA2) {
+            // Both CTAs' loads complete on the leader's barrier, which expects all of them.
+            const uint32_t bar = ptx::map_to_rank(&ctl->full[s], 0);
+            if (leader) ptx::mbar_arrive_expect_tx(&ctl->full[s], 2 * (kTileABytes + G::kTileBBytes));
+            ptx::tma_load_2d_pair(a_dst, &tmA, kb * kBKElems, m0, bar);
+            ptx::tma_load_2d_pair(b_dst, &tmB, kb * kBKElems, n0, bar);
+          } else {
+            uint32_t bytes = kTileABytes + G::kTileBBytes;
+            const bool sfb_hi = (n0 + 128) < p.N;
+            if constexpr (MODE == G_MX) bytes += 512u + (sfb_hi ? 1024u : 512u);
+            ptx::mbar_arrive_expect_tx(&ctl->full[s], bytes);
+            ptx::tma_load_2d(a_dst, &tmA, kb * kBKElems, m0, &ctl->full[s]);
+            ptx::tma_load_2d(b_dst, &tmB, kb * kBKElems, n0, &ctl->full[s]);
+            if constexpr (MODE == G_MX) {
+              uint8_t* sf = sSF + s * kSfStageBytes;
+              ptx::bulk_load(sf, p.sfa + (int64_t(m0 >> 7) * kblocks128 + kb) * 512, 512,
+                             &ctl->full[s]);
+              ptx::bulk_load(sf + 512, p.sfb + (int64_t(n0 >> 7) * kblocks128 + kb) * 512, 512,
+                             &ctl->full[s]);
+              if (sfb_hi)
+                ptx::bulk_load(sf + 1024,
+                               p.sfb + (int64_t((n0 >> 7) + 1) * kblocks128 + kb) * 512, 512,
+                               &ctl->full[s]);
+            }
           }
-          if (++s == kStages) {
+          if (++s == G::kStages) {
             s = 0;
             ph ^= 1u;
           }
@@ -207,14 +239,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     producer_done:;
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = instr_desc<MODE>();
+    // ------------------------------------------------------------ MMA issuer (leader)
+    if (lane == 0 && leader) {
+      const uint32_t idesc = instr_desc<MODE, CTA2>();
       const uint32_t sfa_t = tmem + 256, sfb_t = tmem + 260;   // MX scale-factor columns
       int s = 0;
       uint32_t ph = 0;
       uint32_t u = 0;
-      for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+      auto commit = [&](uint64_t* bar) {
+        if constexpr (CTA2) ptx::mma_commit_pair(bar, 0x3);
+        else ptx::mma_commit(bar);
+      };
+      for (int tile = unit; tile < n_tiles; tile += n_units) {
         uint32_t d_t = tmem;
         if constexpr (MODE != G_BLOCK) {
           const uint32_t b = u % kNumAcc;
@@ -233,8 +269,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if (!wait_bar(&ctl->full[s], ph, ctl, p.status)) goto mma_done;
           ptx::tc_fence_after();
           const uint32_t a_addr = ptx::smem_u32(sA + s * kTileABytes);
-          const uint32_t b_addr = ptx::smem_u32(sB + s * kTileBBytes);
-          if constexpr (MODE == G_MX) {
+          const uint32_t b_addr = ptx::smem_u32(sB + s * G::kTileBBytes);
+          if constexpr (MODE == G_MX && !CTA2) {
             const uint32_t sf = ptx::smem_u32(sSF + s * kSfStageBytes);
             ptx::tmem_cp_32x128b_warpx4(sfa_t, ptx::smem_desc(sf, 0, 128, ptx::kSwizzleNone));
             ptx::tmem_cp_32x128b_warpx4(sfb_t,
@@ -246,29 +282,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           for (int k = 0; k < kBKBytes / 32; ++k) {
             const uint64_t ad = ptx::smem_desc(a_addr + 32 * k, 16, 1024, ptx::kSwizzle128B);
             const uint64_t bd = ptx::smem_desc(b_addr + 32 * k, 16, 1024, ptx::kSwizzle128B);
-            if constexpr (MODE == G_MX) {
+            const uint32_t acc_on = MODE == G_BLOCK ? uint32_t(k != 0) : uint32_t((kb | k) != 0);
+            if constexpr (CTA2) {
+              if constexpr (MODE == G_BF16) ptx::mma_f16_pair(d_t, ad, bd, idesc, acc_on);
+              else ptx::mma_f8f6f4_pair(d_t, ad, bd, idesc, acc_on);
+            } else if constexpr (MODE == G_MX) {
               const uint32_t id = idesc | (uint32_t(k) << 29) | (uint32_t(k) << 4);
-              ptx::mma_mxf8f6f4(d_t, ad, bd, id, sfa_t, sfb_t, (kb | k) != 0);
+              ptx::mma_mxf8f6f4(d_t, ad, bd, id, sfa_t, sfb_t, acc_on);
             } else if constexpr (MODE == G_BF16) {
-              ptx::mma_f16(d_t, ad, bd, idesc, (kb | k) != 0);
-            } else if constexpr (MODE == G_BLOCK) {
-              ptx::mma_f8f6f4(d_t, ad, bd, idesc, k != 0);
+              ptx::mma_f16(d_t, ad, bd, idesc, acc_on);
             } else {
-              ptx::mma_f8f6f4(d_t, ad, bd, idesc, (kb | k) != 0);
+              ptx::mma_f8f6f4(d_t, ad, bd, idesc, acc_on);
             }
           }
-          ptx::mma_commit(&ctl->empty[s]);
+          commit(&ctl->empty[s]);
           if constexpr (MODE == G_BLOCK) {
-            ptx::mma_commit(&ctl->accf[b]);
+            commit(&ctl->accf[b]);
             ++u;
           }
-          if (++s == kStages) {
+          if (++s == G::kStages) {
             s = 0;
             ph ^= 1u;
           }
         }
         if constexpr (MODE != G_BLOCK) {
-          ptx::mma_commit(&ctl->accf[u % kNumAcc]);
+          commit(&ctl->accf[u % kNumAcc]);
           ++u;
         }
       }
@@ -281,12 +319,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int half = ew >> 2;             // which 128 columns of the 256-wide tile
     const int row = 32 * quad + lane;
     const uint32_t t_lane = tmem + (uint32_t(32 * quad) << 16) + uint32_t(half * 128);
+    // accumulator-empty arrivals go to the leader's barrier (a remote arrive from the peer)
+    auto release_acc = [&](uint32_t b) {
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (CTA2) ptx::mbar_arrive_cluster(ptx::map_to_rank(&ctl->acce[b], 0));
+        else ptx::mbar_arrive(&ctl->acce[b]);
+      }
+    };
     float alpha = 1.0f;
     if constexpr (MODE == G_TENSOR) alpha = __fmul_rn(*p.a_sinv, *p.b_sinv);
     uint32_t u = 0;
     float acc[128];
-    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
-      const int m0 = (tile % tiles_m) * kBM, n0 = (tile / tiles_m) * kBN;
+    for (int tile = unit; tile < n_tiles; tile += n_units) {
+      const int m0 = (tile % tiles_m) * G::kTileM + int(rank) * kBM;
+      const int n0 = (tile / tiles_m) * kBN;
       const int m = m0 + row, n = n0 + half * 128;
       if constexpr (MODE != G_BLOCK) {
         const uint32_t b = u % kNumAcc;
@@ -294,9 +342,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         ptx::tc_fence_after();
         tmem_load128(t_lane + b * kBN, acc);
         ptx::tmem_wait_ld();
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&ctl->acce[b]);
+        release_acc(b);
         ++u;
         if constexpr (MODE == G_TENSOR) {
 #pragma unroll
@@ -342,9 +388,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               }
             }
           }
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(&ctl->acce[b]);
+          release_acc(b);
           ++u;
         }
         if (!ok) break;
@@ -360,9 +404,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     while (ptx::clock64_() - t0 < 20000000ull) {
     }
   }
+  if constexpr (CTA2) ptx::cluster_sync();           // the pair is done with both TMEMs
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, kTmemCols);
+    if constexpr (CTA2) ptx::tmem_dealloc_pair(tmem, kTmemCols);
+    else ptx::tmem_dealloc(tmem, kTmemCols);
   }
 }
 
@@ -376,35 +422,59 @@ static bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, i
   return make_tmap_2d(map, base, elem_bytes, k, rows, kBKBytes / elem_bytes, box_rows, true);
 }
 
-template <int MODE, int B128 = 1>
+template <int MODE, int B128, int CTA2>
 static cudaError_t launch_mode(const GemmLaunch& g, cudaStream_t st) {
+  using G = Geo<CTA2>;
   CUtensorMap ma, mb;
   const int eb = MODE == G_BF16 ? 2 : 1;
   if (!make_operand_map(&ma, g.A, g.p.M, g.p.K, eb, kBM)) return cudaErrorInvalidValue;
-  if (!make_operand_map(&mb, g.B, g.p.N, g.p.K, eb, kBN)) return cudaErrorInvalidValue;
+  if (!make_operand_map(&mb, g.B, g.p.N, g.p.K, eb, CTA2 ? kBN / 2 : kBN))
+    return cudaErrorInvalidValue;
+  auto kern = gemm_tn_kernel<MODE, B128, CTA2>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tn_kernel<MODE, B128>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(kGemmSmemBytes));
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(G::kSmemBytes));
     if (e != cudaSuccess) return e;
+    if (CTA2) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+      (void)e;
+    }
     attr_set = true;
   }
   const int sms = num_sms();
-  const int tiles = ((g.p.M + kBM - 1) / kBM) * ((g.p.N + kBN - 1) / kBN);
-  const int grid = std::max(1, std::min(tiles, sms));
-  gemm_tn_kernel<MODE, B128><<<grid, kGemmThreads, kGemmSmemBytes, st>>>(ma, mb, g.p);
-  return cudaGetLastError();
+  const int tiles = ((g.p.M + G::kTileM - 1) / G::kTileM) * ((g.p.N + kBN - 1) / kBN);
+  const int units = std::max(1, std::min(tiles, CTA2 ? sms / 2 : sms));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(units * (CTA2 ? 2 : 1)));
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = G::kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CTA2 ? 2 : 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, ma, mb, g.p);
 }
 
 cudaError_t gemm_launch(const GemmLaunch& g, cudaStream_t st) {
   if (g.p.M == 0 || g.p.N == 0) return cudaSuccess;
+  // CTA pairs whenever there are at least two 128-row halves to give them (MXFP8 keeps the
+  // single-CTA kernel: its scale factors are copied per CTA).
+  const bool pair = g.p.M > kBM && g.mode != G_MX;
   switch (g.mode) {
-    case G_TENSOR: return launch_mode<G_TENSOR>(g, st);
-    case G_MX: return launch_mode<G_MX>(g, st);
+    case G_TENSOR:
+      return pair ? launch_mode<G_TENSOR, 1, 1>(g, st) : launch_mode<G_TENSOR, 1, 0>(g, st);
+    case G_MX: return launch_mode<G_MX, 1, 0>(g, st);
     case G_BLOCK:
-      return g.p.b_is_128 ? launch_mode<G_BLOCK, 1>(g, st) : launch_mode<G_BLOCK, 0>(g, st);
-    case G_BF16: return launch_mode<G_BF16>(g, st);
+      if (g.p.b_is_128)
+        return pair ? launch_mode<G_BLOCK, 1, 1>(g, st) : launch_mode<G_BLOCK, 1, 0>(g, st);
+      return pair ? launch_mode<G_BLOCK, 0, 1>(g, st) : launch_mode<G_BLOCK, 0, 0>(g, st);
+    case G_BF16:
+      return pair ? launch_mode<G_BF16, 1, 1>(g, st) : launch_mode<G_BF16, 1, 0>(g, st);
   }
   return cudaErrorInvalidValue;
 }

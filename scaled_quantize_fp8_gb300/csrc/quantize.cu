@@ -112,12 +112,13 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t* red) {
 
 
 // Shared-memory layout of the quantize kernel (offsets from a 1024-byte aligned base):
-//   [0, 5120)          control and staging (QuantCtl)
-//   [5120, 70656)      two tile buffers, each two 16 KiB halves (64 columns x 128 rows of
-//                      bf16) written by TMA with the 128-byte swizzle: logical 16-byte chunk
-//                      c of row r sits at physical chunk c ^ (r % 8)
-//   [70656, 87040)     row-wise codes of the tile (per-tensor and 128x128 recipes only), same
-//                      swizzle, read back transposed for the column-wise copy
+//   [0, 5120)           control and staging (QuantCtl)
+//   [5120, 103424)      three tile buffers, each two 16 KiB halves (64 columns x 128 rows of
+//                       bf16) written by TMA with the 128-byte swizzle: logical 16-byte chunk
+//                       c of row r sits at physical chunk c ^ (r % 8). Two tiles are in
+//                       flight while the third is converted. For per-tensor and 128x128
+//                       scales the row-wise codes are written back over the first half of the
+//                       buffer being converted (same swizzle) and read back transposed.
 struct QuantCtl {
   uint8_t sc_row[512];              // MXFP8 scale atom of the row copy
   uint8_t sc_col[512];              // ... of the column copy
@@ -125,13 +126,12 @@ struct QuantCtl {
   float scf_col[128];
   uint32_t red[8];
   uint32_t red_col[4][128];
-  uint64_t bar[2];                  // TMA completion, one per buffer
+  uint64_t bar[4];                  // TMA completion, one per buffer
   int abort_flag;
 };
+constexpr int kQBufs = 3;
 constexpr uint32_t kQCtlBytes = 5120;
 constexpr uint32_t kQTileBytes = 32768;
-constexpr uint32_t kQCodesOff = kQCtlBytes + 2 * kQTileBytes;
-constexpr uint32_t kQCodesBytes = 16384;
 static_assert(sizeof(QuantCtl) <= kQCtlBytes, "control block too large");
 constexpr uint64_t kQuantWaitBudget = 4000000000ull;   // ~2 s at 2 GHz
 
@@ -139,12 +139,10 @@ template <int MODE>
 __host__ __device__ constexpr bool uses_code_tile() { return MODE == Q_TENSOR || MODE == Q_BW128; }
 template <int MODE>
 __host__ __device__ constexpr uint32_t quant_smem_bytes() {
-  return 1024 + kQCodesOff + (uses_code_tile<MODE>() ? kQCodesBytes : 0);
+  return 1024 + kQCtlBytes + kQBufs * kQTileBytes;
 }
 template <int MODE, int EPI>
-__host__ __device__ constexpr int quant_ctas_per_sm() {
-  return (uses_code_tile<MODE>() || EPI != EPI_NONE) ? 2 : 3;
-}
+__host__ __device__ constexpr int quant_ctas_per_sm() { return 2; }
 
 // Byte offset of logical 16-byte chunk c (0..7) of row r in a 128-byte-swizzled 128-row block.
 __device__ __forceinline__ uint32_t swz(uint32_t r, uint32_t c) {
@@ -270,6 +268,9 @@ __device__ __forceinline__ void quantize_one_tile(const QuantParams& p, QuantCtl
   }
 
   // ---- row-wise copy (and the code tile for the transposed copy)
+  if constexpr (uses_code_tile<MODE>()) {
+    if (p.col != nullptr) __syncthreads();          // every lane holds its bf16 in registers
+  }
   if (p.row != nullptr || uses_code_tile<MODE>()) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -302,8 +303,9 @@ __device__ __forceinline__ void quantize_one_tile(const QuantParams& p, QuantCtl
       }
       if (p.row != nullptr && (r0 + r < R) && col_ok)
         *reinterpret_cast<uint4*>(p.row + (r0 + r) * C + c0 + ccol) = q4;
-      if constexpr (uses_code_tile<MODE>())
-        *reinterpret_cast<uint4*>(codes + swz(r, 4 * h + cc)) = q4;
+      if constexpr (uses_code_tile<MODE>()) {
+        if (p.col != nullptr) *reinterpret_cast<uint4*>(codes + swz(r, 4 * h + cc)) = q4;
+      }
     }
   }
 
@@ -457,14 +459,12 @@ __global__ void __launch_bounds__(256, quant_ctas_per_sm<MODE, EPI>())
       (reinterpret_cast<uintptr_t>(qsm_raw) + 1023) & ~uintptr_t(1023));
   QuantCtl& S = *reinterpret_cast<QuantCtl*>(base);
   uint8_t* tiles = base + kQCtlBytes;
-  uint8_t* codes = base + kQCodesOff;
   const int t = threadIdx.x;
   const int tiles_r = int((p.R + 127) >> 7);
   const int n_tiles = tiles_r * p.tiles_c;
 
   if (t == 0) {
-    ptx::mbar_init(&S.bar[0], 1);
-    ptx::mbar_init(&S.bar[1], 1);
+    for (int b = 0; b < kQBufs; ++b) ptx::mbar_init(&S.bar[b], 1);
     S.abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -499,15 +499,21 @@ __global__ void __launch_bounds__(256, quant_ctas_per_sm<MODE, EPI>())
     ptx::tma_load_2d(dst + 16384, &tmX, tc * kTile + 64, tr * kTile, &S.bar[b]);
   };
 
+  // prologue: the first kQBufs - 1 tiles in flight
+  if (t == 0) {
+    for (int j = 0; j < kQBufs - 1; ++j) {
+      const int tl = int(blockIdx.x) + j * int(gridDim.x);
+      if (tl < n_tiles) issue(tl, j);
+    }
+  }
   int tile = blockIdx.x;
-  if (t == 0 && tile < n_tiles) issue(tile, 0);
   for (int i = 0; tile < n_tiles; ++i, tile += gridDim.x) {
-    const int b = i & 1;
-    const int next = tile + int(gridDim.x);
-    if (t == 0 && next < n_tiles) issue(next, b ^ 1);
-    if (!quant_wait(S, b, uint32_t(i >> 1) & 1u, p.status)) break;
-    quantize_one_tile<MODE, EPI>(p, S, tiles + b * kQTileBytes, codes, tile, s_tensor,
-                                 tensor_nan);
+    const int b = i % kQBufs;
+    const int ahead = tile + (kQBufs - 1) * int(gridDim.x);
+    if (t == 0 && ahead < n_tiles) issue(ahead, (i + kQBufs - 1) % kQBufs);
+    if (!quant_wait(S, b, uint32_t(i / kQBufs) & 1u, p.status)) break;
+    uint8_t* buf = tiles + b * kQTileBytes;
+    quantize_one_tile<MODE, EPI>(p, S, buf, buf, tile, s_tensor, tensor_nan);
     __syncthreads();                                 // buffer b is refilled next iteration
   }
   if (*reinterpret_cast<volatile int*>(&S.abort_flag)) {
