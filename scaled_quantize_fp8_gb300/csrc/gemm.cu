@@ -139,7 +139,9 @@ __device__ __forceinline__ void tmem_load128(uint32_t taddr, float* out) {
 template <int MODE, int B128, int CTA2>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA,
-                   const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+                   const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmSFA,
+                   const __grid_constant__ CUtensorMap tmSFB, const GemmParams p) {
   using G = Geo<CTA2>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -195,6 +197,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (lane == 0) {
       ptx::prefetch_tmap(&tmA);
       ptx::prefetch_tmap(&tmB);
+      if constexpr (MODE == G_MX && CTA2) {
+        ptx::prefetch_tmap(&tmSFA);
+        ptx::prefetch_tmap(&tmSFB);
+      }
       int s = 0;
       uint32_t ph = 0;
       const int kblocks128 = p.K / 128;       // MX scale atoms per operand row tile
@@ -207,10 +213,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           uint8_t* b_dst = sB + s * G::kTileBBytes;
           if constexpr (CTA2) {
             // Both CTAs' loads complete on the leader's barrier, which expects all of them.
+            // MXFP8: each CTA also brings its own 512-byte A-scale atom and both B-scale atoms
+            // of the pair's 256 B rows (the scale-factor arrays are viewed as rows of 256 B).
             const uint32_t bar = ptx::map_to_rank(&ctl->full[s], 0);
-            if (leader) ptx::mbar_arrive_expect_tx(&ctl->full[s], 2 * (kTileABytes + G::kTileBBytes));
+            constexpr uint32_t sf_bytes = MODE == G_MX ? 512u + 1024u : 0u;
+            if (leader)
+              ptx::mbar_arrive_expect_tx(&ctl->full[s],
+                                         2 * (kTileABytes + G::kTileBBytes + sf_bytes));
             ptx::tma_load_2d_pair(a_dst, &tmA, kb * kBKElems, m0, bar);
             ptx::tma_load_2d_pair(b_dst, &tmB, kb * kBKElems, n0, bar);
+            if constexpr (MODE == G_MX) {
+              uint8_t* sf = sSF + s * kSfStageBytes;
+              const int nb_pair = (tile / tiles_m) * kBN;          // first B row of the pair
+              ptx::tma_load_2d_pair(sf, &tmSFA, 0, 2 * ((m0 >> 7) * kblocks128 + kb), bar);
+              ptx::tma_load_2d_pair(sf + 512, &tmSFB, 0,
+                                    2 * ((nb_pair >> 7) * kblocks128 + kb), bar);
+              ptx::tma_load_2d_pair(sf + 1024, &tmSFB, 0,
+                                    2 * (((nb_pair >> 7) + 1) * kblocks128 + kb), bar);
+            }
           } else {
             uint32_t bytes = kTileABytes + G::kTileBBytes;
             const bool sfb_hi = (n0 + 128) < p.N;
@@ -270,13 +290,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           ptx::tc_fence_after();
           const uint32_t a_addr = ptx::smem_u32(sA + s * kTileABytes);
           const uint32_t b_addr = ptx::smem_u32(sB + s * G::kTileBBytes);
-          if constexpr (MODE == G_MX && !CTA2) {
+          if constexpr (MODE == G_MX) {
             const uint32_t sf = ptx::smem_u32(sSF + s * kSfStageBytes);
-            ptx::tmem_cp_32x128b_warpx4(sfa_t, ptx::smem_desc(sf, 0, 128, ptx::kSwizzleNone));
-            ptx::tmem_cp_32x128b_warpx4(sfb_t,
-                                        ptx::smem_desc(sf + 512, 0, 128, ptx::kSwizzleNone));
-            ptx::tmem_cp_32x128b_warpx4(sfb_t + 4,
-                                        ptx::smem_desc(sf + 1024, 0, 128, ptx::kSwizzleNone));
+            const uint64_t d0 = ptx::smem_desc(sf, 0, 128, ptx::kSwizzleNone);
+            const uint64_t d1 = ptx::smem_desc(sf + 512, 0, 128, ptx::kSwizzleNone);
+            const uint64_t d2 = ptx::smem_desc(sf + 1024, 0, 128, ptx::kSwizzleNone);
+            if constexpr (CTA2) {
+              ptx::tmem_cp_32x128b_warpx4_pair(sfa_t, d0);
+              ptx::tmem_cp_32x128b_warpx4_pair(sfb_t, d1);
+              ptx::tmem_cp_32x128b_warpx4_pair(sfb_t + 4, d2);
+            } else {
+              ptx::tmem_cp_32x128b_warpx4(sfa_t, d0);
+              ptx::tmem_cp_32x128b_warpx4(sfb_t, d1);
+              ptx::tmem_cp_32x128b_warpx4(sfb_t + 4, d2);
+            }
           }
 #pragma unroll
           for (int k = 0; k < kBKBytes / 32; ++k) {
@@ -284,8 +311,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint64_t bd = ptx::smem_desc(b_addr + 32 * k, 16, 1024, ptx::kSwizzle128B);
             const uint32_t acc_on = MODE == G_BLOCK ? uint32_t(k != 0) : uint32_t((kb | k) != 0);
             if constexpr (CTA2) {
-              if constexpr (MODE == G_BF16) ptx::mma_f16_pair(d_t, ad, bd, idesc, acc_on);
-              else ptx::mma_f8f6f4_pair(d_t, ad, bd, idesc, acc_on);
+              if constexpr (MODE == G_BF16) {
+                ptx::mma_f16_pair(d_t, ad, bd, idesc, acc_on);
+              } else if constexpr (MODE == G_MX) {
+                const uint32_t id = idesc | (uint32_t(k) << 29) | (uint32_t(k) << 4);
+                ptx::mma_mxf8f6f4_pair(d_t, ad, bd, id, sfa_t, sfb_t, acc_on);
+              } else {
+                ptx::mma_f8f6f4_pair(d_t, ad, bd, idesc, acc_on);
+              }
             } else if constexpr (MODE == G_MX) {
               const uint32_t id = idesc | (uint32_t(k) << 29) | (uint32_t(k) << 4);
               ptx::mma_mxf8f6f4(d_t, ad, bd, id, sfa_t, sfb_t, acc_on);
@@ -430,6 +463,15 @@ static cudaError_t launch_mode(const GemmLaunch& g, cudaStream_t st) {
   if (!make_operand_map(&ma, g.A, g.p.M, g.p.K, eb, kBM)) return cudaErrorInvalidValue;
   if (!make_operand_map(&mb, g.B, g.p.N, g.p.K, eb, CTA2 ? kBN / 2 : kBN))
     return cudaErrorInvalidValue;
+  // MXFP8 scale arrays viewed as rows of 256 bytes (two rows per 512-byte atom) for TMA.
+  CUtensorMap msfa = ma, msfb = mb;
+  if (MODE == G_MX && CTA2) {
+    const int64_t kb = g.p.K / 128;
+    if (!make_tmap_2d(&msfa, g.p.sfa, 1, 256, 2 * (int64_t(g.p.M) / 128) * kb, 256, 2, false))
+      return cudaErrorInvalidValue;
+    if (!make_tmap_2d(&msfb, g.p.sfb, 1, 256, 2 * (int64_t(g.p.N) / 128) * kb, 256, 2, false))
+      return cudaErrorInvalidValue;
+  }
   auto kern = gemm_tn_kernel<MODE, B128, CTA2>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -457,22 +499,23 @@ static cudaError_t launch_mode(const GemmLaunch& g, cudaStream_t st) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, ma, mb, g.p);
+  return cudaLaunchKernelEx(&cfg, kern, ma, mb, msfa, msfb, g.p);
 }
 
 cudaError_t gemm_launch(const GemmLaunch& g, cudaStream_t st) {
   if (g.p.M == 0 || g.p.N == 0) return cudaSuccess;
-  // CTA pairs whenever there are at least two 128-row halves to give them (MXFP8 keeps the
-  // single-CTA kernel: its scale factors are copied per CTA).
-  const bool pair = g.p.M > kBM && g.mode != G_MX;
+  // CTA pairs whenever there are at least two 128-row halves to give them.
+  // (Blockwise keeps the single CTA: its per-chunk promotion would couple the pair's
+  // epilogues to every K step.)
+  const bool pair = g.p.M > kBM;
   switch (g.mode) {
     case G_TENSOR:
       return pair ? launch_mode<G_TENSOR, 1, 1>(g, st) : launch_mode<G_TENSOR, 1, 0>(g, st);
-    case G_MX: return launch_mode<G_MX, 1, 0>(g, st);
+    case G_MX:
+      return (pair && g.p.N > kBM) ? launch_mode<G_MX, 1, 1>(g, st)
+                                   : launch_mode<G_MX, 1, 0>(g, st);
     case G_BLOCK:
-      if (g.p.b_is_128)
-        return pair ? launch_mode<G_BLOCK, 1, 1>(g, st) : launch_mode<G_BLOCK, 1, 0>(g, st);
-      return pair ? launch_mode<G_BLOCK, 0, 1>(g, st) : launch_mode<G_BLOCK, 0, 0>(g, st);
+      return g.p.b_is_128 ? launch_mode<G_BLOCK, 1, 0>(g, st) : launch_mode<G_BLOCK, 0, 0>(g, st);
     case G_BF16:
       return pair ? launch_mode<G_BF16, 1, 1>(g, st) : launch_mode<G_BF16, 1, 0>(g, st);
   }

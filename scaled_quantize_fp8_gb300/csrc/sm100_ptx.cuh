@@ -227,6 +227,24 @@ __device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t cta_mask
       : "memory");
 }
 
+__device__ __forceinline__ void mma_mxf8f6f4_pair(uint32_t d, uint64_t a, uint64_t b,
+                                                  uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                                  uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+      : "memory");
+}
+// Pair version of the scale-factor copy: each CTA's shared-memory matrix (same offset) goes
+// to that CTA's TMEM.
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4_pair(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
 __device__ __forceinline__ uint64_t clock64_() {
   uint64_t c;
   asm volatile("mov.u64 %0, %%clock64;" : "=l"(c));
