@@ -108,6 +108,7 @@ typedef struct {
   int64_t rows, cols;    /* source shape [R, C] */
   int32_t kind;          /* recipe the codes were made with (set by fp8_quantize) */
   int32_t role;          /* fp8_role */
+  int32_t col_bf16;      /* 1: `col` holds the bf16 transpose (set by fp8_quantize) */
 } fp8_tensor;
 
 /* Delayed-scaling state: a rolling window of the last `len` amax values. */
@@ -131,7 +132,10 @@ size_t fp8_workspace_bytes(const fp8_recipe *recipe, int64_t rows, int64_t cols)
  *   x_bf16     [rows][cols] bf16, 16-byte aligned, read only.
  *   rows, cols >= 0. MXFP8 and BLOCKWISE need both to be multiples of 128; TENSORWISE and
  *              DELAYED need multiples of 16. An empty tensor writes amax 0, scale 1.
- *   want_row / want_col: which copies to write (at least one).
+ *   want_row / want_col: which copies to write (at least one). With recipe->fp8_wgrad == 0
+ *              (--fp8-wgrad off) and a role other than WEIGHT, the column-wise copy is the
+ *              transposed tensor in bf16 ([cols][rows], 2 bytes per element, no scales): it
+ *              is only read by the wgrad GEMM, which then runs in bf16.
  *   out        codes/scales destinations (see the layouts above); out->rows/cols/role/kind
  *              are set by this call.
  *   workspace  device scratch of at least fp8_workspace_bytes() (may be NULL when that is 0).
@@ -166,13 +170,13 @@ fp8_status fp8_linear_fwd(const fp8_recipe *recipe, const fp8_tensor *x, const f
 /*
  * fp8_linear_bwd — dgrad dX[M,K] = deq(dY)[M,N] . deq(W^T)[K,N]^T from dy->row and w->col,
  * and wgrad dW[N,K] = deq(dY^T)[N,M] . deq(X^T)[K,M]^T from dy->col and x_saved->col (the
- * FP8 copies cached in the forward pass). With recipe->fp8_wgrad == 0 the wgrad GEMM runs on
- * the bf16 dy_bf16 [M][N] and x_bf16 [M][K] instead. dx or dw may be NULL to skip that GEMM.
- * Outputs are bf16 (out_fp32 = 0) or fp32 (out_fp32 = 1).
+ * copies cached in the forward pass). With recipe->fp8_wgrad == 0 (--fp8-wgrad off) those two
+ * column copies are bf16 transposes (see fp8_quantize) and the wgrad GEMM runs in bf16 with
+ * fp32 accumulation. dx or dw may be NULL to skip that GEMM. Outputs are bf16 (out_fp32 = 0)
+ * or fp32 (out_fp32 = 1).
  */
 fp8_status fp8_linear_bwd(const fp8_recipe *recipe, const fp8_tensor *dy,
-                          const fp8_tensor *x_saved, const fp8_tensor *w,
-                          const void *x_bf16, const void *dy_bf16, void *dx, void *dw,
+                          const fp8_tensor *x_saved, const fp8_tensor *w, void *dx, void *dw,
                           int32_t out_fp32, int32_t *dev_status, cudaStream_t stream);
 
 /*

@@ -32,7 +32,8 @@ class Tensor(ctypes.Structure):
                 ("row_scale", ctypes.c_void_p), ("col_scale", ctypes.c_void_p),
                 ("amax", ctypes.c_void_p), ("scale", ctypes.c_void_p),
                 ("scale_inv", ctypes.c_void_p), ("rows", ctypes.c_int64),
-                ("cols", ctypes.c_int64), ("kind", ctypes.c_int32), ("role", ctypes.c_int32)]
+                ("cols", ctypes.c_int64), ("kind", ctypes.c_int32), ("role", ctypes.c_int32),
+                ("col_bf16", ctypes.c_int32)]
 
 
 class AmaxHistory(ctypes.Structure):
@@ -51,8 +52,8 @@ _SIG = {
     "fp8_linear_fwd": (_I32, [ctypes.POINTER(Recipe), ctypes.POINTER(Tensor),
                               ctypes.POINTER(Tensor), _P, _I32, _P, _P]),
     "fp8_linear_bwd": (_I32, [ctypes.POINTER(Recipe), ctypes.POINTER(Tensor),
-                              ctypes.POINTER(Tensor), ctypes.POINTER(Tensor), _P, _P, _P, _P,
-                              _I32, _P, _P]),
+                              ctypes.POINTER(Tensor), ctypes.POINTER(Tensor), _P, _P, _I32, _P,
+                              _P]),
     "fp8_gelu_quantize": (_I32, [ctypes.POINTER(Recipe), _P, _I64, _I64, _P,
                                  ctypes.POINTER(Tensor), ctypes.POINTER(Tensor), _P, _P]),
     "fp8_dgelu_quantize": (_I32, [ctypes.POINTER(Recipe), _P, ctypes.POINTER(Tensor), _P,

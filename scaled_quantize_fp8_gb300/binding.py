@@ -58,6 +58,7 @@ class QTensor:
     amax: Optional[torch.Tensor] = None       # float32 [1]
     scale: Optional[torch.Tensor] = None
     scale_inv: Optional[torch.Tensor] = None
+    col_bf16: int = 0                         # 1: `col` is the bf16 transpose (wgrad in bf16)
     _c: object = field(default=None, repr=False)
 
     def c(self):
@@ -66,6 +67,7 @@ class QTensor:
             v = getattr(self, name)
             setattr(t, name, None if v is None else v.data_ptr())
         t.rows, t.cols, t.kind, t.role = self.rows, self.cols, self.kind, self.role
+        t.col_bf16 = self.col_bf16
         self._c = t
         return t
 
@@ -91,10 +93,15 @@ def empty_qtensor(recipe: Recipe, rows, cols, role="activation", want_row=True, 
         if shp is not None:
             q.row_scale = torch.empty(shp, dtype=dt, device=device)
     if want_col:
-        q.col = torch.empty((cols, rows), dtype=torch.uint8, device=device)
-        shp, dt = scale_shape(kind, r, cols, rows)
-        if shp is not None:
-            q.col_scale = torch.empty(shp, dtype=dt, device=device)
+        if not recipe.fp8_wgrad and r != L.ROLE_WEIGHT:
+            # --fp8-wgrad off: the column copy is the bf16 transpose, read by the bf16 wgrad
+            q.col = torch.empty((cols, rows), dtype=torch.bfloat16, device=device)
+            q.col_bf16 = 1
+        else:
+            q.col = torch.empty((cols, rows), dtype=torch.uint8, device=device)
+            shp, dt = scale_shape(kind, r, cols, rows)
+            if shp is not None:
+                q.col_scale = torch.empty(shp, dtype=dt, device=device)
     if kind in (L.RECIPE_DELAYED, L.RECIPE_TENSORWISE):
         q.amax = torch.zeros(1, dtype=torch.float32, device=device)
         q.scale = torch.ones(1, dtype=torch.float32, device=device)
@@ -127,6 +134,7 @@ def quantize(recipe: Recipe, x: torch.Tensor, role="activation", want_row=True, 
                           _stream(stream))
     L.check(st, "fp8_quantize")
     out.rows, out.cols, out.kind, out.role = ct.rows, ct.cols, ct.kind, ct.role
+    out.col_bf16 = ct.col_bf16
     return out
 
 
@@ -147,6 +155,7 @@ def quantize_static_scratch(recipe: Recipe, x: torch.Tensor, role="activation", 
                                          _ptr(status), _stream(stream))
     L.check(st, "fp8_quantize_static_scratch")
     out.rows, out.cols, out.kind, out.role = ct.rows, ct.cols, ct.kind, ct.role
+    out.col_bf16 = ct.col_bf16
     return out
 
 
@@ -189,23 +198,23 @@ def linear_fwd(recipe: Recipe, x: QTensor, w: QTensor, y: Optional[torch.Tensor]
 
 
 def linear_bwd(recipe: Recipe, dy: QTensor, x: Optional[QTensor], w: Optional[QTensor],
-               x_bf16=None, dy_bf16=None, want_dx=True, want_dw=True, dx=None, dw=None,
-               fp32=False, status=None, stream=None):
+               want_dx=True, want_dw=True, dx=None, dw=None, fp32=False, status=None,
+               stream=None):
+    """dgrad (dy row copy x w column copy) and wgrad (dy and x column copies; bf16 when the
+    recipe has fp8_wgrad off)."""
     lib = L.load()
     dt = torch.float32 if fp32 else torch.bfloat16
     dev = (dy.row if dy.row is not None else dy.col).device
     if want_dx and dx is None:
         dx = torch.empty((dy.rows, w.cols), dtype=dt, device=dev)
     if want_dw and dw is None:
-        dw = torch.empty((dy.cols, x.cols if x is not None else x_bf16.shape[1]), dtype=dt,
-                         device=dev)
+        dw = torch.empty((dy.cols, x.cols), dtype=dt, device=dev)
     rc = recipe.c()
     cx = ctypes.byref(x.c()) if x is not None else None
     cw = ctypes.byref(w.c()) if w is not None else None
-    st = lib.fp8_linear_bwd(ctypes.byref(rc), ctypes.byref(dy.c()), cx, cw, _ptr(x_bf16),
-                            _ptr(dy_bf16), _ptr(dx) if want_dx else None,
-                            _ptr(dw) if want_dw else None, int(fp32), _ptr(status),
-                            _stream(stream))
+    st = lib.fp8_linear_bwd(ctypes.byref(rc), ctypes.byref(dy.c()), cx, cw,
+                            _ptr(dx) if want_dx else None, _ptr(dw) if want_dw else None,
+                            int(fp32), _ptr(status), _stream(stream))
     L.check(st, "fp8_linear_bwd")
     return dx, dw
 

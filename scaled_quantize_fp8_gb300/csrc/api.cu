@@ -101,10 +101,14 @@ fp8_status fp8_quantize(const fp8_recipe* recipe, const void* x_bf16, int64_t ro
   if (rows * cols >= (int64_t(1) << 31)) return FP8_ERR_SHAPE;   // 32-bit element offsets
   FP8_TRY(check_scalars(kind, out));
   const bool empty = rows == 0 || cols == 0;
+  const bool col_bf16 = recipe->fp8_wgrad == 0 && role != FP8_ROLE_WEIGHT;
   if (!empty) {
     FP8_TRY(check_ptr(x_bf16));
     if (want_row) FP8_TRY(check_copy(kind, out->row, out->row_scale));
-    if (want_col) FP8_TRY(check_copy(kind, out->col, out->col_scale));
+    if (want_col) {
+      if (col_bf16) FP8_TRY(check_ptr(out->col));
+      else FP8_TRY(check_copy(kind, out->col, out->col_scale));
+    }
     const size_t need = quantize_workspace_bytes(kind, rows, cols);
     if (need > 0 && (workspace == nullptr || ws_bytes < need)) return FP8_ERR_WORKSPACE;
     if (need > 0 && !aligned16(workspace)) return FP8_ERR_ALIGN;
@@ -113,10 +117,11 @@ fp8_status fp8_quantize(const fp8_recipe* recipe, const void* x_bf16, int64_t ro
   out->cols = cols;
   out->role = role;
   out->kind = kind;
+  out->col_bf16 = col_bf16 ? 1 : 0;
   return cuda_status(quantize_launch(kind, role, recipe->margin,
                                      reinterpret_cast<const uint16_t*>(x_bf16), rows, cols,
-                                     want_row != 0, want_col != 0, out, workspace, dev_status,
-                                     stream));
+                                     want_row != 0, want_col != 0, col_bf16, out, workspace,
+                                     dev_status, stream));
 }
 
 fp8_status fp8_amax_update(const fp8_recipe* recipe, fp8_amax_history* hist,
@@ -197,6 +202,30 @@ fp8_status run_gemm(int kind, const Operand& a, const Operand& b, int64_t M, int
   return cuda_status(gemm_launch(g, st));
 }
 
+fp8_status run_bf16_gemm(const void* a, const void* b, int64_t M, int64_t N, int64_t Kr, void* D,
+                         int fp32_out, int32_t* status, cudaStream_t st) {
+  FP8_TRY(check_ptr(a));
+  FP8_TRY(check_ptr(b));
+  FP8_TRY(check_ptr(D));
+  if (M % 16 || N % 16 || Kr % 16) return FP8_ERR_SHAPE;
+  if (M > (int64_t(1) << 30) || N > (int64_t(1) << 30) || Kr > (int64_t(1) << 30))
+    return FP8_ERR_SHAPE;
+  if (M == 0 || N == 0) return FP8_OK;
+  if (Kr == 0) return cuda_status(cudaMemsetAsync(D, 0, size_t(M) * N * (fp32_out ? 4 : 2), st));
+  GemmLaunch g{};
+  g.mode = G_BF16;
+  g.A = a;
+  g.B = b;
+  g.p.M = int(M);
+  g.p.N = int(N);
+  g.p.K = int(Kr);
+  g.p.D = D;
+  g.p.ldd = N;
+  g.p.d_fp32 = fp32_out;
+  g.p.status = status;
+  return cuda_status(gemm_launch(g, st));
+}
+
 fp8_status check_tensor(const fp8_recipe* r, const fp8_tensor* t) {
   if (t == nullptr) return FP8_ERR_NULL;
   if (t->kind != r->kind) return FP8_ERR_UNSUPPORTED;
@@ -219,13 +248,10 @@ fp8_status fp8_linear_fwd(const fp8_recipe* recipe, const fp8_tensor* x, const f
 }
 
 fp8_status fp8_linear_bwd(const fp8_recipe* recipe, const fp8_tensor* dy,
-                          const fp8_tensor* x_saved, const fp8_tensor* w, const void* x_bf16,
-                          const void* dy_bf16, void* dx, void* dw, int32_t out_fp32,
-                          int32_t* dev_status, cudaStream_t stream) {
+                          const fp8_tensor* x_saved, const fp8_tensor* w, void* dx, void* dw,
+                          int32_t out_fp32, int32_t* dev_status, cudaStream_t stream) {
   FP8_TRY(check_recipe(recipe));
   FP8_TRY(check_tensor(recipe, dy));
-  (void)x_bf16;
-  (void)dy_bf16;
   const int64_t M = dy->rows, N = dy->cols;
   if (dx != nullptr) {
     FP8_TRY(check_tensor(recipe, w));
@@ -237,10 +263,16 @@ fp8_status fp8_linear_bwd(const fp8_recipe* recipe, const fp8_tensor* dy,
     FP8_TRY(run_gemm(recipe->kind, a, b, M, K, N, dx, out_fp32, dev_status, stream));
   }
   if (dw != nullptr) {
-    if (!recipe->fp8_wgrad) return FP8_ERR_UNSUPPORTED;
     FP8_TRY(check_tensor(recipe, x_saved));
     if (x_saved->rows != M) return FP8_ERR_SHAPE;
     const int64_t K = x_saved->cols;
+    const bool bf16 = recipe->fp8_wgrad == 0;
+    if (dy->col_bf16 != (bf16 ? 1 : 0) || x_saved->col_bf16 != (bf16 ? 1 : 0))
+      return FP8_ERR_UNSUPPORTED;              // copies quantised under another --fp8-wgrad
+    if (bf16) {
+      // wgrad in bf16: dW[N][K] = (dY^T)[N][M] . (X^T)[K][M]^T from the bf16 transposes
+      return run_bf16_gemm(dy->col, x_saved->col, N, K, M, dw, out_fp32, dev_status, stream);
+    }
     // wgrad: dW[N][K] = (dY^T)[N][M] . (X^T)[K][M]^T
     const Operand a{dy->col, dy->col_scale, dy->scale_inv, dy->role};
     const Operand b{x_saved->col, x_saved->col_scale, x_saved->scale_inv, x_saved->role};

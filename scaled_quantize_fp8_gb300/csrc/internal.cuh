@@ -21,8 +21,9 @@ int num_sms();
 // ---- quantize.cu
 size_t quantize_workspace_bytes(int kind, int64_t R, int64_t C);
 cudaError_t quantize_launch(int kind, int role, int margin, const uint16_t* x, int64_t R,
-                            int64_t C, bool want_row, bool want_col, fp8_tensor* out,
-                            void* workspace, int32_t* status, cudaStream_t st);
+                            int64_t C, bool want_row, bool want_col, bool col_bf16,
+                            fp8_tensor* out, void* workspace, int32_t* status,
+                            cudaStream_t st);
 cudaError_t gelu_quantize_launch(const uint16_t* h, int64_t R, int64_t C, uint16_t* a_bf16,
                                  fp8_tensor* a_q, fp8_tensor* h_q, int32_t* status,
                                  cudaStream_t st);

@@ -26,7 +26,8 @@ struct QuantParams {
   int64_t R, C;
   int tiles_c;
   uint8_t* row;               // [R][C] codes or null
-  uint8_t* col;               // [C][R] codes or null
+  uint8_t* col;               // [C][R] codes (or bf16 when col_bf16), or null
+  bool col_bf16;              // column copy = bf16 transpose (wgrad kept in bf16)
   void* row_scale;
   void* col_scale;
   // per-tensor recipes
@@ -262,16 +263,16 @@ __device__ __forceinline__ void quantize_one_tile(const QuantParams& p, QuantCtl
       if (t == 0) {
         const int tiles_r = int((R + 127) >> 7);
         if (p.row_scale) reinterpret_cast<float*>(p.row_scale)[tr * p.tiles_c + tc] = sinv_tile;
-        if (p.col_scale) reinterpret_cast<float*>(p.col_scale)[tc * tiles_r + tr] = sinv_tile;
+        if (p.col_scale && !p.col_bf16)
+          reinterpret_cast<float*>(p.col_scale)[tc * tiles_r + tr] = sinv_tile;
       }
     }
   }
 
   // ---- row-wise copy (and the code tile for the transposed copy)
-  if constexpr (uses_code_tile<MODE>()) {
-    if (p.col != nullptr) __syncthreads();          // every lane holds its bf16 in registers
-  }
-  if (p.row != nullptr || uses_code_tile<MODE>()) {
+  const bool code_tile = uses_code_tile<MODE>() && !p.col_bf16;
+  if (code_tile && p.col != nullptr) __syncthreads();   // every lane holds its bf16 in registers
+  if (p.row != nullptr || code_tile) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint32_t r = 32u * i + 4u * warp + rr;
@@ -303,15 +304,44 @@ __device__ __forceinline__ void quantize_one_tile(const QuantParams& p, QuantCtl
       }
       if (p.row != nullptr && (r0 + r < R) && col_ok)
         *reinterpret_cast<uint4*>(p.row + (r0 + r) * C + c0 + ccol) = q4;
-      if constexpr (uses_code_tile<MODE>()) {
-        if (p.col != nullptr) *reinterpret_cast<uint4*>(codes + swz(r, 4 * h + cc)) = q4;
-      }
+      if (code_tile && p.col != nullptr) *reinterpret_cast<uint4*>(codes + swz(r, 4 * h + cc)) = q4;
     }
   }
 
   if (p.col != nullptr) {
     __syncthreads();                                   // write-backs / code tile visible
-    if constexpr (uses_code_tile<MODE>()) {
+    if (p.col_bf16) {
+      // ---- column-wise copy in bf16 (wgrad kept in bf16): the plain transpose. Thread
+      // (pp, q) owns source columns 2pp, 2pp+1 over rows 32q .. 32q+31 (64 bytes each).
+      const int pp = t & 63, q = t >> 6;
+      const uint8_t* hb = tile + (pp >> 5) * 16384;
+      const uint32_t chunk = (pp & 31) >> 2, wofs = 4u * (pp & 3);
+      uint32_t lo[16], hi[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const uint32_t x0 = *reinterpret_cast<const uint32_t*>(hb + swz(32u * q + 2 * j, chunk) + wofs);
+        const uint32_t x1 = *reinterpret_cast<const uint32_t*>(hb + swz(32u * q + 2 * j + 1, chunk) + wofs);
+        lo[j] = __byte_perm(x0, x1, 0x5410);
+        hi[j] = __byte_perm(x0, x1, 0x7632);
+      }
+      const uint32_t rr0 = r0 + 32u * q, cA = c0 + 2u * pp;
+      if (cA < C) {
+        uint16_t* dst = reinterpret_cast<uint16_t*>(p.col) + cA * R + rr0;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const uint32_t* src = k == 0 ? lo : hi;
+          uint16_t* d = dst + k * R;
+          if (rr0 < R) {
+            reinterpret_cast<uint4*>(d)[0] = make_uint4(src[0], src[1], src[2], src[3]);
+            reinterpret_cast<uint4*>(d)[1] = make_uint4(src[4], src[5], src[6], src[7]);
+          }
+          if (rr0 + 16 < R) {
+            reinterpret_cast<uint4*>(d)[2] = make_uint4(src[8], src[9], src[10], src[11]);
+            reinterpret_cast<uint4*>(d)[3] = make_uint4(src[12], src[13], src[14], src[15]);
+          }
+        }
+      }
+    } else if constexpr (uses_code_tile<MODE>()) {
       // ---- column-wise copy = byte transpose of the row codes. Thread (c4, g): source
       // columns 4 c4 .. 4 c4 + 3, rows 16 g .. 16 g + 15 (four 4x4 byte transposes).
       const int c4 = t & 31, g = t >> 5;
@@ -419,14 +449,14 @@ __device__ __forceinline__ void quantize_one_tile(const QuantParams& p, QuantCtl
         reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.row_scale) +
                                  (uint32_t(tr) * p.tiles_c + tc) * 512)[t] =
             reinterpret_cast<const uint4*>(S.sc_row)[t];
-      if (t >= 32 && t < 64 && p.col != nullptr)
+      if (t >= 32 && t < 64 && p.col != nullptr && !p.col_bf16)
         reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.col_scale) +
                                  (uint32_t(tc) * tiles_r + tr) * 512)[t - 32] =
             reinterpret_cast<const uint4*>(S.sc_col)[t - 32];
     } else {
       if (t < 128 && p.row != nullptr)
         reinterpret_cast<float*>(p.row_scale)[uint32_t(tc) * R + r0 + t] = S.scf_row[t];
-      if (t >= 128 && p.col != nullptr)
+      if (t >= 128 && p.col != nullptr && !p.col_bf16)
         reinterpret_cast<float*>(p.col_scale)[uint32_t(tr) * C + c0 + (t - 128)] =
             S.scf_col[t - 128];
     }
@@ -648,10 +678,12 @@ static cudaError_t launch_tiles(const QuantParams& p, cudaStream_t st) {
 }
 
 cudaError_t quantize_launch(int kind, int role, int margin, const uint16_t* x, int64_t R,
-                            int64_t C, bool want_row, bool want_col, fp8_tensor* out,
-                            void* workspace, int32_t* status, cudaStream_t st) {
+                            int64_t C, bool want_row, bool want_col, bool col_bf16,
+                            fp8_tensor* out, void* workspace, int32_t* status,
+                            cudaStream_t st) {
   QuantParams p{};
   p.status = status;
+  p.col_bf16 = col_bf16;
   p.x = x;
   p.R = R;
   p.C = C;

@@ -28,7 +28,7 @@ def _rec(kind=L.RECIPE_TENSORWISE, fmt=L.FORMAT_E4M3, margin=0, hist=16, algo=0,
 
 def _tensor(row=0x1000, col=0x2000, rs=0x3000, cs=0x4000, amax=0x5000, scale=0x6000,
             sinv=0x7000):
-    return L.Tensor(row, col, rs, cs, amax, scale, sinv, 0, 0, 0, 0)
+    return L.Tensor(row, col, rs, cs, amax, scale, sinv, 0, 0, 0, 0, 0)
 
 
 def test_exports_every_declared_symbol(lib):
@@ -127,12 +127,16 @@ def test_linear_bwd_checks(lib):
     w = _qt(L.RECIPE_TENSORWISE, 384, 512)
     bwd = lib.fp8_linear_bwd
     assert bwd(ctypes.byref(r), ctypes.byref(dy), ctypes.byref(x),
-               ctypes.byref(_qt(L.RECIPE_TENSORWISE, 320, 512)), None, None, 0x1000, None, 0,
+               ctypes.byref(_qt(L.RECIPE_TENSORWISE, 320, 512)), 0x1000, None, 0,
                None, None) == 3                               # W rows != dY cols
     assert bwd(ctypes.byref(r), ctypes.byref(dy), ctypes.byref(_qt(L.RECIPE_TENSORWISE, 128, 512)),
-               ctypes.byref(w), None, None, None, 0x1000, 0, None, None) == 3
-    assert bwd(ctypes.byref(r), None, ctypes.byref(x), ctypes.byref(w), None, None, 0x1000,
+               ctypes.byref(w), None, 0x1000, 0, None, None) == 3
+    assert bwd(ctypes.byref(r), None, ctypes.byref(x), ctypes.byref(w), 0x1000,
                0x2000, 0, None, None) == 1
+    # --fp8-wgrad off needs column copies made under that recipe (bf16 transposes)
+    r_off = _rec(kind=L.RECIPE_TENSORWISE, wgrad=0)
+    assert bwd(ctypes.byref(r_off), ctypes.byref(dy), ctypes.byref(x), ctypes.byref(w), None,
+               0x1000, 0, None, None) == 4
 
 
 def test_mlp_entry_checks(lib):

@@ -157,3 +157,64 @@ def test_full_size_mxfp8_fprop_sampled():
     assert ok, err
     ok, err = gemm_f32_normwise(y32.cpu().numpy()[rows], ref)
     assert ok, err
+
+
+# ------------------------------------------------------------------ --fp8-wgrad off
+
+@pytest.mark.parametrize("kind", ["tensorwise", "delayed", "mxfp8", "blockwise"])
+@pytest.mark.parametrize("M,N,K", [(256, 384, 512), (512, 256, 128), (640, 512, 384)])
+@pytest.mark.parametrize("fp32", [False, True])
+def test_wgrad_bf16(kind, M, N, K, fp32):
+    """With fp8_wgrad off the column copies of X and dY are bf16 transposes and wgrad is a
+    bf16 GEMM: dW = dY^T X summed in fp32, against the oracle's fp64 sum of the bf16 values."""
+    rec = F.Recipe(kind=kind, fp8_wgrad=False)
+    xb = bf16_bits_normal(M, K, seed=51)
+    dyb = bf16_bits_normal(M, N, seed=52, sigma=1e-3)
+    xq = F.quantize(rec, to_dev_bf16(xb), "activation")
+    dyq = F.quantize(rec, to_dev_bf16(dyb), "grad")
+    assert xq.col_bf16 == 1 and np.array_equal(from_dev_bf16(xq.col), xb.T)
+    assert np.array_equal(from_dev_bf16(dyq.col), dyb.T)
+    _, dw = F.linear_bwd(rec, dyq, xq, None, want_dx=False, fp32=fp32)
+    torch.cuda.synchronize()
+    ref = O.bf16_gemm_tn_f64(np.ascontiguousarray(dyb.T), np.ascontiguousarray(xb.T))
+    _check(dw, ref, fp32)
+
+
+def test_wgrad_bf16_with_fp8_dgrad():
+    """Mixed backward: dgrad stays FP8 (weight column copy) while wgrad runs in bf16."""
+    rec = F.Recipe(kind="mxfp8", fp8_wgrad=False)
+    M, N, K = 384, 256, 512
+    xb = bf16_bits_normal(M, K, seed=53)
+    wb = bf16_bits_normal(N, K, seed=54, sigma=0.02)
+    dyb = bf16_bits_normal(M, N, seed=55, sigma=1e-3)
+    xq, wq, dyq = (F.quantize(rec, to_dev_bf16(b), r)
+                   for b, r in ((xb, "activation"), (wb, "weight"), (dyb, "grad")))
+    assert wq.col_bf16 == 0
+    dx, dw = F.linear_bwd(rec, dyq, xq, wq)
+    torch.cuda.synchronize()
+    _check(dx, O.gemm_tn_f64(_oracle_deq("mxfp8", dyb, "grad", "row"),
+                             _oracle_deq("mxfp8", wb, "weight", "col")), False)
+    _check(dw, O.bf16_gemm_tn_f64(np.ascontiguousarray(dyb.T), np.ascontiguousarray(xb.T)), False)
+
+
+def test_full_size_blockwise_fwd_dgrad_wgrad_sampled():
+    """Blockwise fwd + dgrad + wgrad at 4096 x 4096 x 4096 (X 1x128, W 128x128, dY N(0,1e-3)),
+    in the benchmark's launch configuration; the oracle sums sampled output rows."""
+    rec = F.Recipe(kind="blockwise")
+    xb = bf16_bits_normal(4096, 4096, seed=0, stream=0)
+    wb = bf16_bits_normal(4096, 4096, seed=0, stream=1, sigma=0.02)
+    dyb = bf16_bits_normal(4096, 4096, seed=0, stream=2, sigma=1e-3)
+    xq, wq, dyq = (F.quantize(rec, to_dev_bf16(b), r)
+                   for b, r in ((xb, "activation"), (wb, "weight"), (dyb, "grad")))
+    y = F.linear_fwd(rec, xq, wq)
+    dx, dw = F.linear_bwd(rec, dyq, xq, wq)
+    torch.cuda.synchronize()
+    rows = _sample_rows(4096)
+    qx, qw, qd = (O.quantize_blockwise_1x128(xb), O.quantize_blockwise_128x128(wb),
+                  O.quantize_blockwise_1x128(dyb))
+    d1 = lambda q, c: O.dequant_1x128(q[c], q[c + "_scale_inv"])  # noqa: E731
+    d2 = lambda q, c: O.dequant_128x128(q[c], q[c + "_scale_inv"])  # noqa: E731
+    for got, a, b in ((y, d1(qx, "row"), d2(qw, "row")), (dx, d1(qd, "row"), d2(qw, "col")),
+                      (dw, d1(qd, "col"), d1(qx, "col"))):
+        ok, err = gemm_bf16_close(from_dev_bf16(got)[rows], O.gemm_tn_f64(a[rows], b))
+        assert ok, err
