@@ -162,7 +162,7 @@ def test_full_size_mxfp8_fprop_sampled():
 # ------------------------------------------------------------------ --fp8-wgrad off
 
 @pytest.mark.parametrize("kind", ["tensorwise", "delayed", "mxfp8", "blockwise"])
-@pytest.mark.parametrize("M,N,K", [(256, 384, 512), (512, 256, 128), (640, 512, 384)])
+@pytest.mark.parametrize("M,N,K", [(256, 384, 512), (512, 256, 128), (640, 512, 384), (256, 128, 256)])
 @pytest.mark.parametrize("fp32", [False, True])
 def test_wgrad_bf16(kind, M, N, K, fp32):
     """With fp8_wgrad off the column copies of X and dY are bf16 transposes and wgrad is a
