@@ -21,6 +21,13 @@ namespace fp8lin {
 enum QMode : int { Q_TENSOR = 0, Q_MX = 1, Q_BW1x128 = 2, Q_BW128 = 3 };
 enum QEpi : int { EPI_NONE = 0, EPI_GELU = 1, EPI_DGELU = 2 };
 
+// GeLU tables (see gelu_table_lookup / dgelu_table_lookup), between the control block and the
+// tile buffers for the MLP kernels.
+constexpr int kGeluExpLo = -20, kGeluExps = 24;       // table covers |h| in [2^-20, 2^4)
+constexpr int kGeluEntries = kGeluExps * 128 * 2;     // bf16 input: 7-bit mantissa, sign
+constexpr int kDgeluEntries = kGeluExps * 8 * 2;      // E4M3-derived input: 3-bit mantissa
+constexpr uint32_t kQTableBytes = 12288;              // >= 2 * kGeluEntries, 4 * kDgeluEntries
+
 struct QuantParams {
   const uint16_t* x;          // [R][C] bf16 (h for GELU, da for DGELU)
   int64_t R, C;
@@ -92,6 +99,31 @@ __device__ __forceinline__ float gelu_grad_f32(float h) {
   return fmaf(h, g, c);
 }
 
+// gelu over bf16 inputs through the CTA's shared-memory table: every bf16 h with |h| in
+// [2^-20, 2^4) has an entry holding bf16(gelu_f32(h)), so the lookup returns exactly what the
+// direct evaluation would; other inputs (tiny, large, Inf/NaN) are evaluated directly.
+__device__ __forceinline__ uint32_t gelu_table_lookup(const void* table, uint32_t hb) {
+  const uint32_t e = ((hb >> 7) & 0xFFu) - uint32_t(kGeluExpLo + 127);
+  if (e < uint32_t(kGeluExps)) {
+    const uint32_t idx = (e << 8) | ((hb & 0x7Fu) << 1) | (hb >> 15);
+    return reinterpret_cast<const uint16_t*>(table)[idx];
+  }
+  return bf16_rn_bits(gelu_f32(__uint_as_float(hb << 16)));
+}
+// gelu'(h) for h decoded from an E4M3 code times a power of two (at most 3 mantissa bits):
+// table entries hold gelu_grad_f32 of each such value with |h| in [2^-20, 2^4); zero gives 1/2;
+// anything else is evaluated directly.
+__device__ __forceinline__ float dgelu_table_lookup(const void* table, float h) {
+  const uint32_t bits = __float_as_uint(h);
+  const uint32_t e = ((bits >> 23) & 0xFFu) - uint32_t(kGeluExpLo + 127);
+  if (e < uint32_t(kGeluExps)) {
+    const uint32_t idx = (e << 4) | (((bits >> 20) & 7u) << 1) | (bits >> 31);
+    return reinterpret_cast<const float*>(table)[idx];
+  }
+  if ((bits & 0x7FFFFFFFu) == 0u) return 0.5f;
+  return gelu_grad_f32(h);
+}
+
 // Max of the 15-bit magnitudes of the eight bf16 in a vector.
 __device__ __forceinline__ uint32_t vec_amax_bits(uint4 v) {
   uint32_t m = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(0u, v.x), v.y), v.z), v.w);
@@ -130,17 +162,22 @@ struct QuantCtl {
   uint64_t bar[4];                  // TMA completion, one per buffer
   int abort_flag;
 };
-constexpr int kQBufs = 3;
 constexpr uint32_t kQCtlBytes = 5120;
+template <int EPI>
+__host__ __device__ constexpr int quant_bufs() { return EPI == EPI_NONE ? 3 : 2; }
+template <int EPI>
+__host__ __device__ constexpr uint32_t quant_tiles_off() {
+  return kQCtlBytes + (EPI == EPI_NONE ? 0u : kQTableBytes);
+}
 constexpr uint32_t kQTileBytes = 32768;
 static_assert(sizeof(QuantCtl) <= kQCtlBytes, "control block too large");
 constexpr uint64_t kQuantWaitBudget = 4000000000ull;   // ~2 s at 2 GHz
 
 template <int MODE>
 __host__ __device__ constexpr bool uses_code_tile() { return MODE == Q_TENSOR || MODE == Q_BW128; }
-template <int MODE>
+template <int MODE, int EPI>
 __host__ __device__ constexpr uint32_t quant_smem_bytes() {
-  return 1024 + kQCtlBytes + kQBufs * kQTileBytes;
+  return 1024 + quant_tiles_off<EPI>() + quant_bufs<EPI>() * kQTileBytes;
 }
 template <int MODE, int EPI>
 __host__ __device__ constexpr int quant_ctas_per_sm() { return 2; }
@@ -159,7 +196,8 @@ __device__ __forceinline__ uint32_t swz(uint32_t r, uint32_t c) {
 //   MXFP8 and 1x128); per-tensor and 128x128 scales transpose the row codes instead.
 template <int MODE, int EPI>
 __device__ __forceinline__ void quantize_one_tile(const QuantParams& p, QuantCtl& S,
-                                                  uint8_t* tile, uint8_t* codes, int tile_id,
+                                                  uint8_t* tile, uint8_t* codes,
+                                                  const void* table, int tile_id,
                                                   float s_tensor, bool tensor_nan) {
   const int t = threadIdx.x;
   const int warp = t >> 5, lane = t & 31;
@@ -211,8 +249,8 @@ __device__ __forceinline__ void quantize_one_tile(const QuantParams& p, QuantCtl
         }
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          w[i][k] = bf16_rn_bits(gelu_f32(bf16_lo(w[i][k]))) |
-                    (bf16_rn_bits(gelu_f32(bf16_hi(w[i][k]))) << 16);
+          w[i][k] = gelu_table_lookup(table, w[i][k] & 0xFFFFu) |
+                    (gelu_table_lookup(table, w[i][k] >> 16) << 16);
       } else {
         // dh = bf16(da * gelu'(h)), h decoded from its MXFP8 row copy
         if (ok) {
@@ -223,8 +261,8 @@ __device__ __forceinline__ void quantize_one_tile(const QuantParams& p, QuantCtl
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const float2 hv = e4m3x2_to_f2(uint16_t(cw[k >> 1] >> (16 * (k & 1))));
-            const float d0 = __fmul_rn(bf16_lo(w[i][k]), gelu_grad_f32(__fmul_rn(hv.x, hs)));
-            const float d1 = __fmul_rn(bf16_hi(w[i][k]), gelu_grad_f32(__fmul_rn(hv.y, hs)));
+            const float d0 = __fmul_rn(bf16_lo(w[i][k]), dgelu_table_lookup(table, __fmul_rn(hv.x, hs)));
+            const float d1 = __fmul_rn(bf16_hi(w[i][k]), dgelu_table_lookup(table, __fmul_rn(hv.y, hs)));
             w[i][k] = bf16_rn_bits(d0) | (bf16_rn_bits(d1) << 16);
           }
         } else {
@@ -488,7 +526,9 @@ __global__ void __launch_bounds__(256, quant_ctas_per_sm<MODE, EPI>())
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(qsm_raw) + 1023) & ~uintptr_t(1023));
   QuantCtl& S = *reinterpret_cast<QuantCtl*>(base);
-  uint8_t* tiles = base + kQCtlBytes;
+  constexpr int kQBufs = quant_bufs<EPI>();
+  uint8_t* tiles = base + quant_tiles_off<EPI>();
+  void* table = base + kQCtlBytes;
   const int t = threadIdx.x;
   const int tiles_r = int((p.R + 127) >> 7);
   const int n_tiles = tiles_r * p.tiles_c;
@@ -536,6 +576,25 @@ __global__ void __launch_bounds__(256, quant_ctas_per_sm<MODE, EPI>())
       if (tl < n_tiles) issue(tl, j);
     }
   }
+  // MLP kernels: fill the GeLU table while the first tiles are in flight
+  if constexpr (EPI == EPI_GELU) {
+    uint16_t* tb = reinterpret_cast<uint16_t*>(table);
+    for (int idx = t; idx < kGeluEntries; idx += 256) {
+      const uint32_t bits = (uint32_t(idx & 1) << 15) |
+                            (uint32_t((idx >> 8) + kGeluExpLo + 127) << 7) | uint32_t((idx >> 1) & 0x7F);
+      tb[idx] = uint16_t(bf16_rn_bits(gelu_f32(__uint_as_float(bits << 16))));
+    }
+  } else if constexpr (EPI == EPI_DGELU) {
+    float* tb = reinterpret_cast<float*>(table);
+    for (int idx = t; idx < kDgeluEntries; idx += 256) {
+      const uint32_t bits = (uint32_t(idx & 1) << 31) |
+                            (uint32_t((idx >> 4) + kGeluExpLo + 127) << 23) |
+                            (uint32_t((idx >> 1) & 7) << 20);
+      tb[idx] = gelu_grad_f32(__uint_as_float(bits));
+    }
+  }
+  if constexpr (EPI != EPI_NONE) __syncthreads();
+
   int tile = blockIdx.x;
   for (int i = 0; tile < n_tiles; ++i, tile += gridDim.x) {
     const int b = i % kQBufs;
@@ -543,7 +602,7 @@ __global__ void __launch_bounds__(256, quant_ctas_per_sm<MODE, EPI>())
     if (t == 0 && ahead < n_tiles) issue(ahead, (i + kQBufs - 1) % kQBufs);
     if (!quant_wait(S, b, uint32_t(i / kQBufs) & 1u, p.status)) break;
     uint8_t* buf = tiles + b * kQTileBytes;
-    quantize_one_tile<MODE, EPI>(p, S, buf, buf, tile, s_tensor, tensor_nan);
+    quantize_one_tile<MODE, EPI>(p, S, buf, buf, table, tile, s_tensor, tensor_nan);
     __syncthreads();                                 // buffer b is refilled next iteration
   }
   if (*reinterpret_cast<volatile int*>(&S.abort_flag)) {
@@ -664,7 +723,7 @@ static cudaError_t launch_tiles(const QuantParams& p, cudaStream_t st) {
   const int n = tiles_r * p.tiles_c;
   CUtensorMap map;
   if (!make_tmap_2d(&map, p.x, 2, p.C, p.R, 64, kTile, true)) return cudaErrorInvalidValue;
-  constexpr int smem = int(quant_smem_bytes<MODE>());
+  constexpr int smem = int(quant_smem_bytes<MODE, EPI>());
   static bool attr = false;
   if (!attr) {
     const cudaError_t e = cudaFuncSetAttribute(quantize_tile_kernel<MODE, EPI>,

@@ -125,3 +125,37 @@ def test_mlp_block_small():
 
 def test_mlp_block_multi_tile():
     _mlp(384, 512, 1024, seed=1)
+
+
+def _all_bf16():
+    return np.arange(65536, dtype=np.uint32).astype(np.uint16).reshape(256, 256)
+
+
+def _ulp_ok(gpu_bits, ref_bits):
+    g = O.bf16_to_f32(gpu_bits)
+    r = O.bf16_to_f32(ref_bits)
+    nan = np.isnan(r)
+    assert np.array_equal(np.isnan(g), nan)
+    return int(np.max(_ulp_diff(gpu_bits[~nan], ref_bits[~nan])))
+
+
+def test_gelu_every_bf16_input():
+    """a = gelu(h) for all 65,536 bf16 bit patterns (table range, tiny, huge, Inf, NaN)."""
+    rec = F.Recipe(kind="mxfp8")
+    hb = _all_bf16()
+    _, _, a_bf16 = F.gelu_quantize(rec, to_dev_bf16(hb), want_a_bf16=True)
+    torch.cuda.synchronize()
+    assert _ulp_ok(from_dev_bf16(a_bf16), O.gelu_bf16(hb)) <= 1
+
+
+def test_dgelu_every_bf16_input():
+    """dh = 1 * gelu'(deq(h_fp8)) with h running over all 65,536 bf16 patterns."""
+    rec = F.Recipe(kind="mxfp8")
+    hb = _all_bf16()
+    ones = np.full(hb.shape, 0x3F80, np.uint16)
+    _, h_q, _ = F.gelu_quantize(rec, to_dev_bf16(hb))
+    _, dh = F.dgelu_quantize(rec, to_dev_bf16(ones), h_q, want_dh_bf16=True)
+    torch.cuda.synchronize()
+    qh = O.quantize_mxfp8(hb, want_col=False)
+    ref = O.dgelu_bf16(ones, qh["row"], qh["row_scale"])
+    assert _ulp_ok(from_dev_bf16(dh), ref) <= 1
