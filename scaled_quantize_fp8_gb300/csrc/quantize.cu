@@ -23,10 +23,15 @@ enum QEpi : int { EPI_NONE = 0, EPI_GELU = 1, EPI_DGELU = 2 };
 
 // GeLU tables (see gelu_table_lookup / dgelu_table_lookup), between the control block and the
 // tile buffers for the MLP kernels.
-constexpr int kGeluExpLo = -20, kGeluExps = 24;       // table covers |h| in [2^-20, 2^4)
+constexpr int kGeluExpLo = -14, kGeluExps = 18;       // gelu table: |h| in [2^-14, 2^4)
 constexpr int kGeluEntries = kGeluExps * 128 * 2;     // bf16 input: 7-bit mantissa, sign
-constexpr int kDgeluEntries = kGeluExps * 8 * 2;      // E4M3-derived input: 3-bit mantissa
-constexpr uint32_t kQTableBytes = 12288;              // >= 2 * kGeluEntries, 4 * kDgeluEntries
+constexpr int kDgeluExpLo = -20, kDgeluExps = 24;     // gelu' table: |h| in [2^-20, 2^4)
+constexpr int kDgeluEntries = kDgeluExps * 8 * 2;     // E4M3-derived input: 3-bit mantissa
+// table bytes, rounded so the tile buffers behind them stay 1024-byte aligned
+template <int EPI>
+__host__ __device__ constexpr uint32_t quant_table_bytes() {
+  return EPI == EPI_GELU ? 9216u : (EPI == EPI_DGELU ? 2048u : 0u);
+}
 
 struct QuantParams {
   const uint16_t* x;          // [R][C] bf16 (h for GELU, da for DGELU)
@@ -94,13 +99,17 @@ __device__ __forceinline__ float phi_cdf(float h, float* gauss) {
 // gelu(h) = h Phi(h); gelu'(h) = Phi(h) + h phi(h), phi(h) = exp(-h^2/2) / sqrt(2 pi).
 __device__ __forceinline__ float gelu_f32(float h) { return h * phi_cdf(h, nullptr); }
 __device__ __forceinline__ float gelu_grad_f32(float h) {
+  // A dequantised FP8 value can exceed the fp32 range (a code near 448 times 2^120); its
+  // gelu' is then the limit: 1 above, +0 below. (Inf/NaN inputs never get here as such: their
+  // MXFP8 block carries the NaN scale.)
+  if (fabsf(h) > 3.402823466e38f) return h > 0.0f ? 1.0f : 0.0f;
   float g;
   const float c = phi_cdf(h, &g);
   return fmaf(h, g, c);
 }
 
 // gelu over bf16 inputs through the CTA's shared-memory table: every bf16 h with |h| in
-// [2^-20, 2^4) has an entry holding bf16(gelu_f32(h)), so the lookup returns exactly what the
+// [2^-14, 2^4) has an entry holding bf16(gelu_f32(h)), so the lookup returns exactly what the
 // direct evaluation would; other inputs (tiny, large, Inf/NaN) are evaluated directly.
 __device__ __forceinline__ uint32_t gelu_table_lookup(const void* table, uint32_t hb) {
   const uint32_t e = ((hb >> 7) & 0xFFu) - uint32_t(kGeluExpLo + 127);
@@ -115,8 +124,8 @@ __device__ __forceinline__ uint32_t gelu_table_lookup(const void* table, uint32_
 // anything else is evaluated directly.
 __device__ __forceinline__ float dgelu_table_lookup(const void* table, float h) {
   const uint32_t bits = __float_as_uint(h);
-  const uint32_t e = ((bits >> 23) & 0xFFu) - uint32_t(kGeluExpLo + 127);
-  if (e < uint32_t(kGeluExps)) {
+  const uint32_t e = ((bits >> 23) & 0xFFu) - uint32_t(kDgeluExpLo + 127);
+  if (e < uint32_t(kDgeluExps)) {
     const uint32_t idx = (e << 4) | (((bits >> 20) & 7u) << 1) | (bits >> 31);
     return reinterpret_cast<const float*>(table)[idx];
   }
@@ -164,10 +173,10 @@ struct QuantCtl {
 };
 constexpr uint32_t kQCtlBytes = 5120;
 template <int EPI>
-__host__ __device__ constexpr int quant_bufs() { return EPI == EPI_NONE ? 3 : 2; }
+__host__ __device__ constexpr int quant_bufs() { return 3; }
 template <int EPI>
 __host__ __device__ constexpr uint32_t quant_tiles_off() {
-  return kQCtlBytes + (EPI == EPI_NONE ? 0u : kQTableBytes);
+  return kQCtlBytes + quant_table_bytes<EPI>();
 }
 constexpr uint32_t kQTileBytes = 32768;
 static_assert(sizeof(QuantCtl) <= kQCtlBytes, "control block too large");
@@ -222,6 +231,21 @@ __device__ __forceinline__ void quantize_one_tile(const QuantParams& p, QuantCtl
   }
 
   // ---- MLP epilogues: turn the input into the tensor to quantise (and write it back)
+  uint4 hcodes[4];
+  uint32_t hscale[4];
+  if constexpr (EPI == EPI_DGELU) {
+    // all of this lane's h codes and scales in flight together
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t r = 32u * i + 4u * warp + rr;
+      hcodes[i] = make_uint4(0u, 0u, 0u, 0u);
+      hscale[i] = 127u;
+      if ((r0 + r < R) && col_ok) {
+        hcodes[i] = ldg_nc_v4(p.aux_row + (r0 + r) * C + c0 + ccol);
+        hscale[i] = __ldg(p.aux_scale + mx_scale_offset(r0 + r, (c0 + ccol) >> 5, C));
+      }
+    }
+  }
   if constexpr (EPI != EPI_NONE) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -252,10 +276,10 @@ __device__ __forceinline__ void quantize_one_tile(const QuantParams& p, QuantCtl
           w[i][k] = gelu_table_lookup(table, w[i][k] & 0xFFFFu) |
                     (gelu_table_lookup(table, w[i][k] >> 16) << 16);
       } else {
-        // dh = bf16(da * gelu'(h)), h decoded from its MXFP8 row copy
+        // dh = bf16(da * gelu'(h)), h decoded from its MXFP8 row copy (loaded up front)
         if (ok) {
-          const uint4 hc = *reinterpret_cast<const uint4*>(p.aux_row + off);
-          const uint32_t sb = p.aux_scale[mx_scale_offset(r0 + r, (c0 + ccol) >> 5, C)];
+          const uint4 hc = hcodes[i];
+          const uint32_t sb = hscale[i];
           const float hs = sb == 0xFFu ? __uint_as_float(0x7FC00000u) : exp2i(int(sb) - 127);
           const uint32_t cw[4] = {hc.x, hc.y, hc.z, hc.w};
 #pragma unroll
@@ -588,7 +612,7 @@ __global__ void __launch_bounds__(256, quant_ctas_per_sm<MODE, EPI>())
     float* tb = reinterpret_cast<float*>(table);
     for (int idx = t; idx < kDgeluEntries; idx += 256) {
       const uint32_t bits = (uint32_t(idx & 1) << 31) |
-                            (uint32_t((idx >> 4) + kGeluExpLo + 127) << 23) |
+                            (uint32_t((idx >> 4) + kDgeluExpLo + 127) << 23) |
                             (uint32_t((idx >> 1) & 7) << 20);
       tb[idx] = gelu_grad_f32(__uint_as_float(bits));
     }
