@@ -108,6 +108,13 @@ __device__ __forceinline__ float gelu_grad_f32(float h) {
   return fmaf(h, g, c);
 }
 
+// Direct evaluations for inputs outside the tables: rare, kept out of line so the unrolled
+// tile loop stays small enough for the instruction cache.
+__device__ __noinline__ uint32_t gelu_bf16_direct(uint32_t hb) {
+  return bf16_rn_bits(gelu_f32(__uint_as_float(hb << 16)));
+}
+__device__ __noinline__ float gelu_grad_direct(float h) { return gelu_grad_f32(h); }
+
 // gelu over bf16 inputs through the CTA's shared-memory table: every bf16 h with |h| in
 // [2^-14, 2^4) has an entry holding bf16(gelu_f32(h)), so the lookup returns exactly what the
 // direct evaluation would; other inputs (tiny, large, Inf/NaN) are evaluated directly.
@@ -117,7 +124,7 @@ __device__ __forceinline__ uint32_t gelu_table_lookup(const void* table, uint32_
     const uint32_t idx = (e << 8) | ((hb & 0x7Fu) << 1) | (hb >> 15);
     return reinterpret_cast<const uint16_t*>(table)[idx];
   }
-  return bf16_rn_bits(gelu_f32(__uint_as_float(hb << 16)));
+  return gelu_bf16_direct(hb);
 }
 // gelu'(h) for h decoded from an E4M3 code times a power of two (at most 3 mantissa bits):
 // table entries hold gelu_grad_f32 of each such value with |h| in [2^-20, 2^4); zero gives 1/2;
@@ -130,7 +137,7 @@ __device__ __forceinline__ float dgelu_table_lookup(const void* table, float h) 
     return reinterpret_cast<const float*>(table)[idx];
   }
   if ((bits & 0x7FFFFFFFu) == 0u) return 0.5f;
-  return gelu_grad_f32(h);
+  return gelu_grad_direct(h);
 }
 
 // Max of the 15-bit magnitudes of the eight bf16 in a vector.
