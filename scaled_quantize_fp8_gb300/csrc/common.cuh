@@ -142,6 +142,24 @@ __host__ __device__ __forceinline__ int64_t mx_scale_offset(int64_t r, int64_t k
          (kb & 3);
 }
 
+// One 32-byte global store (256-bit vector; the address must be 32-byte aligned).
+__device__ __forceinline__ void stg_v8(void* p, uint4 a, uint4 b) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a.x),
+               "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+               : "memory");
+}
+// A 32-byte segment whose halves may fall outside the tensor: whole-sector store when
+// allowed (aligned and both halves in range), else one 16-byte store per valid half.
+__device__ __forceinline__ void store_seg32(void* p, uint4 a, uint4 b, bool lo_ok, bool hi_ok,
+                                            bool v8) {
+  if (v8 && lo_ok && hi_ok) {
+    stg_v8(p, a, b);
+  } else {
+    if (lo_ok) reinterpret_cast<uint4*>(p)[0] = a;
+    if (hi_ok) reinterpret_cast<uint4*>(p)[1] = b;
+  }
+}
+
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"

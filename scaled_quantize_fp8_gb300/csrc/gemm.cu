@@ -102,25 +102,31 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 // Store one thread's row segment of 128 fp32 values (columns n .. n+127 of row m).
 __device__ __forceinline__ void store_row128(const GemmParams& p, int m, int n, const float* v) {
   if (m >= p.M) return;
+  const bool v8 = p.d_v8 != 0;
   if (p.d_fp32) {
     float* dst = reinterpret_cast<float*>(p.D) + int64_t(m) * p.ldd + n;
 #pragma unroll
     for (int j = 0; j < 128; j += 8) {
-      if (n + j < p.N) {
-        reinterpret_cast<float4*>(dst + j)[0] = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-        reinterpret_cast<float4*>(dst + j)[1] =
-            make_float4(v[j + 4], v[j + 5], v[j + 6], v[j + 7]);
-      }
+      // N is a multiple of 16, so a segment starting inside the row ends inside it
+      const bool ok = n + j < p.N;
+      store_seg32(dst + j,
+                  make_uint4(__float_as_uint(v[j]), __float_as_uint(v[j + 1]),
+                             __float_as_uint(v[j + 2]), __float_as_uint(v[j + 3])),
+                  make_uint4(__float_as_uint(v[j + 4]), __float_as_uint(v[j + 5]),
+                             __float_as_uint(v[j + 6]), __float_as_uint(v[j + 7])),
+                  ok, ok, v8);
     }
   } else {
     uint16_t* dst = reinterpret_cast<uint16_t*>(p.D) + int64_t(m) * p.ldd + n;
 #pragma unroll
-    for (int j = 0; j < 128; j += 8) {
-      if (n + j < p.N) {
-        *reinterpret_cast<uint4*>(dst + j) =
-            make_uint4(pack_bf16x2(v[j], v[j + 1]), pack_bf16x2(v[j + 2], v[j + 3]),
-                       pack_bf16x2(v[j + 4], v[j + 5]), pack_bf16x2(v[j + 6], v[j + 7]));
-      }
+    for (int j = 0; j < 128; j += 16) {
+      const bool ok = n + j < p.N;
+      store_seg32(dst + j,
+                  make_uint4(pack_bf16x2(v[j], v[j + 1]), pack_bf16x2(v[j + 2], v[j + 3]),
+                             pack_bf16x2(v[j + 4], v[j + 5]), pack_bf16x2(v[j + 6], v[j + 7])),
+                  make_uint4(pack_bf16x2(v[j + 8], v[j + 9]), pack_bf16x2(v[j + 10], v[j + 11]),
+                             pack_bf16x2(v[j + 12], v[j + 13]), pack_bf16x2(v[j + 14], v[j + 15])),
+                  ok, ok, v8);
     }
   }
 }
@@ -504,20 +510,23 @@ static cudaError_t launch_mode(const GemmLaunch& g, cudaStream_t st) {
 
 cudaError_t gemm_launch(const GemmLaunch& g, cudaStream_t st) {
   if (g.p.M == 0 || g.p.N == 0) return cudaSuccess;
+  GemmLaunch gl = g;
+  const int64_t pitch = gl.p.ldd * (gl.p.d_fp32 ? 4 : 2);
+  gl.p.d_v8 = (reinterpret_cast<uintptr_t>(gl.p.D) % 32 == 0) && (pitch % 32 == 0);
   // CTA pairs whenever there are at least two 128-row halves to give them.
   // (Blockwise keeps the single CTA: its per-chunk promotion would couple the pair's
   // epilogues to every K step.)
-  const bool pair = g.p.M > kBM;
-  switch (g.mode) {
+  const bool pair = gl.p.M > kBM;
+  switch (gl.mode) {
     case G_TENSOR:
-      return pair ? launch_mode<G_TENSOR, 1, 1>(g, st) : launch_mode<G_TENSOR, 1, 0>(g, st);
+      return pair ? launch_mode<G_TENSOR, 1, 1>(gl, st) : launch_mode<G_TENSOR, 1, 0>(gl, st);
     case G_MX:
-      return (pair && g.p.N > kBM) ? launch_mode<G_MX, 1, 1>(g, st)
-                                   : launch_mode<G_MX, 1, 0>(g, st);
+      return (pair && gl.p.N > kBM) ? launch_mode<G_MX, 1, 1>(gl, st)
+                                   : launch_mode<G_MX, 1, 0>(gl, st);
     case G_BLOCK:
-      return g.p.b_is_128 ? launch_mode<G_BLOCK, 1, 0>(g, st) : launch_mode<G_BLOCK, 0, 0>(g, st);
+      return gl.p.b_is_128 ? launch_mode<G_BLOCK, 1, 0>(gl, st) : launch_mode<G_BLOCK, 0, 0>(gl, st);
     case G_BF16:
-      return pair ? launch_mode<G_BF16, 1, 1>(g, st) : launch_mode<G_BF16, 1, 0>(g, st);
+      return pair ? launch_mode<G_BF16, 1, 1>(gl, st) : launch_mode<G_BF16, 1, 0>(gl, st);
   }
   return cudaErrorInvalidValue;
 }

@@ -41,6 +41,7 @@ struct GemmParams {
   void* D;
   int64_t ldd;
   int d_fp32;
+  int d_v8;                 // D and its row pitch are 32-byte aligned (256-bit stores)
   const float* a_sinv;      // G_TENSOR: per-tensor dequantisation factors
   const float* b_sinv;
   const uint8_t* sfa;       // G_MX: E8M0 scales in the tiled atom order

@@ -40,6 +40,7 @@ struct QuantParams {
   uint8_t* row;               // [R][C] codes or null
   uint8_t* col;               // [C][R] codes (or bf16 when col_bf16), or null
   bool col_bf16;              // column copy = bf16 transpose (wgrad kept in bf16)
+  bool col_v8;                // column copy rows start on 32-byte boundaries (256-bit stores)
   void* row_scale;
   void* col_scale;
   // per-tensor recipes
@@ -400,43 +401,40 @@ __device__ __forceinline__ void quantize_one_tile(const QuantParams& p, QuantCtl
         for (int k = 0; k < 2; ++k) {
           const uint32_t* src = k == 0 ? lo : hi;
           uint16_t* d = dst + k * R;
-          if (rr0 < R) {
-            reinterpret_cast<uint4*>(d)[0] = make_uint4(src[0], src[1], src[2], src[3]);
-            reinterpret_cast<uint4*>(d)[1] = make_uint4(src[4], src[5], src[6], src[7]);
-          }
-          if (rr0 + 16 < R) {
-            reinterpret_cast<uint4*>(d)[2] = make_uint4(src[8], src[9], src[10], src[11]);
-            reinterpret_cast<uint4*>(d)[3] = make_uint4(src[12], src[13], src[14], src[15]);
-          }
+          const bool ok0 = rr0 < R, ok1 = rr0 + 16 < R;
+          store_seg32(d, make_uint4(src[0], src[1], src[2], src[3]),
+                      make_uint4(src[4], src[5], src[6], src[7]), ok0, ok0, p.col_v8);
+          store_seg32(d + 16, make_uint4(src[8], src[9], src[10], src[11]),
+                      make_uint4(src[12], src[13], src[14], src[15]), ok1, ok1, p.col_v8);
         }
       }
     } else if constexpr (uses_code_tile<MODE>()) {
-      // ---- column-wise copy = byte transpose of the row codes. Thread (c4, g): source
-      // columns 4 c4 .. 4 c4 + 3, rows 16 g .. 16 g + 15 (four 4x4 byte transposes).
-      const int c4 = t & 31, g = t >> 5;
-      uint32_t outw[4][4];
+      // ---- column-wise copy = byte transpose of the row codes. Thread (pp, q): source
+      // columns 2pp, 2pp+1 over rows 32q .. 32q+31; each transposed row segment is one
+      // 32-byte sector.
+      const int pp = t & 63, q = t >> 6;
+      const uint32_t chunk = uint32_t(pp) >> 3, bofs = 2u * (pp & 7);
+      uint32_t ca[8], cb[8];
 #pragma unroll
-      for (int blk = 0; blk < 4; ++blk) {
+      for (int j = 0; j < 8; ++j) {
         uint32_t x[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t r = 16u * g + 4u * blk + j;
-          x[j] = *reinterpret_cast<const uint32_t*>(codes + swz(r, c4 >> 2) + 4 * (c4 & 3));
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t r = 32u * q + 4u * j + k;
+          x[k] = *reinterpret_cast<const uint16_t*>(codes + swz(r, chunk) + bofs);
         }
-        const uint32_t t0 = __byte_perm(x[0], x[1], 0x5140), t1 = __byte_perm(x[0], x[1], 0x7362);
-        const uint32_t t2 = __byte_perm(x[2], x[3], 0x5140), t3 = __byte_perm(x[2], x[3], 0x7362);
-        outw[0][blk] = __byte_perm(t0, t2, 0x5410);
-        outw[1][blk] = __byte_perm(t0, t2, 0x7632);
-        outw[2][blk] = __byte_perm(t1, t3, 0x5410);
-        outw[3][blk] = __byte_perm(t1, t3, 0x7632);
+        const uint32_t lo = __byte_perm(x[0], x[1], 0x5410), hi = __byte_perm(x[2], x[3], 0x5410);
+        ca[j] = __byte_perm(lo, hi, 0x6420);
+        cb[j] = __byte_perm(lo, hi, 0x7531);
       }
-      const uint32_t rr0 = r0 + 16u * g;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint32_t c = c0 + 4u * c4 + k;
-        if (c < C && rr0 < R)
-          *reinterpret_cast<uint4*>(p.col + c * R + rr0) =
-              make_uint4(outw[k][0], outw[k][1], outw[k][2], outw[k][3]);
+      const uint32_t rr0 = r0 + 32u * q, cA = c0 + 2u * pp;
+      if (cA < C) {
+        uint8_t* dst = p.col + cA * R + rr0;
+        const bool ok0 = rr0 < R, ok1 = rr0 + 16 < R;
+        store_seg32(dst, make_uint4(ca[0], ca[1], ca[2], ca[3]), make_uint4(ca[4], ca[5], ca[6], ca[7]),
+                    ok0, ok1, p.col_v8);
+        store_seg32(dst + R, make_uint4(cb[0], cb[1], cb[2], cb[3]),
+                    make_uint4(cb[4], cb[5], cb[6], cb[7]), ok0, ok1, p.col_v8);
       }
     } else {
       // ---- column-wise copy re-quantised along the rows
@@ -500,11 +498,11 @@ __device__ __forceinline__ void quantize_one_tile(const QuantParams& p, QuantCtl
       const uint32_t cA = c0 + 2u * pp;
       if (cA < C) {
         uint8_t* dst = p.col + cA * R + rr0;
-        if (rr0 < R) *reinterpret_cast<uint4*>(dst) = make_uint4(ca[0], ca[1], ca[2], ca[3]);
-        if (rr0 + 16 < R) *reinterpret_cast<uint4*>(dst + 16) = make_uint4(ca[4], ca[5], ca[6], ca[7]);
-        dst += R;
-        if (rr0 < R) *reinterpret_cast<uint4*>(dst) = make_uint4(cb[0], cb[1], cb[2], cb[3]);
-        if (rr0 + 16 < R) *reinterpret_cast<uint4*>(dst + 16) = make_uint4(cb[4], cb[5], cb[6], cb[7]);
+        const bool ok0 = rr0 < R, ok1 = rr0 + 16 < R;
+        store_seg32(dst, make_uint4(ca[0], ca[1], ca[2], ca[3]), make_uint4(ca[4], ca[5], ca[6], ca[7]),
+                    ok0, ok1, p.col_v8);
+        store_seg32(dst + R, make_uint4(cb[0], cb[1], cb[2], cb[3]),
+                    make_uint4(cb[4], cb[5], cb[6], cb[7]), ok0, ok1, p.col_v8);
       }
     }
   }
@@ -749,7 +747,10 @@ size_t quantize_workspace_bytes(int kind, int64_t R, int64_t C) {
 }
 
 template <int MODE, int EPI>
-static cudaError_t launch_tiles(const QuantParams& p, cudaStream_t st) {
+static cudaError_t launch_tiles(QuantParams p, cudaStream_t st) {
+  const int64_t col_row_bytes = p.R * (p.col_bf16 ? 2 : 1);
+  p.col_v8 = p.col != nullptr && (reinterpret_cast<uintptr_t>(p.col) % 32 == 0) &&
+             (col_row_bytes % 32 == 0);
   const int tiles_r = int((p.R + 127) / 128);
   const int n = tiles_r * p.tiles_c;
   CUtensorMap map;
