@@ -2,9 +2,12 @@
 
 One step = one forward + backward pass of an MXFP8 transformer MLP block (8192 tokens,
 hidden 4096, ffn 16384), everything through the library's C ABI:
-    quantize X, W1, W2 (row + column copies) -> fc1 GEMM -> GeLU with its input kept in FP8
-    (fused with the MXFP8 quantize of the activation) -> fc2 GEMM -> quantize dY ->
-    fc2 dgrad + wgrad -> dGeLU (fused with the quantize of dh) -> fc1 dgrad + wgrad.
+    quantize X, W1, W2 (row + column copies) -> fc1 GEMM whose epilogue applies GeLU, keeps
+    its input h in FP8 and writes the MXFP8 copies of the activation -> fc2 GEMM -> quantize
+    dY -> fc2 dgrad (epilogue: dGeLU and the MXFP8 copies of dh) + fc2 wgrad -> fc1 dgrad +
+    wgrad.
+`--unfused` runs the same step with the GEMMs storing h and da in bf16 and the standalone
+GeLU / dGeLU quantize kernels in between.
 Metric: GEMM TFLOP/s of the whole step (quantize time included), plus the quantize kernels'
 algorithmic HBM GB/s. Inputs are seeded synthetic bf16 tensors resident in HBM (about 2 GB
 touched per step, far above the 129 MB L2). `e2e` repeats the step with the inputs copied
@@ -33,7 +36,8 @@ METRIC = "FP8 linear fwd+bwd TFLOPS (incl. quantize) vs FP8 peak; quantize HBM G
 TOKENS, HIDDEN, FFN = 8192, 4096, 16384
 GEMM_FLOPS = 6 * 2.0 * TOKENS * HIDDEN * FFN          # fc1, fc2 fwd; dgrad + wgrad of both
 WORKLOAD = "mxfp8_mlp_fwd_bwd tokens=8192 hidden=4096 ffn=16384"
-KERNELS_PER_STEP = 12                                 # 4 quantize, gelu, dgelu, 6 GEMMs
+KERNELS_PER_STEP = 10                                 # 4 quantize, 6 GEMMs (2 fused)
+KERNELS_PER_STEP_UNFUSED = 12                         # plus standalone gelu and dgelu
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FP8_OVER_BF16 = 2.0                                   # nominal dense fp8 / bf16 rate
@@ -112,8 +116,8 @@ class ClockSampler:
 class MlpStep:
     """Preallocated device buffers and the step itself (device-resident inputs)."""
 
-    def __init__(self, torch, F, dev):
-        self.torch, self.F, self.dev = torch, F, dev
+    def __init__(self, torch, F, dev, fused=True):
+        self.torch, self.F, self.dev, self.fused = torch, F, dev, fused
         from workloads import bf16_bits_normal
         self.rec = F.Recipe(kind="mxfp8")
         M, H, Fd = TOKENS, HIDDEN, FFN
@@ -136,9 +140,10 @@ class MlpStep:
         self.hq = e(self.rec, M, Fd, "activation", want_col=False, device=dev)
         self.dhq = e(self.rec, M, Fd, "grad", device=dev)
         bf = torch.bfloat16
-        self.hbuf = torch.empty((M, Fd), dtype=bf, device=dev)
+        if not fused:
+            self.hbuf = torch.empty((M, Fd), dtype=bf, device=dev)
+            self.da = torch.empty((M, Fd), dtype=bf, device=dev)
         self.y = torch.empty((M, H), dtype=bf, device=dev)
-        self.da = torch.empty((M, Fd), dtype=bf, device=dev)
         self.dw2 = torch.empty((H, Fd), dtype=bf, device=dev)
         self.dx = torch.empty((M, H), dtype=bf, device=dev)
         self.dw1 = torch.empty((Fd, H), dtype=bf, device=dev)
@@ -146,9 +151,11 @@ class MlpStep:
         self.h_out = {k: torch.empty(v.shape, dtype=bf).pin_memory() for k, v in self.outs.items()}
         # algorithmic bytes of the quantize kernels per step
         mx = lambda r, c, copies: r * c * (2 + copies + copies / 32.0)  # noqa: E731
-        self.quant_bytes = (mx(M, H, 2) + mx(Fd, H, 2) + mx(H, Fd, 2) + mx(M, H, 2)
-                            + M * Fd * (2 + 3 + 3 / 32.0)                # gelu: h in, a x2 + h x1
-                            + M * Fd * (2 + 1 + 1 / 32.0 + 2 + 2 / 32.0))  # dgelu: da, h_q in
+        self.quant_bytes = mx(M, H, 2) + mx(Fd, H, 2) + mx(H, Fd, 2) + mx(M, H, 2)
+        if not fused:
+            self.quant_bytes += (M * Fd * (2 + 3 + 3 / 32.0)                # gelu: h in, a x2 + h
+                                 + M * Fd * (2 + 1 + 1 / 32.0 + 2 + 2 / 32.0))  # dgelu
+        self.kernels_per_step = KERNELS_PER_STEP if fused else KERNELS_PER_STEP_UNFUSED
         self.stream = torch.cuda.current_stream(dev)
         self.events = []
 
@@ -169,15 +176,23 @@ class MlpStep:
         T("quant", lambda: F.quantize(rec, d["x"], "activation", out=self.xq))
         T("quant", lambda: F.quantize(rec, d["w1"], "weight", out=self.w1q))
         T("quant", lambda: F.quantize(rec, d["w2"], "weight", out=self.w2q))
-        T("gemm", lambda: F.linear_fwd(rec, self.xq, self.w1q, y=self.hbuf))
-        T("quant", lambda: F.gelu_quantize(rec, self.hbuf, a_q=self.aq, h_q=self.hq))
+        if self.fused:
+            T("gemm", lambda: F.linear_fwd_gelu(rec, self.xq, self.w1q, a_q=self.aq, h_q=self.hq))
+        else:
+            T("gemm", lambda: F.linear_fwd(rec, self.xq, self.w1q, y=self.hbuf))
+            T("quant", lambda: F.gelu_quantize(rec, self.hbuf, a_q=self.aq, h_q=self.hq))
         T("gemm", lambda: F.linear_fwd(rec, self.aq, self.w2q, y=self.y))
         T("quant", lambda: F.quantize(rec, d["dy"], "grad", out=self.dyq))
-        T("gemm", lambda: F.linear_bwd(rec, self.dyq, self.aq, self.w2q, want_dw=False,
-                                       dx=self.da))
+        if self.fused:
+            T("gemm", lambda: F.linear_dgrad_dgelu(rec, self.dyq, self.w2q, self.hq,
+                                                   dh_q=self.dhq))
+        else:
+            T("gemm", lambda: F.linear_bwd(rec, self.dyq, self.aq, self.w2q, want_dw=False,
+                                           dx=self.da))
         T("gemm", lambda: F.linear_bwd(rec, self.dyq, self.aq, self.w2q, want_dx=False,
                                        dw=self.dw2))
-        T("quant", lambda: F.dgelu_quantize(rec, self.da, self.hq, dh_q=self.dhq))
+        if not self.fused:
+            T("quant", lambda: F.dgelu_quantize(rec, self.da, self.hq, dh_q=self.dhq))
         T("gemm", lambda: F.linear_bwd(rec, self.dhq, self.xq, self.w1q, want_dw=False,
                                        dx=self.dx))
         T("gemm", lambda: F.linear_bwd(rec, self.dhq, self.xq, self.w1q, want_dx=False,
@@ -234,7 +249,7 @@ def run_ours(args):
     B.build()
     import scaled_quantize_fp8_gb300 as F
 
-    st = MlpStep(torch, F, dev)
+    st = MlpStep(torch, F, dev, fused=not args.unfused)
 
     def barrier():
         if world > 1:
@@ -292,6 +307,7 @@ def run_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "e4m3 (fp32 accumulate)", "data": "synthetic",
             "config": {"workload": WORKLOAD, "recipe": "mxfp8",
+                       "mlp_epilogues": "fused" if st.fused else "unfused",
                        "parallelism": "replicas" if world > 1 else "single",
                        "l2": "inputs larger than L2 (~2 GB touched per step)",
                        "gemm_flops_per_step": GEMM_FLOPS},
@@ -305,7 +321,7 @@ def run_ours(args):
                          "algorithmic_bytes_per_step": st.quant_bytes, "peak_source": src},
             "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s",
                     "h2d_bytes_per_step": st.h2d_bytes(), "d2h_bytes_per_step": st.d2h_bytes()},
-            "gpu_launches": KERNELS_PER_STEP * args.steps,
+            "gpu_launches": st.kernels_per_step * args.steps,
             "clocks": clk,
             "cpu_baseline": cpu,
         }
@@ -402,16 +418,33 @@ def run_profile_case(args):
     """Launch one kernel kind a few times on its own (for ncu captures; prints no JSON line).
     quant_mx / quant_tensorwise / quant_blockwise: X 16384 x 8192 bf16 (256 MiB, above L2).
     gemm_mx / gemm_tensorwise / gemm_blockwise: fprop 8192 x 4096 x 4096.
-    gelu_mx / dgelu_mx: the fused GeLU / dGeLU + MXFP8 quantize on h 8192 x 16384."""
+    gelu_mx / dgelu_mx: the standalone GeLU / dGeLU + MXFP8 quantize on h 8192 x 16384.
+    gemm_gelu_mx / gemm_dgelu_mx: fc1 with the GeLU epilogue (8192 x 16384 x 4096) and fc2's
+    dgrad with the dGeLU epilogue (8192 x 16384 x 4096)."""
     import torch
     import scaled_quantize_fp8_gb300 as F
     from scaled_quantize_fp8_gb300 import build as B
     B.build()
     case = args.profile
-    kind = {"mx": "mxfp8"}.get(case.split("_", 1)[1], case.split("_", 1)[1])
+    kind = {"mx": "mxfp8"}.get(case.rsplit("_", 1)[1], case.rsplit("_", 1)[1])
     rec = F.Recipe(kind=kind)
     g = torch.Generator(device="cuda").manual_seed(0)
-    if case in ("gelu_mx", "dgelu_mx"):
+    if case in ("gemm_gelu_mx", "gemm_dgelu_mx"):
+        M, H, Fd = TOKENS, HIDDEN, FFN
+        x = torch.randn((M, H), device="cuda", generator=g).to(torch.bfloat16)
+        w1 = (torch.randn((Fd, H), device="cuda", generator=g) * 0.02).to(torch.bfloat16)
+        w2 = (torch.randn((H, Fd), device="cuda", generator=g) * 0.02).to(torch.bfloat16)
+        dy = (torch.randn((M, H), device="cuda", generator=g) * 1e-3).to(torch.bfloat16)
+        xq, w1q = F.quantize(rec, x, "activation"), F.quantize(rec, w1, "weight")
+        w2q, dyq = F.quantize(rec, w2, "weight"), F.quantize(rec, dy, "grad")
+        a_q, h_q = F.linear_fwd_gelu(rec, xq, w1q)
+        dh_q = F.linear_dgrad_dgelu(rec, dyq, w2q, h_q)
+        for _ in range(args.steps):
+            if case == "gemm_gelu_mx":
+                F.linear_fwd_gelu(rec, xq, w1q, a_q=a_q, h_q=h_q)
+            else:
+                F.linear_dgrad_dgelu(rec, dyq, w2q, h_q, dh_q=dh_q)
+    elif case in ("gelu_mx", "dgelu_mx"):
         h = torch.randn((8192, 16384), device="cuda", generator=g).to(torch.bfloat16)
         a_q, h_q, _ = F.gelu_quantize(rec, h)
         for _ in range(args.steps):
@@ -439,11 +472,14 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--profile", default=None,
                     choices=["quant_mx", "quant_tensorwise", "quant_blockwise", "gemm_mx",
-                             "gemm_tensorwise", "gemm_blockwise", "gelu_mx", "dgelu_mx"])
+                             "gemm_tensorwise", "gemm_blockwise", "gelu_mx", "dgelu_mx",
+                             "gemm_gelu_mx", "gemm_dgelu_mx"])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--unfused", action="store_true",
+                    help="standalone GeLU / dGeLU kernels instead of the fused GEMM epilogues")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -199,6 +199,33 @@ fp8_status fp8_dgelu_quantize(const fp8_recipe *recipe, const void *da_bf16,
                               int32_t *dev_status, cudaStream_t stream);
 
 /*
+ * fp8_linear_fwd_gelu — fc1 of the MLP block with the GeLU step fused into the GEMM
+ * epilogue (MXFP8 recipe only): h = bf16(deq(X) . deq(W)^T) exactly as fp8_linear_fwd would
+ * store it, but instead of writing h the epilogue writes h's MXFP8 row copy into h_q (the FP8
+ * input store of the activation) and a = bf16(gelu(h)) as MXFP8 row and column copies into
+ * a_q. Byte-identical to fp8_linear_fwd followed by fp8_gelu_quantize, without the bf16 round
+ * trip of h through memory. x, w as for fp8_linear_fwd (row copies); a_q needs row, col and
+ * both scale arrays, h_q needs row and row_scale, all 16-byte aligned (32-byte aligned code
+ * arrays get 256-bit stores). M = x->rows and N = w->rows multiples of 128. On return a_q and
+ * h_q describe [M][N] MXFP8 activations.
+ */
+fp8_status fp8_linear_fwd_gelu(const fp8_recipe *recipe, const fp8_tensor *x,
+                               const fp8_tensor *w, fp8_tensor *a_q, fp8_tensor *h_q,
+                               int32_t *dev_status, cudaStream_t stream);
+
+/*
+ * fp8_linear_dgrad_dgelu — dgrad of fc2 with the GeLU backward fused into the GEMM epilogue
+ * (MXFP8 only): da = bf16(deq(dY) . deq(W^T)^T) from dy->row and w->col as fp8_linear_bwd
+ * would store it, then dh = bf16(da * gelu'(deq(h_q))) with h read back from its FP8 row copy
+ * (written by fp8_linear_fwd_gelu or fp8_gelu_quantize), quantised as MXFP8 row and column
+ * copies into dh_q. Byte-identical to fp8_linear_bwd (dx only) followed by fp8_dgelu_quantize.
+ * h_q must be [dy->rows][w->cols]; dh_q needs row, col and both scale arrays.
+ */
+fp8_status fp8_linear_dgrad_dgelu(const fp8_recipe *recipe, const fp8_tensor *dy,
+                                  const fp8_tensor *w, const fp8_tensor *h_q, fp8_tensor *dh_q,
+                                  int32_t *dev_status, cudaStream_t stream);
+
+/*
  * fp8_quantize_static_scratch — fp8_quantize for callers that cannot allocate device memory.
  * The pages have no counterpart: this is a convenience of this library. Some callers cannot
  * hand the library a workspace (code inside a host framework whose allocator owns the whole

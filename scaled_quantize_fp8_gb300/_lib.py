@@ -58,6 +58,12 @@ _SIG = {
                                  ctypes.POINTER(Tensor), ctypes.POINTER(Tensor), _P, _P]),
     "fp8_dgelu_quantize": (_I32, [ctypes.POINTER(Recipe), _P, ctypes.POINTER(Tensor), _P,
                                   ctypes.POINTER(Tensor), _P, _P]),
+    "fp8_linear_fwd_gelu": (_I32, [ctypes.POINTER(Recipe), ctypes.POINTER(Tensor),
+                                   ctypes.POINTER(Tensor), ctypes.POINTER(Tensor),
+                                   ctypes.POINTER(Tensor), _P, _P]),
+    "fp8_linear_dgrad_dgelu": (_I32, [ctypes.POINTER(Recipe), ctypes.POINTER(Tensor),
+                                      ctypes.POINTER(Tensor), ctypes.POINTER(Tensor),
+                                      ctypes.POINTER(Tensor), _P, _P]),
     "fp8_quantize_static_scratch": (_I32, [ctypes.POINTER(Recipe), _P, _I64, _I64, _I32, _I32,
                                            _I32, ctypes.POINTER(Tensor), _P, _P]),
     "fp8_status_str": (ctypes.c_char_p, [_I32]),

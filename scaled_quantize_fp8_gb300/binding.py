@@ -248,3 +248,34 @@ def dgelu_quantize(recipe: Recipe, da: torch.Tensor, h_q: QTensor, want_dh_bf16=
                                 ctypes.byref(cd), _ptr(status), _stream(stream))
     L.check(st, "fp8_dgelu_quantize")
     return dh_q, dh_bf16
+
+
+def linear_fwd_gelu(recipe: Recipe, x: QTensor, w: QTensor, a_q=None, h_q=None, status=None,
+                    stream=None):
+    """fc1 with GeLU fused into the GEMM epilogue: returns (a_q, h_q), the MXFP8 row and column
+    copies of a = gelu(h) and the FP8 row copy of h = x . w^T; h is never stored in bf16."""
+    lib = L.load()
+    dev = x.row.device
+    a_q = a_q or empty_qtensor(recipe, x.rows, w.rows, "activation", True, True, device=dev)
+    h_q = h_q or empty_qtensor(recipe, x.rows, w.rows, "activation", True, False, device=dev)
+    rc = recipe.c()
+    st = lib.fp8_linear_fwd_gelu(ctypes.byref(rc), ctypes.byref(x.c()), ctypes.byref(w.c()),
+                                 ctypes.byref(a_q.c()), ctypes.byref(h_q.c()), _ptr(status),
+                                 _stream(stream))
+    L.check(st, "fp8_linear_fwd_gelu")
+    return a_q, h_q
+
+
+def linear_dgrad_dgelu(recipe: Recipe, dy: QTensor, w: QTensor, h_q: QTensor, dh_q=None,
+                       status=None, stream=None):
+    """dgrad of fc2 with the GeLU backward fused: dh = (dy . w) * gelu'(h), h from its FP8 row
+    copy, returned as MXFP8 row and column copies."""
+    lib = L.load()
+    dh_q = dh_q or empty_qtensor(recipe, dy.rows, w.cols, "grad", True, True,
+                                 device=dy.row.device)
+    rc = recipe.c()
+    st = lib.fp8_linear_dgrad_dgelu(ctypes.byref(rc), ctypes.byref(dy.c()), ctypes.byref(w.c()),
+                                    ctypes.byref(h_q.c()), ctypes.byref(dh_q.c()), _ptr(status),
+                                    _stream(stream))
+    L.check(st, "fp8_linear_dgrad_dgelu")
+    return dh_q

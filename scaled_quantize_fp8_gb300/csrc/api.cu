@@ -226,6 +226,44 @@ fp8_status run_bf16_gemm(const void* a, const void* b, int64_t M, int64_t N, int
   return cuda_status(gemm_launch(g, st));
 }
 
+// MXFP8 GEMM whose epilogue quantises the tile (fused MLP steps); D is never written.
+fp8_status run_fused_mx(int epi, const Operand& a, const Operand& b, int64_t M, int64_t N,
+                        int64_t Kr, uint8_t* h_row, uint8_t* h_scale, fp8_tensor* out,
+                        int32_t* status, cudaStream_t st) {
+  if (M % 128 || N % 128 || Kr % 128) return FP8_ERR_SHAPE;
+  if (M > (int64_t(1) << 30) || N > (int64_t(1) << 30) || Kr > (int64_t(1) << 30) ||
+      M * N >= (int64_t(1) << 31))
+    return FP8_ERR_SHAPE;
+  if (M == 0 || N == 0) return FP8_OK;
+  if (Kr == 0) return FP8_ERR_SHAPE;            // no accumulator to quantise
+  FP8_TRY(check_ptr(a.codes));
+  FP8_TRY(check_ptr(b.codes));
+  FP8_TRY(check_ptr(a.scale));
+  FP8_TRY(check_ptr(b.scale));
+  FP8_TRY(check_copy(FP8_RECIPE_MXFP8, h_row, h_scale));
+  FP8_TRY(check_copy(FP8_RECIPE_MXFP8, out->row, out->row_scale));
+  FP8_TRY(check_copy(FP8_RECIPE_MXFP8, out->col, out->col_scale));
+  GemmLaunch g{};
+  g.mode = G_MX;
+  g.epi = epi;
+  g.A = a.codes;
+  g.B = b.codes;
+  g.p.M = int(M);
+  g.p.N = int(N);
+  g.p.K = int(Kr);
+  g.p.ldd = N;
+  g.p.status = status;
+  g.p.sfa = reinterpret_cast<const uint8_t*>(a.scale);
+  g.p.sfb = reinterpret_cast<const uint8_t*>(b.scale);
+  g.p.h_row = h_row;
+  g.p.h_scale = h_scale;
+  g.p.o_row = out->row;
+  g.p.o_row_scale = reinterpret_cast<uint8_t*>(out->row_scale);
+  g.p.o_col = out->col;
+  g.p.o_col_scale = reinterpret_cast<uint8_t*>(out->col_scale);
+  return cuda_status(gemm_launch(g, st));
+}
+
 fp8_status check_tensor(const fp8_recipe* r, const fp8_tensor* t) {
   if (t == nullptr) return FP8_ERR_NULL;
   if (t->kind != r->kind) return FP8_ERR_UNSUPPORTED;
@@ -278,6 +316,54 @@ fp8_status fp8_linear_bwd(const fp8_recipe* recipe, const fp8_tensor* dy,
     const Operand b{x_saved->col, x_saved->col_scale, x_saved->scale_inv, x_saved->role};
     FP8_TRY(run_gemm(recipe->kind, a, b, N, K, M, dw, out_fp32, dev_status, stream));
   }
+  return FP8_OK;
+}
+
+fp8_status fp8_linear_fwd_gelu(const fp8_recipe* recipe, const fp8_tensor* x,
+                               const fp8_tensor* w, fp8_tensor* a_q, fp8_tensor* h_q,
+                               int32_t* dev_status, cudaStream_t stream) {
+  FP8_TRY(check_recipe(recipe));
+  if (recipe->kind != FP8_RECIPE_MXFP8) return FP8_ERR_UNSUPPORTED;
+  FP8_TRY(check_tensor(recipe, x));
+  FP8_TRY(check_tensor(recipe, w));
+  if (a_q == nullptr || h_q == nullptr) return FP8_ERR_NULL;
+  if (x->cols != w->cols) return FP8_ERR_SHAPE;
+  const int64_t M = x->rows, N = w->rows;
+  const Operand a{x->row, x->row_scale, x->scale_inv, x->role};
+  const Operand b{w->row, w->row_scale, w->scale_inv, w->role};
+  FP8_TRY(run_fused_mx(EPI_GELU, a, b, M, N, x->cols, h_q->row,
+                       reinterpret_cast<uint8_t*>(h_q->row_scale), a_q, dev_status, stream));
+  for (fp8_tensor* t : {a_q, h_q}) {
+    t->rows = M;
+    t->cols = N;
+    t->kind = FP8_RECIPE_MXFP8;
+    t->role = FP8_ROLE_ACTIVATION;
+    t->col_bf16 = 0;
+  }
+  return FP8_OK;
+}
+
+fp8_status fp8_linear_dgrad_dgelu(const fp8_recipe* recipe, const fp8_tensor* dy,
+                                  const fp8_tensor* w, const fp8_tensor* h_q, fp8_tensor* dh_q,
+                                  int32_t* dev_status, cudaStream_t stream) {
+  FP8_TRY(check_recipe(recipe));
+  if (recipe->kind != FP8_RECIPE_MXFP8) return FP8_ERR_UNSUPPORTED;
+  FP8_TRY(check_tensor(recipe, dy));
+  FP8_TRY(check_tensor(recipe, w));
+  FP8_TRY(check_tensor(recipe, h_q));
+  if (dh_q == nullptr) return FP8_ERR_NULL;
+  const int64_t M = dy->rows, N = w->cols;
+  if (w->rows != dy->cols || h_q->rows != M || h_q->cols != N) return FP8_ERR_SHAPE;
+  // dgrad: dA[M][N] = dY[M][H] . (W^T)[N][H]^T
+  const Operand a{dy->row, dy->row_scale, dy->scale_inv, dy->role};
+  const Operand b{w->col, w->col_scale, w->scale_inv, w->role};
+  FP8_TRY(run_fused_mx(EPI_DGELU, a, b, M, N, dy->cols, h_q->row,
+                       reinterpret_cast<uint8_t*>(h_q->row_scale), dh_q, dev_status, stream));
+  dh_q->rows = M;
+  dh_q->cols = N;
+  dh_q->kind = FP8_RECIPE_MXFP8;
+  dh_q->role = FP8_ROLE_GRAD;
+  dh_q->col_bf16 = 0;
   return FP8_OK;
 }
 

@@ -27,6 +27,7 @@
 #include <cstdio>
 
 #include "common.cuh"
+#include "gelu.cuh"
 #include "sm100_ptx.cuh"
 #include "internal.cuh"
 
@@ -44,14 +45,25 @@ constexpr uint64_t kWaitBudgetCycles = 4000000000ull;   // ~2 s at 2 GHz
 
 // Per-configuration geometry. A single CTA (CTA2 = 0) owns a 128 x 256 tile and loads the
 // whole 256-row B tile; a CTA pair (CTA2 = 1) owns a 256 x 256 tile, each CTA loading its own
-// 128 rows of A and 128 of the 256 rows of B, so a stage is 32 KiB and six of them fit.
-template <int CTA2>
+// 128 rows of A and 128 of the 256 rows of B, so a stage is 32 KiB and six of them fit. The
+// fused MLP epilogues add a 2 KiB transpose buffer per epilogue warp and a GeLU table behind
+// the control block (the GeLU pair kernel gives up one stage for them).
+constexpr uint32_t kEpiStageBytes = 2048;              // one warp's 32 x 32 bf16 chunk
+template <int EPI>
+__host__ __device__ constexpr uint32_t epi_smem_bytes() {
+  return EPI == EPI_NONE ? 0u
+                         : kEpiWarps * kEpiStageBytes +
+                               (EPI == EPI_GELU ? kGeluTableBytes : kDgeluTableBytes);
+}
+template <int CTA2, int EPI = EPI_NONE>
 struct Geo {
-  static constexpr int kStages = CTA2 ? 6 : 4;
+  static constexpr int kStages = CTA2 ? (EPI == EPI_GELU ? 5 : 6) : 4;
   static constexpr uint32_t kTileBBytes = (CTA2 ? kBN / 2 : kBN) * kBKBytes;
   static constexpr uint32_t kStageBytes = kTileABytes + kTileBBytes + kSfStageBytes;
-  static constexpr uint32_t kSmemBytes = 1024 + kStages * kStageBytes + 512;
+  static constexpr uint32_t kSmemBytes =
+      1024 + kStages * kStageBytes + 512 + epi_smem_bytes<EPI>();
   static constexpr int kTileM = CTA2 ? 2 * kBM : kBM;     // output rows per tile
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
 struct SharedCtl {
@@ -142,13 +154,110 @@ __device__ __forceinline__ void tmem_load128(uint32_t taddr, float* out) {
   }
 }
 
-template <int MODE, int B128, int CTA2>
+// Read 128 accumulator columns and round them to bf16 pairs (low half = even column), the
+// values a bf16 store of the tile would hold. Two batches of 64 keep the raw values short-lived.
+__device__ __forceinline__ void tmem_load128_bf16(uint32_t taddr, uint32_t* out) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t r0[32], r1[32];
+    ptx::tmem_ld_32x32b_x32(taddr + 64 * h, r0);
+    ptx::tmem_ld_32x32b_x32(taddr + 64 * h + 32, r1);
+    ptx::tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      out[32 * h + j] = pack_bf16x2(__uint_as_float(r0[2 * j]), __uint_as_float(r0[2 * j + 1]));
+      out[32 * h + 16 + j] =
+          pack_bf16x2(__uint_as_float(r1[2 * j]), __uint_as_float(r1[2 * j + 1]));
+    }
+  }
+}
+
+// One MXFP8 block of 32 bf16 (16 pairs, in order): E8M0 byte by the ceil rule, codes of
+// x * 2^-e stored as 32 bytes at dst. The same arithmetic as the quantize kernels.
+__device__ __forceinline__ uint32_t quantize_block32(const uint32_t* w, uint8_t* dst, bool v8) {
+  uint32_t mx = 0;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) mx = absmax_bf16x2(mx, w[k]);
+  mx = fold_bf16x2(mx);
+  float mult;
+  const uint32_t sb = mx_scale_byte(mx, &mult);
+  uint32_t c[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) c[q] = encode4(w[2 * q], w[2 * q + 1], mult);
+  if (mx > 0x7F80u) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) c[q] = fix_nan4(c[q], w[2 * q], w[2 * q + 1]);
+  }
+  store_seg32(dst, make_uint4(c[0], c[1], c[2], c[3]), make_uint4(c[4], c[5], c[6], c[7]), true,
+              true, v8);
+  return sb;
+}
+
+// Fused MLP epilogue for one thread: row m, columns n .. n+127 of the output (v: 64 bf16
+// pairs), in four 32-column chunks. GELU writes h's MXFP8 row copy, then a = gelu(h);
+// DGELU forms dh = da * gelu'(h) from h's codes (hc, 128 bytes) and scales (hsc, 4 bytes).
+// The result's row copy is thread-local (a chunk is one 1x32 block); for the column copy
+// the warp parks its 32 x 32 chunk in shared memory and lane c reads back column c over the
+// warp's 32 rows mrow0 .. mrow0+31, which is one 32-row block of the transposed copy.
+template <int EPI>
+__device__ __forceinline__ void mlp_epilogue(const GemmParams& p, const uint32_t* v,
+                                             const uint4* hc, uint32_t hsc, int m, int n,
+                                             int mrow0, uint8_t* stage, const void* table,
+                                             int lane) {
+  const bool v8 = p.o_v8 != 0;
+  uint32_t sc_h = 0, sc_o = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint32_t w[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) w[k] = v[16 * j + k];
+    if constexpr (EPI == EPI_GELU) {
+      sc_h |= quantize_block32(w, p.h_row + int64_t(m) * p.N + n + 32 * j, v8) << (8 * j);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) w[k] = gelu_bf16x2(table, w[k]);
+    } else {
+      const uint32_t sb = (hsc >> (8 * j)) & 0xFFu;
+      const float hs = sb == 0xFFu ? __uint_as_float(0x7FC00000u) : exp2i(int(sb) - 127);
+      const uint32_t hw[8] = {hc[2 * j].x,     hc[2 * j].y,     hc[2 * j].z,     hc[2 * j].w,
+                              hc[2 * j + 1].x, hc[2 * j + 1].y, hc[2 * j + 1].z, hc[2 * j + 1].w};
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        w[k] = dgelu_bf16x2(table, w[k], uint16_t(hw[k >> 1] >> (16 * (k & 1))), hs);
+    }
+    sc_o |= quantize_block32(w, p.o_row + int64_t(m) * p.N + n + 32 * j, v8) << (8 * j);
+
+    // column copy: rows of 64 bytes, 16-byte chunk q of row r at q ^ ((r / 2) % 4)
+    __syncwarp();                                   // the previous chunk has been read
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      *reinterpret_cast<uint4*>(stage + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4)) =
+          make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+    __syncwarp();
+    uint32_t cw[16];
+#pragma unroll
+    for (int r = 0; r < 32; r += 2) {
+      const uint32_t off = (uint32_t(((lane >> 3) ^ ((r >> 1) & 3))) << 4) + 2u * (lane & 7);
+      const uint32_t lo = *reinterpret_cast<const uint16_t*>(stage + r * 64 + off);
+      const uint32_t hi = *reinterpret_cast<const uint16_t*>(stage + (r + 1) * 64 + off);
+      cw[r >> 1] = lo | (hi << 16);
+    }
+    const int c = n + 32 * j + lane;
+    const uint32_t sbc = quantize_block32(cw, p.o_col + int64_t(c) * p.M + mrow0, v8);
+    p.o_col_scale[mx_scale_offset(c, mrow0 >> 5, p.M)] = uint8_t(sbc);
+  }
+  const int64_t so = mx_scale_offset(m, n >> 5, p.N);     // four consecutive blocks
+  if constexpr (EPI == EPI_GELU) *reinterpret_cast<uint32_t*>(p.h_scale + so) = sc_h;
+  *reinterpret_cast<uint32_t*>(p.o_row_scale + so) = sc_o;
+}
+
+template <int MODE, int B128, int CTA2, int EPI>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmSFA,
                    const __grid_constant__ CUtensorMap tmSFB, const GemmParams p) {
-  using G = Geo<CTA2>;
+  using G = Geo<CTA2, EPI>;
+  static_assert(EPI == EPI_NONE || MODE == G_MX, "fused MLP epilogues are MXFP8 only");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -156,6 +265,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint8_t* sB = smem + G::kStages * kTileABytes;
   uint8_t* sSF = sB + G::kStages * G::kTileBBytes;
   SharedCtl* ctl = reinterpret_cast<SharedCtl*>(sSF + G::kStages * kSfStageBytes);
+  uint8_t* sEpi = reinterpret_cast<uint8_t*>(ctl) + 512;   // fused epilogues only
 
   constexpr int kNumAcc = (MODE == G_MX) ? 1 : 2;
   constexpr int kElem = (MODE == G_BF16) ? 2 : 1;
@@ -367,6 +477,41 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         else ptx::mbar_arrive(&ctl->acce[b]);
       }
     };
+    if constexpr (EPI != EPI_NONE) {
+      // ---- fused MLP epilogue (MXFP8, single accumulator)
+      uint8_t* stage = sEpi + ew * kEpiStageBytes;
+      void* table = sEpi + kEpiWarps * kEpiStageBytes;
+      if constexpr (EPI == EPI_GELU) gelu_table_fill(table, int(threadIdx.x) - 64, 32 * kEpiWarps);
+      else dgelu_table_fill(table, int(threadIdx.x) - 64, 32 * kEpiWarps);
+      asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");   // epilogue warps only
+      uint32_t u = 0;
+      for (int tile = unit; tile < n_tiles; tile += n_units) {
+        const int m0 = (tile % tiles_m) * G::kTileM + int(rank) * kBM;
+        const int n0 = (tile / tiles_m) * kBN;
+        const int m = m0 + row, n = n0 + half * 128;
+        const int mrow0 = m0 + 32 * quad;
+        // M and N are multiples of 128, so a warp's 32 rows x 128 columns are all in or all out
+        const bool live = mrow0 < p.M && n < p.N;
+        uint4 hc[8];
+        uint32_t hsc = 0;
+        if constexpr (EPI == EPI_DGELU) {
+          // h's codes and scales do not depend on the accumulator: fetch them first
+          if (live) {
+            const uint8_t* src = p.h_row + int64_t(m) * p.N + n;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) hc[i] = ldg_nc_v4(src + 16 * i);
+            hsc = __ldg(reinterpret_cast<const uint32_t*>(p.h_scale + mx_scale_offset(m, n >> 5, p.N)));
+          }
+        }
+        if (!wait_bar(&ctl->accf[0], u & 1u, ctl, p.status)) break;
+        ptx::tc_fence_after();
+        uint32_t v[64];
+        tmem_load128_bf16(t_lane, v);
+        release_acc(0);
+        ++u;
+        if (live) mlp_epilogue<EPI>(p, v, hc, hsc, m, n, mrow0, stage, table, lane);
+      }
+    } else {
     float alpha = 1.0f;
     if constexpr (MODE == G_TENSOR) alpha = __fmul_rn(*p.a_sinv, *p.b_sinv);
     uint32_t u = 0;
@@ -434,6 +579,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       store_row128(p, m, n, acc);
     }
+    }
   }
 
   __syncthreads();
@@ -461,9 +607,9 @@ static bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, i
   return make_tmap_2d(map, base, elem_bytes, k, rows, kBKBytes / elem_bytes, box_rows, true);
 }
 
-template <int MODE, int B128, int CTA2>
+template <int MODE, int B128, int CTA2, int EPI = EPI_NONE>
 static cudaError_t launch_mode(const GemmLaunch& g, cudaStream_t st) {
-  using G = Geo<CTA2>;
+  using G = Geo<CTA2, EPI>;
   CUtensorMap ma, mb;
   const int eb = MODE == G_BF16 ? 2 : 1;
   if (!make_operand_map(&ma, g.A, g.p.M, g.p.K, eb, kBM)) return cudaErrorInvalidValue;
@@ -478,7 +624,7 @@ static cudaError_t launch_mode(const GemmLaunch& g, cudaStream_t st) {
     if (!make_tmap_2d(&msfb, g.p.sfb, 1, 256, 2 * (int64_t(g.p.N) / 128) * kb, 256, 2, false))
       return cudaErrorInvalidValue;
   }
-  auto kern = gemm_tn_kernel<MODE, B128, CTA2>;
+  auto kern = gemm_tn_kernel<MODE, B128, CTA2, EPI>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -513,6 +659,11 @@ cudaError_t gemm_launch(const GemmLaunch& g, cudaStream_t st) {
   GemmLaunch gl = g;
   const int64_t pitch = gl.p.ldd * (gl.p.d_fp32 ? 4 : 2);
   gl.p.d_v8 = (reinterpret_cast<uintptr_t>(gl.p.D) % 32 == 0) && (pitch % 32 == 0);
+  if (gl.epi != EPI_NONE) {
+    if (gl.mode != G_MX) return cudaErrorInvalidValue;
+    auto a32 = [](const void* q) { return reinterpret_cast<uintptr_t>(q) % 32 == 0; };
+    gl.p.o_v8 = a32(gl.p.o_row) && a32(gl.p.o_col) && (gl.epi != EPI_GELU || a32(gl.p.h_row));
+  }
   // CTA pairs whenever there are at least two 128-row halves to give them.
   // (Blockwise keeps the single CTA: its per-chunk promotion would couple the pair's
   // epilogues to every K step.)
@@ -520,9 +671,16 @@ cudaError_t gemm_launch(const GemmLaunch& g, cudaStream_t st) {
   switch (gl.mode) {
     case G_TENSOR:
       return pair ? launch_mode<G_TENSOR, 1, 1>(gl, st) : launch_mode<G_TENSOR, 1, 0>(gl, st);
-    case G_MX:
-      return (pair && gl.p.N > kBM) ? launch_mode<G_MX, 1, 1>(gl, st)
-                                   : launch_mode<G_MX, 1, 0>(gl, st);
+    case G_MX: {
+      const bool p2 = pair && gl.p.N > kBM;
+      if (gl.epi == EPI_GELU)
+        return p2 ? launch_mode<G_MX, 1, 1, EPI_GELU>(gl, st)
+                  : launch_mode<G_MX, 1, 0, EPI_GELU>(gl, st);
+      if (gl.epi == EPI_DGELU)
+        return p2 ? launch_mode<G_MX, 1, 1, EPI_DGELU>(gl, st)
+                  : launch_mode<G_MX, 1, 0, EPI_DGELU>(gl, st);
+      return p2 ? launch_mode<G_MX, 1, 1>(gl, st) : launch_mode<G_MX, 1, 0>(gl, st);
+    }
     case G_BLOCK:
       return gl.p.b_is_128 ? launch_mode<G_BLOCK, 1, 0>(gl, st) : launch_mode<G_BLOCK, 0, 0>(gl, st);
     case G_BF16:

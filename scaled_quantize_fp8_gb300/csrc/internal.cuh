@@ -36,6 +36,9 @@ cudaError_t amax_update_launch(float* hist, int32_t* head, int len, const float*
 // ---- gemm.cu
 enum GMode : int { G_TENSOR = 0, G_MX = 1, G_BLOCK = 2, G_BF16 = 3 };
 
+// Epilogue kinds of the MLP block's fused steps (GeLU forward / backward).
+enum MlpEpi : int { EPI_NONE = 0, EPI_GELU = 1, EPI_DGELU = 2 };
+
 struct GemmParams {
   int M, N, K;              // D[M][N] = sum_k A[M][K] B[N][K]; K in elements
   void* D;
@@ -50,10 +53,21 @@ struct GemmParams {
   const float* b_bs;        // G_BLOCK: B 128x128 grid [N/128][K/128] or 1x128 [K/128][N]
   int b_is_128;
   int32_t* status;          // device status word (may be null)
+  // Fused MLP epilogues (G_MX only; the tile is quantised instead of stored, D unused):
+  //   GELU : h = bf16(acc) -> h_row/h_scale (MXFP8 row copy), a = gelu(h) -> o_*
+  //   DGELU: da = bf16(acc), h read from h_row/h_scale, dh = da * gelu'(h) -> o_*
+  uint8_t* h_row;           // [M][N] codes
+  uint8_t* h_scale;         // E8M0, tiled atoms of the [M][N] tensor
+  uint8_t* o_row;           // [M][N] codes of a / dh
+  uint8_t* o_row_scale;
+  uint8_t* o_col;           // [N][M] codes (column-wise copy)
+  uint8_t* o_col_scale;     // E8M0, tiled atoms of the [N][M] tensor
+  int o_v8;                 // all of the above code arrays are 32-byte aligned
 };
 
 struct GemmLaunch {
   int mode;                 // GMode
+  int epi;                  // MlpEpi (0 = plain bf16/fp32 store)
   const void* A;            // [M][K] codes (bf16 for G_BF16)
   const void* B;            // [N][K]
   GemmParams p;

@@ -13,24 +13,17 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "gelu.cuh"
 #include "internal.cuh"
 #include "sm100_ptx.cuh"
 
 namespace fp8lin {
 
 enum QMode : int { Q_TENSOR = 0, Q_MX = 1, Q_BW1x128 = 2, Q_BW128 = 3 };
-enum QEpi : int { EPI_NONE = 0, EPI_GELU = 1, EPI_DGELU = 2 };
-
-// GeLU tables (see gelu_table_lookup / dgelu_table_lookup), between the control block and the
-// tile buffers for the MLP kernels.
-constexpr int kGeluExpLo = -14, kGeluExps = 18;       // gelu table: |h| in [2^-14, 2^4)
-constexpr int kGeluEntries = kGeluExps * 128 * 2;     // bf16 input: 7-bit mantissa, sign
-constexpr int kDgeluExpLo = -20, kDgeluExps = 24;     // gelu' table: |h| in [2^-20, 2^4)
-constexpr int kDgeluEntries = kDgeluExps * 8 * 2;     // E4M3-derived input: 3-bit mantissa
-// table bytes, rounded so the tile buffers behind them stay 1024-byte aligned
+// MLP epilogue kinds (MlpEpi) and the GeLU tables come from gelu.cuh.
 template <int EPI>
 __host__ __device__ constexpr uint32_t quant_table_bytes() {
-  return EPI == EPI_GELU ? 9216u : (EPI == EPI_DGELU ? 2048u : 0u);
+  return EPI == EPI_GELU ? kGeluTableBytes : (EPI == EPI_DGELU ? kDgeluTableBytes : 0u);
 }
 
 struct QuantParams {
@@ -58,88 +51,6 @@ struct QuantParams {
   uint8_t* aux_row;           // GELU: h row codes; DGELU: h row codes (read)
   uint8_t* aux_scale;         // GELU: h row E8M0 (written); DGELU: h row E8M0 (read)
 };
-
-__device__ __forceinline__ uint32_t bf16_rn_bits(float f) {
-  return uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(f)));
-}
-
-// E4M3 code pair -> two floats (exact, through the hardware f16x2 conversion).
-__device__ __forceinline__ float2 e4m3x2_to_f2(uint16_t codes) {
-  uint32_t h2;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(codes));
-  const __half2 h = *reinterpret_cast<const __half2*>(&h2);
-  return __half22float2(h);
-}
-
-// Standard normal CDF Phi(h) = 0.5 erfc(-h / sqrt 2) in fp32, and optionally exp(-h^2 / 2).
-// erfc(z), z >= 0, uses the Chebyshev-fitted form of Numerical Recipes ("erfcc", Press et al.,
-// Numerical Recipes in C, 2nd ed., section 6.2): erfc(z) = t exp(-z^2 + P(t)), t = 1/(1 + z/2),
-// with a stated fractional error below 1.2e-7 for all z >= 0. For h >= 0, Phi = 1 - erfc/2.
-// The fast exponential is exact enough here (bf16 output); below h = -13 its result would be
-// flushed, so that rare tail takes the full-range expf.
-__device__ __forceinline__ float phi_cdf(float h, float* gauss) {
-  const float z = fabsf(h) * 0.70710678118654752f;
-  const float t = __fdividef(1.0f, fmaf(0.5f, z, 1.0f));
-  float P = 0.17087277f;
-  P = fmaf(P, t, -0.82215223f);
-  P = fmaf(P, t, 1.48851587f);
-  P = fmaf(P, t, -1.13520398f);
-  P = fmaf(P, t, 0.27886807f);
-  P = fmaf(P, t, -0.18628806f);
-  P = fmaf(P, t, 0.09678418f);
-  P = fmaf(P, t, 0.37409196f);
-  P = fmaf(P, t, 1.00002368f);
-  P = fmaf(P, t, -1.26551223f);
-  const float z2 = z * z;
-  const float arg = P - z2;
-  const float e = z > 9.0f ? expf(arg) : __expf(arg);
-  const float half_erfc = 0.5f * t * e;
-  if (gauss != nullptr) *gauss = 0.3989422804014327f * (z > 9.0f ? expf(-z2) : __expf(-z2));
-  return h >= 0.0f ? 1.0f - half_erfc : half_erfc;
-}
-// gelu(h) = h Phi(h); gelu'(h) = Phi(h) + h phi(h), phi(h) = exp(-h^2/2) / sqrt(2 pi).
-__device__ __forceinline__ float gelu_f32(float h) { return h * phi_cdf(h, nullptr); }
-__device__ __forceinline__ float gelu_grad_f32(float h) {
-  // A dequantised FP8 value can exceed the fp32 range (a code near 448 times 2^120); its
-  // gelu' is then the limit: 1 above, +0 below. (Inf/NaN inputs never get here as such: their
-  // MXFP8 block carries the NaN scale.)
-  if (fabsf(h) > 3.402823466e38f) return h > 0.0f ? 1.0f : 0.0f;
-  float g;
-  const float c = phi_cdf(h, &g);
-  return fmaf(h, g, c);
-}
-
-// Direct evaluations for inputs outside the tables: rare, kept out of line so the unrolled
-// tile loop stays small enough for the instruction cache.
-__device__ __noinline__ uint32_t gelu_bf16_direct(uint32_t hb) {
-  return bf16_rn_bits(gelu_f32(__uint_as_float(hb << 16)));
-}
-__device__ __noinline__ float gelu_grad_direct(float h) { return gelu_grad_f32(h); }
-
-// gelu over bf16 inputs through the CTA's shared-memory table: every bf16 h with |h| in
-// [2^-14, 2^4) has an entry holding bf16(gelu_f32(h)), so the lookup returns exactly what the
-// direct evaluation would; other inputs (tiny, large, Inf/NaN) are evaluated directly.
-__device__ __forceinline__ uint32_t gelu_table_lookup(const void* table, uint32_t hb) {
-  const uint32_t e = ((hb >> 7) & 0xFFu) - uint32_t(kGeluExpLo + 127);
-  if (e < uint32_t(kGeluExps)) {
-    const uint32_t idx = (e << 8) | ((hb & 0x7Fu) << 1) | (hb >> 15);
-    return reinterpret_cast<const uint16_t*>(table)[idx];
-  }
-  return gelu_bf16_direct(hb);
-}
-// gelu'(h) for h decoded from an E4M3 code times a power of two (at most 3 mantissa bits):
-// table entries hold gelu_grad_f32 of each such value with |h| in [2^-20, 2^4); zero gives 1/2;
-// anything else is evaluated directly.
-__device__ __forceinline__ float dgelu_table_lookup(const void* table, float h) {
-  const uint32_t bits = __float_as_uint(h);
-  const uint32_t e = ((bits >> 23) & 0xFFu) - uint32_t(kDgeluExpLo + 127);
-  if (e < uint32_t(kDgeluExps)) {
-    const uint32_t idx = (e << 4) | (((bits >> 20) & 7u) << 1) | (bits >> 31);
-    return reinterpret_cast<const float*>(table)[idx];
-  }
-  if ((bits & 0x7FFFFFFFu) == 0u) return 0.5f;
-  return gelu_grad_direct(h);
-}
 
 // Max of the 15-bit magnitudes of the eight bf16 in a vector.
 __device__ __forceinline__ uint32_t vec_amax_bits(uint4 v) {
@@ -280,9 +191,7 @@ __device__ __forceinline__ void quantize_one_tile(const QuantParams& p, QuantCtl
           if ((cc & 1) == 0) p.aux_scale[mx_scale_offset(r0 + r, (c0 + ccol) >> 5, C)] = uint8_t(sb);
         }
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          w[i][k] = gelu_table_lookup(table, w[i][k] & 0xFFFFu) |
-                    (gelu_table_lookup(table, w[i][k] >> 16) << 16);
+        for (int k = 0; k < 8; ++k) w[i][k] = gelu_bf16x2(table, w[i][k]);
       } else {
         // dh = bf16(da * gelu'(h)), h decoded from its MXFP8 row copy (loaded up front)
         if (ok) {
@@ -291,12 +200,8 @@ __device__ __forceinline__ void quantize_one_tile(const QuantParams& p, QuantCtl
           const float hs = sb == 0xFFu ? __uint_as_float(0x7FC00000u) : exp2i(int(sb) - 127);
           const uint32_t cw[4] = {hc.x, hc.y, hc.z, hc.w};
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const float2 hv = e4m3x2_to_f2(uint16_t(cw[k >> 1] >> (16 * (k & 1))));
-            const float d0 = __fmul_rn(bf16_lo(w[i][k]), dgelu_table_lookup(table, __fmul_rn(hv.x, hs)));
-            const float d1 = __fmul_rn(bf16_hi(w[i][k]), dgelu_table_lookup(table, __fmul_rn(hv.y, hs)));
-            w[i][k] = bf16_rn_bits(d0) | (bf16_rn_bits(d1) << 16);
-          }
+          for (int k = 0; k < 8; ++k)
+            w[i][k] = dgelu_bf16x2(table, w[i][k], uint16_t(cw[k >> 1] >> (16 * (k & 1))), hs);
         } else {
 #pragma unroll
           for (int k = 0; k < 8; ++k) w[i][k] = 0u;
@@ -606,22 +511,8 @@ __global__ void __launch_bounds__(256, quant_ctas_per_sm<MODE, EPI>())
     }
   }
   // MLP kernels: fill the GeLU table while the first tiles are in flight
-  if constexpr (EPI == EPI_GELU) {
-    uint16_t* tb = reinterpret_cast<uint16_t*>(table);
-    for (int idx = t; idx < kGeluEntries; idx += 256) {
-      const uint32_t bits = (uint32_t(idx & 1) << 15) |
-                            (uint32_t((idx >> 8) + kGeluExpLo + 127) << 7) | uint32_t((idx >> 1) & 0x7F);
-      tb[idx] = uint16_t(bf16_rn_bits(gelu_f32(__uint_as_float(bits << 16))));
-    }
-  } else if constexpr (EPI == EPI_DGELU) {
-    float* tb = reinterpret_cast<float*>(table);
-    for (int idx = t; idx < kDgeluEntries; idx += 256) {
-      const uint32_t bits = (uint32_t(idx & 1) << 31) |
-                            (uint32_t((idx >> 4) + kDgeluExpLo + 127) << 23) |
-                            (uint32_t((idx >> 1) & 7) << 20);
-      tb[idx] = gelu_grad_f32(__uint_as_float(bits));
-    }
-  }
+  if constexpr (EPI == EPI_GELU) gelu_table_fill(table, t, 256);
+  else if constexpr (EPI == EPI_DGELU) dgelu_table_fill(table, t, 256);
   if constexpr (EPI != EPI_NONE) __syncthreads();
 
   int tile = blockIdx.x;

@@ -151,3 +151,33 @@ def test_mlp_entry_checks(lib):
     hq = _qt(L.RECIPE_TENSORWISE, 256, 256)
     assert lib.fp8_dgelu_quantize(ctypes.byref(r), 0x1000, ctypes.byref(hq), None,
                                   ctypes.byref(_tensor()), None, None) == 4
+
+
+def test_fused_mlp_entry_checks(lib):
+    r = _rec(kind=L.RECIPE_MXFP8)
+    x, w = _qt(L.RECIPE_MXFP8, 256, 512), _qt(L.RECIPE_MXFP8, 384, 512, 1)
+    a, h = _tensor(), _tensor()
+    fwd = lib.fp8_linear_fwd_gelu
+    assert fwd(ctypes.byref(_rec()), ctypes.byref(x), ctypes.byref(w), ctypes.byref(a),
+               ctypes.byref(h), None, None) == 4                 # MXFP8 only
+    assert fwd(ctypes.byref(r), ctypes.byref(x), ctypes.byref(_qt(L.RECIPE_MXFP8, 384, 256, 1)),
+               ctypes.byref(a), ctypes.byref(h), None, None) == 3   # K mismatch
+    assert fwd(ctypes.byref(r), ctypes.byref(x), ctypes.byref(w), None, ctypes.byref(h), None,
+               None) == 1
+    assert fwd(ctypes.byref(r), ctypes.byref(_qt(L.RECIPE_MXFP8, 200, 512)), ctypes.byref(w),
+               ctypes.byref(a), ctypes.byref(h), None, None) == 3   # M not a multiple of 128
+    assert fwd(ctypes.byref(r), ctypes.byref(x), ctypes.byref(w), ctypes.byref(a),
+               ctypes.byref(_tensor(row=0x1008)), None, None) == 2  # misaligned h codes
+    assert fwd(ctypes.byref(r), ctypes.byref(x), ctypes.byref(w), ctypes.byref(_tensor(cs=0)),
+               ctypes.byref(h), None, None) == 1
+    dgr = lib.fp8_linear_dgrad_dgelu
+    dy, w2 = _qt(L.RECIPE_MXFP8, 256, 384), _qt(L.RECIPE_MXFP8, 384, 512, 1)
+    hq = _qt(L.RECIPE_MXFP8, 256, 512)
+    assert dgr(ctypes.byref(r), ctypes.byref(dy), ctypes.byref(w2),
+               ctypes.byref(_qt(L.RECIPE_MXFP8, 256, 384)), ctypes.byref(_tensor()), None,
+               None) == 3                                        # h is [M][w2 cols]
+    assert dgr(ctypes.byref(r), ctypes.byref(dy), ctypes.byref(w2),
+               ctypes.byref(_qt(L.RECIPE_TENSORWISE, 256, 512)), ctypes.byref(_tensor()), None,
+               None) == 4
+    assert dgr(ctypes.byref(r), ctypes.byref(dy), ctypes.byref(w2), ctypes.byref(hq), None,
+               None, None) == 1
