@@ -159,7 +159,7 @@ class MlpStep:
         self.stream = torch.cuda.current_stream(dev)
         self.events = []
 
-    def _timed(self, kind, fn):
+    def _timed(self, kind, fn, name):
         if self.events is None:
             return fn()
         s = self.torch.cuda.Event(enable_timing=True)
@@ -167,36 +167,39 @@ class MlpStep:
         s.record(self.stream)
         r = fn()
         e.record(self.stream)
-        self.events.append((kind, s, e))
+        self.events.append((kind, name, s, e))
         return r
 
     def run(self, src=None):
         F, rec, T = self.F, self.rec, self._timed
         d = src or self.d
-        T("quant", lambda: F.quantize(rec, d["x"], "activation", out=self.xq))
-        T("quant", lambda: F.quantize(rec, d["w1"], "weight", out=self.w1q))
-        T("quant", lambda: F.quantize(rec, d["w2"], "weight", out=self.w2q))
+        T("quant", lambda: F.quantize(rec, d["x"], "activation", out=self.xq), "quantize_x")
+        T("quant", lambda: F.quantize(rec, d["w1"], "weight", out=self.w1q), "quantize_w1")
+        T("quant", lambda: F.quantize(rec, d["w2"], "weight", out=self.w2q), "quantize_w2")
         if self.fused:
-            T("gemm", lambda: F.linear_fwd_gelu(rec, self.xq, self.w1q, a_q=self.aq, h_q=self.hq))
+            T("gemm_fused", lambda: F.linear_fwd_gelu(rec, self.xq, self.w1q, a_q=self.aq,
+                                                      h_q=self.hq), "fc1_fprop_gelu")
         else:
-            T("gemm", lambda: F.linear_fwd(rec, self.xq, self.w1q, y=self.hbuf))
-            T("quant", lambda: F.gelu_quantize(rec, self.hbuf, a_q=self.aq, h_q=self.hq))
-        T("gemm", lambda: F.linear_fwd(rec, self.aq, self.w2q, y=self.y))
-        T("quant", lambda: F.quantize(rec, d["dy"], "grad", out=self.dyq))
+            T("gemm", lambda: F.linear_fwd(rec, self.xq, self.w1q, y=self.hbuf), "fc1_fprop")
+            T("quant", lambda: F.gelu_quantize(rec, self.hbuf, a_q=self.aq, h_q=self.hq),
+              "gelu_quantize")
+        T("gemm", lambda: F.linear_fwd(rec, self.aq, self.w2q, y=self.y), "fc2_fprop")
+        T("quant", lambda: F.quantize(rec, d["dy"], "grad", out=self.dyq), "quantize_dy")
         if self.fused:
-            T("gemm", lambda: F.linear_dgrad_dgelu(rec, self.dyq, self.w2q, self.hq,
-                                                   dh_q=self.dhq))
+            T("gemm_fused", lambda: F.linear_dgrad_dgelu(rec, self.dyq, self.w2q, self.hq,
+                                                         dh_q=self.dhq), "fc2_dgrad_dgelu")
         else:
             T("gemm", lambda: F.linear_bwd(rec, self.dyq, self.aq, self.w2q, want_dw=False,
-                                           dx=self.da))
+                                           dx=self.da), "fc2_dgrad")
         T("gemm", lambda: F.linear_bwd(rec, self.dyq, self.aq, self.w2q, want_dx=False,
-                                       dw=self.dw2))
+                                       dw=self.dw2), "fc2_wgrad")
         if not self.fused:
-            T("quant", lambda: F.dgelu_quantize(rec, self.da, self.hq, dh_q=self.dhq))
+            T("quant", lambda: F.dgelu_quantize(rec, self.da, self.hq, dh_q=self.dhq),
+              "dgelu_quantize")
         T("gemm", lambda: F.linear_bwd(rec, self.dhq, self.xq, self.w1q, want_dw=False,
-                                       dx=self.dx))
+                                       dx=self.dx), "fc1_dgrad")
         T("gemm", lambda: F.linear_bwd(rec, self.dhq, self.xq, self.w1q, want_dx=False,
-                                       dw=self.dw1))
+                                       dw=self.dw1), "fc1_wgrad")
 
     def run_e2e(self):
         """Inputs copied from pinned host memory, all results copied back, inside the step."""
@@ -212,10 +215,14 @@ class MlpStep:
         return sum(v.numel() * 2 for v in self.outs.values())
 
     def kernel_stats(self):
-        ms = {"gemm": [], "quant": []}
-        for kind, s, e in self.events:
-            ms[kind].append(s.elapsed_time(e))
-        return ms
+        """Per-kind lists of launch times (ms) and the mean time of each named launch."""
+        ms = {"gemm": [], "gemm_fused": [], "quant": []}
+        by_name = {}
+        for kind, name, s, e in self.events:
+            t = s.elapsed_time(e)
+            ms[kind].append(t)
+            by_name.setdefault(name, []).append(t)
+        return ms, {k: round(statistics.mean(v), 4) for k, v in by_name.items()}
 
 
 def max_over_ranks(value, dist=None, device=None):
@@ -273,7 +280,7 @@ def run_ours(args):
     barrier()
     clk = clocks.stop()
     ms_total = max_over_ranks(t0.elapsed_time(t1), dist if world > 1 else None, dev)
-    ks = st.kernel_stats()
+    ks, per_kernel = st.kernel_stats()
 
     # ---- end-to-end leg (host buffers, copies inside the timed region)
     st.events = None
@@ -293,9 +300,12 @@ def run_ours(args):
     value = whole_job_tflops(world, ms_total, args.steps)
     e2e_value = whole_job_tflops(world, ms_e2e, args.steps)
     hbm, fp8_peak, src = peaks()
+    # the roofline kernel: the plain-store MXFP8 GEMM (four of the six GEMM launches when the
+    # MLP epilogues are fused, all six otherwise); every GEMM of the step has the same flops
     gemm_ms = statistics.mean(ks["gemm"])
     gemm_flops_launch = GEMM_FLOPS / 6
     achieved = gemm_flops_launch / (gemm_ms * 1e-3) / 1e12
+    fused_ms = statistics.mean(ks["gemm_fused"]) if ks["gemm_fused"] else None
     quant_ms_step = sum(ks["quant"]) / args.steps
     quant_gbs = st.quant_bytes / (quant_ms_step * 1e-3) / 1e9
 
@@ -311,16 +321,21 @@ def run_ours(args):
                        "parallelism": "replicas" if world > 1 else "single",
                        "l2": "inputs larger than L2 (~2 GB touched per step)",
                        "gemm_flops_per_step": GEMM_FLOPS},
-            "roofline": {"bound": "tensor", "kernel": "gemm_tn_kernel<G_MX>",
+            "roofline": {"bound": "tensor", "kernel": "gemm_tn_kernel<G_MX> (bf16 store)",
                          "achieved": round(achieved, 1), "peak": fp8_peak, "unit": "TFLOP/s",
                          "frac": round(achieved / fp8_peak, 4), "traffic": None,
                          "peak_source": f"{src}: bf16 x {FP8_OVER_BF16} (nominal fp8/bf16)",
                          "avg_launch_ms": round(gemm_ms, 4)},
+            "fused_gemm": None if fused_ms is None else {
+                "kernel": "gemm_mlp_kernel (GeLU / dGeLU + MXFP8 epilogue)",
+                "avg_launch_ms": round(fused_ms, 4),
+                "tflops": round(gemm_flops_launch / (fused_ms * 1e-3) / 1e12, 1)},
             "quantize": {"gbs": round(quant_gbs, 1), "peak_gbs": hbm,
                          "frac": round(quant_gbs / hbm, 4), "ms_per_step": round(quant_ms_step, 4),
                          "algorithmic_bytes_per_step": st.quant_bytes, "peak_source": src},
             "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s",
                     "h2d_bytes_per_step": st.h2d_bytes(), "d2h_bytes_per_step": st.d2h_bytes()},
+            "kernels_ms": per_kernel,
             "gpu_launches": st.kernels_per_step * args.steps,
             "clocks": clk,
             "cpu_baseline": cpu,
@@ -420,13 +435,16 @@ def run_profile_case(args):
     gemm_mx / gemm_tensorwise / gemm_blockwise: fprop 8192 x 4096 x 4096.
     gelu_mx / dgelu_mx: the standalone GeLU / dGeLU + MXFP8 quantize on h 8192 x 16384.
     gemm_gelu_mx / gemm_dgelu_mx: fc1 with the GeLU epilogue (8192 x 16384 x 4096) and fc2's
-    dgrad with the dGeLU epilogue (8192 x 16384 x 4096)."""
+    dgrad with the dGeLU epilogue (8192 x 16384 x 4096).
+    gemm_mx_mlp: the MLP step's four plain-store MXFP8 GEMMs (fc2 fprop, fc2 wgrad, fc1
+    dgrad, fc1 wgrad) at full size, in that order."""
     import torch
     import scaled_quantize_fp8_gb300 as F
     from scaled_quantize_fp8_gb300 import build as B
     B.build()
     case = args.profile
-    kind = {"mx": "mxfp8"}.get(case.rsplit("_", 1)[1], case.rsplit("_", 1)[1])
+    parts = case.split("_")
+    kind = "mxfp8" if "mx" in parts else parts[-1]
     rec = F.Recipe(kind=kind)
     g = torch.Generator(device="cuda").manual_seed(0)
     if case in ("gemm_gelu_mx", "gemm_dgelu_mx"):
@@ -444,6 +462,23 @@ def run_profile_case(args):
                 F.linear_fwd_gelu(rec, xq, w1q, a_q=a_q, h_q=h_q)
             else:
                 F.linear_dgrad_dgelu(rec, dyq, w2q, h_q, dh_q=dh_q)
+    elif case == "gemm_mx_mlp":
+        M, H, Fd = TOKENS, HIDDEN, FFN
+        x = torch.randn((M, H), device="cuda", generator=g).to(torch.bfloat16)
+        w1 = (torch.randn((Fd, H), device="cuda", generator=g) * 0.02).to(torch.bfloat16)
+        w2 = (torch.randn((H, Fd), device="cuda", generator=g) * 0.02).to(torch.bfloat16)
+        a = torch.randn((M, Fd), device="cuda", generator=g).to(torch.bfloat16)
+        dy = (torch.randn((M, H), device="cuda", generator=g) * 1e-3).to(torch.bfloat16)
+        xq, w1q = F.quantize(rec, x, "activation"), F.quantize(rec, w1, "weight")
+        w2q, aq = F.quantize(rec, w2, "weight"), F.quantize(rec, a, "activation")
+        dyq, dhq = F.quantize(rec, dy, "grad"), F.quantize(rec, a, "grad")
+        y, dx = torch.empty_like(x), torch.empty_like(x)
+        dw1, dw2 = torch.empty_like(w1), torch.empty_like(w2)
+        for _ in range(args.steps):
+            F.linear_fwd(rec, aq, w2q, y=y)                                   # fc2 fprop
+            F.linear_bwd(rec, dyq, aq, None, want_dx=False, dw=dw2)           # fc2 wgrad
+            F.linear_bwd(rec, dhq, None, w1q, want_dw=False, dx=dx)           # fc1 dgrad
+            F.linear_bwd(rec, dhq, xq, None, want_dx=False, dw=dw1)           # fc1 wgrad
     elif case in ("gelu_mx", "dgelu_mx"):
         h = torch.randn((8192, 16384), device="cuda", generator=g).to(torch.bfloat16)
         a_q, h_q, _ = F.gelu_quantize(rec, h)
@@ -473,7 +508,7 @@ def main():
     ap.add_argument("--profile", default=None,
                     choices=["quant_mx", "quant_tensorwise", "quant_blockwise", "gemm_mx",
                              "gemm_tensorwise", "gemm_blockwise", "gelu_mx", "dgelu_mx",
-                             "gemm_gelu_mx", "gemm_dgelu_mx"])
+                             "gemm_gelu_mx", "gemm_dgelu_mx", "gemm_mx_mlp"])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)

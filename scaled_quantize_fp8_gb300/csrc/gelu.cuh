@@ -127,6 +127,23 @@ __device__ __forceinline__ void dgelu_table_fill(void* table, int tid, int nthre
   }
 }
 
+// Table lookups for a word of two bf16 without branching: each half's index is its bits
+// rotated left by one ((magnitude << 1) | sign, the table order) minus the first entry's, so
+// inputs outside the table wrap to indices >= kGeluEntries. Those are clamped (a wrong but
+// harmless read) and reported through *miss (the running maximum of the indices): a caller
+// that sees *miss >= kGeluEntries recomputes the word with gelu_bf16x2.
+__device__ __forceinline__ uint32_t gelu_bf16x2_nobranch(const void* table, uint32_t w,
+                                                         uint32_t* miss) {
+  constexpr uint32_t kBias = 0x10000u - (uint32_t(kGeluExpLo + 127) << 8);
+  const uint32_t r = ((w << 1) & 0xFFFEFFFEu) | ((w >> 15) & 0x00010001u);
+  const uint32_t ilo = (r + kBias) & 0xFFFFu;
+  const uint32_t ihi = (r + (kBias << 16)) >> 16;
+  *miss = max(*miss, max(ilo, ihi));
+  const uint16_t* tb = reinterpret_cast<const uint16_t*>(table);
+  const uint32_t last = uint32_t(kGeluEntries - 1);
+  return uint32_t(tb[min(ilo, last)]) | (uint32_t(tb[min(ihi, last)]) << 16);
+}
+
 // gelu over a word of two bf16 (low half first).
 __device__ __forceinline__ uint32_t gelu_bf16x2(const void* table, uint32_t w) {
   return gelu_table_lookup(table, w & 0xFFFFu) | (gelu_table_lookup(table, w >> 16) << 16);
@@ -141,6 +158,30 @@ __device__ __forceinline__ uint32_t dgelu_bf16x2(const void* table, uint32_t da,
                              dgelu_table_lookup(table, __fmul_rn(hv.x, hs)));
   const float d1 = __fmul_rn(__uint_as_float(da & 0xFFFF0000u),
                              dgelu_table_lookup(table, __fmul_rn(hv.y, hs)));
+  return bf16_rn_bits(d0) | (bf16_rn_bits(d1) << 16);
+}
+
+// dgelu_bf16x2 through the table without branching; out-of-table inputs (|h| outside
+// [2^-20, 2^4), zero, Inf, NaN) are clamped and reported through *miss as for
+// gelu_bf16x2_nobranch, and the caller recomputes the word with dgelu_bf16x2. The index is the
+// float's bits rotated left by one, shifted down to (exponent << 4) | (3 mantissa bits << 1)
+// (the lower mantissa bits of an E4M3 value times a power of two are zero), with the sign
+// in bit 0, minus the first entry's.
+__device__ __forceinline__ uint32_t dgelu_index(float h) {
+  const uint32_t b = __float_as_uint(h);
+  const uint32_t u = __funnelshift_l(b, b, 1);
+  return ((u >> 20) | (u & 1u)) - (uint32_t(kDgeluExpLo + 127) << 4);
+}
+__device__ __forceinline__ uint32_t dgelu_bf16x2_nobranch(const void* table, uint32_t da,
+                                                          uint16_t hcodes, float hs,
+                                                          uint32_t* miss) {
+  const float2 hv = e4m3x2_to_f2(hcodes);
+  const uint32_t i0 = dgelu_index(__fmul_rn(hv.x, hs)), i1 = dgelu_index(__fmul_rn(hv.y, hs));
+  *miss = max(*miss, max(i0, i1));
+  const float* tb = reinterpret_cast<const float*>(table);
+  const uint32_t last = uint32_t(kDgeluEntries - 1);
+  const float d0 = __fmul_rn(__uint_as_float(da << 16), tb[min(i0, last)]);
+  const float d1 = __fmul_rn(__uint_as_float(da & 0xFFFF0000u), tb[min(i1, last)]);
   return bf16_rn_bits(d0) | (bf16_rn_bits(d1) << 16);
 }
 

@@ -36,8 +36,14 @@ namespace fp8lin {
 constexpr int kBM = 128;                      // accumulator rows per CTA (TMEM lanes)
 constexpr int kBN = 256;                      // accumulator columns per tile
 constexpr int kBKBytes = 128;                 // one 128-byte swizzle row of K per stage
-constexpr int kEpiWarps = 8;
-constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
+// Epilogue warps: 8 for plain stores (two per TMEM lane quadrant, 128 columns each); 16 for
+// the fused MLP epilogues (four per quadrant, 64 columns each), whose per-element work needs
+// more warps in flight to hide its latency. Warp 0 is the TMA producer, warp 1 the MMA issuer.
+template <int EPI>
+__host__ __device__ constexpr int epi_warps() { return EPI == EPI_NONE ? 8 : 16; }
+template <int EPI>
+__host__ __device__ constexpr int gemm_threads() { return 64 + 32 * epi_warps<EPI>(); }
+constexpr int kGemmThreads = gemm_threads<EPI_NONE>();
 constexpr uint32_t kTileABytes = kBM * kBKBytes;      // 16 KiB
 constexpr uint32_t kSfStageBytes = 2048;              // SFA 512 B at 0, SFB 2 x 512 B at 512
 constexpr uint32_t kTmemCols = 512;
@@ -47,17 +53,18 @@ constexpr uint64_t kWaitBudgetCycles = 4000000000ull;   // ~2 s at 2 GHz
 // whole 256-row B tile; a CTA pair (CTA2 = 1) owns a 256 x 256 tile, each CTA loading its own
 // 128 rows of A and 128 of the 256 rows of B, so a stage is 32 KiB and six of them fit. The
 // fused MLP epilogues add a 2 KiB transpose buffer per epilogue warp and a GeLU table behind
-// the control block (the GeLU pair kernel gives up one stage for them).
+// the control block (those kernels give up stages for them: five for the pair, three for a
+// single CTA).
 constexpr uint32_t kEpiStageBytes = 2048;              // one warp's 32 x 32 bf16 chunk
 template <int EPI>
 __host__ __device__ constexpr uint32_t epi_smem_bytes() {
   return EPI == EPI_NONE ? 0u
-                         : kEpiWarps * kEpiStageBytes +
+                         : epi_warps<EPI>() * kEpiStageBytes +
                                (EPI == EPI_GELU ? kGeluTableBytes : kDgeluTableBytes);
 }
 template <int CTA2, int EPI = EPI_NONE>
 struct Geo {
-  static constexpr int kStages = CTA2 ? (EPI == EPI_GELU ? 5 : 6) : 4;
+  static constexpr int kStages = CTA2 ? (EPI == EPI_NONE ? 6 : 5) : (EPI == EPI_NONE ? 4 : 3);
   static constexpr uint32_t kTileBBytes = (CTA2 ? kBN / 2 : kBN) * kBKBytes;
   static constexpr uint32_t kStageBytes = kTileABytes + kTileBBytes + kSfStageBytes;
   static constexpr uint32_t kSmemBytes =
@@ -74,6 +81,20 @@ struct SharedCtl {
   uint32_t tmem_base;
   int abort_flag;
 };
+
+// Tile order: the persistent CTAs (pairs) take consecutive tile indices, so consecutive
+// indices walk a group of kTileGroup M tiles before the next N tile. The tiles in flight at
+// once then share a few A and B panels (about 8 x 10 of them for 76 pairs) instead of
+// sweeping all of A for one or two B panels, which keeps the re-reads in L2.
+constexpr int kTileGroup = 8;
+__device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int* mt, int* nt) {
+  const int group_tiles = kTileGroup * tiles_n;
+  const int first_m = (tile / group_tiles) * kTileGroup;
+  const int gm = min(tiles_m - first_m, kTileGroup);        // M tiles in this group
+  const int r = tile % group_tiles;
+  *mt = first_m + r % gm;
+  *nt = r / gm;
+}
 
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, SharedCtl* ctl,
                                          int32_t* status) {
@@ -154,21 +175,17 @@ __device__ __forceinline__ void tmem_load128(uint32_t taddr, float* out) {
   }
 }
 
-// Read 128 accumulator columns and round them to bf16 pairs (low half = even column), the
-// values a bf16 store of the tile would hold. Two batches of 64 keep the raw values short-lived.
-__device__ __forceinline__ void tmem_load128_bf16(uint32_t taddr, uint32_t* out) {
+// Read 64 accumulator columns and round them to bf16 pairs (low half = even column), the
+// values a bf16 store of the tile would hold.
+__device__ __forceinline__ void tmem_load64_bf16(uint32_t taddr, uint32_t* out) {
+  uint32_t r0[32], r1[32];
+  ptx::tmem_ld_32x32b_x32(taddr, r0);
+  ptx::tmem_ld_32x32b_x32(taddr + 32, r1);
+  ptx::tmem_wait_ld();
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    uint32_t r0[32], r1[32];
-    ptx::tmem_ld_32x32b_x32(taddr + 64 * h, r0);
-    ptx::tmem_ld_32x32b_x32(taddr + 64 * h + 32, r1);
-    ptx::tmem_wait_ld();
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      out[32 * h + j] = pack_bf16x2(__uint_as_float(r0[2 * j]), __uint_as_float(r0[2 * j + 1]));
-      out[32 * h + 16 + j] =
-          pack_bf16x2(__uint_as_float(r1[2 * j]), __uint_as_float(r1[2 * j + 1]));
-    }
+  for (int j = 0; j < 16; ++j) {
+    out[j] = pack_bf16x2(__uint_as_float(r0[2 * j]), __uint_as_float(r0[2 * j + 1]));
+    out[16 + j] = pack_bf16x2(__uint_as_float(r1[2 * j]), __uint_as_float(r1[2 * j + 1]));
   }
 }
 
@@ -193,9 +210,9 @@ __device__ __forceinline__ uint32_t quantize_block32(const uint32_t* w, uint8_t*
   return sb;
 }
 
-// Fused MLP epilogue for one thread: row m, columns n .. n+127 of the output (v: 64 bf16
-// pairs), in four 32-column chunks. GELU writes h's MXFP8 row copy, then a = gelu(h);
-// DGELU forms dh = da * gelu'(h) from h's codes (hc, 128 bytes) and scales (hsc, 4 bytes).
+// Fused MLP epilogue for one thread: row m, columns n .. n+63 of the output (v: 32 bf16
+// pairs), in two 32-column chunks. GELU writes h's MXFP8 row copy, then a = gelu(h);
+// DGELU forms dh = da * gelu'(h) from h's codes (hc, 64 bytes) and scales (hsc, 2 bytes).
 // The result's row copy is thread-local (a chunk is one 1x32 block); for the column copy
 // the warp parks its 32 x 32 chunk in shared memory and lane c reads back column c over the
 // warp's 32 rows mrow0 .. mrow0+31, which is one 32-row block of the transposed copy.
@@ -207,22 +224,32 @@ __device__ __forceinline__ void mlp_epilogue(const GemmParams& p, const uint32_t
   const bool v8 = p.o_v8 != 0;
   uint32_t sc_h = 0, sc_o = 0;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+  for (int j = 0; j < 2; ++j) {
     uint32_t w[16];
 #pragma unroll
     for (int k = 0; k < 16; ++k) w[k] = v[16 * j + k];
     if constexpr (EPI == EPI_GELU) {
       sc_h |= quantize_block32(w, p.h_row + int64_t(m) * p.N + n + 32 * j, v8) << (8 * j);
 #pragma unroll
-      for (int k = 0; k < 16; ++k) w[k] = gelu_bf16x2(table, w[k]);
+      for (int k = 0; k < 16; ++k) {
+        uint32_t miss = 0;
+        const uint32_t a = gelu_bf16x2_nobranch(table, w[k], &miss);
+        // an input outside the table (rare): the exact per-element path
+        w[k] = miss >= uint32_t(kGeluEntries) ? gelu_bf16x2(table, w[k]) : a;
+      }
     } else {
       const uint32_t sb = (hsc >> (8 * j)) & 0xFFu;
       const float hs = sb == 0xFFu ? __uint_as_float(0x7FC00000u) : exp2i(int(sb) - 127);
       const uint32_t hw[8] = {hc[2 * j].x,     hc[2 * j].y,     hc[2 * j].z,     hc[2 * j].w,
                               hc[2 * j + 1].x, hc[2 * j + 1].y, hc[2 * j + 1].z, hc[2 * j + 1].w};
 #pragma unroll
-      for (int k = 0; k < 16; ++k)
-        w[k] = dgelu_bf16x2(table, w[k], uint16_t(hw[k >> 1] >> (16 * (k & 1))), hs);
+      for (int k = 0; k < 16; ++k) {
+        const uint16_t hk = uint16_t(hw[k >> 1] >> (16 * (k & 1)));
+        uint32_t miss = 0;
+        const uint32_t d = dgelu_bf16x2_nobranch(table, w[k], hk, hs, &miss);
+        // an h outside the table (rare): the exact per-element path
+        w[k] = miss >= uint32_t(kDgeluEntries) ? dgelu_bf16x2(table, w[k], hk, hs) : d;
+      }
     }
     sc_o |= quantize_block32(w, p.o_row + int64_t(m) * p.N + n + 32 * j, v8) << (8 * j);
 
@@ -245,18 +272,17 @@ __device__ __forceinline__ void mlp_epilogue(const GemmParams& p, const uint32_t
     const uint32_t sbc = quantize_block32(cw, p.o_col + int64_t(c) * p.M + mrow0, v8);
     p.o_col_scale[mx_scale_offset(c, mrow0 >> 5, p.M)] = uint8_t(sbc);
   }
-  const int64_t so = mx_scale_offset(m, n >> 5, p.N);     // four consecutive blocks
-  if constexpr (EPI == EPI_GELU) *reinterpret_cast<uint32_t*>(p.h_scale + so) = sc_h;
-  *reinterpret_cast<uint32_t*>(p.o_row_scale + so) = sc_o;
+  const int64_t so = mx_scale_offset(m, n >> 5, p.N);     // two consecutive blocks
+  if constexpr (EPI == EPI_GELU) *reinterpret_cast<uint16_t*>(p.h_scale + so) = uint16_t(sc_h);
+  *reinterpret_cast<uint16_t*>(p.o_row_scale + so) = uint16_t(sc_o);
 }
 
 template <int MODE, int B128, int CTA2, int EPI>
-__global__ void __launch_bounds__(kGemmThreads, 1)
-    gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA,
-                   const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmSFA,
-                   const __grid_constant__ CUtensorMap tmSFB, const GemmParams p) {
+__device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                             const CUtensorMap& tmSFA, const CUtensorMap& tmSFB,
+                                             const GemmParams& p) {
   using G = Geo<CTA2, EPI>;
+  constexpr int kEpiWarps = epi_warps<EPI>();
   static_assert(EPI == EPI_NONE || MODE == G_MX, "fused MLP epilogues are MXFP8 only");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -321,8 +347,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t ph = 0;
       const int kblocks128 = p.K / 128;       // MX scale atoms per operand row tile
       for (int tile = unit; tile < n_tiles; tile += n_units) {
-        const int m0 = (tile % tiles_m) * G::kTileM + int(rank) * kBM;
-        const int n0 = (tile / tiles_m) * kBN + int(rank) * int(kBRows);
+        int mt, nt;
+        tile_coords(tile, tiles_m, tiles_n, &mt, &nt);
+        const int m0 = mt * G::kTileM + int(rank) * kBM;
+        const int n0 = nt * kBN + int(rank) * int(kBRows);
         for (int kb = 0; kb < nk; ++kb) {
           if (!wait_bar(&ctl->empty[s], ph ^ 1u, ctl, p.status)) goto producer_done;
           uint8_t* a_dst = sA + s * kTileABytes;
@@ -340,7 +368,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             ptx::tma_load_2d_pair(b_dst, &tmB, kb * kBKElems, n0, bar);
             if constexpr (MODE == G_MX) {
               uint8_t* sf = sSF + s * kSfStageBytes;
-              const int nb_pair = (tile / tiles_m) * kBN;          // first B row of the pair
+              const int nb_pair = nt * kBN;                        // first B row of the pair
               ptx::tma_load_2d_pair(sf, &tmSFA, 0, 2 * ((m0 >> 7) * kblocks128 + kb), bar);
               ptx::tma_load_2d_pair(sf + 512, &tmSFB, 0,
                                     2 * ((nb_pair >> 7) * kblocks128 + kb), bar);
@@ -465,9 +493,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ------------------------------------------------------------ epilogue warps
     const int ew = warp - 2;
     const int quad = warp & 3;            // TMEM lane quadrant this warp may access
-    const int half = ew >> 2;             // which 128 columns of the 256-wide tile
+    constexpr int kCols = 4 * kBN / kEpiWarps;              // accumulator columns per warp
+    static_assert(EPI != EPI_NONE || kCols == 128, "plain epilogue: 128 columns per warp");
+    const int slice = ew >> 2;            // which kCols columns of the 256-wide tile
     const int row = 32 * quad + lane;
-    const uint32_t t_lane = tmem + (uint32_t(32 * quad) << 16) + uint32_t(half * 128);
+    const uint32_t t_lane = tmem + (uint32_t(32 * quad) << 16) + uint32_t(slice * kCols);
     // accumulator-empty arrivals go to the leader's barrier (a remote arrive from the peer)
     auto release_acc = [&](uint32_t b) {
       ptx::tc_fence_before();
@@ -486,27 +516,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");   // epilogue warps only
       uint32_t u = 0;
       for (int tile = unit; tile < n_tiles; tile += n_units) {
-        const int m0 = (tile % tiles_m) * G::kTileM + int(rank) * kBM;
-        const int n0 = (tile / tiles_m) * kBN;
-        const int m = m0 + row, n = n0 + half * 128;
+        int mt, nt;
+        tile_coords(tile, tiles_m, tiles_n, &mt, &nt);
+        const int m0 = mt * G::kTileM + int(rank) * kBM;
+        const int n0 = nt * kBN;
+        const int m = m0 + row, n = n0 + slice * kCols;
         const int mrow0 = m0 + 32 * quad;
-        // M and N are multiples of 128, so a warp's 32 rows x 128 columns are all in or all out
+        // M and N are multiples of 128, so a warp's 32 rows x 64 columns are all in or all out
         const bool live = mrow0 < p.M && n < p.N;
-        uint4 hc[8];
+        uint4 hc[4];
         uint32_t hsc = 0;
         if constexpr (EPI == EPI_DGELU) {
           // h's codes and scales do not depend on the accumulator: fetch them first
           if (live) {
             const uint8_t* src = p.h_row + int64_t(m) * p.N + n;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) hc[i] = ldg_nc_v4(src + 16 * i);
-            hsc = __ldg(reinterpret_cast<const uint32_t*>(p.h_scale + mx_scale_offset(m, n >> 5, p.N)));
+            for (int i = 0; i < 4; ++i) hc[i] = ldg_nc_v4(src + 16 * i);
+            hsc = __ldg(reinterpret_cast<const uint16_t*>(p.h_scale +
+                                                          mx_scale_offset(m, n >> 5, p.N)));
           }
         }
         if (!wait_bar(&ctl->accf[0], u & 1u, ctl, p.status)) break;
         ptx::tc_fence_after();
-        uint32_t v[64];
-        tmem_load128_bf16(t_lane, v);
+        uint32_t v[32];
+        tmem_load64_bf16(t_lane, v);
         release_acc(0);
         ++u;
         if (live) mlp_epilogue<EPI>(p, v, hc, hsc, m, n, mrow0, stage, table, lane);
@@ -517,9 +550,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t u = 0;
     float acc[128];
     for (int tile = unit; tile < n_tiles; tile += n_units) {
-      const int m0 = (tile % tiles_m) * G::kTileM + int(rank) * kBM;
-      const int n0 = (tile / tiles_m) * kBN;
-      const int m = m0 + row, n = n0 + half * 128;
+      int mt, nt;
+      tile_coords(tile, tiles_m, tiles_n, &mt, &nt);
+      const int m0 = mt * G::kTileM + int(rank) * kBM;
+      const int n0 = nt * kBN;
+      const int m = m0 + row, n = n0 + slice * kCols;
       if constexpr (MODE != G_BLOCK) {
         const uint32_t b = u % kNumAcc;
         if (!wait_bar(&ctl->accf[b], (u / kNumAcc) & 1u, ctl, p.status)) break;
@@ -597,6 +632,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 }
 
+// Plain GEMMs: 10 warps; two SM sub-partitions hold three of them, so 168 registers a thread.
+template <int MODE, int B128, int CTA2>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA,
+                   const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmSFA,
+                   const __grid_constant__ CUtensorMap tmSFB, const GemmParams p) {
+  gemm_tn_body<MODE, B128, CTA2, EPI_NONE>(tmA, tmB, tmSFA, tmSFB, p);
+}
+
+// Fused MLP GEMMs: 18 warps, five on two of the sub-partitions, so at most 96 registers.
+template <int CTA2, int EPI>
+__global__ void __maxnreg__(96)
+    gemm_mlp_kernel(const __grid_constant__ CUtensorMap tmA,
+                    const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmSFA,
+                    const __grid_constant__ CUtensorMap tmSFB, const GemmParams p) {
+  gemm_tn_body<G_MX, 1, CTA2, EPI>(tmA, tmB, tmSFA, tmSFB, p);
+}
+
 // ------------------------------------------------------------------------------------
 // Host side: tensor maps and launch
 // ------------------------------------------------------------------------------------
@@ -610,6 +665,7 @@ static bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, i
 template <int MODE, int B128, int CTA2, int EPI = EPI_NONE>
 static cudaError_t launch_mode(const GemmLaunch& g, cudaStream_t st) {
   using G = Geo<CTA2, EPI>;
+  static_assert(EPI == EPI_NONE || (MODE == G_MX && B128 == 1), "fused: MXFP8 only");
   CUtensorMap ma, mb;
   const int eb = MODE == G_BF16 ? 2 : 1;
   if (!make_operand_map(&ma, g.A, g.p.M, g.p.K, eb, kBM)) return cudaErrorInvalidValue;
@@ -624,7 +680,10 @@ static cudaError_t launch_mode(const GemmLaunch& g, cudaStream_t st) {
     if (!make_tmap_2d(&msfb, g.p.sfb, 1, 256, 2 * (int64_t(g.p.N) / 128) * kb, 256, 2, false))
       return cudaErrorInvalidValue;
   }
-  auto kern = gemm_tn_kernel<MODE, B128, CTA2, EPI>;
+  auto kern = [] {
+    if constexpr (EPI == EPI_NONE) return gemm_tn_kernel<MODE, B128, CTA2>;
+    else return gemm_mlp_kernel<CTA2, EPI>;
+  }();
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -641,7 +700,7 @@ static cudaError_t launch_mode(const GemmLaunch& g, cudaStream_t st) {
   const int units = std::max(1, std::min(tiles, CTA2 ? sms / 2 : sms));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(units * (CTA2 ? 2 : 1)));
-  cfg.blockDim = dim3(kGemmThreads);
+  cfg.blockDim = dim3(gemm_threads<EPI>());
   cfg.dynamicSmemBytes = G::kSmemBytes;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
