@@ -41,12 +41,17 @@ constexpr int kBKBytes = 128;                 // one 128-byte swizzle row of K p
 // more warps in flight to hide its latency. Warp 0 is the TMA producer, warp 1 the MMA issuer.
 template <int EPI>
 __host__ __device__ constexpr int epi_warps() { return EPI == EPI_NONE ? 8 : 16; }
-template <int EPI>
-__host__ __device__ constexpr int gemm_threads() { return 64 + 32 * epi_warps<EPI>(); }
-constexpr int kGemmThreads = gemm_threads<EPI_NONE>();
+// MXFP8 kernels add one warp that copies each stage's scale factors into TMEM, so the MMA
+// issuer's instruction stream holds nothing but MMAs.
+template <int MODE, int EPI>
+__host__ __device__ constexpr int gemm_threads() {
+  return 64 + 32 * epi_warps<EPI>() + (MODE == G_MX ? 32 : 0);
+}
 constexpr uint32_t kTileABytes = kBM * kBKBytes;      // 16 KiB
 constexpr uint32_t kSfStageBytes = 2048;              // SFA 512 B at 0, SFB 2 x 512 B at 512
 constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSfCols = 16;                      // MX scale-factor columns per stage
+static_assert(256 + kSfCols * 6 <= 512, "MX scale-factor columns behind the accumulator");
 constexpr uint64_t kWaitBudgetCycles = 4000000000ull;   // ~2 s at 2 GHz
 
 // Per-configuration geometry. A single CTA (CTA2 = 0) owns a 128 x 256 tile and loads the
@@ -76,6 +81,7 @@ struct Geo {
 struct SharedCtl {
   uint64_t full[6];
   uint64_t empty[6];
+  uint64_t sfr[6];                  // MX: stage's scale factors are in TMEM
   uint64_t accf[2];
   uint64_t acce[2];
   uint32_t tmem_base;
@@ -312,6 +318,7 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
     for (int s = 0; s < G::kStages; ++s) {
       ptx::mbar_init(&ctl->full[s], 1);
       ptx::mbar_init(&ctl->empty[s], 1);
+      ptx::mbar_init(&ctl->sfr[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&ctl->accf[b], 1);
@@ -406,7 +413,7 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
     // ------------------------------------------------------------ MMA issuer (leader)
     if (lane == 0 && leader) {
       const uint32_t idesc = instr_desc<MODE, CTA2>();
-      const uint32_t sfa_t = tmem + 256, sfb_t = tmem + 260;   // MX scale-factor columns
+      const uint32_t sf_base = tmem + 256;      // MX scale factors: kSfCols columns a stage
       int s = 0;
       uint32_t ph = 0;
       uint32_t u = 0;
@@ -430,25 +437,14 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
             ptx::tc_fence_after();
             d_t = tmem + b * kBN;
           }
-          if (!wait_bar(&ctl->full[s], ph, ctl, p.status)) goto mma_done;
+          // MX: the scale-factor warp signals once the stage's operands have landed and its
+          // scales are in TMEM; other modes wait for the operands themselves
+          uint64_t* ready = MODE == G_MX ? &ctl->sfr[s] : &ctl->full[s];
+          if (!wait_bar(ready, ph, ctl, p.status)) goto mma_done;
           ptx::tc_fence_after();
           const uint32_t a_addr = ptx::smem_u32(sA + s * kTileABytes);
           const uint32_t b_addr = ptx::smem_u32(sB + s * G::kTileBBytes);
-          if constexpr (MODE == G_MX) {
-            const uint32_t sf = ptx::smem_u32(sSF + s * kSfStageBytes);
-            const uint64_t d0 = ptx::smem_desc(sf, 0, 128, ptx::kSwizzleNone);
-            const uint64_t d1 = ptx::smem_desc(sf + 512, 0, 128, ptx::kSwizzleNone);
-            const uint64_t d2 = ptx::smem_desc(sf + 1024, 0, 128, ptx::kSwizzleNone);
-            if constexpr (CTA2) {
-              ptx::tmem_cp_32x128b_warpx4_pair(sfa_t, d0);
-              ptx::tmem_cp_32x128b_warpx4_pair(sfb_t, d1);
-              ptx::tmem_cp_32x128b_warpx4_pair(sfb_t + 4, d2);
-            } else {
-              ptx::tmem_cp_32x128b_warpx4(sfa_t, d0);
-              ptx::tmem_cp_32x128b_warpx4(sfb_t, d1);
-              ptx::tmem_cp_32x128b_warpx4(sfb_t + 4, d2);
-            }
-          }
+          const uint32_t sfa_t = sf_base + kSfCols * uint32_t(s), sfb_t = sfa_t + 4;
 #pragma unroll
           for (int k = 0; k < kBKBytes / 32; ++k) {
             const uint64_t ad = ptx::smem_desc(a_addr + 32 * k, 16, 1024, ptx::kSwizzle128B);
@@ -489,7 +485,7 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
       }
     mma_done:;
     }
-  } else {
+  } else if (warp < 2 + kEpiWarps) {
     // ------------------------------------------------------------ epilogue warps
     const int ew = warp - 2;
     const int quad = warp & 3;            // TMEM lane quadrant this warp may access
@@ -615,6 +611,44 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
       store_row128(p, m, n, acc);
     }
     }
+  } else if constexpr (MODE == G_MX) {
+    // ------------------------------------------------------------ scale-factor copier
+    // (leader) Once a stage's loads have landed, copy its E8M0 atoms from shared memory into
+    // that stage's TMEM columns (A's own atom, then the pair's two B atoms) and signal the MMA
+    // issuer through sfr. A stage's columns are rewritten only after its smem slot has been
+    // released by the MMAs that read them and refilled.
+    if (lane == 0 && leader) {
+      const uint32_t sf_base = tmem + 256;
+      int s = 0;
+      uint32_t ph = 0;
+      for (int tile = unit; tile < n_tiles; tile += n_units) {
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!wait_bar(&ctl->full[s], ph, ctl, p.status)) goto sf_done;
+          ptx::tc_fence_after();
+          const uint32_t sfa_t = sf_base + kSfCols * uint32_t(s), sfb_t = sfa_t + 4;
+          const uint32_t sf = ptx::smem_u32(sSF + s * kSfStageBytes);
+          const uint64_t d0 = ptx::smem_desc(sf, 0, 128, ptx::kSwizzleNone);
+          const uint64_t d1 = ptx::smem_desc(sf + 512, 0, 128, ptx::kSwizzleNone);
+          const uint64_t d2 = ptx::smem_desc(sf + 1024, 0, 128, ptx::kSwizzleNone);
+          if constexpr (CTA2) {
+            ptx::tmem_cp_32x128b_warpx4_pair(sfa_t, d0);
+            ptx::tmem_cp_32x128b_warpx4_pair(sfb_t, d1);
+            ptx::tmem_cp_32x128b_warpx4_pair(sfb_t + 4, d2);
+            ptx::mma_commit_pair(&ctl->sfr[s], 0x1);     // the leader's barrier only
+          } else {
+            ptx::tmem_cp_32x128b_warpx4(sfa_t, d0);
+            ptx::tmem_cp_32x128b_warpx4(sfb_t, d1);
+            ptx::tmem_cp_32x128b_warpx4(sfb_t + 4, d2);
+            ptx::mma_commit(&ctl->sfr[s]);
+          }
+          if (++s == G::kStages) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+    sf_done:;
+    }
   }
 
   __syncthreads();
@@ -632,9 +666,10 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
   }
 }
 
-// Plain GEMMs: 10 warps; two SM sub-partitions hold three of them, so 168 registers a thread.
+// Plain GEMMs: 10 warps (11 for MXFP8); some SM sub-partitions hold three of them, so at most
+// 168 registers a thread.
 template <int MODE, int B128, int CTA2>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __maxnreg__(168)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmSFA,
@@ -642,7 +677,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   gemm_tn_body<MODE, B128, CTA2, EPI_NONE>(tmA, tmB, tmSFA, tmSFB, p);
 }
 
-// Fused MLP GEMMs: 18 warps, five on two of the sub-partitions, so at most 96 registers.
+// Fused MLP GEMMs: 19 warps, five on three of the sub-partitions, so at most 96 registers.
 template <int CTA2, int EPI>
 __global__ void __maxnreg__(96)
     gemm_mlp_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -700,7 +735,7 @@ static cudaError_t launch_mode(const GemmLaunch& g, cudaStream_t st) {
   const int units = std::max(1, std::min(tiles, CTA2 ? sms / 2 : sms));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(units * (CTA2 ? 2 : 1)));
-  cfg.blockDim = dim3(gemm_threads<EPI>());
+  cfg.blockDim = dim3(gemm_threads<MODE, EPI>());
   cfg.dynamicSmemBytes = G::kSmemBytes;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
