@@ -161,27 +161,37 @@ __device__ __forceinline__ uint32_t dgelu_bf16x2(const void* table, uint32_t da,
   return bf16_rn_bits(d0) | (bf16_rn_bits(d1) << 16);
 }
 
-// dgelu_bf16x2 through the table without branching; out-of-table inputs (|h| outside
-// [2^-20, 2^4), zero, Inf, NaN) are clamped and reported through *miss as for
-// gelu_bf16x2_nobranch, and the caller recomputes the word with dgelu_bf16x2. The index is the
-// float's bits rotated left by one, shifted down to (exponent << 4) | (3 mantissa bits << 1)
-// (the lower mantissa bits of an E4M3 value times a power of two are zero), with the sign
-// in bit 0, minus the first entry's.
-__device__ __forceinline__ uint32_t dgelu_index(float h) {
-  const uint32_t b = __float_as_uint(h);
-  const uint32_t u = __funnelshift_l(b, b, 1);
-  return ((u >> 20) | (u & 1u)) - (uint32_t(kDgeluExpLo + 127) << 4);
+// gelu'(h) as the standalone kernels define it: 1/2 at h = +-0, gelu_grad_f32 elsewhere (the
+// values their table lookups return).
+__device__ __forceinline__ float gelu_grad_value(float h) {
+  return (__float_as_uint(h) & 0x7FFFFFFFu) == 0u ? 0.5f : gelu_grad_f32(h);
 }
-__device__ __forceinline__ uint32_t dgelu_bf16x2_nobranch(const void* table, uint32_t da,
-                                                          uint16_t hcodes, float hs,
-                                                          uint32_t* miss) {
-  const float2 hv = e4m3x2_to_f2(hcodes);
-  const uint32_t i0 = dgelu_index(__fmul_rn(hv.x, hs)), i1 = dgelu_index(__fmul_rn(hv.y, hs));
-  *miss = max(*miss, max(i0, i1));
-  const float* tb = reinterpret_cast<const float*>(table);
-  const uint32_t last = uint32_t(kDgeluEntries - 1);
-  const float d0 = __fmul_rn(__uint_as_float(da << 16), tb[min(i0, last)]);
-  const float d1 = __fmul_rn(__uint_as_float(da & 0xFFFF0000u), tb[min(i1, last)]);
+
+// gelu' by (E8M0 scale byte, E4M3 code) for the fused dgrad epilogue. Within one MXFP8 block the
+// scale byte is fixed, so h = decode(code) * 2^(sb - 127) is a function of the code byte alone:
+// row sb - kDgeluSbLo of the table holds gelu_grad_value of each of the 256 codes (zero,
+// subnormals and NaN included), and the per-element work is a single indexed load. Blocks whose
+// scale byte falls outside the rows (|h| above about 2^5 or below 2^-17 in the whole block) take
+// the direct evaluation.
+constexpr int kDgeluSbLo = 110, kDgeluSbRows = 16;
+constexpr uint32_t kDgeluCodeTableBytes = kDgeluSbRows * 256 * 4;
+
+__device__ __forceinline__ void dgelu_code_table_fill(void* table, int tid, int nthreads) {
+  float* tb = reinterpret_cast<float*>(table);
+  for (int idx = tid; idx < kDgeluSbRows * 256; idx += nthreads) {
+    const int sb = kDgeluSbLo + (idx >> 8);
+    const float hv = e4m3x2_to_f2(uint16_t(idx & 0xFF)).x;
+    tb[idx] = gelu_grad_value(__fmul_rn(hv, exp2i(sb - 127)));
+  }
+}
+
+// dh for two elements of a block outside the table rows: direct evaluation (rare, out of line).
+static __device__ __noinline__ uint32_t dgelu_bf16x2_direct(uint32_t da, uint32_t hcodes,
+                                                           float hs) {
+  const float2 hv = e4m3x2_to_f2(uint16_t(hcodes));
+  const float d0 = __fmul_rn(__uint_as_float(da << 16), gelu_grad_value(__fmul_rn(hv.x, hs)));
+  const float d1 =
+      __fmul_rn(__uint_as_float(da & 0xFFFF0000u), gelu_grad_value(__fmul_rn(hv.y, hs)));
   return bf16_rn_bits(d0) | (bf16_rn_bits(d1) << 16);
 }
 

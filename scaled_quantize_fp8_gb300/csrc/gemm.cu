@@ -65,7 +65,7 @@ template <int EPI>
 __host__ __device__ constexpr uint32_t epi_smem_bytes() {
   return EPI == EPI_NONE ? 0u
                          : epi_warps<EPI>() * kEpiStageBytes +
-                               (EPI == EPI_GELU ? kGeluTableBytes : kDgeluTableBytes);
+                               (EPI == EPI_GELU ? kGeluTableBytes : kDgeluCodeTableBytes);
 }
 template <int CTA2, int EPI = EPI_NONE>
 struct Geo {
@@ -245,16 +245,23 @@ __device__ __forceinline__ void mlp_epilogue(const GemmParams& p, const uint32_t
       }
     } else {
       const uint32_t sb = (hsc >> (8 * j)) & 0xFFu;
-      const float hs = sb == 0xFFu ? __uint_as_float(0x7FC00000u) : exp2i(int(sb) - 127);
       const uint32_t hw[8] = {hc[2 * j].x,     hc[2 * j].y,     hc[2 * j].z,     hc[2 * j].w,
                               hc[2 * j + 1].x, hc[2 * j + 1].y, hc[2 * j + 1].z, hc[2 * j + 1].w};
+      if (sb - uint32_t(kDgeluSbLo) < uint32_t(kDgeluSbRows)) {
+        // gelu' straight from the code byte through this block's table row
+        const float* row = reinterpret_cast<const float*>(table) + (sb - kDgeluSbLo) * 256;
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const uint16_t hk = uint16_t(hw[k >> 1] >> (16 * (k & 1)));
-        uint32_t miss = 0;
-        const uint32_t d = dgelu_bf16x2_nobranch(table, w[k], hk, hs, &miss);
-        // an h outside the table (rare): the exact per-element path
-        w[k] = miss >= uint32_t(kDgeluEntries) ? dgelu_bf16x2(table, w[k], hk, hs) : d;
+        for (int k = 0; k < 16; ++k) {
+          const uint32_t c = hw[k >> 1] >> (16 * (k & 1));
+          const float d0 = __fmul_rn(bf16_lo(w[k]), row[c & 0xFFu]);
+          const float d1 = __fmul_rn(bf16_hi(w[k]), row[(c >> 8) & 0xFFu]);
+          w[k] = bf16_rn_bits(d0) | (bf16_rn_bits(d1) << 16);
+        }
+      } else {
+        const float hs = sb == 0xFFu ? __uint_as_float(0x7FC00000u) : exp2i(int(sb) - 127);
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          w[k] = dgelu_bf16x2_direct(w[k], hw[k >> 1] >> (16 * (k & 1)), hs);
       }
     }
     sc_o |= quantize_block32(w, p.o_row + int64_t(m) * p.N + n + 32 * j, v8) << (8 * j);
@@ -508,7 +515,7 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
       uint8_t* stage = sEpi + ew * kEpiStageBytes;
       void* table = sEpi + kEpiWarps * kEpiStageBytes;
       if constexpr (EPI == EPI_GELU) gelu_table_fill(table, int(threadIdx.x) - 64, 32 * kEpiWarps);
-      else dgelu_table_fill(table, int(threadIdx.x) - 64, 32 * kEpiWarps);
+      else dgelu_code_table_fill(table, int(threadIdx.x) - 64, 32 * kEpiWarps);
       asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");   // epilogue warps only
       uint32_t u = 0;
       for (int tile = unit; tile < n_tiles; tile += n_units) {

@@ -116,6 +116,51 @@ def test_fc2_dgrad_dgelu_fused(M, Fd, H):
                      np.ascontiguousarray(dh_g.T), np.ascontiguousarray(dh_r.T))
 
 
+def test_fc2_dgrad_dgelu_fused_wide_scales():
+    """h blocks spread over many MXFP8 scales (tiny, ordinary, large), plus zero, Inf and NaN
+    blocks: the epilogue's per-block gelu' table rows and its direct path for blocks outside
+    them must give the unfused kernels' bytes, and the oracle's where dh is finite."""
+    rec = F.Recipe(kind="mxfp8")
+    M, Fd, H = 256, 512, 256
+    hb = bf16_bits_normal(M, Fd, seed=61, stream=0, sigma=1.0)
+    h = O.bf16_to_f32(hb).reshape(M, Fd // 32, 32).astype(np.float64)
+    factors = np.array([2.0 ** -30, 2.0 ** -20, 2.0 ** -12, 1e-3, 1.0, 4.0, 2.0 ** 6, 2.0 ** 9,
+                        2.0 ** 14, 2.0 ** 40])
+    h *= factors[np.arange(M * (Fd // 32)).reshape(M, Fd // 32) % len(factors)][:, :, None]
+    h[3, 5, :] = 0.0
+    h[7, 2, 4] = np.inf
+    h[9, 1, 7] = np.nan
+    h[11, 3, 0] = -np.inf
+    hb = O.f64_to_bf16(h.reshape(M, Fd))
+    dyb = bf16_bits_normal(M, H, seed=62, stream=2, sigma=1e-3)
+    w2b = bf16_bits_normal(H, Fd, seed=63, stream=3, sigma=0.02)
+    _, h_q, _ = F.gelu_quantize(rec, to_dev_bf16(hb))
+    dyq = F.quantize(rec, to_dev_bf16(dyb), "grad")
+    w2q = F.quantize(rec, to_dev_bf16(w2b), "weight")
+    dh_q = F.linear_dgrad_dgelu(rec, dyq, w2q, h_q)
+    da, _ = F.linear_bwd(rec, dyq, None, w2q, want_dw=False)
+    dh_u, dh_bf16 = F.dgelu_quantize(rec, da, h_q, want_dh_bf16=True)
+    torch.cuda.synchronize()
+    _same_qtensor(dh_q, dh_u, ("row", "row_scale", "col", "col_scale"))
+    qh = O.quantize_mxfp8(hb, want_col=False)
+    assert np.array_equal(_np(h_q.row), qh["row"])
+    sc = mx_untile(_np(h_q.row_scale), M, Fd)
+    assert np.array_equal(sc, qh["row_scale"])
+    assert sc.min() < 110 and 126 <= sc[sc < 255].max() and (sc == 255).any()
+    qdy = O.quantize_mxfp8(dyb, want_col=False)
+    qw2t = O.quantize_mxfp8(np.ascontiguousarray(w2b.T), want_col=False)
+    da_r = O.f64_to_bf16(O.gemm_tn_f64(O.dequant_mx(qdy["row"], qdy["row_scale"]),
+                                       O.dequant_mx(qw2t["row"], qw2t["row_scale"])))
+    dh_r = O.dgelu_bf16(da_r, qh["row"], qh["row_scale"])
+    dh_g = from_dev_bf16(dh_bf16)
+    # NaN blocks of dh (from the Inf / NaN h blocks): codes and scale marked NaN on both sides
+    nan_r = np.isnan(O.bf16_to_f32(dh_r)).reshape(M, Fd // 32, 32).any(axis=2)
+    assert np.array_equal(nan_r, (mx_untile(_np(dh_q.row_scale), M, Fd) == 255))
+    fin_rows = ~nan_r.any(axis=1)
+    _check_mx_blocks(_np(dh_q.row)[fin_rows], mx_untile(_np(dh_q.row_scale), M, Fd)[fin_rows],
+                     dh_g[fin_rows], dh_r[fin_rows])
+
+
 def _mlp_fused(M, H, Fd, seed):
     """The whole MXFP8 MLP block through the fused steps, final GEMM outputs against the oracle
     run end to end on the same seeded inputs.
