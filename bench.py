@@ -41,6 +41,11 @@ KERNELS_PER_STEP_UNFUSED = 12                         # plus standalone gelu and
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FP8_OVER_BF16 = 2.0                                   # nominal dense fp8 / bf16 rate
+# DRAM bytes (read + write) per launch of the plain-store MXFP8 GEMM: the average over the
+# step's four such launches in one capture of `ncu --metrics dram__bytes_read.sum,
+# dram__bytes_write.sum -k regex:gemm_tn_kernel -s 4 -c 4 python bench.py --profile
+# gemm_mx_mlp --steps 2`. Reset to None whenever that kernel changes.
+GEMM_TRAFFIC_BYTES = 550.0e6
 
 
 def peaks():
@@ -323,7 +328,8 @@ def run_ours(args):
                        "gemm_flops_per_step": GEMM_FLOPS},
             "roofline": {"bound": "tensor", "kernel": "gemm_tn_kernel<G_MX> (bf16 store)",
                          "achieved": round(achieved, 1), "peak": fp8_peak, "unit": "TFLOP/s",
-                         "frac": round(achieved / fp8_peak, 4), "traffic": None,
+                         "frac": round(achieved / fp8_peak, 4),
+                         "traffic": GEMM_TRAFFIC_BYTES if st.fused else None,
                          "peak_source": f"{src}: bf16 x {FP8_OVER_BF16} (nominal fp8/bf16)",
                          "avg_launch_ms": round(gemm_ms, 4)},
             "fused_gemm": None if fused_ms is None else {
@@ -503,6 +509,52 @@ def run_profile_case(args):
     print(f"profile case {case}: {args.steps} launches done")
 
 
+def run_kernels(args):
+    """Per-recipe kernel timings (prints one JSON object; not the benchmark line): quantize of an
+    8192 x 4096 bf16 activation (row + column copies) and the fprop GEMM 8192 x 4096 x 4096 and
+    4096^3, each the mean of 20 launches timed with CUDA events after 5 warm-up launches."""
+    import torch
+    import scaled_quantize_fp8_gb300 as F
+    from scaled_quantize_fp8_gb300 import build as B
+    B.build()
+
+    def timed(fn, reps=20, warm=5):
+        for _ in range(warm):
+            fn()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(reps):
+            fn()
+        e.record()
+        torch.cuda.synchronize()
+        return s.elapsed_time(e) / reps
+
+    g = torch.Generator(device="cuda").manual_seed(0)
+    M, N, K = 8192, 4096, 4096
+    x = torch.randn((M, K), device="cuda", generator=g).to(torch.bfloat16)
+    w = (torch.randn((N, K), device="cuda", generator=g) * 0.02).to(torch.bfloat16)
+    out = {}
+    for kind in ("mxfp8", "tensorwise", "delayed", "blockwise"):
+        rec = F.Recipe(kind=kind)
+        qx = F.empty_qtensor(rec, M, K, "activation")
+        ws = torch.empty(max(1, F.workspace_bytes(rec, M, K)), dtype=torch.uint8, device="cuda")
+        ms = timed(lambda: F.quantize(rec, x, "activation", out=qx, workspace=ws))
+        per_elt = {"mxfp8": 2 + 2 + 2 / 32.0, "blockwise": 2 + 2 + 2 * 4 / 128.0}.get(kind, 4.0)
+        out[f"quantize_{kind}"] = {"ms": round(ms, 4),
+                                   "GB/s": round(M * K * per_elt / ms / 1e6, 1)}
+        qw = F.quantize(rec, w, "weight")
+        y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        ms = timed(lambda: F.linear_fwd(rec, qx, qw, y=y))
+        qx4 = F.quantize(rec, x[:4096].contiguous(), "activation")
+        y4 = torch.empty((4096, N), dtype=torch.bfloat16, device="cuda")
+        ms4 = timed(lambda: F.linear_fwd(rec, qx4, qw, y=y4))
+        out[f"gemm_{kind}"] = {"8192x4096x4096_TFLOP/s": round(2 * M * N * K / ms / 1e9, 1),
+                               "4096^3_TFLOP/s": round(2 * 4096 ** 3 / ms4 / 1e9, 1)}
+    torch.cuda.synchronize()
+    print(json.dumps({"kernels": out}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--profile", default=None,
@@ -513,6 +565,8 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--kernels", action="store_true",
+                    help="per-recipe quantize and GEMM timings instead of the benchmark step")
     ap.add_argument("--unfused", action="store_true",
                     help="standalone GeLU / dGeLU kernels instead of the fused GEMM epilogues")
     args = ap.parse_args()
@@ -520,6 +574,8 @@ def main():
         args.warmup = 3
     if args.profile:
         run_profile_case(args)
+    elif args.kernels:
+        run_kernels(args)
     elif args.impl == "reference":
         run_reference(args)
     else:
