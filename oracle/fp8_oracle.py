@@ -15,6 +15,12 @@ where they are silent the readings below are the plainest ones the rest supports
   * E4M3 is the OCP 8-bit "E4M3FN" format: bias 7, no infinities, 0x7F/0xFF NaN,
     max 448 (0x7E), min subnormal 2^-9 (0x01). Encoding rounds to nearest, ties to even,
     and saturates finite overflow and +-inf to +-448; -0 keeps its sign.
+  * The "hybrid" format (--fp8-format hybrid, delayed / tensorwise / blockwise only) keeps
+    activations and weights in E4M3 and stores gradients in E5M2, the OCP 8-bit format with
+    bias 15, two mantissa bits, +-inf at 0x7C/0xFC, NaN 0x7D-0x7F, max 57344 (0x7B), min
+    subnormal 2^-16 (0x01). It is encoded like E4M3 (round to nearest even, finite overflow
+    and +-inf saturate to +-57344, NaN -> 0x7F with the input's sign) and its scales use
+    57344 in place of 448.
   * Per-tensor scale (tensorwise, delayed, and per block for blockwise):
     s = fp32(448 / amax) * 2^-margin, one IEEE fp32 division; s = 1 when amax is 0 or not
     finite; an infinite s is clamped to FLT_MAX; the stored dequantisation factor is
@@ -52,6 +58,10 @@ import numpy as np
 E4M3_MAX = 448.0
 E4M3_MIN_NORMAL_EXP = -6      # smallest normal binade: [2^-6, 2^-5)
 E4M3_MANTISSA_BITS = 3
+E5M2_MAX = 57344.0
+E5M2_MIN_NORMAL_EXP = -14
+E5M2_MANTISSA_BITS = 2
+FP8_MAX = {"e4m3": E4M3_MAX, "e5m2": E5M2_MAX}
 FLT_MAX = np.float32(np.finfo(np.float32).max)
 MX_BLOCK = 32
 BW_BLOCK = 128
@@ -142,11 +152,71 @@ def e4m3_encode(v):
 
 
 # --------------------------------------------------------------------------------------
+# E5M2 (OCP E5M2), the gradient format of the hybrid recipe
+# --------------------------------------------------------------------------------------
+
+def e5m2_decode(codes):
+    """E5M2 codes -> float64: e == 0 gives m * 2^-16, e == 31 gives +-inf (m = 0) or NaN,
+    else (1 + m/4) * 2^(e-15)."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    s = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 2) & 0x1F
+    m = c & 0x3
+    mag = np.where(e == 0, m * 2.0 ** -16, (1.0 + m / 4.0) * np.ldexp(1.0, e - 15))
+    mag = np.where(e == 31, np.where(m == 0, np.inf, np.nan), mag)
+    return s * mag
+
+
+def e5m2_encode(v):
+    """float32 values -> E5M2 codes, round to nearest with ties to even, saturating.
+
+    As for E4M3: the binade [2^E, 2^(E+1)) (E never below -14) has the quantum 2^(E-2); the
+    magnitude is rounded half-to-even to a count of quanta (a count of 8 carries into the next
+    binade). Magnitudes >= 57344, infinity included, give 57344; NaN gives 0x7F (with sign).
+    """
+    v = np.asarray(v, dtype=np.float32)
+    a = np.abs(v.astype(np.float64))
+    sign = np.where(np.signbit(v), 0x80, 0x00).astype(np.int64)
+    nan = np.isnan(v)
+    sat = (a >= E5M2_MAX) & ~nan
+    a_ok = np.where(sat | nan, 0.0, a)
+    _, ex = np.frexp(a_ok)
+    E = np.maximum(ex - 1, E5M2_MIN_NORMAL_EXP)
+    quantum = np.ldexp(1.0, E - E5M2_MANTISSA_BITS)
+    val = np.rint(a_ok / quantum) * quantum      # an E5M2 magnitude, <= 57344
+    _, vex = np.frexp(val)
+    vE = vex - 1
+    normal = val >= 2.0 ** E5M2_MIN_NORMAL_EXP
+    e_field = np.where(normal, vE + 15, 0)
+    m_field = np.where(normal,
+                       np.rint((val / np.ldexp(1.0, np.where(normal, vE, 0)) - 1.0) * 4.0),
+                       np.rint(val / 2.0 ** -16))
+    code = (e_field.astype(np.int64) << 2) | m_field.astype(np.int64)
+    code = np.where(sat, 0x7B, code)
+    code = np.where(nan, 0x7F, code)
+    return (code | sign).astype(np.uint8)
+
+
+def fp8_encode(v, fmt="e4m3"):
+    return e5m2_encode(v) if fmt == "e5m2" else e4m3_encode(v)
+
+
+def fp8_decode(codes, fmt="e4m3"):
+    return e5m2_decode(codes) if fmt == "e5m2" else e4m3_decode(codes)
+
+
+def hybrid_format(role):
+    """Format of a tensor under --fp8-format hybrid: gradients E5M2, the rest E4M3."""
+    return "e5m2" if role == "grad" else "e4m3"
+
+
+# --------------------------------------------------------------------------------------
 # Per-tensor scale (tensorwise, delayed; per block for blockwise)
 # --------------------------------------------------------------------------------------
 
-def scales_from_amax(amax, margin=0):
-    """(s, s_inv) as float32 arrays from amax values: s = fp32(448/amax) * 2^-margin, s_inv = 1/s.
+def scales_from_amax(amax, margin=0, fmt="e4m3"):
+    """(s, s_inv) as float32 arrays from amax values: s = fp32(448/amax) * 2^-margin, s_inv = 1/s
+    (57344 in place of 448 for E5M2).
 
     The tensorwise entry derives the scale from the tensor being cast; --fp8-margin
     (Numerical Stability Knobs) gives the scale M extra bits of headroom. The division
@@ -156,7 +226,7 @@ def scales_from_amax(amax, margin=0):
     a = np.asarray(amax, dtype=np.float32)
     ok = np.isfinite(a) & (a != 0)
     with np.errstate(over="ignore", divide="ignore", invalid="ignore"):
-        s = np.where(ok, np.float32(E4M3_MAX) / np.where(ok, a, np.float32(1.0)),
+        s = np.where(ok, np.float32(FP8_MAX[fmt]) / np.where(ok, a, np.float32(1.0)),
                      np.float32(1.0)).astype(np.float32)
         s = np.ldexp(s.astype(np.float64), -int(margin)).astype(np.float32)
     s = np.where(np.isinf(s), FLT_MAX, s).astype(np.float32)
@@ -164,9 +234,9 @@ def scales_from_amax(amax, margin=0):
     return s, s_inv
 
 
-def scale_from_amax(amax, margin=0):
+def scale_from_amax(amax, margin=0, fmt="e4m3"):
     """Scalar form of scales_from_amax: returns (s, s_inv) as numpy float32 scalars."""
-    s, s_inv = scales_from_amax(np.float32(amax), margin)
+    s, s_inv = scales_from_amax(np.float32(amax), margin, fmt)
     return np.float32(s), np.float32(s_inv)
 
 
@@ -178,21 +248,21 @@ def amax_of(x_bf16):
     return np.float32(np.max(np.abs(x)))
 
 
-def cast_with_scale(x_bf16, s):
-    """codes = encode(fp32(x * s)): one fp32 product, then the E4M3 rounding."""
+def cast_with_scale(x_bf16, s, fmt="e4m3"):
+    """codes = encode(fp32(x * s)): one fp32 product, then the FP8 rounding."""
     x = bf16_to_f32(x_bf16)
-    return e4m3_encode((x * np.float32(s)).astype(np.float32))
+    return fp8_encode((x * np.float32(s)).astype(np.float32), fmt)
 
 
-def quantize_tensorwise(x_bf16, margin=0):
+def quantize_tensorwise(x_bf16, margin=0, fmt="e4m3"):
     """Tensorwise current scaling (recipe entry "tensorwise").
 
     Returns dict(amax, scale, scale_inv, row=[R,C] codes, col=[C,R] codes); the column-wise
     copy is the byte transpose of the row-wise copy (one scale for the whole tensor).
     """
     amax = amax_of(x_bf16)
-    s, s_inv = scale_from_amax(amax, margin)
-    row = cast_with_scale(x_bf16, s)
+    s, s_inv = scale_from_amax(amax, margin, fmt)
+    row = cast_with_scale(x_bf16, s, fmt)
     return dict(amax=amax, scale=s, scale_inv=s_inv, row=row, col=np.ascontiguousarray(row.T))
 
 
@@ -206,11 +276,12 @@ class DelayedScaling:
     --fp8-amax-history-len L, --fp8-amax-compute-algo max, --fp8-margin M.
     """
 
-    def __init__(self, history_len, margin=0):
+    def __init__(self, history_len, margin=0, fmt="e4m3"):
         if history_len < 1:
             raise ValueError("amax history length must be >= 1")
         self.L = int(history_len)
         self.margin = int(margin)
+        self.fmt = fmt
         self.history = np.zeros(self.L, dtype=np.float32)
         self.head = 0
         self.scale = np.float32(1.0)
@@ -219,7 +290,7 @@ class DelayedScaling:
     def quantize(self, x_bf16):
         """Quantise with the current scale; return codes and this tensor's amax."""
         amax = amax_of(x_bf16)
-        row = cast_with_scale(x_bf16, self.scale)
+        row = cast_with_scale(x_bf16, self.scale, self.fmt)
         return dict(amax=amax, scale=self.scale, scale_inv=self.scale_inv, row=row,
                     col=np.ascontiguousarray(row.T))
 
@@ -227,7 +298,8 @@ class DelayedScaling:
         """Push amax_new (oldest entry evicted) and derive the next scale from the max."""
         self.history[self.head] = np.float32(amax_new)
         self.head = (self.head + 1) % self.L
-        self.scale, self.scale_inv = scale_from_amax(np.max(self.history), self.margin)
+        self.scale, self.scale_inv = scale_from_amax(np.max(self.history), self.margin,
+                                                     self.fmt)
         return self.scale, self.scale_inv
 
 
@@ -288,29 +360,29 @@ def e8m0_decode(bytes_):
 # Blockwise (recipe entry "blockwise": 1x128 activation blocks, 128x128 weight blocks)
 # --------------------------------------------------------------------------------------
 
-def _bw_quantize_1x128_lastdim(x_bf16, margin):
+def _bw_quantize_1x128_lastdim(x_bf16, margin, fmt="e4m3"):
     """Per 1x128 block along the last dim: codes [R,C], s_inv [R, C/128] (float32)."""
     x = bf16_to_f32(x_bf16)
     R, C = x.shape
     blocks = x.reshape(R, C // BW_BLOCK, BW_BLOCK)
-    s, s_inv = scales_from_amax(np.max(np.abs(blocks), axis=2), margin)
-    codes = e4m3_encode((blocks * s[:, :, None]).astype(np.float32)).reshape(R, C)
+    s, s_inv = scales_from_amax(np.max(np.abs(blocks), axis=2), margin, fmt)
+    codes = fp8_encode((blocks * s[:, :, None]).astype(np.float32), fmt).reshape(R, C)
     return codes, s_inv
 
 
-def quantize_blockwise_1x128(x_bf16, margin=0):
+def quantize_blockwise_1x128(x_bf16, margin=0, fmt="e4m3"):
     """Activations / gradients: row copy with 1x128 blocks along C, column copy of X^T
     re-quantised from bf16 with 1x128 blocks along R.
 
     Returns dict(row=[R,C], row_scale_inv=[R,C/128], col=[C,R], col_scale_inv=[C,R/128]).
     """
     x = np.asarray(x_bf16, dtype=np.uint16)
-    row, row_si = _bw_quantize_1x128_lastdim(x, margin)
-    col, col_si = _bw_quantize_1x128_lastdim(np.ascontiguousarray(x.T), margin)
+    row, row_si = _bw_quantize_1x128_lastdim(x, margin, fmt)
+    col, col_si = _bw_quantize_1x128_lastdim(np.ascontiguousarray(x.T), margin, fmt)
     return dict(row=row, row_scale_inv=row_si, col=col, col_scale_inv=col_si)
 
 
-def quantize_blockwise_128x128(x_bf16, margin=0):
+def quantize_blockwise_128x128(x_bf16, margin=0, fmt="e4m3"):
     """Weights: one scale per 128x128 tile; column copy = byte transpose, grid transposed.
 
     Returns dict(row=[R,C], row_scale_inv=[R/128, C/128], col=[C,R], col_scale_inv=[C/128,R/128]).
@@ -319,8 +391,8 @@ def quantize_blockwise_128x128(x_bf16, margin=0):
     R, C = x.shape
     gr, gc = R // BW_BLOCK, C // BW_BLOCK
     tiles = x.reshape(gr, BW_BLOCK, gc, BW_BLOCK)            # [i, r, j, c]
-    s, s_inv = scales_from_amax(np.max(np.abs(tiles), axis=(1, 3)), margin)
-    codes = e4m3_encode((tiles * s[:, None, :, None]).astype(np.float32)).reshape(R, C)
+    s, s_inv = scales_from_amax(np.max(np.abs(tiles), axis=(1, 3)), margin, fmt)
+    codes = fp8_encode((tiles * s[:, None, :, None]).astype(np.float32), fmt).reshape(R, C)
     return dict(row=codes, row_scale_inv=s_inv, col=np.ascontiguousarray(codes.T),
                 col_scale_inv=np.ascontiguousarray(s_inv.T))
 
@@ -329,9 +401,9 @@ def quantize_blockwise_128x128(x_bf16, margin=0):
 # Dequantisation and the fp64 GEMM reference
 # --------------------------------------------------------------------------------------
 
-def dequant_tensor(codes, scale_inv):
+def dequant_tensor(codes, scale_inv, fmt="e4m3"):
     """Per-tensor: decode(code) * s_inv, in float64."""
-    return e4m3_decode(codes) * np.float64(np.float32(scale_inv))
+    return fp8_decode(codes, fmt) * np.float64(np.float32(scale_inv))
 
 
 def dequant_mx(codes, e8m0):
@@ -340,17 +412,17 @@ def dequant_mx(codes, e8m0):
     return e4m3_decode(codes) * f
 
 
-def dequant_1x128(codes, s_inv):
+def dequant_1x128(codes, s_inv, fmt="e4m3"):
     """1x128 blocks along the last dim: decode(code) * s_inv of the element's block."""
     f = np.repeat(np.asarray(s_inv, dtype=np.float32).astype(np.float64), BW_BLOCK, axis=1)
-    return e4m3_decode(codes) * f
+    return fp8_decode(codes, fmt) * f
 
 
-def dequant_128x128(codes, s_inv):
+def dequant_128x128(codes, s_inv, fmt="e4m3"):
     """128x128 tiles: decode(code) * s_inv of the element's tile."""
     f = np.asarray(s_inv, dtype=np.float32).astype(np.float64)
     f = np.repeat(np.repeat(f, BW_BLOCK, axis=0), BW_BLOCK, axis=1)
-    return e4m3_decode(codes) * f
+    return fp8_decode(codes, fmt) * f
 
 
 def gemm_tn_f64(a_deq, b_deq):

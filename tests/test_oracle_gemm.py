@@ -142,3 +142,23 @@ def test_dgelu_reads_h_from_fp8_copy():
         [0.5 * math.erfc(-v / math.sqrt(2)) + v * math.exp(-v * v / 2) / math.sqrt(2 * math.pi)
          for v in hq.ravel()]).reshape(hq.shape)
     assert np.array_equal(dh, O.f64_to_bf16(ref))
+
+
+def _frac_decode_e5m2(code):
+    code = int(code)
+    e, m = (code >> 2) & 0x1F, code & 3
+    v = Fraction(m, 65536) if e == 0 else (1 + Fraction(m, 4)) * Fraction(2) ** (e - 15)
+    return -v if code & 0x80 else v
+
+
+def test_hybrid_dgrad_8x8_exact():
+    """Hybrid format: an E5M2 gradient times an E4M3 weight (dgrad), decoded by hand."""
+    dy = bf16_bits_normal(8, 8, seed=25, sigma=1e-3)
+    w = bf16_bits_normal(8, 8, seed=26, sigma=0.02)
+    qd, qw = O.quantize_tensorwise(dy, fmt="e5m2"), O.quantize_tensorwise(w)
+    c = O.gemm_tn_f64(O.dequant_tensor(qd["row"], qd["scale_inv"], fmt="e5m2"),
+                      O.dequant_tensor(qw["col"], qw["scale_inv"]))
+    sd, sw = Fraction(float(qd["scale_inv"])), Fraction(float(qw["scale_inv"]))
+    A = [[_frac_decode_e5m2(v) * sd for v in r] for r in qd["row"]]
+    B = [[_frac_decode(v) * sw for v in r] for r in qw["col"]]
+    _close(c, _exact_tn(A, B))
