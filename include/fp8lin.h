@@ -77,8 +77,12 @@ typedef enum {
   FP8_RECIPE_BLOCKWISE = 3
 } fp8_recipe_kind;
 
-/* --fp8-format values. HYBRID is accepted by the recipe table but never defined on the
- * pages; this build returns FP8_ERR_UNSUPPORTED for it. MXFP8 takes E4M3 only. */
+/* --fp8-format values ("Hardware and Recipe Compatibility": e4m3 for every recipe, hybrid for
+ * delayed, tensorwise and blockwise). The pages do not define hybrid; this build reads it as
+ * E4M3 for activations and weights and E5M2 for gradients (role FP8_ROLE_GRAD): OCP E5M2, bias
+ * 15, 2 mantissa bits, largest finite value 57344, encoded like E4M3 (round to nearest even,
+ * finite overflow and infinities saturate to +-57344, NaN -> 0x7F with its sign) with 57344 in
+ * place of 448 in the scale rule. MXFP8 takes E4M3 only (hybrid -> FP8_ERR_UNSUPPORTED). */
 typedef enum { FP8_FORMAT_E4M3 = 0, FP8_FORMAT_HYBRID = 1 } fp8_format;
 
 /* Which block shape the blockwise recipe uses for a tensor: 1x128 for activations and
@@ -98,8 +102,8 @@ typedef struct {
 /* A quantised tensor: codes and scales of both copies, all device memory owned by the
  * caller. row / col may be NULL when that copy is not wanted. */
 typedef struct {
-  uint8_t *row;          /* [rows][cols] E4M3 codes */
-  uint8_t *col;          /* [cols][rows] E4M3 codes */
+  uint8_t *row;          /* [rows][cols] FP8 codes (E5M2 for gradients under hybrid) */
+  uint8_t *col;          /* [cols][rows] FP8 codes */
   void *row_scale;       /* MXFP8: uint8 E8M0; BLOCKWISE: float s_inv; else unused */
   void *col_scale;       /* same for the column-wise copy */
   float *amax;           /* DELAYED/TENSORWISE: amax of this tensor (written) */
@@ -123,7 +127,8 @@ typedef struct {
 size_t fp8_workspace_bytes(const fp8_recipe *recipe, int64_t rows, int64_t cols);
 
 /*
- * fp8_quantize — bf16 tensor -> E4M3 codes plus scales, row-wise and/or column-wise copy.
+ * fp8_quantize — bf16 tensor -> FP8 codes plus scales, row-wise and/or column-wise copy
+ * (E4M3; E5M2 for role FP8_ROLE_GRAD under the hybrid format).
  *
  * Recipe entries "tensorwise" (scale from this tensor's own amax), "delayed" (scale read from
  * out->scale / out->scale_inv, which fp8_amax_update derived from earlier steps; this call
@@ -150,9 +155,10 @@ fp8_status fp8_quantize(const fp8_recipe *recipe, const void *x_bf16, int64_t ro
  * fp8_amax_update — delayed scaling: push *amax_new into the history (the oldest of `len`
  * entries drops out) and write scale = f(max(history)), scale_inv = 1/scale with f the
  * per-tensor rule above (--fp8-amax-history-len, --fp8-amax-compute-algo max, --fp8-margin).
- * One CTA; reads and writes device memory only.
+ * role: fp8_role of the tensor this history belongs to (under the hybrid format a gradient's
+ * scale uses the E5M2 maximum 57344). One CTA; reads and writes device memory only.
  */
-fp8_status fp8_amax_update(const fp8_recipe *recipe, fp8_amax_history *hist,
+fp8_status fp8_amax_update(const fp8_recipe *recipe, fp8_amax_history *hist, int32_t role,
                            const float *amax_new, float *scale, float *scale_inv,
                            cudaStream_t stream);
 

@@ -162,8 +162,9 @@ def quantize_static_scratch(recipe: Recipe, x: torch.Tensor, role="activation", 
 class DelayedState:
     """Device-resident delayed-scaling state: amax history, head, scale, scale_inv."""
 
-    def __init__(self, recipe: Recipe, device="cuda"):
+    def __init__(self, recipe: Recipe, device="cuda", role="activation"):
         self.recipe = recipe
+        self.role = role
         self.history = torch.zeros(recipe.amax_history_len, dtype=torch.float32, device=device)
         self.head = torch.zeros(1, dtype=torch.int32, device=device)
         self.scale = torch.ones(1, dtype=torch.float32, device=device)
@@ -179,8 +180,8 @@ def amax_update(recipe: Recipe, state: DelayedState, amax_new: torch.Tensor, str
     lib = L.load()
     rc = recipe.c()
     h = L.AmaxHistory(state.history.data_ptr(), state.head.data_ptr(), state.history.numel())
-    st = lib.fp8_amax_update(ctypes.byref(rc), ctypes.byref(h), _ptr(amax_new), _ptr(state.scale),
-                             _ptr(state.scale_inv), _stream(stream))
+    st = lib.fp8_amax_update(ctypes.byref(rc), ctypes.byref(h), ROLES[state.role], _ptr(amax_new),
+                             _ptr(state.scale), _ptr(state.scale_inv), _stream(stream))
     L.check(st, "fp8_amax_update")
 
 

@@ -28,11 +28,19 @@ fp8_status check_ptr(const void* p) {
 fp8_status check_recipe(const fp8_recipe* r) {
   if (r == nullptr) return FP8_ERR_NULL;
   if (r->kind < FP8_RECIPE_DELAYED || r->kind > FP8_RECIPE_BLOCKWISE) return FP8_ERR_UNSUPPORTED;
-  if (r->format != FP8_FORMAT_E4M3) return FP8_ERR_UNSUPPORTED;   // hybrid: not defined
+  if (r->format != FP8_FORMAT_E4M3 && r->format != FP8_FORMAT_HYBRID) return FP8_ERR_UNSUPPORTED;
+  if (r->format == FP8_FORMAT_HYBRID && r->kind == FP8_RECIPE_MXFP8)
+    return FP8_ERR_UNSUPPORTED;                                  // mxfp8 is E4M3 only
   if (r->margin < -64 || r->margin > 64) return FP8_ERR_UNSUPPORTED;
   if (r->amax_compute_algo != 0) return FP8_ERR_UNSUPPORTED;      // only `max`
   if (r->kind == FP8_RECIPE_DELAYED && r->amax_history_len < 1) return FP8_ERR_SHAPE;
   return FP8_OK;
+}
+
+// Storage format of a tensor with this role: E5M2 (1) for gradients under the hybrid format,
+// E4M3 (0) otherwise.
+int fmt_of(const fp8_recipe* r, int role) {
+  return (r->format == FP8_FORMAT_HYBRID && role == FP8_ROLE_GRAD) ? 1 : 0;
 }
 
 // Row/column multiple a recipe needs: 128 for the block recipes, 16 for per-tensor scales.
@@ -118,23 +126,25 @@ fp8_status fp8_quantize(const fp8_recipe* recipe, const void* x_bf16, int64_t ro
   out->role = role;
   out->kind = kind;
   out->col_bf16 = col_bf16 ? 1 : 0;
-  return cuda_status(quantize_launch(kind, role, recipe->margin,
+  return cuda_status(quantize_launch(kind, role, fmt_of(recipe, role), recipe->margin,
                                      reinterpret_cast<const uint16_t*>(x_bf16), rows, cols,
                                      want_row != 0, want_col != 0, col_bf16, out, workspace,
                                      dev_status, stream));
 }
 
-fp8_status fp8_amax_update(const fp8_recipe* recipe, fp8_amax_history* hist,
+fp8_status fp8_amax_update(const fp8_recipe* recipe, fp8_amax_history* hist, int32_t role,
                            const float* amax_new, float* scale, float* scale_inv,
                            cudaStream_t stream) {
   FP8_TRY(check_recipe(recipe));
   if (recipe->kind != FP8_RECIPE_DELAYED) return FP8_ERR_UNSUPPORTED;
+  if (role < FP8_ROLE_ACTIVATION || role > FP8_ROLE_GRAD) return FP8_ERR_UNSUPPORTED;
   if (hist == nullptr || hist->history == nullptr || hist->head == nullptr || amax_new == nullptr ||
       scale == nullptr || scale_inv == nullptr)
     return FP8_ERR_NULL;
   if (hist->len < 1 || hist->len != recipe->amax_history_len) return FP8_ERR_SHAPE;
+  const float fmax = fmt_of(recipe, role) == 1 ? 57344.0f : 448.0f;
   return cuda_status(amax_update_launch(hist->history, hist->head, hist->len, amax_new, scale,
-                                        scale_inv, recipe->margin, stream));
+                                        scale_inv, recipe->margin, fmax, stream));
 }
 
 }  // extern "C"
@@ -147,6 +157,7 @@ struct Operand {
   const void* scale;        // per recipe (see fp8lin.h)
   const float* scale_inv;   // per-tensor recipes
   int role;
+  int fmt;                  // 0 = E4M3, 1 = E5M2
 };
 
 fp8_status run_gemm(int kind, const Operand& a, const Operand& b, int64_t M, int64_t N,
@@ -172,6 +183,8 @@ fp8_status run_gemm(int kind, const Operand& a, const Operand& b, int64_t M, int
   g.p.ldd = N;
   g.p.d_fp32 = fp32_out;
   g.p.status = status;
+  g.p.a_fmt = a.fmt;
+  g.p.b_fmt = b.fmt;
   switch (kind) {
     case FP8_RECIPE_TENSORWISE:
     case FP8_RECIPE_DELAYED:
@@ -280,8 +293,10 @@ fp8_status fp8_linear_fwd(const fp8_recipe* recipe, const fp8_tensor* x, const f
   FP8_TRY(check_tensor(recipe, x));
   FP8_TRY(check_tensor(recipe, w));
   if (x->cols != w->cols) return FP8_ERR_SHAPE;
-  const Operand a{x->row, x->row_scale, x->scale_inv, x->role};
-  const Operand b{w->row, w->row_scale, w->scale_inv, w->role};
+  const Operand a{x->row, x->row_scale, x->scale_inv, x->role,
+                    fmt_of(recipe, x->role)};
+  const Operand b{w->row, w->row_scale, w->scale_inv, w->role,
+                    fmt_of(recipe, w->role)};
   return run_gemm(recipe->kind, a, b, x->rows, w->rows, x->cols, y, y_fp32, dev_status, stream);
 }
 
@@ -296,8 +311,10 @@ fp8_status fp8_linear_bwd(const fp8_recipe* recipe, const fp8_tensor* dy,
     if (w->rows != N) return FP8_ERR_SHAPE;
     const int64_t K = w->cols;
     // dgrad: dX[M][K] = dY[M][N] . (W^T)[K][N]^T
-    const Operand a{dy->row, dy->row_scale, dy->scale_inv, dy->role};
-    const Operand b{w->col, w->col_scale, w->scale_inv, w->role};
+    const Operand a{dy->row, dy->row_scale, dy->scale_inv, dy->role,
+                    fmt_of(recipe, dy->role)};
+    const Operand b{w->col, w->col_scale, w->scale_inv, w->role,
+                    fmt_of(recipe, w->role)};
     FP8_TRY(run_gemm(recipe->kind, a, b, M, K, N, dx, out_fp32, dev_status, stream));
   }
   if (dw != nullptr) {
@@ -312,8 +329,10 @@ fp8_status fp8_linear_bwd(const fp8_recipe* recipe, const fp8_tensor* dy,
       return run_bf16_gemm(dy->col, x_saved->col, N, K, M, dw, out_fp32, dev_status, stream);
     }
     // wgrad: dW[N][K] = (dY^T)[N][M] . (X^T)[K][M]^T
-    const Operand a{dy->col, dy->col_scale, dy->scale_inv, dy->role};
-    const Operand b{x_saved->col, x_saved->col_scale, x_saved->scale_inv, x_saved->role};
+    const Operand a{dy->col, dy->col_scale, dy->scale_inv, dy->role,
+                    fmt_of(recipe, dy->role)};
+    const Operand b{x_saved->col, x_saved->col_scale, x_saved->scale_inv, x_saved->role,
+                    fmt_of(recipe, x_saved->role)};
     FP8_TRY(run_gemm(recipe->kind, a, b, N, K, M, dw, out_fp32, dev_status, stream));
   }
   return FP8_OK;
@@ -329,8 +348,10 @@ fp8_status fp8_linear_fwd_gelu(const fp8_recipe* recipe, const fp8_tensor* x,
   if (a_q == nullptr || h_q == nullptr) return FP8_ERR_NULL;
   if (x->cols != w->cols) return FP8_ERR_SHAPE;
   const int64_t M = x->rows, N = w->rows;
-  const Operand a{x->row, x->row_scale, x->scale_inv, x->role};
-  const Operand b{w->row, w->row_scale, w->scale_inv, w->role};
+  const Operand a{x->row, x->row_scale, x->scale_inv, x->role,
+                    fmt_of(recipe, x->role)};
+  const Operand b{w->row, w->row_scale, w->scale_inv, w->role,
+                    fmt_of(recipe, w->role)};
   FP8_TRY(run_fused_mx(EPI_GELU, a, b, M, N, x->cols, h_q->row,
                        reinterpret_cast<uint8_t*>(h_q->row_scale), a_q, dev_status, stream));
   for (fp8_tensor* t : {a_q, h_q}) {
@@ -355,8 +376,10 @@ fp8_status fp8_linear_dgrad_dgelu(const fp8_recipe* recipe, const fp8_tensor* dy
   const int64_t M = dy->rows, N = w->cols;
   if (w->rows != dy->cols || h_q->rows != M || h_q->cols != N) return FP8_ERR_SHAPE;
   // dgrad: dA[M][N] = dY[M][H] . (W^T)[N][H]^T
-  const Operand a{dy->row, dy->row_scale, dy->scale_inv, dy->role};
-  const Operand b{w->col, w->col_scale, w->scale_inv, w->role};
+  const Operand a{dy->row, dy->row_scale, dy->scale_inv, dy->role,
+                    fmt_of(recipe, dy->role)};
+  const Operand b{w->col, w->col_scale, w->scale_inv, w->role,
+                    fmt_of(recipe, w->role)};
   FP8_TRY(run_fused_mx(EPI_DGELU, a, b, M, N, dy->cols, h_q->row,
                        reinterpret_cast<uint8_t*>(h_q->row_scale), dh_q, dev_status, stream));
   dh_q->rows = M;

@@ -11,6 +11,11 @@
 namespace fp8lin {
 
 constexpr int kTile = 128;          // quantize tile: 128 x 128 source elements
+
+// FP8 storage formats: E4M3 for everything, E5M2 for gradients under the hybrid format.
+enum Fp8Fmt : int { F8_E4M3 = 0, F8_E5M2 = 1 };
+template <int F8>
+__host__ __device__ constexpr float fp8_max() { return F8 == F8_E5M2 ? 57344.0f : 448.0f; }
 constexpr int kMxBlock = 32;        // MXFP8 block length
 constexpr int kBwBlock = 128;       // blockwise block length
 
@@ -76,14 +81,16 @@ __device__ __forceinline__ float exp2i(int k) {
                    : __uint_as_float(1u << (k + 149));
 }
 
-// Per-tensor / per-block scale from an amax: s = fp32(448/amax) * 2^-margin, s = 1 for
+// Per-tensor / per-block scale from an amax: s = fp32(fmax/amax) * 2^-margin (fmax = 448 for
+// E4M3, 57344 for E5M2), s = 1 for
 // amax 0 / Inf / NaN, an infinite s becomes FLT_MAX. Returns s; *s_inv = fp32(1/s).
-__device__ __forceinline__ float scale_from_amax(float amax, int margin, float* s_inv) {
+__device__ __forceinline__ float scale_from_amax(float amax, int margin, float* s_inv,
+                                                 float fmax = 448.0f) {
   float s;
   if (!(amax > 0.0f) || !(amax <= 3.402823466e38f)) {
     s = 1.0f;
   } else {
-    s = __fdiv_rn(448.0f, amax);
+    s = __fdiv_rn(fmax, amax);
   }
   if (margin != 0) s = __fmul_rn(s, exp2i(-margin));
   if (s > 3.402823466e38f) s = 3.402823466e38f;
@@ -116,10 +123,28 @@ __device__ __forceinline__ uint32_t cvt_e4m3x4(float x0, float x1, float x2, flo
   return r;
 }
 
+// Four floats -> four E5M2 codes (round to nearest even, saturating to +-57344).
+__device__ __forceinline__ uint32_t cvt_e5m2x4(float x0, float x1, float x2, float x3) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e5m2x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e5m2x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "f"(x0), "f"(x1), "f"(x2), "f"(x3));
+  return r;
+}
+template <int F8>
+__device__ __forceinline__ uint32_t cvt_fp8x4(float x0, float x1, float x2, float x3) {
+  if constexpr (F8 == F8_E5M2) return cvt_e5m2x4(x0, x1, x2, x3);
+  else return cvt_e4m3x4(x0, x1, x2, x3);
+}
+
 // Two words of packed bf16 (4 values) times s -> one word of 4 codes.
+template <int F8 = F8_E4M3>
 __device__ __forceinline__ uint32_t encode4(uint32_t w0, uint32_t w1, float s) {
-  return cvt_e4m3x4(__fmul_rn(bf16_lo(w0), s), __fmul_rn(bf16_hi(w0), s),
-                    __fmul_rn(bf16_lo(w1), s), __fmul_rn(bf16_hi(w1), s));
+  return cvt_fp8x4<F8>(__fmul_rn(bf16_lo(w0), s), __fmul_rn(bf16_hi(w0), s),
+                       __fmul_rn(bf16_lo(w1), s), __fmul_rn(bf16_hi(w1), s));
 }
 
 // Give the codes of NaN inputs the NaN code with the input's sign (rare path).

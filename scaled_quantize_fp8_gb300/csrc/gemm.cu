@@ -419,7 +419,10 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (leader)
     if (lane == 0 && leader) {
-      const uint32_t idesc = instr_desc<MODE, CTA2>();
+      // operand formats (E4M3 = 0, E5M2 = 1) in descriptor bits 7-9 (A) and 10-12 (B)
+      uint32_t idesc = instr_desc<MODE, CTA2>();
+      if constexpr (MODE == G_TENSOR || MODE == G_BLOCK)
+        idesc |= (uint32_t(p.a_fmt) << 7) | (uint32_t(p.b_fmt) << 10);
       const uint32_t sf_base = tmem + 256;      // MX scale factors: kSfCols columns a stage
       int s = 0;
       uint32_t ph = 0;

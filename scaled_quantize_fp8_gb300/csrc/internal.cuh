@@ -20,8 +20,9 @@ int num_sms();
 
 // ---- quantize.cu
 size_t quantize_workspace_bytes(int kind, int64_t R, int64_t C);
-cudaError_t quantize_launch(int kind, int role, int margin, const uint16_t* x, int64_t R,
-                            int64_t C, bool want_row, bool want_col, bool col_bf16,
+// fmt: 0 = E4M3, 1 = E5M2 (gradients under the hybrid format; not for MXFP8)
+cudaError_t quantize_launch(int kind, int role, int fmt, int margin, const uint16_t* x,
+                            int64_t R, int64_t C, bool want_row, bool want_col, bool col_bf16,
                             fp8_tensor* out, void* workspace, int32_t* status,
                             cudaStream_t st);
 cudaError_t gelu_quantize_launch(const uint16_t* h, int64_t R, int64_t C, uint16_t* a_bf16,
@@ -31,7 +32,8 @@ cudaError_t dgelu_quantize_launch(const uint16_t* da, const fp8_tensor* h_q, int
                                   int64_t C, uint16_t* dh_bf16, fp8_tensor* dh_q,
                                   int32_t* status, cudaStream_t st);
 cudaError_t amax_update_launch(float* hist, int32_t* head, int len, const float* amax_new,
-                               float* scale, float* scale_inv, int margin, cudaStream_t st);
+                               float* scale, float* scale_inv, int margin, float fmax,
+                               cudaStream_t st);
 
 // ---- gemm.cu
 enum GMode : int { G_TENSOR = 0, G_MX = 1, G_BLOCK = 2, G_BF16 = 3 };
@@ -53,6 +55,7 @@ struct GemmParams {
   const float* b_bs;        // G_BLOCK: B 128x128 grid [N/128][K/128] or 1x128 [K/128][N]
   int b_is_128;
   int32_t* status;          // device status word (may be null)
+  int a_fmt, b_fmt;         // G_TENSOR / G_BLOCK operand formats: 0 = E4M3, 1 = E5M2
   // Fused MLP epilogues (G_MX only; the tile is quantised instead of stored, D unused):
   //   GELU : h = bf16(acc) -> h_row/h_scale (MXFP8 row copy), a = gelu(h) -> o_*
   //   DGELU: da = bf16(acc), h read from h_row/h_scale, dh = da * gelu'(h) -> o_*

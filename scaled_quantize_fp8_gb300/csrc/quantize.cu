@@ -122,7 +122,7 @@ __device__ __forceinline__ uint32_t swz(uint32_t r, uint32_t c) {
 //   Column pass: thread (pp = t % 64, q = t / 64) owns source columns 2pp, 2pp+1 over rows
 //   32q .. 32q+31 and writes 32 consecutive bytes of each transposed row (re-quantised for
 //   MXFP8 and 1x128); per-tensor and 128x128 scales transpose the row codes instead.
-template <int MODE, int EPI>
+template <int MODE, int EPI, int F8>
 __device__ __forceinline__ void quantize_one_tile(const QuantParams& p, QuantCtl& S,
                                                   uint8_t* tile, uint8_t* codes,
                                                   const void* table, int tile_id,
@@ -180,8 +180,8 @@ __device__ __forceinline__ void quantize_one_tile(const QuantParams& p, QuantCtl
         m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
         float mult;
         const uint32_t sb = mx_scale_byte(m, &mult);
-        uint4 hc = make_uint4(encode4(w[i][0], w[i][1], mult), encode4(w[i][2], w[i][3], mult),
-                              encode4(w[i][4], w[i][5], mult), encode4(w[i][6], w[i][7], mult));
+        uint4 hc = make_uint4(encode4<F8>(w[i][0], w[i][1], mult), encode4<F8>(w[i][2], w[i][3], mult),
+                              encode4<F8>(w[i][4], w[i][5], mult), encode4<F8>(w[i][6], w[i][7], mult));
         if (m > 0x7F80u) {
           hc.x = fix_nan4(hc.x, w[i][0], w[i][1]); hc.y = fix_nan4(hc.y, w[i][2], w[i][3]);
           hc.z = fix_nan4(hc.z, w[i][4], w[i][5]); hc.w = fix_nan4(hc.w, w[i][6], w[i][7]);
@@ -234,7 +234,7 @@ __device__ __forceinline__ void quantize_one_tile(const QuantParams& p, QuantCtl
     if constexpr (MODE == Q_TENSOR) {
       if (t == 0) p.part_out[tile_id] = tm;               // delayed: record this tile's amax
     } else {
-      s_tile = scale_from_amax(amax_from_bits(tm), p.margin, &sinv_tile);
+      s_tile = scale_from_amax(amax_from_bits(tm), p.margin, &sinv_tile, fp8_max<F8>());
       if (t == 0) {
         const int tiles_r = int((R + 127) >> 7);
         if (p.row_scale) reinterpret_cast<float*>(p.row_scale)[tr * p.tiles_c + tc] = sinv_tile;
@@ -266,13 +266,13 @@ __device__ __forceinline__ void quantize_one_tile(const QuantParams& p, QuantCtl
           m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
           m = max(m, __shfl_xor_sync(0xffffffffu, m, 16));
           float sinv;
-          s = scale_from_amax(amax_from_bits(m), p.margin, &sinv);
+          s = scale_from_amax(amax_from_bits(m), p.margin, &sinv, fp8_max<F8>());
           if (h == 0 && cc == 0) S.scf_row[r] = sinv;
         }
         nan = m > 0x7F80u;
       }
-      uint4 q4 = make_uint4(encode4(w[i][0], w[i][1], s), encode4(w[i][2], w[i][3], s),
-                            encode4(w[i][4], w[i][5], s), encode4(w[i][6], w[i][7], s));
+      uint4 q4 = make_uint4(encode4<F8>(w[i][0], w[i][1], s), encode4<F8>(w[i][2], w[i][3], s),
+                            encode4<F8>(w[i][4], w[i][5], s), encode4<F8>(w[i][6], w[i][7], s));
       if (nan) {
         q4.x = fix_nan4(q4.x, w[i][0], w[i][1]); q4.y = fix_nan4(q4.y, w[i][2], w[i][3]);
         q4.z = fix_nan4(q4.z, w[i][4], w[i][5]); q4.w = fix_nan4(q4.w, w[i][6], w[i][7]);
@@ -371,8 +371,8 @@ __device__ __forceinline__ void quantize_one_tile(const QuantParams& p, QuantCtl
         const uint32_t fb = max(max(S.red_col[0][2 * pp + 1], S.red_col[1][2 * pp + 1]),
                                 max(S.red_col[2][2 * pp + 1], S.red_col[3][2 * pp + 1]));
         float ia, ib;
-        sa = scale_from_amax(amax_from_bits(fa), p.margin, &ia);
-        sb = scale_from_amax(amax_from_bits(fb), p.margin, &ib);
+        sa = scale_from_amax(amax_from_bits(fa), p.margin, &ia, fp8_max<F8>());
+        sb = scale_from_amax(amax_from_bits(fb), p.margin, &ib, fp8_max<F8>());
         if (q == 0) {
           S.scf_col[2 * pp] = ia;
           S.scf_col[2 * pp + 1] = ib;
@@ -383,9 +383,9 @@ __device__ __forceinline__ void quantize_one_tile(const QuantParams& p, QuantCtl
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const uint32_t x0 = x[4 * j], x1 = x[4 * j + 1], x2 = x[4 * j + 2], x3 = x[4 * j + 3];
-        ca[j] = cvt_e4m3x4(__fmul_rn(bf16_lo(x0), sa), __fmul_rn(bf16_lo(x1), sa),
+        ca[j] = cvt_fp8x4<F8>(__fmul_rn(bf16_lo(x0), sa), __fmul_rn(bf16_lo(x1), sa),
                            __fmul_rn(bf16_lo(x2), sa), __fmul_rn(bf16_lo(x3), sa));
-        cb[j] = cvt_e4m3x4(__fmul_rn(bf16_hi(x0), sb), __fmul_rn(bf16_hi(x1), sb),
+        cb[j] = cvt_fp8x4<F8>(__fmul_rn(bf16_hi(x0), sb), __fmul_rn(bf16_hi(x1), sb),
                            __fmul_rn(bf16_hi(x2), sb), __fmul_rn(bf16_hi(x3), sb));
       }
       if ((mw & 0x7FFFu) > 0x7F80u || ((mw >> 16) & 0x7FFFu) > 0x7F80u) {   // NaN present
@@ -453,9 +453,10 @@ __device__ __forceinline__ bool quant_wait(QuantCtl& S, int b, uint32_t parity, 
 // Persistent quantize kernel: each CTA walks tiles blockIdx.x, +gridDim.x, ...; thread 0
 // issues the TMA loads of the next tile into the other buffer before the current one is
 // processed, so HBM reads overlap the conversion and the stores.
-template <int MODE, int EPI>
+template <int MODE, int EPI, int F8>
 __global__ void __launch_bounds__(256, quant_ctas_per_sm<MODE, EPI>())
     quantize_tile_kernel(const __grid_constant__ CUtensorMap tmX, const QuantParams p) {
+  static_assert(F8 == F8_E4M3 || (MODE != Q_MX && EPI == EPI_NONE), "E5M2: per-tensor / blockwise");
   extern __shared__ uint8_t qsm_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(qsm_raw) + 1023) & ~uintptr_t(1023));
@@ -486,7 +487,7 @@ __global__ void __launch_bounds__(256, quant_ctas_per_sm<MODE, EPI>())
       m = block_max_u32(m, S.red);
       tensor_nan = m > 0x7F80u;
       float sinv;
-      s_tensor = scale_from_amax(amax_from_bits(m), p.margin, &sinv);
+      s_tensor = scale_from_amax(amax_from_bits(m), p.margin, &sinv, fp8_max<F8>());
       if (blockIdx.x == 0 && t == 0) {
         *p.amax_out = amax_from_bits(m);
         *p.scale_out = s_tensor;
@@ -522,7 +523,7 @@ __global__ void __launch_bounds__(256, quant_ctas_per_sm<MODE, EPI>())
     if (t == 0 && ahead < n_tiles) issue(ahead, (i + kQBufs - 1) % kQBufs);
     if (!quant_wait(S, b, uint32_t(i / kQBufs) & 1u, p.status)) break;
     uint8_t* buf = tiles + b * kQTileBytes;
-    quantize_one_tile<MODE, EPI>(p, S, buf, buf, table, tile, s_tensor, tensor_nan);
+    quantize_one_tile<MODE, EPI, F8>(p, S, buf, buf, table, tile, s_tensor, tensor_nan);
     __syncthreads();                                 // buffer b is refilled next iteration
   }
   if (*reinterpret_cast<volatile int*>(&S.abort_flag)) {
@@ -576,11 +577,12 @@ __global__ void __launch_bounds__(1024) amax_finalize_kernel(const uint32_t* __r
 }
 
 // Empty tensor: amax 0; tensorwise also writes scale/scale_inv for amax 0.
-__global__ void empty_scalars_kernel(float* amax, float* scale, float* scale_inv, int margin) {
+__global__ void empty_scalars_kernel(float* amax, float* scale, float* scale_inv, int margin,
+                                     float fmax) {
   if (amax) *amax = 0.0f;
   if (scale) {
     float si;
-    *scale = scale_from_amax(0.0f, margin, &si);
+    *scale = scale_from_amax(0.0f, margin, &si, fmax);
     if (scale_inv) *scale_inv = si;
   }
 }
@@ -590,7 +592,7 @@ __global__ void empty_scalars_kernel(float* amax, float* scale, float* scale_inv
 __global__ void __launch_bounds__(1024) amax_history_update_kernel(
     float* __restrict__ hist, int32_t* __restrict__ head, int len,
     const float* __restrict__ amax_new, float* __restrict__ scale,
-    float* __restrict__ scale_inv, int margin) {
+    float* __restrict__ scale_inv, int margin, float fmax) {
   __shared__ float red[32];
   __shared__ int nan_seen;
   const int h = *head;
@@ -614,7 +616,7 @@ __global__ void __launch_bounds__(1024) amax_history_update_kernel(
     hist[h] = a_new;
     *head = (h + 1) % len;
     float si;
-    *scale = scale_from_amax(r, margin, &si);
+    *scale = scale_from_amax(r, margin, &si, fmax);
     *scale_inv = si;
   }
 }
@@ -637,7 +639,7 @@ size_t quantize_workspace_bytes(int kind, int64_t R, int64_t C) {
   return size_t(parts) * sizeof(uint32_t);
 }
 
-template <int MODE, int EPI>
+template <int MODE, int EPI, int F8 = F8_E4M3>
 static cudaError_t launch_tiles(QuantParams p, cudaStream_t st) {
   const int64_t col_row_bytes = p.R * (p.col_bf16 ? 2 : 1);
   p.col_v8 = p.col != nullptr && (reinterpret_cast<uintptr_t>(p.col) % 32 == 0) &&
@@ -649,20 +651,21 @@ static cudaError_t launch_tiles(QuantParams p, cudaStream_t st) {
   constexpr int smem = int(quant_smem_bytes<MODE, EPI>());
   static bool attr = false;
   if (!attr) {
-    const cudaError_t e = cudaFuncSetAttribute(quantize_tile_kernel<MODE, EPI>,
+    const cudaError_t e = cudaFuncSetAttribute(quantize_tile_kernel<MODE, EPI, F8>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr = true;
   }
   const int grid = std::max(1, std::min(n, num_sms() * quant_ctas_per_sm<MODE, EPI>()));
-  quantize_tile_kernel<MODE, EPI><<<grid, 256, smem, st>>>(map, p);
+  quantize_tile_kernel<MODE, EPI, F8><<<grid, 256, smem, st>>>(map, p);
   return cudaGetLastError();
 }
 
-cudaError_t quantize_launch(int kind, int role, int margin, const uint16_t* x, int64_t R,
-                            int64_t C, bool want_row, bool want_col, bool col_bf16,
+cudaError_t quantize_launch(int kind, int role, int fmt, int margin, const uint16_t* x,
+                            int64_t R, int64_t C, bool want_row, bool want_col, bool col_bf16,
                             fp8_tensor* out, void* workspace, int32_t* status,
                             cudaStream_t st) {
+  const bool e5 = fmt == F8_E5M2;
   QuantParams p{};
   p.status = status;
   p.col_bf16 = col_bf16;
@@ -679,7 +682,8 @@ cudaError_t quantize_launch(int kind, int role, int margin, const uint16_t* x, i
     if (kind == FP8_RECIPE_TENSORWISE || kind == FP8_RECIPE_DELAYED) {
       empty_scalars_kernel<<<1, 1, 0, st>>>(out->amax,
                                             kind == FP8_RECIPE_TENSORWISE ? out->scale : nullptr,
-                                            out->scale_inv, margin);
+                                            out->scale_inv, margin,
+                                            e5 ? fp8_max<F8_E5M2>() : fp8_max<F8_E4M3>());
       return cudaGetLastError();
     }
     return cudaSuccess;
@@ -697,22 +701,28 @@ cudaError_t quantize_launch(int kind, int role, int margin, const uint16_t* x, i
       p.amax_out = out->amax;
       p.scale_out = out->scale;
       p.scale_inv_out = out->scale_inv;
-      return launch_tiles<Q_TENSOR, EPI_NONE>(p, st);
+      return e5 ? launch_tiles<Q_TENSOR, EPI_NONE, F8_E5M2>(p, st)
+                : launch_tiles<Q_TENSOR, EPI_NONE>(p, st);
     }
     case FP8_RECIPE_DELAYED: {
       p.scale_in = out->scale;
       p.part_out = reinterpret_cast<uint32_t*>(workspace);
-      cudaError_t e = launch_tiles<Q_TENSOR, EPI_NONE>(p, st);
+      cudaError_t e = e5 ? launch_tiles<Q_TENSOR, EPI_NONE, F8_E5M2>(p, st)
+                         : launch_tiles<Q_TENSOR, EPI_NONE>(p, st);
       if (e != cudaSuccess) return e;
       const int n = int((R + 127) / 128) * p.tiles_c;
       amax_finalize_kernel<<<1, 1024, 0, st>>>(p.part_out, n, out->amax);
       return cudaGetLastError();
     }
     case FP8_RECIPE_MXFP8:
+      if (e5) return cudaErrorInvalidValue;
       return launch_tiles<Q_MX, EPI_NONE>(p, st);
     case FP8_RECIPE_BLOCKWISE:
-      return role == FP8_ROLE_WEIGHT ? launch_tiles<Q_BW128, EPI_NONE>(p, st)
-                                     : launch_tiles<Q_BW1x128, EPI_NONE>(p, st);
+      if (role == FP8_ROLE_WEIGHT)
+        return e5 ? launch_tiles<Q_BW128, EPI_NONE, F8_E5M2>(p, st)
+                  : launch_tiles<Q_BW128, EPI_NONE>(p, st);
+      return e5 ? launch_tiles<Q_BW1x128, EPI_NONE, F8_E5M2>(p, st)
+                : launch_tiles<Q_BW1x128, EPI_NONE>(p, st);
   }
   return cudaErrorInvalidValue;
 }
@@ -758,9 +768,10 @@ cudaError_t dgelu_quantize_launch(const uint16_t* da, const fp8_tensor* h_q, int
 }
 
 cudaError_t amax_update_launch(float* hist, int32_t* head, int len, const float* amax_new,
-                               float* scale, float* scale_inv, int margin, cudaStream_t st) {
+                               float* scale, float* scale_inv, int margin, float fmax,
+                               cudaStream_t st) {
   amax_history_update_kernel<<<1, 1024, 0, st>>>(hist, head, len, amax_new, scale, scale_inv,
-                                                 margin);
+                                                 margin, fmax);
   return cudaGetLastError();
 }
 

@@ -55,7 +55,8 @@ def test_quantize_rejects_bad_arguments(lib):
     r = _rec()
     assert lib.fp8_quantize(None, 0x8000, 16, 16, 0, 1, 1, ctypes.byref(_tensor()), None, 0, None,
                             None) == 1
-    assert _q(lib, _rec(fmt=L.FORMAT_HYBRID)) == 4             # hybrid is not defined
+    assert _q(lib, _rec(kind=L.RECIPE_MXFP8, fmt=L.FORMAT_HYBRID)) == 4   # mxfp8: E4M3 only
+    assert _q(lib, _rec(fmt=3)) == 4                           # no such format
     assert _q(lib, _rec(kind=9)) == 4
     assert _q(lib, _rec(margin=65)) == 4
     assert _q(lib, _rec(algo=1)) == 4                          # only `max`
@@ -88,12 +89,15 @@ def test_quantize_workspace_checks(lib):
 def test_amax_update_checks(lib):
     r = _rec(kind=L.RECIPE_DELAYED, hist=8)
     h = L.AmaxHistory(0x1000, 0x2000, 8)
-    assert lib.fp8_amax_update(ctypes.byref(_rec(kind=L.RECIPE_MXFP8)), ctypes.byref(h), 0x3000,
-                               0x4000, 0x5000, None) == 4
+    assert lib.fp8_amax_update(ctypes.byref(_rec(kind=L.RECIPE_MXFP8)), ctypes.byref(h), 0,
+                               0x3000, 0x4000, 0x5000, None) == 4
     bad = L.AmaxHistory(0x1000, 0x2000, 4)                    # length differs from the recipe
-    assert lib.fp8_amax_update(ctypes.byref(r), ctypes.byref(bad), 0x3000, 0x4000, 0x5000,
+    assert lib.fp8_amax_update(ctypes.byref(r), ctypes.byref(bad), 0, 0x3000, 0x4000, 0x5000,
                                None) == 3
-    assert lib.fp8_amax_update(ctypes.byref(r), ctypes.byref(h), None, 0x4000, 0x5000, None) == 1
+    assert lib.fp8_amax_update(ctypes.byref(r), ctypes.byref(h), 0, None, 0x4000, 0x5000,
+                               None) == 1
+    assert lib.fp8_amax_update(ctypes.byref(r), ctypes.byref(h), 5, 0x3000, 0x4000, 0x5000,
+                               None) == 4                      # no such role
 
 
 def _qt(kind, rows, cols, role=0):

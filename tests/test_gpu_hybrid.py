@@ -1,0 +1,149 @@
+"""GPU parity of the hybrid format (--fp8-format hybrid): gradients stored in E5M2, activations
+and weights in E4M3, for the delayed, tensorwise and blockwise recipes, and the mixed
+E5M2 x E4M3 dgrad / wgrad GEMMs. Codes and scales are bit-exact against the oracle; GEMMs are
+graded like the E4M3 ones (elementwise 1e-2 on bf16 outputs, normwise 1e-5 in fp32 mode).
+"""
+import numpy as np
+import pytest
+import torch
+
+from helpers import (bw_untile, cuda_ok, from_dev_bf16, gemm_bf16_close, gemm_f32_normwise,
+                     same_f32, to_dev_bf16)
+from oracle import fp8_oracle as O
+from workloads import bf16_bits_normal
+
+pytestmark = pytest.mark.gpu
+
+if cuda_ok():
+    import scaled_quantize_fp8_gb300 as F
+
+
+def _np(t):
+    return t.cpu().numpy()
+
+
+def _q(kind, x_bits, role, margin=0, scale=None):
+    rec = F.Recipe(kind=kind, format="hybrid", margin=margin)
+    out = F.empty_qtensor(rec, x_bits.shape[0], x_bits.shape[1], role)
+    if scale is not None:
+        out.scale.fill_(float(scale))
+        out.scale_inv.fill_(float(np.float32(1.0) / np.float32(scale)))
+    F.quantize(rec, to_dev_bf16(x_bits), role, out=out)
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("role", ["grad", "activation", "weight"])
+@pytest.mark.parametrize("margin", [0, 2])
+def test_tensorwise_hybrid(role, margin):
+    x = bf16_bits_normal(256, 384, seed=71, sigma=1e-3 if role == "grad" else 1.0)
+    q = _q("tensorwise", x, role, margin)
+    ref = O.quantize_tensorwise(x, margin, fmt=O.hybrid_format(role))
+    assert same_f32(_np(q.scale)[0], ref["scale"])
+    assert same_f32(_np(q.scale_inv)[0], ref["scale_inv"])
+    assert np.array_equal(_np(q.row), ref["row"])
+    assert np.array_equal(_np(q.col), ref["col"])
+
+
+@pytest.mark.parametrize("role", ["grad", "weight"])
+def test_blockwise_hybrid(role):
+    x = bf16_bits_normal(256, 384, seed=72, sigma=1e-3, outlier_p=1e-2, outlier_factor=30.0)
+    R, C = x.shape
+    q = _q("blockwise", x, role)
+    fmt = O.hybrid_format(role)
+    if role == "weight":
+        ref = O.quantize_blockwise_128x128(x, fmt=fmt)
+        assert np.array_equal(_np(q.row_scale), ref["row_scale_inv"])
+    else:
+        ref = O.quantize_blockwise_1x128(x, fmt=fmt)
+        assert np.array_equal(bw_untile(_np(q.row_scale), R, C), ref["row_scale_inv"])
+        assert np.array_equal(bw_untile(_np(q.col_scale), C, R), ref["col_scale_inv"])
+    assert np.array_equal(_np(q.row), ref["row"])
+    assert np.array_equal(_np(q.col), ref["col"])
+
+
+@pytest.mark.parametrize("scale", [1.0, 3.0, 2.0 ** -14, 2.0 ** 10, 1e-30, 1e30])
+def test_exhaustive_bf16_e5m2_cast(scale):
+    """Every bf16 bit pattern (zeros, subnormals, the largest values, Inf, NaN) cast to E5M2
+    with a fixed delayed scale: the hardware conversion against the oracle's reading."""
+    x = np.arange(65536, dtype=np.uint32).astype(np.uint16).reshape(256, 256)
+    q = _q("delayed", x, "grad", scale=scale)
+    d = O.DelayedScaling(4, fmt="e5m2")
+    d.scale = np.float32(scale)
+    ref = d.quantize(x)
+    assert np.array_equal(_np(q.row), ref["row"])
+    assert np.array_equal(_np(q.col), ref["col"])
+
+
+def test_delayed_hybrid_history():
+    """A gradient's delayed history under hybrid derives its scale from 57344."""
+    rec = F.Recipe(kind="delayed", format="hybrid", amax_history_len=4)
+    state = F.DelayedState(rec, role="grad")
+    d = O.DelayedScaling(4, fmt="e5m2")
+    for t, sigma in enumerate([1e-3, 4e-3, 2e-4, 1e-2, 5e-4, 3e-3]):
+        x = bf16_bits_normal(128, 256, seed=80 + t, sigma=sigma)
+        q = F.empty_qtensor(rec, 128, 256, "grad")
+        state.bind(q)
+        F.quantize(rec, to_dev_bf16(x), "grad", out=q)
+        F.amax_update(rec, state, q.amax)
+        torch.cuda.synchronize()
+        ref = d.quantize(x)
+        d.update(ref["amax"])
+        assert np.array_equal(_np(q.row), ref["row"]), t
+        assert same_f32(_np(state.scale)[0], d.scale), t
+        assert same_f32(_np(state.scale_inv)[0], d.scale_inv), t
+
+
+def _oracle_q(kind, b, role, delayed_scale=None):
+    """The oracle's quantisation of a seeded bf16 tensor: (row deq, col deq) in float64."""
+    fmt = O.hybrid_format(role)
+    if kind == "tensorwise":
+        q = O.quantize_tensorwise(b, fmt=fmt)
+    elif kind == "delayed":
+        d = O.DelayedScaling(4, fmt=fmt)
+        d.scale, d.scale_inv = delayed_scale
+        q = d.quantize(b)
+    if kind in ("tensorwise", "delayed"):
+        return (O.dequant_tensor(q["row"], q["scale_inv"], fmt),
+                O.dequant_tensor(q["col"], q["scale_inv"], fmt))
+    if role == "weight":
+        q = O.quantize_blockwise_128x128(b, fmt=fmt)
+        return (O.dequant_128x128(q["row"], q["row_scale_inv"], fmt),
+                O.dequant_128x128(q["col"], q["col_scale_inv"], fmt))
+    q = O.quantize_blockwise_1x128(b, fmt=fmt)
+    return (O.dequant_1x128(q["row"], q["row_scale_inv"], fmt),
+            O.dequant_1x128(q["col"], q["col_scale_inv"], fmt))
+
+
+@pytest.mark.parametrize("kind", ["tensorwise", "delayed", "blockwise"])
+@pytest.mark.parametrize("fp32", [False, True])
+def test_hybrid_dgrad_wgrad(kind, fp32):
+    """dX = dY . W and dW = dY^T . X with dY in E5M2, W and X in E4M3, against the oracle's
+    GEMMs over its own quantisation of the same seeded inputs."""
+    M, N, K = 256, 384, 512
+    rec = F.Recipe(kind=kind, format="hybrid")
+    xb = bf16_bits_normal(M, K, seed=91)
+    wb = bf16_bits_normal(N, K, seed=92, sigma=0.02)
+    dyb = bf16_bits_normal(M, N, seed=93, sigma=1e-3)
+    qs, refs = {}, {}
+    for name, b, role in (("x", xb, "activation"), ("w", wb, "weight"), ("dy", dyb, "grad")):
+        q = F.empty_qtensor(rec, b.shape[0], b.shape[1], role)
+        ds = None
+        if kind == "delayed":                               # a scale from an earlier step
+            s, si = O.scale_from_amax(O.amax_of(b) * np.float32(1.5), 0, O.hybrid_format(role))
+            ds = (s, si)
+            q.scale.fill_(float(s))
+            q.scale_inv.fill_(float(si))
+        F.quantize(rec, to_dev_bf16(b), role, out=q)
+        qs[name] = q
+        refs[name] = _oracle_q(kind, b, role, ds)
+    dx, dw = F.linear_bwd(rec, qs["dy"], qs["x"], qs["w"], fp32=fp32)
+    torch.cuda.synchronize()
+    dx_ref = O.gemm_tn_f64(refs["dy"][0], refs["w"][1])
+    dw_ref = O.gemm_tn_f64(refs["dy"][1], refs["x"][1])
+    for got, ref in ((dx, dx_ref), (dw, dw_ref)):
+        if fp32:
+            ok, err = gemm_f32_normwise(_np(got), ref)
+        else:
+            ok, err = gemm_bf16_close(from_dev_bf16(got), ref)
+        assert ok, err
