@@ -95,8 +95,12 @@ typedef struct {
   int32_t format;             /* fp8_format (--fp8-format) */
   int32_t margin;             /* --fp8-margin, in [-64, 64]; s is multiplied by 2^-margin */
   int32_t amax_history_len;   /* --fp8-amax-history-len (DELAYED), >= 1 */
-  int32_t amax_compute_algo;  /* --fp8-amax-compute-algo: 0 = max (the only one built) */
+  int32_t amax_compute_algo;  /* --fp8-amax-compute-algo: 0 = max (the page's minimum
+                                 config), 1 = most_recent (the newest amax alone) */
   int32_t fp8_wgrad;          /* --fp8-wgrad: 1 = wgrad GEMM in FP8, 0 = in bf16 */
+  int32_t power_2_scales;     /* BLOCKWISE only: 1 = each block scale rounded down to a power
+                                 of two (exact s_inv; maps onto power-of-two hardware
+                                 scaling), 0 = plain fp32 scales. Other recipes: must be 0 */
 } fp8_recipe;
 
 /* A quantised tensor: codes and scales of both copies, all device memory owned by the
@@ -154,7 +158,8 @@ fp8_status fp8_quantize(const fp8_recipe *recipe, const void *x_bf16, int64_t ro
 /*
  * fp8_amax_update — delayed scaling: push *amax_new into the history (the oldest of `len`
  * entries drops out) and write scale = f(max(history)), scale_inv = 1/scale with f the
- * per-tensor rule above (--fp8-amax-history-len, --fp8-amax-compute-algo max, --fp8-margin).
+ * per-tensor rule above (--fp8-amax-history-len, --fp8-margin), or with
+ * --fp8-amax-compute-algo most_recent scale = f(*amax_new) (the history is still recorded).
  * role: fp8_role of the tensor this history belongs to (under the hybrid format a gradient's
  * scale uses the E5M2 maximum 57344). One CTA; reads and writes device memory only.
  */

@@ -33,6 +33,8 @@ where they are silent the readings below are the plainest ones the rest supports
   * Delayed: the history starts as L zeros and s = 1; a step quantises with the scale from
     the history of the previous steps only, then pushes its own amax (evicting the oldest
     entry once L are held) and derives the next scale from max(history).
+  * Power-of-two block scales (the blockwise recipe's option that maps onto power-of-two
+    hardware scaling): the block scale above is rounded down to a power of two.
   * Blockwise: 1x128 blocks for activations and gradients, whose column-wise copy is
     re-quantised from bf16 with 1x128 blocks along the other dimension; 128x128 blocks for
     weights, whose column-wise copy is the byte transpose with the scale grid transposed.
@@ -214,9 +216,18 @@ def hybrid_format(role):
 # Per-tensor scale (tensorwise, delayed; per block for blockwise)
 # --------------------------------------------------------------------------------------
 
-def scales_from_amax(amax, margin=0, fmt="e4m3"):
+def pow2_floor(s):
+    """Largest power of two <= s for positive finite float32 s (exact, through the exponent);
+    0 stays 0."""
+    s = np.asarray(s, dtype=np.float32).astype(np.float64)
+    _, ex = np.frexp(s)                           # s = f * 2^ex, f in [0.5, 1)
+    return np.where(s > 0, np.ldexp(1.0, ex - 1), 0.0).astype(np.float32)
+
+
+def scales_from_amax(amax, margin=0, fmt="e4m3", pow2=False):
     """(s, s_inv) as float32 arrays from amax values: s = fp32(448/amax) * 2^-margin, s_inv = 1/s
-    (57344 in place of 448 for E5M2).
+    (57344 in place of 448 for E5M2). With pow2 (power-of-two block scales), s is then rounded
+    down to a power of two, so s_inv is exact and no element can exceed the format's maximum.
 
     The tensorwise entry derives the scale from the tensor being cast; --fp8-margin
     (Numerical Stability Knobs) gives the scale M extra bits of headroom. The division
@@ -230,6 +241,8 @@ def scales_from_amax(amax, margin=0, fmt="e4m3"):
                      np.float32(1.0)).astype(np.float32)
         s = np.ldexp(s.astype(np.float64), -int(margin)).astype(np.float32)
     s = np.where(np.isinf(s), FLT_MAX, s).astype(np.float32)
+    if pow2:
+        s = pow2_floor(s)
     s_inv = (np.float32(1.0) / s).astype(np.float32)
     return s, s_inv
 
@@ -271,17 +284,22 @@ def quantize_tensorwise(x_bf16, margin=0, fmt="e4m3"):
 # --------------------------------------------------------------------------------------
 
 class DelayedScaling:
-    """Rolling amax history of length L with the `max` compute algorithm.
+    """Rolling amax history of length L with the `max` (or `most_recent`) compute algorithm.
 
-    --fp8-amax-history-len L, --fp8-amax-compute-algo max, --fp8-margin M.
+    --fp8-amax-history-len L, --fp8-amax-compute-algo {max, most_recent}, --fp8-margin M.
+    The page's minimum config names `max`; `most_recent` is the knob's other setting (the
+    newest amax alone decides the next scale).
     """
 
-    def __init__(self, history_len, margin=0, fmt="e4m3"):
+    def __init__(self, history_len, margin=0, fmt="e4m3", algo="max"):
         if history_len < 1:
             raise ValueError("amax history length must be >= 1")
+        if algo not in ("max", "most_recent"):
+            raise ValueError("amax compute algo is max or most_recent")
         self.L = int(history_len)
         self.margin = int(margin)
         self.fmt = fmt
+        self.algo = algo
         self.history = np.zeros(self.L, dtype=np.float32)
         self.head = 0
         self.scale = np.float32(1.0)
@@ -295,11 +313,12 @@ class DelayedScaling:
                     col=np.ascontiguousarray(row.T))
 
     def update(self, amax_new):
-        """Push amax_new (oldest entry evicted) and derive the next scale from the max."""
+        """Push amax_new (oldest entry evicted) and derive the next scale from the window's max
+        (`max`) or from amax_new alone (`most_recent`, the history is still recorded)."""
         self.history[self.head] = np.float32(amax_new)
         self.head = (self.head + 1) % self.L
-        self.scale, self.scale_inv = scale_from_amax(np.max(self.history), self.margin,
-                                                     self.fmt)
+        a = np.max(self.history) if self.algo == "max" else np.float32(amax_new)
+        self.scale, self.scale_inv = scale_from_amax(a, self.margin, self.fmt)
         return self.scale, self.scale_inv
 
 
@@ -360,29 +379,29 @@ def e8m0_decode(bytes_):
 # Blockwise (recipe entry "blockwise": 1x128 activation blocks, 128x128 weight blocks)
 # --------------------------------------------------------------------------------------
 
-def _bw_quantize_1x128_lastdim(x_bf16, margin, fmt="e4m3"):
+def _bw_quantize_1x128_lastdim(x_bf16, margin, fmt="e4m3", pow2=False):
     """Per 1x128 block along the last dim: codes [R,C], s_inv [R, C/128] (float32)."""
     x = bf16_to_f32(x_bf16)
     R, C = x.shape
     blocks = x.reshape(R, C // BW_BLOCK, BW_BLOCK)
-    s, s_inv = scales_from_amax(np.max(np.abs(blocks), axis=2), margin, fmt)
+    s, s_inv = scales_from_amax(np.max(np.abs(blocks), axis=2), margin, fmt, pow2)
     codes = fp8_encode((blocks * s[:, :, None]).astype(np.float32), fmt).reshape(R, C)
     return codes, s_inv
 
 
-def quantize_blockwise_1x128(x_bf16, margin=0, fmt="e4m3"):
+def quantize_blockwise_1x128(x_bf16, margin=0, fmt="e4m3", pow2=False):
     """Activations / gradients: row copy with 1x128 blocks along C, column copy of X^T
     re-quantised from bf16 with 1x128 blocks along R.
 
     Returns dict(row=[R,C], row_scale_inv=[R,C/128], col=[C,R], col_scale_inv=[C,R/128]).
     """
     x = np.asarray(x_bf16, dtype=np.uint16)
-    row, row_si = _bw_quantize_1x128_lastdim(x, margin, fmt)
-    col, col_si = _bw_quantize_1x128_lastdim(np.ascontiguousarray(x.T), margin, fmt)
+    row, row_si = _bw_quantize_1x128_lastdim(x, margin, fmt, pow2)
+    col, col_si = _bw_quantize_1x128_lastdim(np.ascontiguousarray(x.T), margin, fmt, pow2)
     return dict(row=row, row_scale_inv=row_si, col=col, col_scale_inv=col_si)
 
 
-def quantize_blockwise_128x128(x_bf16, margin=0, fmt="e4m3"):
+def quantize_blockwise_128x128(x_bf16, margin=0, fmt="e4m3", pow2=False):
     """Weights: one scale per 128x128 tile; column copy = byte transpose, grid transposed.
 
     Returns dict(row=[R,C], row_scale_inv=[R/128, C/128], col=[C,R], col_scale_inv=[C/128,R/128]).
@@ -391,7 +410,7 @@ def quantize_blockwise_128x128(x_bf16, margin=0, fmt="e4m3"):
     R, C = x.shape
     gr, gc = R // BW_BLOCK, C // BW_BLOCK
     tiles = x.reshape(gr, BW_BLOCK, gc, BW_BLOCK)            # [i, r, j, c]
-    s, s_inv = scales_from_amax(np.max(np.abs(tiles), axis=(1, 3)), margin, fmt)
+    s, s_inv = scales_from_amax(np.max(np.abs(tiles), axis=(1, 3)), margin, fmt, pow2)
     codes = fp8_encode((tiles * s[:, None, :, None]).astype(np.float32), fmt).reshape(R, C)
     return dict(row=codes, row_scale_inv=s_inv, col=np.ascontiguousarray(codes.T),
                 col_scale_inv=np.ascontiguousarray(s_inv.T))

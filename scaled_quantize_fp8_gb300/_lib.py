@@ -24,7 +24,7 @@ ROLE_ACTIVATION, ROLE_WEIGHT, ROLE_GRAD = 0, 1, 2
 class Recipe(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int32), ("format", ctypes.c_int32), ("margin", ctypes.c_int32),
                 ("amax_history_len", ctypes.c_int32), ("amax_compute_algo", ctypes.c_int32),
-                ("fp8_wgrad", ctypes.c_int32)]
+                ("fp8_wgrad", ctypes.c_int32), ("power_2_scales", ctypes.c_int32)]
 
 
 class Tensor(ctypes.Structure):

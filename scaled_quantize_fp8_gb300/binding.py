@@ -28,11 +28,12 @@ class Recipe:
     amax_history_len: int = 1024
     amax_compute_algo: str = "max"
     fp8_wgrad: bool = True
+    power_2_scales: bool = False
 
     def c(self):
         return L.Recipe(KINDS[self.kind], 0 if self.format == "e4m3" else 1, int(self.margin),
                         int(self.amax_history_len), 0 if self.amax_compute_algo == "max" else 1,
-                        1 if self.fp8_wgrad else 0)
+                        1 if self.fp8_wgrad else 0, 1 if self.power_2_scales else 0)
 
 
 def _ptr(t: Optional[torch.Tensor]):

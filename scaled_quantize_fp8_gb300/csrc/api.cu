@@ -32,8 +32,10 @@ fp8_status check_recipe(const fp8_recipe* r) {
   if (r->format == FP8_FORMAT_HYBRID && r->kind == FP8_RECIPE_MXFP8)
     return FP8_ERR_UNSUPPORTED;                                  // mxfp8 is E4M3 only
   if (r->margin < -64 || r->margin > 64) return FP8_ERR_UNSUPPORTED;
-  if (r->amax_compute_algo != 0) return FP8_ERR_UNSUPPORTED;      // only `max`
+  if (r->amax_compute_algo != 0 && r->amax_compute_algo != 1)   // max, most_recent
+    return FP8_ERR_UNSUPPORTED;
   if (r->kind == FP8_RECIPE_DELAYED && r->amax_history_len < 1) return FP8_ERR_SHAPE;
+  if (r->power_2_scales != 0 && r->kind != FP8_RECIPE_BLOCKWISE) return FP8_ERR_UNSUPPORTED;
   return FP8_OK;
 }
 
@@ -126,7 +128,8 @@ fp8_status fp8_quantize(const fp8_recipe* recipe, const void* x_bf16, int64_t ro
   out->role = role;
   out->kind = kind;
   out->col_bf16 = col_bf16 ? 1 : 0;
-  return cuda_status(quantize_launch(kind, role, fmt_of(recipe, role), recipe->margin,
+  return cuda_status(quantize_launch(kind, role, fmt_of(recipe, role),
+                                     recipe->power_2_scales != 0, recipe->margin,
                                      reinterpret_cast<const uint16_t*>(x_bf16), rows, cols,
                                      want_row != 0, want_col != 0, col_bf16, out, workspace,
                                      dev_status, stream));
@@ -144,7 +147,8 @@ fp8_status fp8_amax_update(const fp8_recipe* recipe, fp8_amax_history* hist, int
   if (hist->len < 1 || hist->len != recipe->amax_history_len) return FP8_ERR_SHAPE;
   const float fmax = fmt_of(recipe, role) == 1 ? 57344.0f : 448.0f;
   return cuda_status(amax_update_launch(hist->history, hist->head, hist->len, amax_new, scale,
-                                        scale_inv, recipe->margin, fmax, stream));
+                                        scale_inv, recipe->margin, fmax,
+                                        recipe->amax_compute_algo, stream));
 }
 
 }  // extern "C"

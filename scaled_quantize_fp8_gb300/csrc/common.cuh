@@ -82,10 +82,10 @@ __device__ __forceinline__ float exp2i(int k) {
 }
 
 // Per-tensor / per-block scale from an amax: s = fp32(fmax/amax) * 2^-margin (fmax = 448 for
-// E4M3, 57344 for E5M2), s = 1 for
+// E4M3, 57344 for E5M2), rounded down to a power of two when pow2 is set, s = 1 for
 // amax 0 / Inf / NaN, an infinite s becomes FLT_MAX. Returns s; *s_inv = fp32(1/s).
 __device__ __forceinline__ float scale_from_amax(float amax, int margin, float* s_inv,
-                                                 float fmax = 448.0f) {
+                                                 float fmax = 448.0f, bool pow2 = false) {
   float s;
   if (!(amax > 0.0f) || !(amax <= 3.402823466e38f)) {
     s = 1.0f;
@@ -94,6 +94,12 @@ __device__ __forceinline__ float scale_from_amax(float amax, int margin, float* 
   }
   if (margin != 0) s = __fmul_rn(s, exp2i(-margin));
   if (s > 3.402823466e38f) s = 3.402823466e38f;
+  if (pow2) {
+    // largest power of two <= s: keep the exponent (normal), or the top set bit (subnormal)
+    const uint32_t b = __float_as_uint(s);
+    s = __uint_as_float(b >= 0x00800000u ? (b & 0xFF800000u)
+                                         : (b == 0u ? 0u : (0x80000000u >> __clz(b))));
+  }
   *s_inv = __fdiv_rn(1.0f, s);
   return s;
 }

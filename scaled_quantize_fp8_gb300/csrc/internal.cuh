@@ -21,10 +21,11 @@ int num_sms();
 // ---- quantize.cu
 size_t quantize_workspace_bytes(int kind, int64_t R, int64_t C);
 // fmt: 0 = E4M3, 1 = E5M2 (gradients under the hybrid format; not for MXFP8)
-cudaError_t quantize_launch(int kind, int role, int fmt, int margin, const uint16_t* x,
-                            int64_t R, int64_t C, bool want_row, bool want_col, bool col_bf16,
-                            fp8_tensor* out, void* workspace, int32_t* status,
-                            cudaStream_t st);
+// pow2: power-of-two block scales (blockwise only)
+cudaError_t quantize_launch(int kind, int role, int fmt, bool pow2, int margin,
+                            const uint16_t* x, int64_t R, int64_t C, bool want_row,
+                            bool want_col, bool col_bf16, fp8_tensor* out, void* workspace,
+                            int32_t* status, cudaStream_t st);
 cudaError_t gelu_quantize_launch(const uint16_t* h, int64_t R, int64_t C, uint16_t* a_bf16,
                                  fp8_tensor* a_q, fp8_tensor* h_q, int32_t* status,
                                  cudaStream_t st);
@@ -33,7 +34,7 @@ cudaError_t dgelu_quantize_launch(const uint16_t* da, const fp8_tensor* h_q, int
                                   int32_t* status, cudaStream_t st);
 cudaError_t amax_update_launch(float* hist, int32_t* head, int len, const float* amax_new,
                                float* scale, float* scale_inv, int margin, float fmax,
-                               cudaStream_t st);
+                               int algo, cudaStream_t st);
 
 // ---- gemm.cu
 enum GMode : int { G_TENSOR = 0, G_MX = 1, G_BLOCK = 2, G_BF16 = 3 };

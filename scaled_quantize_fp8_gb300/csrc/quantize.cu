@@ -34,6 +34,7 @@ struct QuantParams {
   uint8_t* col;               // [C][R] codes (or bf16 when col_bf16), or null
   bool col_bf16;              // column copy = bf16 transpose (wgrad kept in bf16)
   bool col_v8;                // column copy rows start on 32-byte boundaries (256-bit stores)
+  bool pow2;                  // blockwise: power-of-two block scales
   void* row_scale;
   void* col_scale;
   // per-tensor recipes
@@ -234,7 +235,7 @@ __device__ __forceinline__ void quantize_one_tile(const QuantParams& p, QuantCtl
     if constexpr (MODE == Q_TENSOR) {
       if (t == 0) p.part_out[tile_id] = tm;               // delayed: record this tile's amax
     } else {
-      s_tile = scale_from_amax(amax_from_bits(tm), p.margin, &sinv_tile, fp8_max<F8>());
+      s_tile = scale_from_amax(amax_from_bits(tm), p.margin, &sinv_tile, fp8_max<F8>(), p.pow2);
       if (t == 0) {
         const int tiles_r = int((R + 127) >> 7);
         if (p.row_scale) reinterpret_cast<float*>(p.row_scale)[tr * p.tiles_c + tc] = sinv_tile;
@@ -266,7 +267,7 @@ __device__ __forceinline__ void quantize_one_tile(const QuantParams& p, QuantCtl
           m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
           m = max(m, __shfl_xor_sync(0xffffffffu, m, 16));
           float sinv;
-          s = scale_from_amax(amax_from_bits(m), p.margin, &sinv, fp8_max<F8>());
+          s = scale_from_amax(amax_from_bits(m), p.margin, &sinv, fp8_max<F8>(), p.pow2);
           if (h == 0 && cc == 0) S.scf_row[r] = sinv;
         }
         nan = m > 0x7F80u;
@@ -371,8 +372,8 @@ __device__ __forceinline__ void quantize_one_tile(const QuantParams& p, QuantCtl
         const uint32_t fb = max(max(S.red_col[0][2 * pp + 1], S.red_col[1][2 * pp + 1]),
                                 max(S.red_col[2][2 * pp + 1], S.red_col[3][2 * pp + 1]));
         float ia, ib;
-        sa = scale_from_amax(amax_from_bits(fa), p.margin, &ia, fp8_max<F8>());
-        sb = scale_from_amax(amax_from_bits(fb), p.margin, &ib, fp8_max<F8>());
+        sa = scale_from_amax(amax_from_bits(fa), p.margin, &ia, fp8_max<F8>(), p.pow2);
+        sb = scale_from_amax(amax_from_bits(fb), p.margin, &ib, fp8_max<F8>(), p.pow2);
         if (q == 0) {
           S.scf_col[2 * pp] = ia;
           S.scf_col[2 * pp + 1] = ib;
@@ -487,7 +488,7 @@ __global__ void __launch_bounds__(256, quant_ctas_per_sm<MODE, EPI>())
       m = block_max_u32(m, S.red);
       tensor_nan = m > 0x7F80u;
       float sinv;
-      s_tensor = scale_from_amax(amax_from_bits(m), p.margin, &sinv, fp8_max<F8>());
+      s_tensor = scale_from_amax(amax_from_bits(m), p.margin, &sinv, fp8_max<F8>(), p.pow2);
       if (blockIdx.x == 0 && t == 0) {
         *p.amax_out = amax_from_bits(m);
         *p.scale_out = s_tensor;
@@ -588,11 +589,12 @@ __global__ void empty_scalars_kernel(float* amax, float* scale, float* scale_inv
 }
 
 // Delayed scaling history update (one CTA): push amax_new at head, advance head, and derive
-// the next scale from the max over the whole window (the `max` compute algorithm).
+// the next scale from the max over the whole window (compute algorithm `max`, algo 0) or from
+// amax_new alone (`most_recent`, algo 1).
 __global__ void __launch_bounds__(1024) amax_history_update_kernel(
     float* __restrict__ hist, int32_t* __restrict__ head, int len,
     const float* __restrict__ amax_new, float* __restrict__ scale,
-    float* __restrict__ scale_inv, int margin, float fmax) {
+    float* __restrict__ scale_inv, int margin, float fmax, int algo) {
   __shared__ float red[32];
   __shared__ int nan_seen;
   const int h = *head;
@@ -613,6 +615,7 @@ __global__ void __launch_bounds__(1024) amax_history_update_kernel(
     float r = red[0];
     for (int k = 1; k < int(blockDim.x >> 5); ++k) r = fmaxf(r, red[k]);
     if (nan_seen) r = __uint_as_float(0x7FC00000u);
+    if (algo == 1) r = a_new;
     hist[h] = a_new;
     *head = (h + 1) % len;
     float si;
@@ -661,12 +664,13 @@ static cudaError_t launch_tiles(QuantParams p, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-cudaError_t quantize_launch(int kind, int role, int fmt, int margin, const uint16_t* x,
-                            int64_t R, int64_t C, bool want_row, bool want_col, bool col_bf16,
-                            fp8_tensor* out, void* workspace, int32_t* status,
-                            cudaStream_t st) {
+cudaError_t quantize_launch(int kind, int role, int fmt, bool pow2, int margin,
+                            const uint16_t* x, int64_t R, int64_t C, bool want_row,
+                            bool want_col, bool col_bf16, fp8_tensor* out, void* workspace,
+                            int32_t* status, cudaStream_t st) {
   const bool e5 = fmt == F8_E5M2;
   QuantParams p{};
+  p.pow2 = pow2 && kind == FP8_RECIPE_BLOCKWISE;
   p.status = status;
   p.col_bf16 = col_bf16;
   p.x = x;
@@ -769,9 +773,9 @@ cudaError_t dgelu_quantize_launch(const uint16_t* da, const fp8_tensor* h_q, int
 
 cudaError_t amax_update_launch(float* hist, int32_t* head, int len, const float* amax_new,
                                float* scale, float* scale_inv, int margin, float fmax,
-                               cudaStream_t st) {
+                               int algo, cudaStream_t st) {
   amax_history_update_kernel<<<1, 1024, 0, st>>>(hist, head, len, amax_new, scale, scale_inv,
-                                                 margin, fmax);
+                                                 margin, fmax, algo);
   return cudaGetLastError();
 }
 

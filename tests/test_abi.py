@@ -59,7 +59,10 @@ def test_quantize_rejects_bad_arguments(lib):
     assert _q(lib, _rec(fmt=3)) == 4                           # no such format
     assert _q(lib, _rec(kind=9)) == 4
     assert _q(lib, _rec(margin=65)) == 4
-    assert _q(lib, _rec(algo=1)) == 4                          # only `max`
+    assert _q(lib, _rec(algo=2)) == 4                          # max or most_recent
+    pow2 = _rec()
+    pow2.power_2_scales = 1
+    assert _q(lib, pow2) == 4                                  # power-of-two: blockwise only
     assert _q(lib, _rec(kind=L.RECIPE_DELAYED, hist=0)) == 3
     assert _q(lib, r, rows=-16) == 3
     assert _q(lib, r, rows=24) == 3                            # not a multiple of 16

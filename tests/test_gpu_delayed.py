@@ -15,10 +15,10 @@ if cuda_ok():
     import scaled_quantize_fp8_gb300 as F
 
 
-def _run_sequence(M, K, steps, L, margin=0, check_codes_every=1, gemm=False):
-    rec = F.Recipe(kind="delayed", amax_history_len=L, margin=margin)
+def _run_sequence(M, K, steps, L, margin=0, check_codes_every=1, gemm=False, algo="max"):
+    rec = F.Recipe(kind="delayed", amax_history_len=L, margin=margin, amax_compute_algo=algo)
     state = F.DelayedState(rec)
-    oracle = O.DelayedScaling(L, margin)
+    oracle = O.DelayedScaling(L, margin, algo=algo)
     sig = sigma_schedule(steps)
     wb = bf16_bits_normal(K, K, seed=0, stream=1, sigma=0.02)
     wstate = F.DelayedState(rec)
@@ -60,6 +60,11 @@ def _run_sequence(M, K, steps, L, margin=0, check_codes_every=1, gemm=False):
 
 def test_short_history_wraps():
     _run_sequence(256, 384, steps=12, L=4, gemm=True)
+
+
+def test_most_recent_algo():
+    """--fp8-amax-compute-algo most_recent: the newest amax alone sets the next scale."""
+    _run_sequence(256, 384, steps=10, L=4, algo="most_recent")
 
 
 def test_margin_and_long_history():

@@ -147,3 +147,45 @@ def test_hybrid_dgrad_wgrad(kind, fp32):
         else:
             ok, err = gemm_bf16_close(from_dev_bf16(got), ref)
         assert ok, err
+
+
+@pytest.mark.parametrize("role", ["activation", "weight"])
+@pytest.mark.parametrize("margin", [0, 3])
+def test_blockwise_power_of_two_scales(role, margin):
+    """Blockwise with power-of-two block scales: codes and s_inv bit-exact, every s_inv a
+    power of two, and the GEMM over them within the usual tolerance."""
+    rec = F.Recipe(kind="blockwise", power_2_scales=True, margin=margin)
+    x = bf16_bits_normal(256, 384, seed=101, outlier_p=1e-2, outlier_factor=40.0)
+    R, C = x.shape
+    q = F.empty_qtensor(rec, R, C, role)
+    F.quantize(rec, to_dev_bf16(x), role, out=q)
+    torch.cuda.synchronize()
+    if role == "weight":
+        ref = O.quantize_blockwise_128x128(x, margin, pow2=True)
+        assert np.array_equal(_np(q.row_scale), ref["row_scale_inv"])
+        assert np.array_equal(_np(q.col_scale), ref["col_scale_inv"])
+    else:
+        ref = O.quantize_blockwise_1x128(x, margin, pow2=True)
+        assert np.array_equal(bw_untile(_np(q.row_scale), R, C), ref["row_scale_inv"])
+        assert np.array_equal(bw_untile(_np(q.col_scale), C, R), ref["col_scale_inv"])
+    assert np.array_equal(_np(q.row), ref["row"])
+    assert np.array_equal(_np(q.col), ref["col"])
+    f, _ = np.frexp(ref["row_scale_inv"].astype(np.float64))
+    assert np.all(f == 0.5)
+
+
+def test_blockwise_power_of_two_fprop():
+    rec = F.Recipe(kind="blockwise", power_2_scales=True)
+    M, N, K = 256, 384, 512
+    xb = bf16_bits_normal(M, K, seed=102)
+    wb = bf16_bits_normal(N, K, seed=103, sigma=0.02)
+    xq = F.quantize(rec, to_dev_bf16(xb), "activation")
+    wq = F.quantize(rec, to_dev_bf16(wb), "weight")
+    y = F.linear_fwd(rec, xq, wq, fp32=True)
+    torch.cuda.synchronize()
+    qx = O.quantize_blockwise_1x128(xb, pow2=True)
+    qw = O.quantize_blockwise_128x128(wb, pow2=True)
+    ref = O.gemm_tn_f64(O.dequant_1x128(qx["row"], qx["row_scale_inv"]),
+                        O.dequant_128x128(qw["row"], qw["row_scale_inv"]))
+    ok, err = gemm_f32_normwise(_np(y), ref)
+    assert ok, err

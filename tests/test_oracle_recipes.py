@@ -103,6 +103,24 @@ def test_delayed_scripted_sequence():
         assert d.history.dtype == np.float32
 
 
+def test_delayed_scripted_sequence_most_recent():
+    hdr = [l for l in open(os.path.join(GOLDEN, "delayed_sequence_most_recent.txt"))
+           if l.startswith("# ")]
+    L = int([h for h in hdr if h.startswith("# history_len")][0].split()[2])
+    amaxes = [float(t) for t in [h for h in hdr if h.startswith("# amax ")][0].split()[2:]]
+    want = {int(t[0]): Fraction(t[1]) for t in _lines("delayed_sequence_most_recent.txt")}
+    d = O.DelayedScaling(L, algo="most_recent")
+    got = [d.scale]
+    for a in amaxes:
+        d.update(a)
+        got.append(d.scale)
+    for step, w in want.items():
+        s = got[step]
+        # fp32 of the rational value, correctly rounded
+        assert abs(Fraction(float(s)) - w) <= Fraction(float(np.spacing(np.float32(s)))) / 2
+    assert list(d.history) == [np.float32(0.25), np.float32(0.125), 2.0, 0.5]   # still recorded
+
+
 def test_delayed_quantizes_with_previous_scale_and_saturates():
     d = O.DelayedScaling(8)
     x0 = bf16_bits_from_f32(np.full((4, 32), 2.0, np.float32))
@@ -223,3 +241,24 @@ def test_mx_nonfinite_block_gets_nan_scale():
     assert q["row"][3, 40] == 0x7E and (q["row"][7, 2] & 0x7F) == 0x7F
     assert q["row"][3, 41] == O.e4m3_encode(np.float32(1.0))                 # e = 0 in the NaN block
     assert np.isnan(O.e8m0_decode(np.uint8(255)))
+
+
+def test_power_of_two_block_scales():
+    """pow2 block scales are the largest power of two not above 448/amax: checked by brute
+    search over the exponent, with the no-saturation property and exact s_inv."""
+    rng = np.random.default_rng(11)
+    amax = np.float32(np.exp(rng.uniform(-30, 30, 2000))).astype(np.float32)
+    s, s_inv = O.scales_from_amax(amax, pow2=True)
+    for a, v in zip(amax[:200], s[:200]):
+        q = np.float32(np.float32(448.0) / a)
+        k = max(e for e in range(-149, 128) if 2.0 ** e <= float(q))
+        assert float(v) == 2.0 ** k
+    assert np.all(s.astype(np.float64) * amax.astype(np.float64) <= 448.0)
+    assert np.all(s.astype(np.float64) * s_inv.astype(np.float64) == 1.0)
+    # margin: one more halving per bit
+    s2, _ = O.scales_from_amax(amax, margin=2, pow2=True)
+    assert np.array_equal(s2, (s / 4).astype(np.float32))
+    x = bf16_bits_from_f32(rng.standard_normal((128, 256)).astype(np.float32))
+    q = O.quantize_blockwise_1x128(x, pow2=True)
+    f, _ = np.frexp(q["row_scale_inv"].astype(np.float64))
+    assert np.all(f == 0.5)                                   # every s_inv a power of two
