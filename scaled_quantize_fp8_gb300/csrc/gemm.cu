@@ -37,15 +37,18 @@ constexpr int kBM = 128;                      // accumulator rows per CTA (TMEM 
 constexpr int kBN = 256;                      // accumulator columns per tile
 constexpr int kBKBytes = 128;                 // one 128-byte swizzle row of K per stage
 // Epilogue warps: 8 for plain stores (two per TMEM lane quadrant, 128 columns each); 16 for
-// the fused MLP epilogues (four per quadrant, 64 columns each), whose per-element work needs
-// more warps in flight to hide its latency. Warp 0 is the TMA producer, warp 1 the MMA issuer.
-template <int EPI>
-__host__ __device__ constexpr int epi_warps() { return EPI == EPI_NONE ? 8 : 16; }
+// the fused MLP epilogues and the blockwise promotion (four per quadrant, 64 columns each),
+// whose per-chunk work needs more warps in flight to hide its latency. Warp 0 is the TMA
+// producer, warp 1 the MMA issuer.
+template <int MODE, int EPI>
+__host__ __device__ constexpr int epi_warps() {
+  return (EPI != EPI_NONE || MODE == G_BLOCK) ? 16 : 8;
+}
 // MXFP8 kernels add one warp that copies each stage's scale factors into TMEM, so the MMA
 // issuer's instruction stream holds nothing but MMAs.
 template <int MODE, int EPI>
 __host__ __device__ constexpr int gemm_threads() {
-  return 64 + 32 * epi_warps<EPI>() + (MODE == G_MX ? 32 : 0);
+  return 64 + 32 * epi_warps<MODE, EPI>() + (MODE == G_MX ? 32 : 0);
 }
 constexpr uint32_t kTileABytes = kBM * kBKBytes;      // 16 KiB
 constexpr uint32_t kSfStageBytes = 2048;              // SFA 512 B at 0, SFB 2 x 512 B at 512
@@ -64,7 +67,7 @@ constexpr uint32_t kEpiStageBytes = 2048;              // one warp's 32 x 32 bf1
 template <int EPI>
 __host__ __device__ constexpr uint32_t epi_smem_bytes() {
   return EPI == EPI_NONE ? 0u
-                         : epi_warps<EPI>() * kEpiStageBytes +
+                         : epi_warps<G_MX, EPI>() * kEpiStageBytes +
                                (EPI == EPI_GELU ? kGeluTableBytes : kDgeluCodeTableBytes);
 }
 template <int CTA2, int EPI = EPI_NONE>
@@ -138,14 +141,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// Store one thread's row segment of 128 fp32 values (columns n .. n+127 of row m).
-__device__ __forceinline__ void store_row128(const GemmParams& p, int m, int n, const float* v) {
+// Store one thread's row segment of NC fp32 values (columns n .. n+NC-1 of row m).
+template <int NC>
+__device__ __forceinline__ void store_row(const GemmParams& p, int m, int n, const float* v) {
   if (m >= p.M) return;
   const bool v8 = p.d_v8 != 0;
   if (p.d_fp32) {
     float* dst = reinterpret_cast<float*>(p.D) + int64_t(m) * p.ldd + n;
 #pragma unroll
-    for (int j = 0; j < 128; j += 8) {
+    for (int j = 0; j < NC; j += 8) {
       // N is a multiple of 16, so a segment starting inside the row ends inside it
       const bool ok = n + j < p.N;
       store_seg32(dst + j,
@@ -158,7 +162,7 @@ __device__ __forceinline__ void store_row128(const GemmParams& p, int m, int n, 
   } else {
     uint16_t* dst = reinterpret_cast<uint16_t*>(p.D) + int64_t(m) * p.ldd + n;
 #pragma unroll
-    for (int j = 0; j < 128; j += 16) {
+    for (int j = 0; j < NC; j += 16) {
       const bool ok = n + j < p.N;
       store_seg32(dst + j,
                   make_uint4(pack_bf16x2(v[j], v[j + 1]), pack_bf16x2(v[j + 2], v[j + 3]),
@@ -295,7 +299,7 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
                                              const CUtensorMap& tmSFA, const CUtensorMap& tmSFB,
                                              const GemmParams& p) {
   using G = Geo<CTA2, EPI>;
-  constexpr int kEpiWarps = epi_warps<EPI>();
+  constexpr int kEpiWarps = epi_warps<MODE, EPI>();
   static_assert(EPI == EPI_NONE || MODE == G_MX, "fused MLP epilogues are MXFP8 only");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -500,7 +504,8 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
     const int ew = warp - 2;
     const int quad = warp & 3;            // TMEM lane quadrant this warp may access
     constexpr int kCols = 4 * kBN / kEpiWarps;              // accumulator columns per warp
-    static_assert(EPI != EPI_NONE || kCols == 128, "plain epilogue: 128 columns per warp");
+    static_assert(EPI != EPI_NONE || MODE == G_BLOCK || kCols == 128,
+                  "plain epilogue: 128 columns per warp");
     const int slice = ew >> 2;            // which kCols columns of the 256-wide tile
     const int row = 32 * quad + lane;
     const uint32_t t_lane = tmem + (uint32_t(32 * quad) << 16) + uint32_t(slice * kCols);
@@ -554,7 +559,7 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
     float alpha = 1.0f;
     if constexpr (MODE == G_TENSOR) alpha = __fmul_rn(*p.a_sinv, *p.b_sinv);
     uint32_t u = 0;
-    float acc[128];
+    float acc[kCols];
     for (int tile = unit; tile < n_tiles; tile += n_units) {
       int mt, nt;
       tile_coords(tile, tiles_m, tiles_n, &mt, &nt);
@@ -571,11 +576,11 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
         ++u;
         if constexpr (MODE == G_TENSOR) {
 #pragma unroll
-          for (int j = 0; j < 128; ++j) acc[j] = __fmul_rn(acc[j], alpha);
+          for (int j = 0; j < kCols; ++j) acc[j] = __fmul_rn(acc[j], alpha);
         }
       } else {
 #pragma unroll
-        for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+        for (int j = 0; j < kCols; ++j) acc[j] = 0.0f;
         const int kblocks = p.K / 128;
         bool ok = true;
         for (int kb = 0; kb < kblocks; ++kb) {
@@ -588,24 +593,24 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
             break;
           }
           ptx::tc_fence_after();
-          // Promote the chunk 32 columns at a time (keeps the partials out of registers).
+          // Promote the chunk 16 columns at a time (keeps the partials out of registers).
           const float f = __fmul_rn(sa, sb);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t r[32];
-            ptx::tmem_ld_32x32b_x32(t_lane + b * kBN + 32 * c, r);
+          for (int c = 0; c < kCols / 16; ++c) {
+            uint32_t r[16];
+            ptx::tmem_ld_32x32b_x16(t_lane + b * kBN + 16 * c, r);
             ptx::tmem_wait_ld();
             if constexpr (B128 != 0) {
 #pragma unroll
-              for (int j = 0; j < 32; ++j)
-                acc[32 * c + j] = __fmaf_rn(__uint_as_float(r[j]), f, acc[32 * c + j]);
+              for (int j = 0; j < 16; ++j)
+                acc[16 * c + j] = __fmaf_rn(__uint_as_float(r[j]), f, acc[16 * c + j]);
             } else {
-              const float* sbv = p.b_bs + int64_t(kb) * p.N + n + 32 * c;
+              const float* sbv = p.b_bs + int64_t(kb) * p.N + n + 16 * c;
 #pragma unroll
-              for (int j = 0; j < 32; j += 4) {
+              for (int j = 0; j < 16; j += 4) {
                 float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (n + 32 * c + j < p.N) q = *reinterpret_cast<const float4*>(sbv + j);
-                const int i = 32 * c + j;
+                if (n + 16 * c + j < p.N) q = *reinterpret_cast<const float4*>(sbv + j);
+                const int i = 16 * c + j;
                 acc[i] = __fmaf_rn(__uint_as_float(r[j]), __fmul_rn(sa, q.x), acc[i]);
                 acc[i + 1] = __fmaf_rn(__uint_as_float(r[j + 1]), __fmul_rn(sa, q.y), acc[i + 1]);
                 acc[i + 2] = __fmaf_rn(__uint_as_float(r[j + 2]), __fmul_rn(sa, q.z), acc[i + 2]);
@@ -618,7 +623,7 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
         }
         if (!ok) break;
       }
-      store_row128(p, m, n, acc);
+      store_row<kCols>(p, m, n, acc);
     }
     }
   } else if constexpr (MODE == G_MX) {
@@ -697,6 +702,16 @@ __global__ void __maxnreg__(96)
   gemm_tn_body<G_MX, 1, CTA2, EPI>(tmA, tmB, tmSFA, tmSFB, p);
 }
 
+// Blockwise GEMMs: 18 warps (16 promoting), five on two of the sub-partitions: 96 registers.
+template <int B128>
+__global__ void __maxnreg__(96)
+    gemm_block_kernel(const __grid_constant__ CUtensorMap tmA,
+                      const __grid_constant__ CUtensorMap tmB,
+                      const __grid_constant__ CUtensorMap tmSFA,
+                      const __grid_constant__ CUtensorMap tmSFB, const GemmParams p) {
+  gemm_tn_body<G_BLOCK, B128, 0, EPI_NONE>(tmA, tmB, tmSFA, tmSFB, p);
+}
+
 // ------------------------------------------------------------------------------------
 // Host side: tensor maps and launch
 // ------------------------------------------------------------------------------------
@@ -726,8 +741,9 @@ static cudaError_t launch_mode(const GemmLaunch& g, cudaStream_t st) {
       return cudaErrorInvalidValue;
   }
   auto kern = [] {
-    if constexpr (EPI == EPI_NONE) return gemm_tn_kernel<MODE, B128, CTA2>;
-    else return gemm_mlp_kernel<CTA2, EPI>;
+    if constexpr (EPI != EPI_NONE) return gemm_mlp_kernel<CTA2, EPI>;
+    else if constexpr (MODE == G_BLOCK) return gemm_block_kernel<B128>;
+    else return gemm_tn_kernel<MODE, B128, CTA2>;
   }();
   static bool attr_set = false;
   if (!attr_set) {
