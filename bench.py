@@ -551,6 +551,13 @@ def run_kernels(args):
         ms4 = timed(lambda: F.linear_fwd(rec, qx4, qw, y=y4))
         out[f"gemm_{kind}"] = {"8192x4096x4096_TFLOP/s": round(2 * M * N * K / ms / 1e9, 1),
                                "4096^3_TFLOP/s": round(2 * 4096 ** 3 / ms4 / 1e9, 1)}
+    # fp32 master weight W1 16384 x 4096 -> MXFP8 row + column copies (4 B in, 2.06 B out)
+    w32 = torch.randn((16384, 4096), device="cuda", generator=g) * 0.02
+    rec = F.Recipe(kind="mxfp8")
+    qm = F.empty_qtensor(rec, 16384, 4096, "weight")
+    ms = timed(lambda: F.quantize_master(rec, w32, out=qm))
+    out["quantize_master_mxfp8_16384x4096"] = {
+        "ms": round(ms, 4), "GB/s": round(16384 * 4096 * (4 + 2 + 2 / 32.0) / ms / 1e6, 1)}
     torch.cuda.synchronize()
     print(json.dumps({"kernels": out}), flush=True)
 

@@ -156,6 +156,21 @@ fp8_status fp8_quantize(const fp8_recipe *recipe, const void *x_bf16, int64_t ro
                         int32_t *dev_status, cudaStream_t stream);
 
 /*
+ * fp8_quantize_master — fp32 master weights -> E4M3 codes plus scales (role WEIGHT), with no
+ * bf16 rounding in between (the weight cast of an optimizer that keeps fp32 weights). The
+ * recipes are those of fp8_quantize for a weight: tensorwise / delayed per-tensor scale,
+ * MXFP8 1x32 blocks (row copy along cols, column copy along rows), blockwise 128x128 tiles;
+ * amaxes are taken over the fp32 values and a code is encode(fp32(x * s)). The column copy is
+ * always FP8. Arguments, layouts, workspace (fp8_workspace_bytes of the same shape) and
+ * errors as for fp8_quantize; w_f32 is [rows][cols] fp32, 16-byte aligned.
+ * power_2_scales is not supported here (FP8_ERR_UNSUPPORTED).
+ */
+fp8_status fp8_quantize_master(const fp8_recipe *recipe, const float *w_f32, int64_t rows,
+                               int64_t cols, int32_t want_row, int32_t want_col,
+                               fp8_tensor *out, void *workspace, size_t ws_bytes,
+                               int32_t *dev_status, cudaStream_t stream);
+
+/*
  * fp8_amax_update — delayed scaling: push *amax_new into the history (the oldest of `len`
  * entries drops out) and write scale = f(max(history)), scale_inv = 1/scale with f the
  * per-tensor rule above (--fp8-amax-history-len, --fp8-margin), or with

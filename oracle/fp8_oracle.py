@@ -79,6 +79,17 @@ def bf16_to_f32(bits):
     return (b.astype(np.uint32) << 16).view(np.float32)
 
 
+def as_f32(x):
+    """A quantiser's input as float32 values: bf16 bit patterns (uint16) are widened exactly;
+    float32 arrays (fp32 master weights, cast without a bf16 rounding) pass through."""
+    x = np.asarray(x)
+    if x.dtype == np.float32:
+        return x
+    if x.dtype == np.uint16:
+        return bf16_to_f32(x)
+    raise TypeError("quantiser input: bf16 bit patterns (uint16) or float32")
+
+
 def f64_to_bf16(v):
     """float64 -> bf16 bit pattern, one rounding to nearest, ties to even, on the bf16 grid.
 
@@ -254,8 +265,8 @@ def scale_from_amax(amax, margin=0, fmt="e4m3"):
 
 
 def amax_of(x_bf16):
-    """max |x| over a bf16 tensor, as float32 (exact). NaN if any element is NaN."""
-    x = bf16_to_f32(x_bf16)
+    """max |x| over a bf16 (or float32) tensor, as float32 (exact). NaN if any element is NaN."""
+    x = as_f32(x_bf16)
     if x.size == 0:
         return np.float32(0.0)
     return np.float32(np.max(np.abs(x)))
@@ -263,7 +274,7 @@ def amax_of(x_bf16):
 
 def cast_with_scale(x_bf16, s, fmt="e4m3"):
     """codes = encode(fp32(x * s)): one fp32 product, then the FP8 rounding."""
-    x = bf16_to_f32(x_bf16)
+    x = as_f32(x_bf16)
     return fp8_encode((x * np.float32(s)).astype(np.float32), fmt)
 
 
@@ -361,7 +372,7 @@ def quantize_mxfp8(x_bf16, want_col=True):
     entries are omitted when want_col is False (the row copy of any subset of rows is then
     the same as that subset of the full tensor's row copy).
     """
-    x = bf16_to_f32(x_bf16)
+    x = as_f32(x_bf16)
     row, row_scale = _mx_quantize_lastdim(x)
     out = dict(row=row, row_scale=row_scale)
     if want_col:
@@ -381,7 +392,7 @@ def e8m0_decode(bytes_):
 
 def _bw_quantize_1x128_lastdim(x_bf16, margin, fmt="e4m3", pow2=False):
     """Per 1x128 block along the last dim: codes [R,C], s_inv [R, C/128] (float32)."""
-    x = bf16_to_f32(x_bf16)
+    x = as_f32(x_bf16)
     R, C = x.shape
     blocks = x.reshape(R, C // BW_BLOCK, BW_BLOCK)
     s, s_inv = scales_from_amax(np.max(np.abs(blocks), axis=2), margin, fmt, pow2)
@@ -395,7 +406,7 @@ def quantize_blockwise_1x128(x_bf16, margin=0, fmt="e4m3", pow2=False):
 
     Returns dict(row=[R,C], row_scale_inv=[R,C/128], col=[C,R], col_scale_inv=[C,R/128]).
     """
-    x = np.asarray(x_bf16, dtype=np.uint16)
+    x = as_f32(x_bf16)
     row, row_si = _bw_quantize_1x128_lastdim(x, margin, fmt, pow2)
     col, col_si = _bw_quantize_1x128_lastdim(np.ascontiguousarray(x.T), margin, fmt, pow2)
     return dict(row=row, row_scale_inv=row_si, col=col, col_scale_inv=col_si)
@@ -406,7 +417,7 @@ def quantize_blockwise_128x128(x_bf16, margin=0, fmt="e4m3", pow2=False):
 
     Returns dict(row=[R,C], row_scale_inv=[R/128, C/128], col=[C,R], col_scale_inv=[C/128,R/128]).
     """
-    x = bf16_to_f32(x_bf16)
+    x = as_f32(x_bf16)
     R, C = x.shape
     gr, gc = R // BW_BLOCK, C // BW_BLOCK
     tiles = x.reshape(gr, BW_BLOCK, gc, BW_BLOCK)            # [i, r, j, c]

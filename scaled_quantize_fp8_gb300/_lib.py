@@ -47,6 +47,8 @@ _SIG = {
     "fp8_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(Recipe), _I64, _I64]),
     "fp8_quantize": (_I32, [ctypes.POINTER(Recipe), _P, _I64, _I64, _I32, _I32, _I32,
                             ctypes.POINTER(Tensor), _P, ctypes.c_size_t, _P, _P]),
+    "fp8_quantize_master": (_I32, [ctypes.POINTER(Recipe), _P, _I64, _I64, _I32, _I32,
+                                   ctypes.POINTER(Tensor), _P, ctypes.c_size_t, _P, _P]),
     "fp8_amax_update": (_I32, [ctypes.POINTER(Recipe), ctypes.POINTER(AmaxHistory), _I32, _P,
                                _P, _P, _P]),
     "fp8_linear_fwd": (_I32, [ctypes.POINTER(Recipe), ctypes.POINTER(Tensor),

@@ -139,6 +139,32 @@ def quantize(recipe: Recipe, x: torch.Tensor, role="activation", want_row=True, 
     return out
 
 
+def quantize_master(recipe: Recipe, w: torch.Tensor, want_row=True, want_col=True,
+                    out: Optional[QTensor] = None, workspace: Optional[torch.Tensor] = None,
+                    status: Optional[torch.Tensor] = None, stream=None):
+    """fp8_quantize_master on an fp32 [rows, cols] master weight (role weight, no bf16
+    rounding). For delayed scaling pass `out` bound to the weight's DelayedState."""
+    if w.dtype != torch.float32:
+        raise TypeError("quantize_master takes fp32 master weights")
+    lib = L.load()
+    rows, cols = w.shape
+    if out is None:
+        out = empty_qtensor(recipe, rows, cols, "weight", want_row, want_col, device=w.device)
+    rc = recipe.c()
+    need = int(lib.fp8_workspace_bytes(ctypes.byref(rc), rows, cols))
+    if need and (workspace is None or workspace.numel() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=w.device)
+    ct = out.c()
+    st = lib.fp8_quantize_master(ctypes.byref(rc), _ptr(w), rows, cols, int(want_row),
+                                 int(want_col), ctypes.byref(ct), _ptr(workspace),
+                                 0 if workspace is None else workspace.numel(), _ptr(status),
+                                 _stream(stream))
+    L.check(st, "fp8_quantize_master")
+    out.rows, out.cols, out.kind, out.role = ct.rows, ct.cols, ct.kind, ct.role
+    out.col_bf16 = ct.col_bf16
+    return out
+
+
 def quantize_static_scratch(recipe: Recipe, x: torch.Tensor, role="activation", want_row=True,
                             want_col=True, out: Optional[QTensor] = None, status=None,
                             stream=None):

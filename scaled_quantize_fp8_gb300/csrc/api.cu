@@ -135,6 +135,39 @@ fp8_status fp8_quantize(const fp8_recipe* recipe, const void* x_bf16, int64_t ro
                                      dev_status, stream));
 }
 
+fp8_status fp8_quantize_master(const fp8_recipe* recipe, const float* w_f32, int64_t rows,
+                               int64_t cols, int32_t want_row, int32_t want_col, fp8_tensor* out,
+                               void* workspace, size_t ws_bytes, int32_t* dev_status,
+                               cudaStream_t stream) {
+  (void)dev_status;                         // no device-side waits in this path
+  FP8_TRY(check_recipe(recipe));
+  if (out == nullptr) return FP8_ERR_NULL;
+  if (recipe->power_2_scales != 0) return FP8_ERR_UNSUPPORTED;
+  if (!want_row && !want_col) return FP8_ERR_SHAPE;
+  const int kind = recipe->kind;
+  const int64_t q = shape_quantum(kind);
+  if (rows < 0 || cols < 0 || rows % q != 0 || cols % q != 0) return FP8_ERR_SHAPE;
+  if (rows * cols >= (int64_t(1) << 31)) return FP8_ERR_SHAPE;
+  FP8_TRY(check_scalars(kind, out));
+  const bool empty = rows == 0 || cols == 0;
+  if (!empty) {
+    FP8_TRY(check_ptr(w_f32));
+    if (want_row) FP8_TRY(check_copy(kind, out->row, out->row_scale));
+    if (want_col) FP8_TRY(check_copy(kind, out->col, out->col_scale));
+    const size_t need = quantize_workspace_bytes(kind, rows, cols);
+    if (need > 0 && (workspace == nullptr || ws_bytes < need)) return FP8_ERR_WORKSPACE;
+    if (need > 0 && !aligned16(workspace)) return FP8_ERR_ALIGN;
+  }
+  out->rows = rows;
+  out->cols = cols;
+  out->role = FP8_ROLE_WEIGHT;
+  out->kind = kind;
+  out->col_bf16 = 0;
+  return cuda_status(quantize_master_launch(kind, recipe->margin, w_f32, rows, cols,
+                                            want_row != 0, want_col != 0, out, workspace,
+                                            stream));
+}
+
 fp8_status fp8_amax_update(const fp8_recipe* recipe, fp8_amax_history* hist, int32_t role,
                            const float* amax_new, float* scale, float* scale_inv,
                            cudaStream_t stream) {

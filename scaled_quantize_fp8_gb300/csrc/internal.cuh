@@ -20,6 +20,7 @@ int num_sms();
 
 // ---- quantize.cu
 size_t quantize_workspace_bytes(int kind, int64_t R, int64_t C);
+int amax_partial_ctas(int64_t n_vec);      // CTAs (= partials) of the tensorwise amax pass
 // fmt: 0 = E4M3, 1 = E5M2 (gradients under the hybrid format; not for MXFP8)
 // pow2: power-of-two block scales (blockwise only)
 cudaError_t quantize_launch(int kind, int role, int fmt, bool pow2, int margin,
@@ -35,6 +36,11 @@ cudaError_t dgelu_quantize_launch(const uint16_t* da, const fp8_tensor* h_q, int
 cudaError_t amax_update_launch(float* hist, int32_t* head, int len, const float* amax_new,
                                float* scale, float* scale_inv, int margin, float fmax,
                                int algo, cudaStream_t st);
+
+// ---- master.cu (fp32 master weights -> E4M3, role WEIGHT)
+cudaError_t quantize_master_launch(int kind, int margin, const float* x, int64_t R, int64_t C,
+                                   bool want_row, bool want_col, fp8_tensor* out,
+                                   void* workspace, cudaStream_t st);
 
 // ---- gemm.cu
 enum GMode : int { G_TENSOR = 0, G_MX = 1, G_BLOCK = 2, G_BF16 = 3 };

@@ -262,3 +262,29 @@ def test_power_of_two_block_scales():
     q = O.quantize_blockwise_1x128(x, pow2=True)
     f, _ = np.frexp(q["row_scale_inv"].astype(np.float64))
     assert np.all(f == 0.5)                                   # every s_inv a power of two
+
+
+def test_fp32_master_weight_inputs():
+    """Quantising fp32 master weights: fp32 values that bf16 holds exactly give the bf16
+    path's bytes; other fp32 values are cast without a bf16 rounding (codes follow the fp32
+    product), and the MX exponent is the smallest e with amax <= 448 * 2^e by brute search."""
+    rng = np.random.default_rng(12)
+    w32 = (rng.standard_normal((256, 256)) * 0.02).astype(np.float32)
+    wb = O.f64_to_bf16(w32.astype(np.float64))
+    w_exact = O.bf16_to_f32(wb)                               # fp32 copies of the bf16 values
+    for f in (lambda x: O.quantize_tensorwise(x), lambda x: O.quantize_mxfp8(x),
+              lambda x: O.quantize_blockwise_128x128(x)):
+        a, b = f(wb), f(w_exact)
+        for k in a:
+            assert np.array_equal(np.asarray(a[k]), np.asarray(b[k])), k
+    q = O.quantize_tensorwise(w32)
+    s = np.float32(np.float32(448.0) / np.max(np.abs(w32)))
+    assert q["scale"] == s
+    assert np.array_equal(q["row"], O.e4m3_encode((w32 * s).astype(np.float32)))
+    assert not np.array_equal(q["row"], O.quantize_tensorwise(wb)["row"])
+    mx = O.quantize_mxfp8(w32, want_col=False)
+    amax = np.max(np.abs(w32.reshape(256, 8, 32)), axis=2)
+    for i in range(0, 256, 37):
+        for j in range(8):
+            e = min(k for k in range(-127, 128) if float(amax[i, j]) <= 448.0 * 2.0 ** k)
+            assert mx["row_scale"][i, j] == e + 127
