@@ -174,10 +174,11 @@ __device__ __forceinline__ void store_row(const GemmParams& p, int m, int n, con
   }
 }
 
-// Read 128 consecutive accumulator columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_load128(uint32_t taddr, float* out) {
+// Read NC consecutive accumulator columns of this thread's TMEM lane.
+template <int NC>
+__device__ __forceinline__ void tmem_load_cols(uint32_t taddr, float* out) {
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
+  for (int c = 0; c < NC / 32; ++c) {
     uint32_t r[32];
     ptx::tmem_ld_32x32b_x32(taddr + 32 * c, r);
 #pragma unroll
@@ -504,8 +505,7 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
     const int ew = warp - 2;
     const int quad = warp & 3;            // TMEM lane quadrant this warp may access
     constexpr int kCols = 4 * kBN / kEpiWarps;              // accumulator columns per warp
-    static_assert(EPI != EPI_NONE || MODE == G_BLOCK || kCols == 128,
-                  "plain epilogue: 128 columns per warp");
+
     const int slice = ew >> 2;            // which kCols columns of the 256-wide tile
     const int row = 32 * quad + lane;
     const uint32_t t_lane = tmem + (uint32_t(32 * quad) << 16) + uint32_t(slice * kCols);
@@ -570,7 +570,7 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
         const uint32_t b = u % kNumAcc;
         if (!wait_bar(&ctl->accf[b], (u / kNumAcc) & 1u, ctl, p.status)) break;
         ptx::tc_fence_after();
-        tmem_load128(t_lane + b * kBN, acc);
+        tmem_load_cols<kCols>(t_lane + b * kBN, acc);
         ptx::tmem_wait_ld();
         release_acc(b);
         ++u;
@@ -702,14 +702,15 @@ __global__ void __maxnreg__(96)
   gemm_tn_body<G_MX, 1, CTA2, EPI>(tmA, tmB, tmSFA, tmSFB, p);
 }
 
-// Blockwise GEMMs: 18 warps (16 promoting), five on two of the sub-partitions: 96 registers.
-template <int B128>
+// Blockwise GEMMs: 16 promoting epilogue warps (18 warps, five on two of the sub-partitions):
+// 96 registers.
+template <int MODE, int B128, int CTA2>
 __global__ void __maxnreg__(96)
-    gemm_block_kernel(const __grid_constant__ CUtensorMap tmA,
-                      const __grid_constant__ CUtensorMap tmB,
-                      const __grid_constant__ CUtensorMap tmSFA,
-                      const __grid_constant__ CUtensorMap tmSFB, const GemmParams p) {
-  gemm_tn_body<G_BLOCK, B128, 0, EPI_NONE>(tmA, tmB, tmSFA, tmSFB, p);
+    gemm_wide_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmSFA,
+                     const __grid_constant__ CUtensorMap tmSFB, const GemmParams p) {
+  gemm_tn_body<MODE, B128, CTA2, EPI_NONE>(tmA, tmB, tmSFA, tmSFB, p);
 }
 
 // ------------------------------------------------------------------------------------
@@ -742,7 +743,7 @@ static cudaError_t launch_mode(const GemmLaunch& g, cudaStream_t st) {
   }
   auto kern = [] {
     if constexpr (EPI != EPI_NONE) return gemm_mlp_kernel<CTA2, EPI>;
-    else if constexpr (MODE == G_BLOCK) return gemm_block_kernel<B128>;
+    else if constexpr (MODE == G_BLOCK) return gemm_wide_kernel<MODE, B128, CTA2>;
     else return gemm_tn_kernel<MODE, B128, CTA2>;
   }();
   static bool attr_set = false;
