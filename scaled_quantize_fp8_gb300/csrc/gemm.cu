@@ -746,17 +746,15 @@ static cudaError_t launch_mode(const GemmLaunch& g, cudaStream_t st) {
     else if constexpr (MODE == G_BLOCK) return gemm_wide_kernel<MODE, B128, CTA2>;
     else return gemm_tn_kernel<MODE, B128, CTA2>;
   }();
-  static bool attr_set = false;
-  if (!attr_set) {
+  static std::atomic<uint64_t> attr_done{0};
+  cudaError_t ae = once_per_device(attr_done, [&] {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(G::kSmemBytes));
-    if (e != cudaSuccess) return e;
-    if (CTA2) {
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
-      (void)e;
-    }
-    attr_set = true;
-  }
+    if (e == cudaSuccess && CTA2)
+      (void)cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+    return e;
+  });
+  if (ae != cudaSuccess) return ae;
   const int sms = num_sms();
   const int tiles = ((g.p.M + G::kTileM - 1) / G::kTileM) * ((g.p.N + kBN - 1) / kBN);
   const int units = std::max(1, std::min(tiles, CTA2 ? sms / 2 : sms));

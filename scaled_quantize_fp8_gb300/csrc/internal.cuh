@@ -1,6 +1,7 @@
 // Host-side interfaces between the C ABI (api.cu) and the kernel files.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -16,7 +17,22 @@ namespace fp8lin {
 // box_inner x box_rows elements; optional 128-byte swizzle; out-of-bounds reads fill zeros.
 bool make_tmap_2d(CUtensorMap_st* map, const void* base, int elem_bytes, int64_t inner,
                   int64_t rows, int box_inner, int box_rows, bool swizzle128);
-int num_sms();
+int num_sms();      // of the current device
+
+// Run set() (a per-device, idempotent setup such as cudaFuncSetAttribute) the first time a
+// device reaches this flag word; later calls on that device skip it. Thread-safe: concurrent
+// first calls may both run set(), which is harmless. Devices beyond 63 run it every time.
+template <class Set>
+cudaError_t once_per_device(std::atomic<uint64_t>& done, Set set) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = set();
+  if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 // ---- quantize.cu
 size_t quantize_workspace_bytes(int kind, int64_t R, int64_t C);

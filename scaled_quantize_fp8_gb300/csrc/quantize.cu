@@ -652,13 +652,12 @@ static cudaError_t launch_tiles(QuantParams p, cudaStream_t st) {
   CUtensorMap map;
   if (!make_tmap_2d(&map, p.x, 2, p.C, p.R, 64, kTile, true)) return cudaErrorInvalidValue;
   constexpr int smem = int(quant_smem_bytes<MODE, EPI>());
-  static bool attr = false;
-  if (!attr) {
-    const cudaError_t e = cudaFuncSetAttribute(quantize_tile_kernel<MODE, EPI, F8>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  const cudaError_t ae = once_per_device(attr_done, [&] {
+    return cudaFuncSetAttribute(quantize_tile_kernel<MODE, EPI, F8>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  });
+  if (ae != cudaSuccess) return ae;
   const int grid = std::max(1, std::min(n, num_sms() * quant_ctas_per_sm<MODE, EPI>()));
   quantize_tile_kernel<MODE, EPI, F8><<<grid, 256, smem, st>>>(map, p);
   return cudaGetLastError();

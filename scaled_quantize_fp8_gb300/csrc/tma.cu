@@ -12,16 +12,19 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 static EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (fn == nullptr) {
+  static std::atomic<EncodeTiledFn> fn{nullptr};
+  EncodeTiledFn f = fn.load(std::memory_order_acquire);
+  if (f == nullptr) {
     void* ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+        q == cudaDriverEntryPointSuccess) {
+      f = reinterpret_cast<EncodeTiledFn>(ptr);
+      fn.store(f, std::memory_order_release);
+    }
   }
-  return fn;
+  return f;
 }
 
 bool make_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, int64_t inner, int64_t rows,
@@ -42,16 +45,18 @@ bool make_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, int64_t in
 }
 
 int num_sms() {
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
-      sms = v;
-    else
-      return 148;
+  static std::atomic<int> sms[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev < 64) {
+    const int v = sms[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
   }
-  return sms;
+  int v = 0;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+    return 148;
+  if (dev < 64) sms[dev].store(v, std::memory_order_relaxed);
+  return v;
 }
 
 }  // namespace fp8lin
