@@ -46,7 +46,7 @@ FP8_OVER_BF16 = 2.0                                   # nominal dense fp8 / bf16
 # step's four such launches in one capture of `ncu --metrics dram__bytes_read.sum,
 # dram__bytes_write.sum -k regex:gemm_tn_kernel -s 4 -c 4 python bench.py --profile
 # gemm_mx_mlp --steps 2`. Reset to None whenever that kernel changes.
-GEMM_TRAFFIC_BYTES = 550.0e6
+GEMM_TRAFFIC_BYTES = None
 
 
 def peaks():
@@ -363,6 +363,8 @@ def run_ours(args):
                          "achieved": round(achieved, 1), "peak": fp8_peak, "unit": "TFLOP/s",
                          "frac": round(achieved / fp8_peak, 4),
                          "traffic": GEMM_TRAFFIC_BYTES if st.fused else None,
+                         "traffic_source": "ncu dram bytes read + write per launch"
+                         if GEMM_TRAFFIC_BYTES else "not captured for this kernel version",
                          "peak_source": f"{src}: bf16 x {FP8_OVER_BF16} (nominal fp8/bf16)",
                          "avg_launch_ms": round(gemm_ms, 4)},
             "fused_gemm": None if fused_ms is None else {
