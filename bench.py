@@ -594,6 +594,22 @@ def run_kernels(args):
         ms4 = timed(lambda: F.linear_fwd(rec, qx4, qw, y=y4))
         out[f"gemm_{kind}"] = {"8192x4096x4096_TFLOP/s": round(2 * M * N * K / ms / 1e9, 1),
                                "4096^3_TFLOP/s": round(2 * 4096 ** 3 / ms4 / 1e9, 1)}
+    # tensorwise dgrad 8192 x 4096 x 4096 reading W's column copy (K-major) or, with the column
+    # copy never written, W's row copy as an MN-major operand; and the quantize without it
+    rec = F.Recipe(kind="tensorwise")
+    dy = (torch.randn((M, N), device="cuda", generator=g) * 1e-3).to(torch.bfloat16)
+    dyq = F.quantize(rec, dy, "grad", want_col=False)
+    w_col = F.quantize(rec, w, "weight")
+    w_row = F.quantize(rec, w, "weight", want_col=False)
+    dx = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    for name, wq in (("col_copy", w_col), ("row_copy_mn_major", w_row)):
+        ms = timed(lambda: F.linear_bwd(rec, dyq, None, wq, want_dw=False, dx=dx))
+        out[f"gemm_tensorwise_dgrad_{name}"] = {"TFLOP/s": round(2 * M * N * K / ms / 1e9, 1)}
+    qx = F.empty_qtensor(rec, M, K, "activation", True, False)
+    ws = torch.empty(max(1, F.workspace_bytes(rec, M, K)), dtype=torch.uint8, device="cuda")
+    ms = timed(lambda: F.quantize(rec, x, "activation", want_col=False, out=qx, workspace=ws))
+    out["quantize_tensorwise_row_only"] = {"ms": round(ms, 4),
+                                           "GB/s": round(M * K * 3.0 / ms / 1e6, 1)}
     # fp32 master weight W1 16384 x 4096 -> MXFP8 row + column copies (4 B in, 2.06 B out)
     w32 = torch.randn((16384, 4096), device="cuda", generator=g) * 0.02
     rec = F.Recipe(kind="mxfp8")

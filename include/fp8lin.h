@@ -196,7 +196,10 @@ fp8_status fp8_linear_fwd(const fp8_recipe *recipe, const fp8_tensor *x, const f
 /*
  * fp8_linear_bwd — dgrad dX[M,K] = deq(dY)[M,N] . deq(W^T)[K,N]^T from dy->row and w->col,
  * and wgrad dW[N,K] = deq(dY^T)[N,M] . deq(X^T)[K,M]^T from dy->col and x_saved->col (the
- * copies cached in the forward pass). With recipe->fp8_wgrad == 0 (--fp8-wgrad off) those two
+ * copies cached in the forward pass). Where both copies hold the same codes — per-tensor
+ * scales (DELAYED, TENSORWISE) and 128x128 weight tiles (BLOCKWISE, role WEIGHT) — a tensor
+ * whose col is NULL is read from its row copy instead, as an MN-major (transposed) tensor-core
+ * operand, so those tensors can be quantised with want_col = 0. With recipe->fp8_wgrad == 0 (--fp8-wgrad off) those two
  * column copies are bf16 transposes (see fp8_quantize) and the wgrad GEMM runs in bf16 with
  * fp32 accumulation. dx or dw may be NULL to skip that GEMM. Outputs are bf16 (out_fp32 = 0)
  * or fp32 (out_fp32 = 1).

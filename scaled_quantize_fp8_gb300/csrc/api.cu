@@ -195,7 +195,21 @@ struct Operand {
   const float* scale_inv;   // per-tensor recipes
   int role;
   int fmt;                  // 0 = E4M3, 1 = E5M2
+  int mn = 0;               // 1: codes are the other copy, read MN-major (transposed)
 };
+
+// The copy a backward GEMM reads for the transposed operand: the column-wise copy (K-major)
+// when it exists; otherwise, for per-tensor scales and 128x128 weight tiles (where both copies
+// hold the same codes), the row-wise copy read MN-major, so the quantizer may skip the column
+// copy for those tensors.
+Operand transposed_operand(const fp8_recipe* recipe, const fp8_tensor* t) {
+  const bool same_codes = recipe->kind == FP8_RECIPE_TENSORWISE ||
+                          recipe->kind == FP8_RECIPE_DELAYED ||
+                          (recipe->kind == FP8_RECIPE_BLOCKWISE && t->role == FP8_ROLE_WEIGHT);
+  if (t->col == nullptr && t->row != nullptr && same_codes)
+    return Operand{t->row, t->row_scale, t->scale_inv, t->role, fmt_of(recipe, t->role), 1};
+  return Operand{t->col, t->col_scale, t->scale_inv, t->role, fmt_of(recipe, t->role), 0};
+}
 
 fp8_status run_gemm(int kind, const Operand& a, const Operand& b, int64_t M, int64_t N,
                     int64_t Kr, void* D, int fp32_out, int32_t* status, cudaStream_t st) {
@@ -222,6 +236,8 @@ fp8_status run_gemm(int kind, const Operand& a, const Operand& b, int64_t M, int
   g.p.status = status;
   g.p.a_fmt = a.fmt;
   g.p.b_fmt = b.fmt;
+  g.p.a_mn = a.mn;
+  g.p.b_mn = b.mn;
   switch (kind) {
     case FP8_RECIPE_TENSORWISE:
     case FP8_RECIPE_DELAYED:
@@ -350,8 +366,7 @@ fp8_status fp8_linear_bwd(const fp8_recipe* recipe, const fp8_tensor* dy,
     // dgrad: dX[M][K] = dY[M][N] . (W^T)[K][N]^T
     const Operand a{dy->row, dy->row_scale, dy->scale_inv, dy->role,
                     fmt_of(recipe, dy->role)};
-    const Operand b{w->col, w->col_scale, w->scale_inv, w->role,
-                    fmt_of(recipe, w->role)};
+    const Operand b = transposed_operand(recipe, w);
     FP8_TRY(run_gemm(recipe->kind, a, b, M, K, N, dx, out_fp32, dev_status, stream));
   }
   if (dw != nullptr) {
@@ -366,10 +381,8 @@ fp8_status fp8_linear_bwd(const fp8_recipe* recipe, const fp8_tensor* dy,
       return run_bf16_gemm(dy->col, x_saved->col, N, K, M, dw, out_fp32, dev_status, stream);
     }
     // wgrad: dW[N][K] = (dY^T)[N][M] . (X^T)[K][M]^T
-    const Operand a{dy->col, dy->col_scale, dy->scale_inv, dy->role,
-                    fmt_of(recipe, dy->role)};
-    const Operand b{x_saved->col, x_saved->col_scale, x_saved->scale_inv, x_saved->role,
-                    fmt_of(recipe, x_saved->role)};
+    const Operand a = transposed_operand(recipe, dy);
+    const Operand b = transposed_operand(recipe, x_saved);
     FP8_TRY(run_gemm(recipe->kind, a, b, N, K, M, dw, out_fp32, dev_status, stream));
   }
   return FP8_OK;

@@ -384,8 +384,11 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
             if (leader)
               ptx::mbar_arrive_expect_tx(&ctl->full[s],
                                          2 * (kTileABytes + G::kTileBBytes + sf_bytes));
-            ptx::tma_load_2d_pair(a_dst, &tmA, kb * kBKElems, m0, bar);
-            ptx::tma_load_2d_pair(b_dst, &tmB, kb * kBKElems, n0, bar);
+            // a K-major tile is 128 bytes of K x rows; an MN-major one 128 of M (N) x 128 K rows
+            if (p.a_mn) ptx::tma_load_2d_pair(a_dst, &tmA, m0, kb * kBKElems, bar);
+            else ptx::tma_load_2d_pair(a_dst, &tmA, kb * kBKElems, m0, bar);
+            if (p.b_mn) ptx::tma_load_2d_pair(b_dst, &tmB, n0, kb * kBKElems, bar);
+            else ptx::tma_load_2d_pair(b_dst, &tmB, kb * kBKElems, n0, bar);
             if constexpr (MODE == G_MX) {
               uint8_t* sf = sSF + s * kSfStageBytes;
               const int nb_pair = nt * kBN;                        // first B row of the pair
@@ -400,8 +403,15 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
             const bool sfb_hi = (n0 + 128) < p.N;
             if constexpr (MODE == G_MX) bytes += 512u + (sfb_hi ? 1024u : 512u);
             ptx::mbar_arrive_expect_tx(&ctl->full[s], bytes);
-            ptx::tma_load_2d(a_dst, &tmA, kb * kBKElems, m0, &ctl->full[s]);
-            ptx::tma_load_2d(b_dst, &tmB, kb * kBKElems, n0, &ctl->full[s]);
+            if (p.a_mn) ptx::tma_load_2d(a_dst, &tmA, m0, kb * kBKElems, &ctl->full[s]);
+            else ptx::tma_load_2d(a_dst, &tmA, kb * kBKElems, m0, &ctl->full[s]);
+            if (p.b_mn) {
+              // the 256-wide B tile as two 128-column boxes, 16 KiB apart
+              ptx::tma_load_2d(b_dst, &tmB, n0, kb * kBKElems, &ctl->full[s]);
+              ptx::tma_load_2d(b_dst + 16384, &tmB, n0 + 128, kb * kBKElems, &ctl->full[s]);
+            } else {
+              ptx::tma_load_2d(b_dst, &tmB, kb * kBKElems, n0, &ctl->full[s]);
+            }
             if constexpr (MODE == G_MX) {
               uint8_t* sf = sSF + s * kSfStageBytes;
               ptx::bulk_load(sf, p.sfa + (int64_t(m0 >> 7) * kblocks128 + kb) * 512, 512,
@@ -428,7 +438,8 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
       // operand formats (E4M3 = 0, E5M2 = 1) in descriptor bits 7-9 (A) and 10-12 (B)
       uint32_t idesc = instr_desc<MODE, CTA2>();
       if constexpr (MODE == G_TENSOR || MODE == G_BLOCK)
-        idesc |= (uint32_t(p.a_fmt) << 7) | (uint32_t(p.b_fmt) << 10);
+        idesc |= (uint32_t(p.a_fmt) << 7) | (uint32_t(p.b_fmt) << 10) |
+                 (uint32_t(p.a_mn) << 15) | (uint32_t(p.b_mn) << 16);   // operand majorness
       const uint32_t sf_base = tmem + 256;      // MX scale factors: kSfCols columns a stage
       int s = 0;
       uint32_t ph = 0;
@@ -463,8 +474,15 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
           const uint32_t sfa_t = sf_base + kSfCols * uint32_t(s), sfb_t = sfa_t + 4;
 #pragma unroll
           for (int k = 0; k < kBKBytes / 32; ++k) {
-            const uint64_t ad = ptx::smem_desc(a_addr + 32 * k, 16, 1024, ptx::kSwizzle128B);
-            const uint64_t bd = ptx::smem_desc(b_addr + 32 * k, 16, 1024, ptx::kSwizzle128B);
+            // K-major: rows of 128 bytes of K, the k-th K=32 slice 32 bytes in. MN-major: rows
+            // of 128 MN elements, one per K, the slice 32 rows = 4 KiB in; 8-row swizzle atoms
+            // 1 KiB apart (SBO), 128-column chunks 16 KiB apart (LBO).
+            const uint64_t ad =
+                p.a_mn ? ptx::smem_desc(a_addr + 4096 * k, 16384, 1024, ptx::kSwizzle128B)
+                       : ptx::smem_desc(a_addr + 32 * k, 16, 1024, ptx::kSwizzle128B);
+            const uint64_t bd =
+                p.b_mn ? ptx::smem_desc(b_addr + 4096 * k, 16384, 1024, ptx::kSwizzle128B)
+                       : ptx::smem_desc(b_addr + 32 * k, 16, 1024, ptx::kSwizzle128B);
             const uint32_t acc_on = MODE == G_BLOCK ? uint32_t(k != 0) : uint32_t((kb | k) != 0);
             if constexpr (CTA2) {
               if constexpr (MODE == G_BF16) {
@@ -587,7 +605,9 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
         for (int kb = 0; kb < kblocks; ++kb) {
           const float sa = (m < p.M) ? p.a_bs[int64_t(kb) * p.M + m] : 0.0f;
           float sb = 0.0f;
-          if (B128 && n < p.N) sb = p.b_bs[int64_t(n >> 7) * kblocks + kb];
+          if (B128 && n < p.N)
+            sb = p.b_mn ? p.b_bs[int64_t(kb) * (p.N >> 7) + (n >> 7)]     // row grid [K][N]
+                        : p.b_bs[int64_t(n >> 7) * kblocks + kb];         // col grid [N][K]
           const uint32_t b = u & 1u;
           if (!wait_bar(&ctl->accf[b], (u >> 1) & 1u, ctl, p.status)) {
             ok = false;
@@ -730,9 +750,13 @@ static cudaError_t launch_mode(const GemmLaunch& g, cudaStream_t st) {
   static_assert(EPI == EPI_NONE || (MODE == G_MX && B128 == 1), "fused: MXFP8 only");
   CUtensorMap ma, mb;
   const int eb = MODE == G_BF16 ? 2 : 1;
-  if (!make_operand_map(&ma, g.A, g.p.M, g.p.K, eb, kBM)) return cudaErrorInvalidValue;
-  if (!make_operand_map(&mb, g.B, g.p.N, g.p.K, eb, CTA2 ? kBN / 2 : kBN))
-    return cudaErrorInvalidValue;
+  // K-major operands [rows][K]: boxes of 128 bytes of K x the tile's rows; MN-major operands
+  // [K][rows]: boxes of 128 rows' worth of columns x 128 K rows
+  const bool okA = g.p.a_mn ? make_tmap_2d(&ma, g.A, 1, g.p.M, g.p.K, 128, kBKBytes, true)
+                            : make_operand_map(&ma, g.A, g.p.M, g.p.K, eb, kBM);
+  const bool okB = g.p.b_mn ? make_tmap_2d(&mb, g.B, 1, g.p.N, g.p.K, 128, kBKBytes, true)
+                            : make_operand_map(&mb, g.B, g.p.N, g.p.K, eb, CTA2 ? kBN / 2 : kBN);
+  if (!okA || !okB) return cudaErrorInvalidValue;
   // MXFP8 scale arrays viewed as rows of 256 bytes (two rows per 512-byte atom) for TMA.
   CUtensorMap msfa = ma, msfb = mb;
   if (MODE == G_MX && CTA2) {
@@ -779,6 +803,9 @@ cudaError_t gemm_launch(const GemmLaunch& g, cudaStream_t st) {
   GemmLaunch gl = g;
   const int64_t pitch = gl.p.ldd * (gl.p.d_fp32 ? 4 : 2);
   gl.p.d_v8 = (reinterpret_cast<uintptr_t>(gl.p.D) % 32 == 0) && (pitch % 32 == 0);
+  if ((gl.p.a_mn && gl.mode != G_TENSOR) ||
+      (gl.p.b_mn && gl.mode != G_TENSOR && !(gl.mode == G_BLOCK && gl.p.b_is_128)))
+    return cudaErrorInvalidValue;                       // MN-major: per-tensor / 128x128 only
   if (gl.epi != EPI_NONE) {
     if (gl.mode != G_MX) return cudaErrorInvalidValue;
     auto a32 = [](const void* q) { return reinterpret_cast<uintptr_t>(q) % 32 == 0; };

@@ -79,6 +79,10 @@ struct GemmParams {
   int b_is_128;
   int32_t* status;          // device status word (may be null)
   int a_fmt, b_fmt;         // G_TENSOR / G_BLOCK operand formats: 0 = E4M3, 1 = E5M2
+  // MN-major operands (G_TENSOR: A and/or B; G_BLOCK: B, a 128x128 weight): the operand is
+  // stored [K][M] / [K][N] (the other copy of the tensor) and read transposed by the MMA. For
+  // G_BLOCK the B scales are then the row grid [K/128][N/128].
+  int a_mn, b_mn;
   // Fused MLP epilogues (G_MX only; the tile is quantised instead of stored, D unused):
   //   GELU : h = bf16(acc) -> h_row/h_scale (MXFP8 row copy), a = gelu(h) -> o_*
   //   DGELU: da = bf16(acc), h read from h_row/h_scale, dh = da * gelu'(h) -> o_*
