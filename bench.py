@@ -594,6 +594,12 @@ def run_kernels(args):
         ms4 = timed(lambda: F.linear_fwd(rec, qx4, qw, y=y4))
         out[f"gemm_{kind}"] = {"8192x4096x4096_TFLOP/s": round(2 * M * N * K / ms / 1e9, 1),
                                "4096^3_TFLOP/s": round(2 * 4096 ** 3 / ms4 / 1e9, 1)}
+    # blockwise with power-of-two scales: E8M0 scales in the MXFP8 layout, MXFP8 GEMM path
+    rec = F.Recipe(kind="blockwise", power_2_scales=True)
+    xq2, wq2 = F.quantize(rec, x, "activation"), F.quantize(rec, w, "weight")
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    ms = timed(lambda: F.linear_fwd(rec, xq2, wq2, y=y))
+    out["gemm_blockwise_pow2"] = {"8192x4096x4096_TFLOP/s": round(2 * M * N * K / ms / 1e9, 1)}
     # tensorwise dgrad 8192 x 4096 x 4096 reading W's column copy (K-major) or, with the column
     # copy never written, W's row copy as an MN-major operand; and the quantize without it
     rec = F.Recipe(kind="tensorwise")

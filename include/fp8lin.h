@@ -99,8 +99,10 @@ typedef struct {
                                  config), 1 = most_recent (the newest amax alone) */
   int32_t fp8_wgrad;          /* --fp8-wgrad: 1 = wgrad GEMM in FP8, 0 = in bf16 */
   int32_t power_2_scales;     /* BLOCKWISE only: 1 = each block scale rounded down to a power
-                                 of two (exact s_inv; maps onto power-of-two hardware
-                                 scaling), 0 = plain fp32 scales. Other recipes: must be 0 */
+                                 of two, stored as E8M0 bytes in the MXFP8 scale layout (each
+                                 1x128 or 128x128 block's byte repeated for its 1x32 blocks),
+                                 and the GEMMs run on the MXFP8 block-scaled tensor-core path;
+                                 0 = plain fp32 s_inv. Other recipes: must be 0 */
 } fp8_recipe;
 
 /* A quantised tensor: codes and scales of both copies, all device memory owned by the
@@ -108,7 +110,8 @@ typedef struct {
 typedef struct {
   uint8_t *row;          /* [rows][cols] FP8 codes (E5M2 for gradients under hybrid) */
   uint8_t *col;          /* [cols][rows] FP8 codes */
-  void *row_scale;       /* MXFP8: uint8 E8M0; BLOCKWISE: float s_inv; else unused */
+  void *row_scale;       /* MXFP8: uint8 E8M0; BLOCKWISE: float s_inv (E8M0 in the MXFP8
+                            layout with power_2_scales); else unused */
   void *col_scale;       /* same for the column-wise copy */
   float *amax;           /* DELAYED/TENSORWISE: amax of this tensor (written) */
   float *scale;          /* TENSORWISE: written. DELAYED: read (the scale from history) */

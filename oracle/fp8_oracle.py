@@ -427,6 +427,23 @@ def quantize_blockwise_128x128(x_bf16, margin=0, fmt="e4m3", pow2=False):
                 col_scale_inv=np.ascontiguousarray(s_inv.T))
 
 
+def pow2_scales_as_e8m0(s_inv, block_rows, rows, cols):
+    """Power-of-two block scales written as MXFP8 E8M0 bytes [rows][cols/32]: a power-of-two
+    s_inv = 2^k is exactly the E8M0 byte k + 127, repeated for the four 1x32 blocks of each
+    128-wide block (and, for 128x128 tiles, for the tile's 128 rows). s_inv is [rows][cols/128]
+    for 1x128 blocks (block_rows 1) or [rows/128][cols/128] for 128x128 tiles."""
+    s = np.asarray(s_inv, dtype=np.float32).astype(np.float64)
+    f, ex = np.frexp(s)
+    if not np.all(f == 0.5):
+        raise ValueError("not a power-of-two scale")
+    b = (ex - 1 + 127).astype(np.int64)
+    b = np.repeat(b, 4, axis=1)
+    if block_rows == 128:
+        b = np.repeat(b, 128, axis=0)
+    assert b.shape == (rows, cols // 32)
+    return b.astype(np.uint8)
+
+
 # --------------------------------------------------------------------------------------
 # Dequantisation and the fp64 GEMM reference
 # --------------------------------------------------------------------------------------

@@ -73,9 +73,10 @@ class QTensor:
         return t
 
 
-def scale_shape(kind, role, rows, cols):
-    """Storage of the scales of one copy whose codes are [rows, cols] (blocks along cols)."""
-    if kind == L.RECIPE_MXFP8:
+def scale_shape(kind, role, rows, cols, pow2=False):
+    """Storage of the scales of one copy whose codes are [rows, cols] (blocks along cols).
+    Blockwise with power-of-two scales stores E8M0 bytes in the MXFP8 layout."""
+    if kind == L.RECIPE_MXFP8 or (kind == L.RECIPE_BLOCKWISE and pow2):
         return (rows * cols // 32,), torch.uint8
     if kind == L.RECIPE_BLOCKWISE:
         if role == L.ROLE_WEIGHT:
@@ -90,7 +91,7 @@ def empty_qtensor(recipe: Recipe, rows, cols, role="activation", want_row=True, 
     q = QTensor(rows, cols, kind, r)
     if want_row:
         q.row = torch.empty((rows, cols), dtype=torch.uint8, device=device)
-        shp, dt = scale_shape(kind, r, rows, cols)
+        shp, dt = scale_shape(kind, r, rows, cols, recipe.power_2_scales)
         if shp is not None:
             q.row_scale = torch.empty(shp, dtype=dt, device=device)
     if want_col:
@@ -100,7 +101,7 @@ def empty_qtensor(recipe: Recipe, rows, cols, role="activation", want_row=True, 
             q.col_bf16 = 1
         else:
             q.col = torch.empty((cols, rows), dtype=torch.uint8, device=device)
-            shp, dt = scale_shape(kind, r, cols, rows)
+            shp, dt = scale_shape(kind, r, cols, rows, recipe.power_2_scales)
             if shp is not None:
                 q.col_scale = torch.empty(shp, dtype=dt, device=device)
     if kind in (L.RECIPE_DELAYED, L.RECIPE_TENSORWISE):

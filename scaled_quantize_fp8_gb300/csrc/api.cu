@@ -45,6 +45,13 @@ int fmt_of(const fp8_recipe* r, int role) {
   return (r->format == FP8_FORMAT_HYBRID && role == FP8_ROLE_GRAD) ? 1 : 0;
 }
 
+// The GEMM path of a recipe: blockwise with power-of-two scales stores its scales as E8M0
+// bytes in the MXFP8 layout, so its GEMMs run on the block-scaled (MXFP8) tensor-core path.
+int gemm_kind(const fp8_recipe* r) {
+  return (r->kind == FP8_RECIPE_BLOCKWISE && r->power_2_scales != 0) ? int(FP8_RECIPE_MXFP8)
+                                                                      : r->kind;
+}
+
 // Row/column multiple a recipe needs: 128 for the block recipes, 16 for per-tensor scales.
 int64_t shape_quantum(int kind) {
   return (kind == FP8_RECIPE_MXFP8 || kind == FP8_RECIPE_BLOCKWISE) ? 128 : 16;
@@ -205,7 +212,8 @@ struct Operand {
 Operand transposed_operand(const fp8_recipe* recipe, const fp8_tensor* t) {
   const bool same_codes = recipe->kind == FP8_RECIPE_TENSORWISE ||
                           recipe->kind == FP8_RECIPE_DELAYED ||
-                          (recipe->kind == FP8_RECIPE_BLOCKWISE && t->role == FP8_ROLE_WEIGHT);
+                          (recipe->kind == FP8_RECIPE_BLOCKWISE && t->role == FP8_ROLE_WEIGHT &&
+                           recipe->power_2_scales == 0);   // pow2: the MX path is K-major only
   if (t->col == nullptr && t->row != nullptr && same_codes)
     return Operand{t->row, t->row_scale, t->scale_inv, t->role, fmt_of(recipe, t->role), 1};
   return Operand{t->col, t->col_scale, t->scale_inv, t->role, fmt_of(recipe, t->role), 0};
@@ -350,7 +358,7 @@ fp8_status fp8_linear_fwd(const fp8_recipe* recipe, const fp8_tensor* x, const f
                     fmt_of(recipe, x->role)};
   const Operand b{w->row, w->row_scale, w->scale_inv, w->role,
                     fmt_of(recipe, w->role)};
-  return run_gemm(recipe->kind, a, b, x->rows, w->rows, x->cols, y, y_fp32, dev_status, stream);
+  return run_gemm(gemm_kind(recipe), a, b, x->rows, w->rows, x->cols, y, y_fp32, dev_status, stream);
 }
 
 fp8_status fp8_linear_bwd(const fp8_recipe* recipe, const fp8_tensor* dy,
@@ -367,7 +375,7 @@ fp8_status fp8_linear_bwd(const fp8_recipe* recipe, const fp8_tensor* dy,
     const Operand a{dy->row, dy->row_scale, dy->scale_inv, dy->role,
                     fmt_of(recipe, dy->role)};
     const Operand b = transposed_operand(recipe, w);
-    FP8_TRY(run_gemm(recipe->kind, a, b, M, K, N, dx, out_fp32, dev_status, stream));
+    FP8_TRY(run_gemm(gemm_kind(recipe), a, b, M, K, N, dx, out_fp32, dev_status, stream));
   }
   if (dw != nullptr) {
     FP8_TRY(check_tensor(recipe, x_saved));
@@ -383,7 +391,7 @@ fp8_status fp8_linear_bwd(const fp8_recipe* recipe, const fp8_tensor* dy,
     // wgrad: dW[N][K] = (dY^T)[N][M] . (X^T)[K][M]^T
     const Operand a = transposed_operand(recipe, dy);
     const Operand b = transposed_operand(recipe, x_saved);
-    FP8_TRY(run_gemm(recipe->kind, a, b, N, K, M, dw, out_fp32, dev_status, stream));
+    FP8_TRY(run_gemm(gemm_kind(recipe), a, b, N, K, M, dw, out_fp32, dev_status, stream));
   }
   return FP8_OK;
 }

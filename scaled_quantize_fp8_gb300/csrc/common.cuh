@@ -117,6 +117,12 @@ __device__ __forceinline__ uint32_t mx_scale_byte(uint32_t amax_bits, float* mul
   return nan ? 0xFFu : uint32_t(e + 127);
 }
 
+// E8M0 byte of a power-of-two dequantisation factor 2^k, k in [-127, 127]: the float's biased
+// exponent field (2^-127, a float subnormal, has field 0, which is also its E8M0 byte).
+__device__ __forceinline__ uint32_t e8m0_of_pow2(float s_inv) {
+  return (__float_as_uint(s_inv) >> 23) & 0xFFu;
+}
+
 // Four floats -> four E4M3 codes in one word (byte i holds the code of x_i).
 __device__ __forceinline__ uint32_t cvt_e4m3x4(float x0, float x1, float x2, float x3) {
   uint32_t r;

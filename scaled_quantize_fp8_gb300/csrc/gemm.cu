@@ -440,6 +440,8 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
       if constexpr (MODE == G_TENSOR || MODE == G_BLOCK)
         idesc |= (uint32_t(p.a_fmt) << 7) | (uint32_t(p.b_fmt) << 10) |
                  (uint32_t(p.a_mn) << 15) | (uint32_t(p.b_mn) << 16);   // operand majorness
+      if constexpr (MODE == G_MX)      // E5M2 gradients of power-of-two blockwise under hybrid
+        idesc |= (uint32_t(p.a_fmt) << 7) | (uint32_t(p.b_fmt) << 10);
       const uint32_t sf_base = tmem + 256;      // MX scale factors: kSfCols columns a stage
       int s = 0;
       uint32_t ph = 0;

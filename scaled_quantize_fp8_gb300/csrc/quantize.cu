@@ -236,8 +236,19 @@ __device__ __forceinline__ void quantize_one_tile(const QuantParams& p, QuantCtl
       if (t == 0) p.part_out[tile_id] = tm;               // delayed: record this tile's amax
     } else {
       s_tile = scale_from_amax(amax_from_bits(tm), p.margin, &sinv_tile, fp8_max<F8>(), p.pow2);
-      if (t == 0) {
-        const int tiles_r = int((R + 127) >> 7);
+      const int tiles_r = int((R + 127) >> 7);
+      if (p.pow2) {
+        // power-of-two scales are stored as E8M0 bytes in the MXFP8 layout (one 512-byte atom
+        // per 128 x 128 tile and copy, every byte the tile's scale)
+        const uint32_t b = e8m0_of_pow2(sinv_tile) * 0x01010101u;
+        const uint4 v = make_uint4(b, b, b, b);
+        if (t < 32 && p.row_scale)
+          reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.row_scale) +
+                                   (uint32_t(tr) * p.tiles_c + tc) * 512)[t] = v;
+        if (t >= 32 && t < 64 && p.col_scale && !p.col_bf16)
+          reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.col_scale) +
+                                   (uint32_t(tc) * tiles_r + tr) * 512)[t - 32] = v;
+      } else if (t == 0) {
         if (p.row_scale) reinterpret_cast<float*>(p.row_scale)[tr * p.tiles_c + tc] = sinv_tile;
         if (p.col_scale && !p.col_bf16)
           reinterpret_cast<float*>(p.col_scale)[tc * tiles_r + tr] = sinv_tile;
@@ -426,6 +437,19 @@ __device__ __forceinline__ void quantize_one_tile(const QuantParams& p, QuantCtl
         reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.col_scale) +
                                  (uint32_t(tc) * tiles_r + tr) * 512)[t - 32] =
             reinterpret_cast<const uint4*>(S.sc_col)[t - 32];
+    } else if (p.pow2) {
+      // E8M0 bytes in the MXFP8 layout: each 1x128 block's byte for its four 1x32 blocks, the
+      // 128 rows (columns) of this tile filling one 512-byte atom of the row (column) copy
+      const int u = t & 127;
+      const uint32_t off = uint32_t(u & 31) * 16 + uint32_t(u >> 5) * 4;
+      if (t < 128 && p.row != nullptr)
+        *reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(p.row_scale) +
+                                     (uint32_t(tr) * p.tiles_c + tc) * 512 + off) =
+            e8m0_of_pow2(S.scf_row[u]) * 0x01010101u;
+      if (t >= 128 && p.col != nullptr && !p.col_bf16)
+        *reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(p.col_scale) +
+                                     (uint32_t(tc) * uint32_t(R >> 7) + tr) * 512 + off) =
+            e8m0_of_pow2(S.scf_col[u]) * 0x01010101u;
     } else {
       if (t < 128 && p.row != nullptr)
         reinterpret_cast<float*>(p.row_scale)[uint32_t(tc) * R + r0 + t] = S.scf_row[t];

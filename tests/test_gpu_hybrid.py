@@ -8,7 +8,7 @@ import pytest
 import torch
 
 from helpers import (bw_untile, cuda_ok, from_dev_bf16, gemm_bf16_close, gemm_f32_normwise,
-                     same_f32, to_dev_bf16)
+                     mx_untile, same_f32, to_dev_bf16)
 from oracle import fp8_oracle as O
 from workloads import bf16_bits_normal
 
@@ -152,8 +152,8 @@ def test_hybrid_dgrad_wgrad(kind, fp32):
 @pytest.mark.parametrize("role", ["activation", "weight"])
 @pytest.mark.parametrize("margin", [0, 3])
 def test_blockwise_power_of_two_scales(role, margin):
-    """Blockwise with power-of-two block scales: codes and s_inv bit-exact, every s_inv a
-    power of two, and the GEMM over them within the usual tolerance."""
+    """Blockwise with power-of-two block scales: codes bit-exact, and the scales stored as E8M0
+    bytes in the MXFP8 layout equal to the oracle's power-of-two s_inv."""
     rec = F.Recipe(kind="blockwise", power_2_scales=True, margin=margin)
     x = bf16_bits_normal(256, 384, seed=101, outlier_p=1e-2, outlier_factor=40.0)
     R, C = x.shape
@@ -162,30 +162,49 @@ def test_blockwise_power_of_two_scales(role, margin):
     torch.cuda.synchronize()
     if role == "weight":
         ref = O.quantize_blockwise_128x128(x, margin, pow2=True)
-        assert np.array_equal(_np(q.row_scale), ref["row_scale_inv"])
-        assert np.array_equal(_np(q.col_scale), ref["col_scale_inv"])
+        rows_b = 128
     else:
         ref = O.quantize_blockwise_1x128(x, margin, pow2=True)
-        assert np.array_equal(bw_untile(_np(q.row_scale), R, C), ref["row_scale_inv"])
-        assert np.array_equal(bw_untile(_np(q.col_scale), C, R), ref["col_scale_inv"])
+        rows_b = 1
+    assert np.array_equal(mx_untile(_np(q.row_scale), R, C),
+                          O.pow2_scales_as_e8m0(ref["row_scale_inv"], rows_b, R, C))
+    assert np.array_equal(mx_untile(_np(q.col_scale), C, R),
+                          O.pow2_scales_as_e8m0(ref["col_scale_inv"], rows_b, C, R))
     assert np.array_equal(_np(q.row), ref["row"])
     assert np.array_equal(_np(q.col), ref["col"])
-    f, _ = np.frexp(ref["row_scale_inv"].astype(np.float64))
-    assert np.all(f == 0.5)
 
 
-def test_blockwise_power_of_two_fprop():
-    rec = F.Recipe(kind="blockwise", power_2_scales=True)
+@pytest.mark.parametrize("fmt", ["e4m3", "hybrid"])
+@pytest.mark.parametrize("fp32", [False, True])
+def test_blockwise_power_of_two_gemms(fmt, fp32):
+    """fprop, dgrad and wgrad of power-of-two blockwise tensors, which run on the MXFP8
+    block-scaled tensor-core path, against the oracle's blockwise GEMMs."""
+    rec = F.Recipe(kind="blockwise", power_2_scales=True, format=fmt)
     M, N, K = 256, 384, 512
     xb = bf16_bits_normal(M, K, seed=102)
     wb = bf16_bits_normal(N, K, seed=103, sigma=0.02)
+    dyb = bf16_bits_normal(M, N, seed=104, sigma=1e-3)
+    gf = "e5m2" if fmt == "hybrid" else "e4m3"
     xq = F.quantize(rec, to_dev_bf16(xb), "activation")
     wq = F.quantize(rec, to_dev_bf16(wb), "weight")
-    y = F.linear_fwd(rec, xq, wq, fp32=True)
+    dyq = F.quantize(rec, to_dev_bf16(dyb), "grad")
+    y = F.linear_fwd(rec, xq, wq, fp32=fp32)
+    dx, dw = F.linear_bwd(rec, dyq, xq, wq, fp32=fp32)
     torch.cuda.synchronize()
     qx = O.quantize_blockwise_1x128(xb, pow2=True)
     qw = O.quantize_blockwise_128x128(wb, pow2=True)
-    ref = O.gemm_tn_f64(O.dequant_1x128(qx["row"], qx["row_scale_inv"]),
-                        O.dequant_128x128(qw["row"], qw["row_scale_inv"]))
-    ok, err = gemm_f32_normwise(_np(y), ref)
-    assert ok, err
+    qd = O.quantize_blockwise_1x128(dyb, pow2=True, fmt=gf)
+    refs = (
+        (y, O.gemm_tn_f64(O.dequant_1x128(qx["row"], qx["row_scale_inv"]),
+                          O.dequant_128x128(qw["row"], qw["row_scale_inv"]))),
+        (dx, O.gemm_tn_f64(O.dequant_1x128(qd["row"], qd["row_scale_inv"], gf),
+                           O.dequant_128x128(qw["col"], qw["col_scale_inv"]))),
+        (dw, O.gemm_tn_f64(O.dequant_1x128(qd["col"], qd["col_scale_inv"], gf),
+                           O.dequant_1x128(qx["col"], qx["col_scale_inv"]))),
+    )
+    for got, ref in refs:
+        if fp32:
+            ok, err = gemm_f32_normwise(_np(got), ref)
+        else:
+            ok, err = gemm_bf16_close(from_dev_bf16(got), ref)
+        assert ok, err

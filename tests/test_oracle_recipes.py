@@ -288,3 +288,20 @@ def test_fp32_master_weight_inputs():
         for j in range(8):
             e = min(k for k in range(-127, 128) if float(amax[i, j]) <= 448.0 * 2.0 ** k)
             assert mx["row_scale"][i, j] == e + 127
+
+
+def test_pow2_scales_as_e8m0_dequantise_identically():
+    """The E8M0 view of power-of-two block scales dequantises every code exactly as the fp32
+    s_inv does (1x128 activations and 128x128 weights, both copies)."""
+    rng = np.random.default_rng(13)
+    x = bf16_bits_from_f32((rng.standard_normal((256, 384)) *
+                            np.exp(rng.uniform(-6, 6, (256, 1)))).astype(np.float32))
+    q = O.quantize_blockwise_1x128(x, pow2=True)
+    b = O.pow2_scales_as_e8m0(q["row_scale_inv"], 1, 256, 384)
+    assert np.array_equal(O.dequant_mx(q["row"], b), O.dequant_1x128(q["row"], q["row_scale_inv"]))
+    bc = O.pow2_scales_as_e8m0(q["col_scale_inv"], 1, 384, 256)
+    assert np.array_equal(O.dequant_mx(q["col"], bc), O.dequant_1x128(q["col"], q["col_scale_inv"]))
+    w = O.quantize_blockwise_128x128(x, pow2=True)
+    bw = O.pow2_scales_as_e8m0(w["row_scale_inv"], 128, 256, 384)
+    assert np.array_equal(O.dequant_mx(w["row"], bw), O.dequant_128x128(w["row"], w["row_scale_inv"]))
+    assert np.all(O.e8m0_decode(b) == np.repeat(q["row_scale_inv"], 4, axis=1))
