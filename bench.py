@@ -394,6 +394,292 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ----------------------------------------------------------------------------- other configs
+
+CONFIGS = {
+    "mxfp8_fprop": "mxfp8 quantize X 8192x4096 (0.1% outliers x50) + W 4096x4096 + fprop",
+    "blockwise_fwd_bwd": "blockwise quantize X, W, dY 4096x4096 + fprop + dgrad + wgrad",
+    "delayed_step": "delayed quantize X_t 8192x4096 (log-uniform sigma) + fprop (W 4096x4096) "
+                    "+ amax history update (length 1024)",
+}
+
+
+class ConfigStep:
+    """One step of a smaller configuration of the layer (device-resident buffers)."""
+
+    def __init__(self, torch, F, dev, name):
+        from workloads import STREAM_STEP0, bf16_bits_normal, sigma_schedule
+        self.torch, self.F, self.dev, self.name = torch, F, dev, name
+        bf = torch.bfloat16
+
+        def host(bits):
+            return torch.from_numpy(bits.view(np.int16)).view(bf).pin_memory()
+
+        e = F.empty_qtensor
+        self.events = None
+        if name == "mxfp8_fprop":
+            self.rec = F.Recipe(kind="mxfp8")
+            M, N, K = 8192, 4096, 4096
+            self.h = {"x": host(bf16_bits_normal(M, K, seed=0, stream=0, outlier_p=1e-3,
+                                                 outlier_factor=50.0)),
+                      "w": host(bf16_bits_normal(N, K, seed=0, stream=1, sigma=0.02))}
+            self.q = {"x": e(self.rec, M, K, "activation", device=dev),
+                      "w": e(self.rec, N, K, "weight", device=dev)}
+            self.outs = {"y": torch.empty((M, N), dtype=bf, device=dev)}
+            self.flops = 2.0 * M * N * K
+            self.quant_bytes = (M * K + N * K) * (2 + 2 + 2 / 32.0)
+            self.launches = 3
+        elif name == "blockwise_fwd_bwd":
+            self.rec = F.Recipe(kind="blockwise")
+            n = 4096
+            self.h = {"x": host(bf16_bits_normal(n, n, seed=0, stream=0)),
+                      "w": host(bf16_bits_normal(n, n, seed=0, stream=1, sigma=0.02)),
+                      "dy": host(bf16_bits_normal(n, n, seed=0, stream=2, sigma=1e-3))}
+            self.q = {"x": e(self.rec, n, n, "activation", device=dev),
+                      "w": e(self.rec, n, n, "weight", device=dev),
+                      "dy": e(self.rec, n, n, "grad", device=dev)}
+            self.outs = {k: torch.empty((n, n), dtype=bf, device=dev) for k in ("y", "dx", "dw")}
+            self.flops = 3 * 2.0 * n ** 3
+            self.quant_bytes = 2 * n * n * (2 + 2 + 2 * 4 / 128.0) + n * n * (2 + 2)
+            self.launches = 6
+        else:
+            self.rec = F.Recipe(kind="delayed", amax_history_len=1024)
+            M, N, K = 8192, 4096, 4096
+            sig = sigma_schedule(8)
+            # eight inputs of drifting scale, cycled through the timed steps
+            self.xs_host = [host(bf16_bits_normal(M, K, seed=0, stream=STREAM_STEP0 + t,
+                                                  sigma=sig[t])) for t in range(8)]
+            self.xs = [x.to(dev) for x in self.xs_host]
+            self.h = {"x": self.xs_host[0]}
+            self.state = F.DelayedState(self.rec, device=dev)
+            wstate = F.DelayedState(self.rec, device=dev, role="weight")
+            wd = torch.from_numpy(bf16_bits_normal(N, K, seed=0, stream=1, sigma=0.02)
+                                  .view(np.int16)).view(bf).to(dev)
+            self.wq = F.quantize(self.rec, wd, "weight",
+                                 out=wstate.bind(e(self.rec, N, K, "weight", device=dev)))
+            self.q = {"x": self.state.bind(e(self.rec, M, K, "activation", device=dev))}
+            self.ws = torch.empty(F.workspace_bytes(self.rec, M, K), dtype=torch.uint8, device=dev)
+            self.outs = {"y": torch.empty((M, N), dtype=bf, device=dev)}
+            self.flops = 2.0 * M * N * K
+            self.quant_bytes = M * K * 4.0
+            self.launches = 4                    # cast, amax finalize, GEMM, history update
+            self.t = 0
+        self.d = {k: v.to(dev) for k, v in self.h.items()}
+        self.stream = torch.cuda.current_stream(dev)
+
+    def _t(self, kind, fn, name):
+        if self.events is None:
+            return fn()
+        s, e = self.torch.cuda.Event(enable_timing=True), self.torch.cuda.Event(enable_timing=True)
+        s.record(self.stream)
+        fn()
+        e.record(self.stream)
+        self.events.append((kind, name, s, e))
+
+    def run(self, d=None):
+        F, rec, T, q, o = self.F, self.rec, self._t, self.q, self.outs
+        resident = d is None
+        d = self.d if resident else d
+        if self.name == "mxfp8_fprop":
+            T("quant", lambda: F.quantize(rec, d["x"], "activation", out=q["x"]), "quantize_x")
+            T("quant", lambda: F.quantize(rec, d["w"], "weight", out=q["w"]), "quantize_w")
+            T("gemm", lambda: F.linear_fwd(rec, q["x"], q["w"], y=o["y"]), "fprop")
+        elif self.name == "blockwise_fwd_bwd":
+            T("quant", lambda: F.quantize(rec, d["x"], "activation", out=q["x"]), "quantize_x")
+            T("quant", lambda: F.quantize(rec, d["w"], "weight", out=q["w"]), "quantize_w")
+            T("gemm", lambda: F.linear_fwd(rec, q["x"], q["w"], y=o["y"]), "fprop")
+            T("quant", lambda: F.quantize(rec, d["dy"], "grad", out=q["dy"]), "quantize_dy")
+            T("gemm", lambda: F.linear_bwd(rec, q["dy"], q["x"], q["w"], want_dw=False,
+                                           dx=o["dx"]), "dgrad")
+            T("gemm", lambda: F.linear_bwd(rec, q["dy"], q["x"], q["w"], want_dx=False,
+                                           dw=o["dw"]), "wgrad")
+        else:
+            x = self.xs[self.t % 8] if resident else d["x"]
+            self.t += 1
+            T("quant", lambda: F.quantize(rec, x, "activation", out=q["x"], workspace=self.ws),
+              "quantize_x")
+            T("gemm", lambda: F.linear_fwd(rec, q["x"], self.wq, y=o["y"]), "fprop")
+            T("other", lambda: F.amax_update(rec, self.state, q["x"].amax), "amax_update")
+
+    def run_e2e(self, steps):
+        """Each step uploads its inputs from pinned host memory and downloads its outputs,
+        serialised with the step on one stream."""
+        torch = self.torch
+        h_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in self.outs.items()}
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(self.stream)
+        for i in range(steps):
+            src = {"x": self.xs_host[i % 8]} if self.name == "delayed_step" else self.h
+            for k, v in src.items():
+                self.d[k].copy_(v, non_blocking=True)
+            self.run(self.d)
+            for k, v in self.outs.items():
+                h_out[k].copy_(v, non_blocking=True)
+        t1.record(self.stream)
+        t1.synchronize()
+        return t0.elapsed_time(t1)
+
+    def h2d_bytes(self):
+        return sum(v.numel() * 2 for v in self.h.values())
+
+    def d2h_bytes(self):
+        return sum(v.numel() * 2 for v in self.outs.values())
+
+
+_CFG_SETUP = {}
+
+
+def cpu_baseline_config(name, m_sample=1024):
+    """The oracle on a bounded sample of a configuration's step: quantisation and GEMM rows of
+    m_sample of the activation rows (scaled up), weight quantisation of m_sample of its rows
+    (scaled up)."""
+    from oracle import fp8_oracle as O
+    from workloads import bf16_bits_normal
+    n_rows = {"mxfp8_fprop": 8192, "blockwise_fwd_bwd": 4096, "delayed_step": 8192}[name]
+    K = 4096
+    if name == "blockwise_fwd_bwd":                # whole 128-row blocks of the column copies
+        m_sample = max(128, m_sample // 128 * 128)
+    xs = bf16_bits_normal(m_sample, K, seed=0, stream=0)
+    ws = bf16_bits_normal(m_sample, K, seed=0, stream=1, sigma=0.02)
+    if name not in _CFG_SETUP:                    # untimed: the full weight's quantised copies
+        wfull = bf16_bits_normal(4096, K, seed=0, stream=1, sigma=0.02)
+        if name == "mxfp8_fprop":
+            qw = O.quantize_mxfp8(wfull, want_col=False)
+            _CFG_SETUP[name] = dict(wr=O.dequant_mx(qw["row"], qw["row_scale"]))
+        elif name == "blockwise_fwd_bwd":
+            qw = O.quantize_blockwise_128x128(wfull)
+            _CFG_SETUP[name] = dict(wr=O.dequant_128x128(qw["row"], qw["row_scale_inv"]),
+                                    wc=O.dequant_128x128(qw["col"], qw["col_scale_inv"]))
+        else:
+            qw = O.DelayedScaling(1024).quantize(wfull)
+            _CFG_SETUP[name] = dict(wr=O.dequant_tensor(qw["row"], qw["scale_inv"]))
+    S = _CFG_SETUP[name]
+    t0 = time.perf_counter()
+    if name == "mxfp8_fprop":
+        O.quantize_mxfp8(ws)
+        t_w = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        qx = O.quantize_mxfp8(xs)
+        O.f64_to_bf16(O.gemm_tn_f64(O.dequant_mx(qx["row"], qx["row_scale"]), S["wr"]))
+        t_x = time.perf_counter() - t0
+        flops = 2.0 * 8192 * 4096 * K
+    elif name == "blockwise_fwd_bwd":
+        O.quantize_blockwise_128x128(bf16_bits_normal(128, K, seed=0, stream=1, sigma=0.02))
+        t_w = (time.perf_counter() - t0) * m_sample / 128.0      # per m_sample weight rows
+        wr, wc = S["wr"], S["wc"]
+        t0 = time.perf_counter()
+        qx = O.quantize_blockwise_1x128(xs)
+        qd = O.quantize_blockwise_1x128(bf16_bits_normal(m_sample, K, seed=0, stream=2,
+                                                         sigma=1e-3))
+        O.gemm_tn_f64(O.dequant_1x128(qx["row"], qx["row_scale_inv"]), wr)
+        O.gemm_tn_f64(O.dequant_1x128(qd["row"], qd["row_scale_inv"]), wc)
+        # wgrad: each sampled token row adds its outer product to every dW element
+        O.gemm_tn_f64(O.dequant_1x128(qd["col"], qd["col_scale_inv"]),
+                      O.dequant_1x128(qx["col"], qx["col_scale_inv"]))
+        t_x = time.perf_counter() - t0
+        flops = 3 * 2.0 * 4096 ** 3
+    else:
+        t_w = 0.0
+        d = O.DelayedScaling(1024)
+        t0 = time.perf_counter()
+        q = d.quantize(xs)
+        O.f64_to_bf16(O.gemm_tn_f64(O.dequant_tensor(q["row"], q["scale_inv"]), S["wr"]))
+        d.update(q["amax"])
+        t_x = time.perf_counter() - t0
+        flops = 2.0 * 8192 * 4096 * K
+    step_s = t_w * (4096 / m_sample) + t_x * (n_rows / m_sample)
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": round(flops / step_s / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
+            "kind": "oracle", "step_seconds_estimate": round(step_s, 2),
+            "sample": f"oracle step on {m_sample} of {n_rows} activation rows and {m_sample} "
+                      f"weight rows, scaled by {n_rows // m_sample}"}
+
+
+def run_config(args):
+    """`--workload` other than the MLP step: the same JSON contract for that configuration."""
+    import torch
+    import scaled_quantize_fp8_gb300 as F
+    from scaled_quantize_fp8_gb300 import build as B
+    B.build()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    st = ConfigStep(torch, F, dev, args.workload)
+    for _ in range(args.warmup):
+        st.run()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local)
+    clocks.start()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(st.stream)
+    for _ in range(args.steps):
+        st.run()
+    t1.record(st.stream)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    ms_total = max_over_ranks(t0.elapsed_time(t1), dist, dev)
+    st.events = []
+    for _ in range(max(1, min(args.steps, 20))):
+        st.run()
+    torch.cuda.synchronize(dev)
+    ms = {"gemm": [], "quant": [], "other": []}
+    per_name = {}
+    for kind, name, s, e in st.events:
+        ms[kind].append(s.elapsed_time(e))
+        per_name.setdefault(name, []).append(s.elapsed_time(e))
+    st.events = None
+    st.run_e2e(max(2, args.warmup))
+    ms_e2e = max_over_ranks(st.run_e2e(args.steps), dist, dev)
+    n_pk = max(1, min(args.steps, 20))
+    value = world * st.flops / (ms_total / args.steps * 1e-3) / 1e12
+    hbm, fp8_peak, src = peaks()
+    gemm_ms = statistics.mean(ms["gemm"])
+    gemm_flops = st.flops / (3 if args.workload == "blockwise_fwd_bwd" else 1)
+    achieved = gemm_flops / (gemm_ms * 1e-3) / 1e12
+    quant_ms = sum(ms["quant"]) / n_pk
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms_total / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate)",
+            "data": "synthetic",
+            "config": {"workload": CONFIGS[args.workload], "recipe": st.rec.kind,
+                       "parallelism": "replicas" if world > 1 else "single",
+                       "l2": "inputs above L2 (64-128 MB per tensor, eight X_t for delayed)",
+                       "gemm_flops_per_step": st.flops},
+            "roofline": {"bound": "tensor", "kernel": f"gemm_tn_kernel ({st.rec.kind})",
+                         "achieved": round(achieved, 1), "peak": fp8_peak, "unit": "TFLOP/s",
+                         "frac": round(achieved / fp8_peak, 4), "traffic": None,
+                         "peak_source": f"{src}: bf16 x {FP8_OVER_BF16} (nominal fp8/bf16)",
+                         "avg_launch_ms": round(gemm_ms, 4)},
+            "quantize": {"gbs": round(st.quant_bytes / (quant_ms * 1e-3) / 1e9, 1),
+                         "peak_gbs": hbm, "ms_per_step": round(quant_ms, 4),
+                         "algorithmic_bytes_per_step": st.quant_bytes, "peak_source": src},
+            "e2e": {"value": round(world * st.flops / (ms_e2e / args.steps * 1e-3) / 1e12, 2),
+                    "unit": "TFLOP/s", "h2d_bytes_per_step": st.h2d_bytes(),
+                    "d2h_bytes_per_step": st.d2h_bytes(),
+                    "copies": "pinned host, serialised with each step"},
+            "kernels_ms": {k: round(statistics.mean(v), 4) for k, v in per_name.items()},
+            "gpu_launches": st.launches * args.steps,
+            "clocks": clk,
+            "cpu_baseline": cpu_baseline_config(args.workload),
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
 # ----------------------------------------------------------------------------- CPU oracle
 
 _ORACLE_SETUP = {}
@@ -456,12 +742,21 @@ def run_reference(args):
     if world > 1 and rank != 0:
         return
     vals = []
-    _oracle_setup()
+    if args.workload == "mlp":
+        def one():
+            return cpu_baseline(m_sample=32, w_frac=64)
+        workload = WORKLOAD
+    else:
+        def one():
+            return cpu_baseline_config(args.workload, m_sample=128)
+        workload = CONFIGS[args.workload]
+    if args.workload == "mlp":
+        _oracle_setup()
     for _ in range(min(args.warmup, 1)):
-        cpu_baseline(m_sample=32, w_frac=64)
+        one()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        vals.append(cpu_baseline(m_sample=32, w_frac=64))
+        vals.append(one())
     elapsed = time.perf_counter() - t0
     v = statistics.median(x["value"] for x in vals)
     c = dict(vals[0])
@@ -472,7 +767,8 @@ def run_reference(args):
         "ms_per_step": round(statistics.median(x["step_seconds_estimate"] for x in vals) * 1e3, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64 (oracle)", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "recipe": "mxfp8", "parallelism": "single"},
+        "config": {"workload": workload, "recipe": {"mlp": "mxfp8"}.get(
+            args.workload, args.workload.split("_")[0]), "parallelism": "single"},
         "cpu_baseline": c, "wall_seconds": round(elapsed, 1),
         "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
@@ -482,6 +778,7 @@ def run_profile_case(args):
     """Launch one kernel kind a few times on its own (for ncu captures; prints no JSON line).
     quant_mx / quant_tensorwise / quant_blockwise: X 16384 x 8192 bf16 (256 MiB, above L2).
     gemm_mx / gemm_tensorwise / gemm_blockwise: fprop 8192 x 4096 x 4096.
+    gemm_wgrad_blockwise: blockwise wgrad 4096 x 4096 x 8192 (1x128 scales on both operands).
     gelu_mx / dgelu_mx: the standalone GeLU / dGeLU + MXFP8 quantize on h 8192 x 16384.
     gemm_gelu_mx / gemm_dgelu_mx: fc1 with the GeLU epilogue (8192 x 16384 x 4096) and fc2's
     dgrad with the dGeLU epilogue (8192 x 16384 x 4096).
@@ -536,6 +833,13 @@ def run_profile_case(args):
                 F.gelu_quantize(rec, h, a_q=a_q, h_q=h_q)
             else:
                 F.dgelu_quantize(rec, h, h_q, dh_q=a_q)
+    elif case == "gemm_wgrad_blockwise":
+        x = torch.randn((8192, 4096), device="cuda", generator=g).to(torch.bfloat16)
+        dy = (torch.randn((8192, 4096), device="cuda", generator=g) * 1e-3).to(torch.bfloat16)
+        xq, dyq = F.quantize(rec, x, "activation"), F.quantize(rec, dy, "grad")
+        dw = torch.empty((4096, 4096), dtype=torch.bfloat16, device="cuda")
+        for _ in range(args.steps):
+            F.linear_bwd(rec, dyq, xq, None, want_dx=False, dw=dw)
     elif case.startswith("quant"):
         x = torch.randn((16384, 8192), device="cuda", generator=g).to(torch.bfloat16)
         q = F.empty_qtensor(rec, 16384, 8192, "activation")
@@ -632,11 +936,14 @@ def main():
     ap.add_argument("--profile", default=None,
                     choices=["quant_mx", "quant_tensorwise", "quant_blockwise", "gemm_mx",
                              "gemm_tensorwise", "gemm_blockwise", "gelu_mx", "dgelu_mx",
-                             "gemm_gelu_mx", "gemm_dgelu_mx", "gemm_mx_mlp"])
+                             "gemm_gelu_mx", "gemm_dgelu_mx", "gemm_mx_mlp",
+                             "gemm_wgrad_blockwise"])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="mlp", choices=["mlp"] + sorted(CONFIGS),
+                    help="the MXFP8 MLP step (default) or one of the smaller configurations")
     ap.add_argument("--kernels", action="store_true",
                     help="per-recipe quantize and GEMM timings instead of the benchmark step")
     ap.add_argument("--unfused", action="store_true",
@@ -648,6 +955,8 @@ def main():
         run_profile_case(args)
     elif args.kernels:
         run_kernels(args)
+    elif args.workload != "mlp" and args.impl != "reference":
+        run_config(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

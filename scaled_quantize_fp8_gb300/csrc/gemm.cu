@@ -600,49 +600,109 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
           for (int j = 0; j < kCols; ++j) acc[j] = __fmul_rn(acc[j], alpha);
         }
       } else {
-#pragma unroll
-        for (int j = 0; j < kCols; ++j) acc[j] = 0.0f;
+        // Blockwise promotion: chunk kb's partial sum P (fp32 in TMEM) is added into the
+        // register accumulator as acc += P * (s_inv(A row, kb) * s_inv(B, kb)), two columns
+        // per packed FMA. Chunk kb + 1's scales are fetched while chunk kb is promoted. With
+        // per-row B scales (1x128, wgrad) the warp's 64 column scales of a chunk go straight
+        // from global to the warp's slice of the (otherwise unused) scale-factor region of
+        // shared memory with cp.async, two chunk buffers a warp, and are read back as
+        // broadcasts, so no registers hold them in flight.
+        static_assert(MODE != G_BLOCK || B128 || kEpiWarps * kCols * 8 <= G::kStages * kSfStageBytes,
+                      "per-warp B-scale buffers fit in the scale-factor region");
         const int kblocks = p.K / 128;
+        float2 acc2[kCols / 2];
+#pragma unroll
+        for (int j = 0; j < kCols / 2; ++j) acc2[j] = make_float2(0.0f, 0.0f);
+        auto load_sa = [&](int kb) { return m < p.M ? __ldg(p.a_bs + int64_t(kb) * p.M + m) : 0.0f; };
+        auto load_sb = [&](int kb) {
+          float v = 0.0f;
+          if (n < p.N)
+            v = p.b_mn ? __ldg(p.b_bs + int64_t(kb) * (p.N >> 7) + (n >> 7))   // grid [K][N]
+                       : __ldg(p.b_bs + int64_t(n >> 7) * kblocks + kb);        // grid [N][K]
+          return v;
+        };
+        float2* sbw = reinterpret_cast<float2*>(sSF) + ew * kCols;      // 2 x 32 float2
+        auto fetch_sb = [&](int kb) {
+          float2* dst = sbw + (kb & 1) * (kCols / 2) + lane;
+          if (n < p.N) ptx::cp_async_8(dst, p.b_bs + int64_t(kb) * p.N + n + 2 * lane);
+          else *dst = make_float2(0.0f, 0.0f);
+          ptx::cp_async_commit();
+        };
+        float sa_nx = load_sa(0);
+        float sb_nx = 0.0f;
+        if constexpr (B128 != 0) sb_nx = load_sb(0);
+        else {
+          __syncwarp();                    // the previous tile's reads of buffer 0 are done
+          fetch_sb(0);
+        }
         bool ok = true;
         for (int kb = 0; kb < kblocks; ++kb) {
-          const float sa = (m < p.M) ? p.a_bs[int64_t(kb) * p.M + m] : 0.0f;
-          float sb = 0.0f;
-          if (B128 && n < p.N)
-            sb = p.b_mn ? p.b_bs[int64_t(kb) * (p.N >> 7) + (n >> 7)]     // row grid [K][N]
-                        : p.b_bs[int64_t(n >> 7) * kblocks + kb];         // col grid [N][K]
+          const float sa = sa_nx;
+          const float sb = sb_nx;
+          if (kb + 1 < kblocks) {
+            sa_nx = load_sa(kb + 1);
+            if constexpr (B128 != 0) sb_nx = load_sb(kb + 1);
+          }
+          if constexpr (B128 == 0) {
+            __syncwarp();                  // chunk kb - 1's reads of the other buffer are done
+            if (kb + 1 < kblocks) {
+              fetch_sb(kb + 1);
+              ptx::cp_async_wait<1>();     // chunk kb's group has landed
+            } else {
+              ptx::cp_async_wait<0>();
+            }
+            __syncwarp();
+          }
           const uint32_t b = u & 1u;
           if (!wait_bar(&ctl->accf[b], (u >> 1) & 1u, ctl, p.status)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
-          // Promote the chunk 16 columns at a time (keeps the partials out of registers).
           const float f = __fmul_rn(sa, sb);
+          const float2 f2 = make_float2(f, f), sa2 = make_float2(sa, sa);
+          if constexpr (B128 != 0) {
 #pragma unroll
-          for (int c = 0; c < kCols / 16; ++c) {
-            uint32_t r[16];
-            ptx::tmem_ld_32x32b_x16(t_lane + b * kBN + 16 * c, r);
-            ptx::tmem_wait_ld();
-            if constexpr (B128 != 0) {
+            for (int c = 0; c < kCols / 16; ++c) {
+              uint32_t r[16];
+              ptx::tmem_ld_32x32b_x16(t_lane + b * kBN + 16 * c, r);
+              ptx::tmem_wait_ld();
 #pragma unroll
-              for (int j = 0; j < 16; ++j)
-                acc[16 * c + j] = __fmaf_rn(__uint_as_float(r[j]), f, acc[16 * c + j]);
-            } else {
-              const float* sbv = p.b_bs + int64_t(kb) * p.N + n + 16 * c;
+              for (int j = 0; j < 8; ++j) {
+                const float2 pr = make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+                acc2[8 * c + j] = __ffma2_rn(pr, f2, acc2[8 * c + j]);
+              }
+            }
+          } else {
+            // 8 columns a load: the per-column path has fewer registers to spare
+            const float4* sb4 = reinterpret_cast<const float4*>(sbw + (kb & 1) * (kCols / 2));
 #pragma unroll
-              for (int j = 0; j < 16; j += 4) {
-                float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (n + 16 * c + j < p.N) q = *reinterpret_cast<const float4*>(sbv + j);
-                const int i = 16 * c + j;
-                acc[i] = __fmaf_rn(__uint_as_float(r[j]), __fmul_rn(sa, q.x), acc[i]);
-                acc[i + 1] = __fmaf_rn(__uint_as_float(r[j + 1]), __fmul_rn(sa, q.y), acc[i + 1]);
-                acc[i + 2] = __fmaf_rn(__uint_as_float(r[j + 2]), __fmul_rn(sa, q.z), acc[i + 2]);
-                acc[i + 3] = __fmaf_rn(__uint_as_float(r[j + 3]), __fmul_rn(sa, q.w), acc[i + 3]);
+            for (int c = 0; c < kCols / 8; ++c) {
+              uint32_t r[8];
+              ptx::tmem_ld_32x32b_x8(t_lane + b * kBN + 8 * c, r);
+              ptx::tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 4; j += 2) {
+                // (P * s_inv(B column)) * s_inv(A row): the partials take the column scale in
+                // place, so no product registers are needed
+                const float4 q = sb4[2 * c + j / 2];
+                float2 p0 = make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+                float2 p1 = make_float2(__uint_as_float(r[2 * j + 2]), __uint_as_float(r[2 * j + 3]));
+                p0 = __fmul2_rn(p0, make_float2(q.x, q.y));
+                p1 = __fmul2_rn(p1, make_float2(q.z, q.w));
+                acc2[4 * c + j] = __ffma2_rn(p0, sa2, acc2[4 * c + j]);
+                acc2[4 * c + j + 1] = __ffma2_rn(p1, sa2, acc2[4 * c + j + 1]);
               }
             }
           }
           release_acc(b);
           ++u;
+        }
+        if constexpr (B128 == 0) ptx::cp_async_wait<0>();   // nothing left in flight on exit
+#pragma unroll
+        for (int j = 0; j < kCols / 2; ++j) {
+          acc[2 * j] = acc2[j].x;
+          acc[2 * j + 1] = acc2[j].y;
         }
         if (!ok) break;
       }
