@@ -321,7 +321,7 @@ def run_ours(args):
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(st.stream)
     for _ in range(args.steps):
-        st.run()
+        step()
     t1.record(st.stream)
     barrier()
     clk = clocks.stop()
@@ -397,6 +397,8 @@ def run_ours(args):
 # ----------------------------------------------------------------------------- other configs
 
 CONFIGS = {
+    "tensorwise_256": "tensorwise quantize X, W 256x256 (N(0,1)) + fprop 256^3, one CUDA graph "
+                      "a step",
     "mxfp8_fprop": "mxfp8 quantize X 8192x4096 (0.1% outliers x50) + W 4096x4096 + fprop",
     "blockwise_fwd_bwd": "blockwise quantize X, W, dY 4096x4096 + fprop + dgrad + wgrad",
     "delayed_step": "delayed quantize X_t 8192x4096 (log-uniform sigma) + fprop (W 4096x4096) "
@@ -417,7 +419,20 @@ class ConfigStep:
 
         e = F.empty_qtensor
         self.events = None
-        if name == "mxfp8_fprop":
+        if name == "tensorwise_256":
+            self.rec = F.Recipe(kind="tensorwise")
+            n = 256
+            self.h = {"x": host(bf16_bits_normal(n, n, seed=0, stream=0)),
+                      "w": host(bf16_bits_normal(n, n, seed=0, stream=1))}
+            self.q = {"x": e(self.rec, n, n, "activation", device=dev),
+                      "w": e(self.rec, n, n, "weight", device=dev)}
+            self.ws = torch.empty(F.workspace_bytes(self.rec, n, n), dtype=torch.uint8,
+                                  device=dev)
+            self.outs = {"y": torch.empty((n, n), dtype=bf, device=dev)}
+            self.flops = 2.0 * n ** 3
+            self.quant_bytes = 2 * n * n * 4.0
+            self.launches = 5                    # amax + cast for X and W, GEMM
+        elif name == "mxfp8_fprop":
             self.rec = F.Recipe(kind="mxfp8")
             M, N, K = 8192, 4096, 4096
             self.h = {"x": host(bf16_bits_normal(M, K, seed=0, stream=0, outlier_p=1e-3,
@@ -476,11 +491,18 @@ class ConfigStep:
         e.record(self.stream)
         self.events.append((kind, name, s, e))
 
-    def run(self, d=None):
-        F, rec, T, q, o = self.F, self.rec, self._t, self.q, self.outs
+    def run(self, d=None, o=None):
+        F, rec, T, q = self.F, self.rec, self._t, self.q
         resident = d is None
         d = self.d if resident else d
-        if self.name == "mxfp8_fprop":
+        o = self.outs if o is None else o
+        if self.name == "tensorwise_256":
+            T("quant", lambda: F.quantize(rec, d["x"], "activation", out=q["x"],
+                                          workspace=self.ws), "quantize_x")
+            T("quant", lambda: F.quantize(rec, d["w"], "weight", out=q["w"], workspace=self.ws),
+              "quantize_w")
+            T("gemm", lambda: F.linear_fwd(rec, q["x"], q["w"], y=o["y"]), "fprop")
+        elif self.name == "mxfp8_fprop":
             T("quant", lambda: F.quantize(rec, d["x"], "activation", out=q["x"]), "quantize_x")
             T("quant", lambda: F.quantize(rec, d["w"], "weight", out=q["w"]), "quantize_w")
             T("gemm", lambda: F.linear_fwd(rec, q["x"], q["w"], y=o["y"]), "fprop")
@@ -502,20 +524,48 @@ class ConfigStep:
             T("other", lambda: F.amax_update(rec, self.state, q["x"].amax), "amax_update")
 
     def run_e2e(self, steps):
-        """Each step uploads its inputs from pinned host memory and downloads its outputs,
-        serialised with the step on one stream."""
+        """`steps` steps whose inputs are copied from pinned host memory and whose outputs are
+        copied back to pinned host memory, pipelined like the MLP step's: uploads on one
+        stream, the step on the compute stream, downloads on a third, two buffer sets
+        alternating. Returns the elapsed ms from the first upload to the last download."""
         torch = self.torch
-        h_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in self.outs.items()}
+        comp = self.stream
+        if not hasattr(self, "d_sets"):
+            self.d_sets = [self.d, {k: torch.empty_like(v) for k, v in self.d.items()}]
+            self.o_sets = [self.outs, {k: torch.empty_like(v) for k, v in self.outs.items()}]
+            self.h_out = [{k: torch.empty(v.shape, dtype=v.dtype).pin_memory()
+                           for k, v in self.outs.items()} for _ in range(2)]
+        s_in, s_out = torch.cuda.Stream(self.dev), torch.cuda.Stream(self.dev)
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_comp = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        t0.record(self.stream)
+        t0.record(comp)
+        s_in.wait_stream(comp)
+        s_out.wait_stream(comp)
         for i in range(steps):
+            b = i % 2
             src = {"x": self.xs_host[i % 8]} if self.name == "delayed_step" else self.h
-            for k, v in src.items():
-                self.d[k].copy_(v, non_blocking=True)
-            self.run(self.d)
-            for k, v in self.outs.items():
-                h_out[k].copy_(v, non_blocking=True)
-        t1.record(self.stream)
+            if i >= 2:
+                s_in.wait_event(ev_comp[b])               # step i-2 is done with these inputs
+            with torch.cuda.stream(s_in):
+                for k, v in src.items():
+                    self.d_sets[b][k].copy_(v, non_blocking=True)
+                ev_in[b].record(s_in)
+            comp.wait_event(ev_in[b])
+            if i >= 2:
+                comp.wait_event(ev_out[b])                # step i-2's outputs are downloaded
+            with torch.cuda.stream(comp):
+                self.run(self.d_sets[b], self.o_sets[b])
+                ev_comp[b].record(comp)
+            s_out.wait_event(ev_comp[b])
+            with torch.cuda.stream(s_out):
+                for k, v in self.o_sets[b].items():
+                    self.h_out[b][k].copy_(v, non_blocking=True)
+                ev_out[b].record(s_out)
+        comp.wait_stream(s_in)
+        comp.wait_stream(s_out)
+        t1.record(comp)
         t1.synchronize()
         return t0.elapsed_time(t1)
 
@@ -535,6 +585,20 @@ def cpu_baseline_config(name, m_sample=1024):
     (scaled up)."""
     from oracle import fp8_oracle as O
     from workloads import bf16_bits_normal
+    if name == "tensorwise_256":                 # small enough for the whole step
+        x = bf16_bits_normal(256, 256, seed=0, stream=0)
+        w = bf16_bits_normal(256, 256, seed=0, stream=1)
+        reps = 20
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            qx, qw = O.quantize_tensorwise(x), O.quantize_tensorwise(w)
+            O.f64_to_bf16(O.gemm_tn_f64(O.dequant_tensor(qx["row"], qx["scale_inv"]),
+                                        O.dequant_tensor(qw["row"], qw["scale_inv"])))
+        step_s = (time.perf_counter() - t0) / reps
+        cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+        return {"value": round(2.0 * 256 ** 3 / step_s / 1e12, 6), "unit": "TFLOP/s",
+                "cores": cores, "kind": "oracle", "step_seconds_estimate": round(step_s, 5),
+                "sample": f"the whole oracle step, mean of {reps}"}
     n_rows = {"mxfp8_fprop": 8192, "blockwise_fwd_bwd": 4096, "delayed_step": 8192}[name]
     K = 4096
     if name == "blockwise_fwd_bwd":                # whole 128-row blocks of the column copies
@@ -613,6 +677,20 @@ def run_config(args):
     st = ConfigStep(torch, F, dev, args.workload)
     for _ in range(args.warmup):
         st.run()
+    step = st.run
+    if args.workload == "tensorwise_256":
+        # launch-bound: one step is one replay of a CUDA graph holding its five kernels
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(st.stream)
+        with torch.cuda.stream(side):
+            st.run()
+        st.stream.wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            st.run()
+        step = graph.replay
+        for _ in range(args.warmup):
+            step()
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -621,7 +699,7 @@ def run_config(args):
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(st.stream)
     for _ in range(args.steps):
-        st.run()
+        step()
     t1.record(st.stream)
     if dist is not None:
         dist.barrier()
@@ -656,7 +734,12 @@ def run_config(args):
             "data": "synthetic",
             "config": {"workload": CONFIGS[args.workload], "recipe": st.rec.kind,
                        "parallelism": "replicas" if world > 1 else "single",
-                       "l2": "inputs above L2 (64-128 MB per tensor, eight X_t for delayed)",
+                       "l2": ("inputs fit in L2 and are not flushed: a launch-bound "
+                              "configuration, timed as graph replays"
+                              if args.workload == "tensorwise_256" else
+                              "not flushed: each step touches more than L2 (129 MB): "
+                              "0.26-0.3 GB of inputs, codes and outputs; the delayed step "
+                              "also cycles eight 64 MB X_t"),
                        "gemm_flops_per_step": st.flops},
             "roofline": {"bound": "tensor", "kernel": f"gemm_tn_kernel ({st.rec.kind})",
                          "achieved": round(achieved, 1), "peak": fp8_peak, "unit": "TFLOP/s",
@@ -669,7 +752,7 @@ def run_config(args):
             "e2e": {"value": round(world * st.flops / (ms_e2e / args.steps * 1e-3) / 1e12, 2),
                     "unit": "TFLOP/s", "h2d_bytes_per_step": st.h2d_bytes(),
                     "d2h_bytes_per_step": st.d2h_bytes(),
-                    "copies": "pinned host, serialised with each step"},
+                    "copies": "pinned host, own streams, overlapped with the adjacent steps"},
             "kernels_ms": {k: round(statistics.mean(v), 4) for k, v in per_name.items()},
             "gpu_launches": st.launches * args.steps,
             "clocks": clk,
