@@ -64,8 +64,8 @@ __device__ __forceinline__ uint2 encode8(uint4 v, float s, bool has_nan) {
   uint32_t c[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float a = __fmul_rn(bf16_lo(w[i]), s);
-    const float b = __fmul_rn(bf16_hi(w[i]), s);
+    const float2 ab = __fmul2_rn(make_float2(bf16_lo(w[i]), bf16_hi(w[i])), make_float2(s, s));
+    const float a = ab.x, b = ab.y;
     uint32_t p = cvt_e4m3x2(a, b);
     if (has_nan) {
       p = fix_nan_code(p & 0xFFu, bf16_lo(w[i])) | (fix_nan_code(p >> 8, bf16_hi(w[i])) << 8);
@@ -153,10 +153,20 @@ __device__ __forceinline__ uint32_t cvt_fp8x4(float x0, float x1, float x2, floa
 }
 
 // Two words of packed bf16 (4 values) times s -> one word of 4 codes.
+// Two packed fp32 multiplies, each lane rounded like __fmul_rn (the quantize kernels, which
+// have registers to spare); encode4_scalar is the same arithmetic in four scalar multiplies,
+// for register-bound callers (a packed operand needs an aligned register pair).
 template <int F8 = F8_E4M3>
-__device__ __forceinline__ uint32_t encode4(uint32_t w0, uint32_t w1, float s) {
+__device__ __forceinline__ uint32_t encode4_scalar(uint32_t w0, uint32_t w1, float s) {
   return cvt_fp8x4<F8>(__fmul_rn(bf16_lo(w0), s), __fmul_rn(bf16_hi(w0), s),
                        __fmul_rn(bf16_lo(w1), s), __fmul_rn(bf16_hi(w1), s));
+}
+template <int F8 = F8_E4M3>
+__device__ __forceinline__ uint32_t encode4(uint32_t w0, uint32_t w1, float s) {
+  const float2 s2 = make_float2(s, s);
+  const float2 a = __fmul2_rn(make_float2(bf16_lo(w0), bf16_hi(w0)), s2);
+  const float2 b = __fmul2_rn(make_float2(bf16_lo(w1), bf16_hi(w1)), s2);
+  return cvt_fp8x4<F8>(a.x, a.y, b.x, b.y);
 }
 
 // Give the codes of NaN inputs the NaN code with the input's sign (rare path).

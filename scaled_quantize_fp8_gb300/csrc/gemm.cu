@@ -212,7 +212,7 @@ __device__ __forceinline__ uint32_t quantize_block32(const uint32_t* w, uint8_t*
   const uint32_t sb = mx_scale_byte(mx, &mult);
   uint32_t c[8];
 #pragma unroll
-  for (int q = 0; q < 8; ++q) c[q] = encode4(w[2 * q], w[2 * q + 1], mult);
+  for (int q = 0; q < 8; ++q) c[q] = encode4_scalar(w[2 * q], w[2 * q + 1], mult);
   if (mx > 0x7F80u) {
 #pragma unroll
     for (int q = 0; q < 8; ++q) c[q] = fix_nan4(c[q], w[2 * q], w[2 * q + 1]);

@@ -62,8 +62,9 @@ __device__ __forceinline__ void encode32_store(const float* v, float s, bool has
   uint32_t c[8];
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
-    c[q] = cvt_e4m3x4(__fmul_rn(v[4 * q], s), __fmul_rn(v[4 * q + 1], s),
-                      __fmul_rn(v[4 * q + 2], s), __fmul_rn(v[4 * q + 3], s));
+    const float2 a = __fmul2_rn(make_float2(v[4 * q], v[4 * q + 1]), make_float2(s, s));
+    const float2 b = __fmul2_rn(make_float2(v[4 * q + 2], v[4 * q + 3]), make_float2(s, s));
+    c[q] = cvt_e4m3x4(a.x, a.y, b.x, b.y);
     if (has_nan) {
 #pragma unroll
       for (int k = 0; k < 4; ++k)

@@ -392,13 +392,16 @@ __device__ __forceinline__ void quantize_one_tile(const QuantParams& p, QuantCtl
       }
       // codes of column 2pp (low halves) and 2pp+1 (high halves), 32 rows each
       uint32_t ca[8], cb[8];
+      const float2 sab = make_float2(sa, sb);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const uint32_t x0 = x[4 * j], x1 = x[4 * j + 1], x2 = x[4 * j + 2], x3 = x[4 * j + 3];
-        ca[j] = cvt_fp8x4<F8>(__fmul_rn(bf16_lo(x0), sa), __fmul_rn(bf16_lo(x1), sa),
-                           __fmul_rn(bf16_lo(x2), sa), __fmul_rn(bf16_lo(x3), sa));
-        cb[j] = cvt_fp8x4<F8>(__fmul_rn(bf16_hi(x0), sb), __fmul_rn(bf16_hi(x1), sb),
-                           __fmul_rn(bf16_hi(x2), sb), __fmul_rn(bf16_hi(x3), sb));
+        // one packed multiply a word: (low half x sa, high half x sb)
+        float2 y[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          y[k] = __fmul2_rn(make_float2(bf16_lo(x[4 * j + k]), bf16_hi(x[4 * j + k])), sab);
+        ca[j] = cvt_fp8x4<F8>(y[0].x, y[1].x, y[2].x, y[3].x);
+        cb[j] = cvt_fp8x4<F8>(y[0].y, y[1].y, y[2].y, y[3].y);
       }
       if ((mw & 0x7FFFu) > 0x7F80u || ((mw >> 16) & 0x7FFFu) > 0x7F80u) {   // NaN present
 #pragma unroll
