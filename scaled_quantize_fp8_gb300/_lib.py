@@ -10,6 +10,7 @@ import re
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libfp8lin.so")
 HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "fp8lin.h")
+HEADER_DIR = os.path.dirname(HEADER_PATH)
 
 FP8_OK = 0
 STATUS_NAMES = {0: "FP8_OK", 1: "FP8_ERR_NULL", 2: "FP8_ERR_ALIGN", 3: "FP8_ERR_SHAPE",
@@ -53,6 +54,8 @@ _SIG = {
                                _P, _P, _P]),
     "fp8_linear_fwd": (_I32, [ctypes.POINTER(Recipe), ctypes.POINTER(Tensor),
                               ctypes.POINTER(Tensor), _P, _I32, _P, _P]),
+    "fp8_test_linear_fwd_stalled": (_I32, [ctypes.POINTER(Recipe), ctypes.POINTER(Tensor),
+                                           ctypes.POINTER(Tensor), _P, _P, _P]),
     "fp8_linear_bwd": (_I32, [ctypes.POINTER(Recipe), ctypes.POINTER(Tensor),
                               ctypes.POINTER(Tensor), ctypes.POINTER(Tensor), _P, _P, _I32, _P,
                               _P]),
@@ -76,10 +79,15 @@ _lib = None
 
 
 def header_functions():
-    """Names of every function the public header declares."""
-    text = open(HEADER_PATH).read()
-    return sorted(set(re.findall(r"^\s*(?:fp8_status|size_t|const char \*)\s*(fp8_\w+)\s*\(",
-                                 text, flags=re.M)))
+    """Names of every function the headers in include/ declare (the public ABI and its test
+    hooks)."""
+    names = set()
+    for h in sorted(os.listdir(HEADER_DIR)):
+        if h.endswith(".h"):
+            text = open(os.path.join(HEADER_DIR, h)).read()
+            names |= set(re.findall(r"^\s*(?:fp8_status|size_t|const char \*)\s*(fp8_\w+)\s*\(",
+                                    text, flags=re.M))
+    return sorted(names)
 
 
 def load():

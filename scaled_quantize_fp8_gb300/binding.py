@@ -226,6 +226,20 @@ def linear_fwd(recipe: Recipe, x: QTensor, w: QTensor, y: Optional[torch.Tensor]
     return y
 
 
+def linear_fwd_stalled(recipe: Recipe, x: QTensor, w: QTensor, y: torch.Tensor,
+                       status: torch.Tensor, stream=None):
+    """Test hook (fp8_test_linear_fwd_stalled): fp8_linear_fwd with a pipeline stage that
+    never becomes ready, so the kernel's bounded wait runs out (about two seconds) and it
+    records FP8_ERR_TIMEOUT in `status` (an int32 device word, zeroed by the caller)."""
+    lib = L.load()
+    rc = recipe.c()
+    st = lib.fp8_test_linear_fwd_stalled(ctypes.byref(rc), ctypes.byref(x.c()),
+                                         ctypes.byref(w.c()), _ptr(y), _ptr(status),
+                                         _stream(stream))
+    L.check(st, "fp8_test_linear_fwd_stalled")
+    return y
+
+
 def linear_bwd(recipe: Recipe, dy: QTensor, x: Optional[QTensor], w: Optional[QTensor],
                want_dx=True, want_dw=True, dx=None, dw=None, fp32=False, status=None,
                stream=None):

@@ -5,6 +5,7 @@
 #include <cstring>
 
 #include "internal.cuh"
+#include "fp8lin_test.h"
 
 
 using namespace fp8lin;
@@ -220,7 +221,8 @@ Operand transposed_operand(const fp8_recipe* recipe, const fp8_tensor* t) {
 }
 
 fp8_status run_gemm(int kind, const Operand& a, const Operand& b, int64_t M, int64_t N,
-                    int64_t Kr, void* D, int fp32_out, int32_t* status, cudaStream_t st) {
+                    int64_t Kr, void* D, int fp32_out, int32_t* status, cudaStream_t st,
+                    uint32_t stall_tx = 0) {
   FP8_TRY(check_ptr(a.codes));
   FP8_TRY(check_ptr(b.codes));
   FP8_TRY(check_ptr(D));
@@ -246,6 +248,7 @@ fp8_status run_gemm(int kind, const Operand& a, const Operand& b, int64_t M, int
   g.p.b_fmt = b.fmt;
   g.p.a_mn = a.mn;
   g.p.b_mn = b.mn;
+  g.p.stall_tx = stall_tx;
   switch (kind) {
     case FP8_RECIPE_TENSORWISE:
     case FP8_RECIPE_DELAYED:
@@ -359,6 +362,20 @@ fp8_status fp8_linear_fwd(const fp8_recipe* recipe, const fp8_tensor* x, const f
   const Operand b{w->row, w->row_scale, w->scale_inv, w->role,
                     fmt_of(recipe, w->role)};
   return run_gemm(gemm_kind(recipe), a, b, x->rows, w->rows, x->cols, y, y_fp32, dev_status, stream);
+}
+
+fp8_status fp8_test_linear_fwd_stalled(const fp8_recipe* recipe, const fp8_tensor* x,
+                                       const fp8_tensor* w, void* y, int32_t* dev_status,
+                                       cudaStream_t stream) {
+  FP8_TRY(check_recipe(recipe));
+  FP8_TRY(check_tensor(recipe, x));
+  FP8_TRY(check_tensor(recipe, w));
+  if (x->cols != w->cols) return FP8_ERR_SHAPE;
+  if (dev_status == nullptr) return FP8_ERR_NULL;     // the outcome is only visible there
+  const Operand a{x->row, x->row_scale, x->scale_inv, x->role, fmt_of(recipe, x->role)};
+  const Operand b{w->row, w->row_scale, w->scale_inv, w->role, fmt_of(recipe, w->role)};
+  return run_gemm(gemm_kind(recipe), a, b, x->rows, w->rows, x->cols, y, 0, dev_status, stream,
+                  16u);
 }
 
 fp8_status fp8_linear_bwd(const fp8_recipe* recipe, const fp8_tensor* dy,

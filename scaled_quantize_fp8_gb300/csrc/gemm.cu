@@ -373,6 +373,7 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
         const int n0 = nt * kBN + int(rank) * int(kBRows);
         for (int kb = 0; kb < nk; ++kb) {
           if (!wait_bar(&ctl->empty[s], ph ^ 1u, ctl, p.status)) goto producer_done;
+          const uint32_t stall = (unit == 0 && tile == 0 && kb == 0) ? p.stall_tx : 0u;
           uint8_t* a_dst = sA + s * kTileABytes;
           uint8_t* b_dst = sB + s * G::kTileBBytes;
           if constexpr (CTA2) {
@@ -383,7 +384,7 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
             constexpr uint32_t sf_bytes = MODE == G_MX ? 512u + 1024u : 0u;
             if (leader)
               ptx::mbar_arrive_expect_tx(&ctl->full[s],
-                                         2 * (kTileABytes + G::kTileBBytes + sf_bytes));
+                                         2 * (kTileABytes + G::kTileBBytes + sf_bytes) + stall);
             // a K-major tile is 128 bytes of K x rows; an MN-major one 128 of M (N) x 128 K rows
             if (p.a_mn) ptx::tma_load_2d_pair(a_dst, &tmA, m0, kb * kBKElems, bar);
             else ptx::tma_load_2d_pair(a_dst, &tmA, kb * kBKElems, m0, bar);
@@ -399,7 +400,7 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
                                     2 * (((nb_pair >> 7) + 1) * kblocks128 + kb), bar);
             }
           } else {
-            uint32_t bytes = kTileABytes + G::kTileBBytes;
+            uint32_t bytes = kTileABytes + G::kTileBBytes + stall;
             const bool sfb_hi = (n0 + 128) < p.N;
             if constexpr (MODE == G_MX) bytes += 512u + (sfb_hi ? 1024u : 512u);
             ptx::mbar_arrive_expect_tx(&ctl->full[s], bytes);

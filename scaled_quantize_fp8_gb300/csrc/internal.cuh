@@ -93,6 +93,10 @@ struct GemmParams {
   uint8_t* o_col;           // [N][M] codes (column-wise copy)
   uint8_t* o_col_scale;     // E8M0, tiled atoms of the [N][M] tensor
   int o_v8;                 // all of the above code arrays are 32-byte aligned
+  // Failure-detection test hook (0 otherwise): extra bytes the first stage of the first CTA
+  // (pair) expects, so that stage's barrier never completes and the kernel's bounded waits
+  // run out (fp8_test_linear_fwd_stalled).
+  uint32_t stall_tx;
 };
 
 struct GemmLaunch {

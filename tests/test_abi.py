@@ -127,6 +127,17 @@ def test_linear_fwd_checks(lib):
     assert fwd(ctypes.byref(rb), ctypes.byref(xa), ctypes.byref(wb), 0x1000, 0, None, None) == 4
 
 
+def test_stalled_fwd_hook_checks(lib):
+    """The failure-detection hook validates like fp8_linear_fwd and needs a status word."""
+    r = _rec(kind=L.RECIPE_MXFP8)
+    x, w = _qt(L.RECIPE_MXFP8, 256, 512), _qt(L.RECIPE_MXFP8, 384, 512, 1)
+    hook = lib.fp8_test_linear_fwd_stalled
+    assert hook(ctypes.byref(r), ctypes.byref(x), ctypes.byref(w), 0x1000, None, None) == 1
+    assert hook(ctypes.byref(r), ctypes.byref(x), ctypes.byref(_qt(L.RECIPE_MXFP8, 384, 256)),
+                0x1000, 0x9000, None) == 3                   # K mismatch
+    assert hook(ctypes.byref(r), ctypes.byref(x), ctypes.byref(w), 0, 0x9000, None) == 1
+
+
 def test_linear_bwd_checks(lib):
     r = _rec(kind=L.RECIPE_TENSORWISE)
     dy = _qt(L.RECIPE_TENSORWISE, 256, 384)

@@ -1,0 +1,79 @@
+"""Failure detection on the GPU without a fault: a GEMM whose first pipeline stage never becomes
+ready (the test hook plants 16 bytes that no copy delivers) must come back on its own with
+FP8_ERR_TIMEOUT in the caller's status word. After it, the context is still usable: the next
+GEMMs on the same stream give the oracle's results.
+
+Each stalled launch takes about two seconds, the kernel's wait budget. The hook stalls only
+the first CTA (pair); the other CTAs, and every later launch, run normally."""
+import pytest
+import torch
+
+from helpers import cuda_ok, from_dev_bf16, gemm_bf16_close, to_dev_bf16
+from oracle import fp8_oracle as O
+from workloads import bf16_bits_normal
+
+pytestmark = pytest.mark.gpu
+
+if cuda_ok():
+    import scaled_quantize_fp8_gb300 as F
+    from scaled_quantize_fp8_gb300.binding import linear_fwd_stalled
+
+FP8_ERR_TIMEOUT = 6
+
+
+def _operands(kind, M, N, K, seed):
+    rec = F.Recipe(kind=kind)
+    xb = bf16_bits_normal(M, K, seed=seed)
+    wb = bf16_bits_normal(N, K, seed=seed + 1, sigma=0.02)
+    xq = F.quantize(rec, to_dev_bf16(xb), "activation")
+    wq = F.quantize(rec, to_dev_bf16(wb), "weight")
+    return rec, xb, wb, xq, wq
+
+
+def _oracle_fprop(kind, xb, wb):
+    if kind == "mxfp8":
+        qx, qw = O.quantize_mxfp8(xb, want_col=False), O.quantize_mxfp8(wb, want_col=False)
+        return O.gemm_tn_f64(O.dequant_mx(qx["row"], qx["row_scale"]),
+                             O.dequant_mx(qw["row"], qw["row_scale"]))
+    if kind == "tensorwise":
+        qx, qw = O.quantize_tensorwise(xb), O.quantize_tensorwise(wb)
+        return O.gemm_tn_f64(O.dequant_tensor(qx["row"], qx["scale_inv"]),
+                             O.dequant_tensor(qw["row"], qw["scale_inv"]))
+    qx, qw = O.quantize_blockwise_1x128(xb), O.quantize_blockwise_128x128(wb)
+    return O.gemm_tn_f64(O.dequant_1x128(qx["row"], qx["row_scale_inv"]),
+                         O.dequant_128x128(qw["row"], qw["row_scale_inv"]))
+
+
+# mxfp8: CTA pair with the scale-factor warp; tensorwise: CTA pair, two accumulators;
+# blockwise: single CTA with the per-chunk promotion
+@pytest.mark.parametrize("kind,M,N,K", [("mxfp8", 256, 256, 512), ("tensorwise", 512, 512, 256),
+                                         ("blockwise", 256, 512, 512)])
+def test_stalled_gemm_reports_timeout_and_context_survives(kind, M, N, K):
+    rec, xb, wb, xq, wq = _operands(kind, M, N, K, seed=120)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
+    linear_fwd_stalled(rec, xq, wq, y, status)
+    torch.cuda.synchronize()                     # returns: the kernel gave up on its own
+    assert int(status.item()) == FP8_ERR_TIMEOUT
+    # the stalled pair's tile is left unwritten; with one tile per CTA (pair) here, the
+    # first 128 (single CTA) or 256 (pair) rows x 256 columns stay zero
+    rows = 128 if kind == "blockwise" else 256
+    assert not torch.any(y[:rows, :256].view(torch.int16) != 0)
+
+    # the same stream and context still work: a normal GEMM matches the oracle
+    status2 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y2 = F.linear_fwd(rec, xq, wq, status=status2)
+    torch.cuda.synchronize()
+    assert int(status2.item()) == 0
+    ok, err = gemm_bf16_close(from_dev_bf16(y2), _oracle_fprop(kind, xb, wb))
+    assert ok, err
+
+
+def test_timeout_keeps_the_first_status():
+    """The status word keeps the first nonzero code written to it."""
+    rec, _, _, xq, wq = _operands("mxfp8", 256, 256, 256, seed=121)
+    status = torch.full((1,), 5, dtype=torch.int32, device="cuda")
+    y = torch.zeros((256, 256), dtype=torch.bfloat16, device="cuda")
+    linear_fwd_stalled(rec, xq, wq, y, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 5
