@@ -20,6 +20,14 @@ constexpr int kMxBlock = 32;        // MXFP8 block length
 constexpr int kBwBlock = 128;       // blockwise block length
 
 // First error wins: a device-side condition is recorded once, later ones are dropped.
+// Programmatic dependent launch (no-ops when the kernel was launched without the attribute):
+// let the next kernel in the stream begin launching, and wait until the previous kernel has
+// completed and its writes are visible (before this kernel's first global memory access).
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void report_status(int32_t* st, int32_t code) {
   if (st != nullptr) atomicCAS(st, 0, code);
 }

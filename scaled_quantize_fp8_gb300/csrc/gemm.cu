@@ -327,6 +327,7 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
   const int n_tiles = tiles_m * tiles_n;
   const int nk = (p.K + kBKElems - 1) / kBKElems;
 
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < G::kStages; ++s) {
       ptx::mbar_init(&ctl->full[s], 1);
@@ -353,6 +354,7 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
   if constexpr (CTA2) ptx::cluster_sync();           // peer barriers initialised
   ptx::tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
+  pdl_wait();                      // the previous kernel's writes are visible from here on
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -846,19 +848,14 @@ static cudaError_t launch_mode(const GemmLaunch& g, cudaStream_t st) {
   const int sms = num_sms();
   const int tiles = ((g.p.M + G::kTileM - 1) / G::kTileM) * ((g.p.N + kBN - 1) / kBN);
   const int units = std::max(1, std::min(tiles, CTA2 ? sms / 2 : sms));
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(units * (CTA2 ? 2 : 1)));
-  cfg.blockDim = dim3(gemm_threads<MODE, EPI>());
-  cfg.dynamicSmemBytes = G::kSmemBytes;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CTA2 ? 2 : 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, ma, mb, msfa, msfb, g.p);
+  cudaLaunchAttribute cluster;
+  cluster.id = cudaLaunchAttributeClusterDimension;
+  cluster.val.clusterDim.x = CTA2 ? 2 : 1;
+  cluster.val.clusterDim.y = 1;
+  cluster.val.clusterDim.z = 1;
+  return launch_kernel(kern, dim3(unsigned(units * (CTA2 ? 2 : 1))),
+                       dim3(gemm_threads<MODE, EPI>()), G::kSmemBytes, st, &cluster, ma, mb,
+                       msfa, msfb, g.p);
 }
 
 cudaError_t gemm_launch(const GemmLaunch& g, cudaStream_t st) {

@@ -4,6 +4,7 @@
 #include <atomic>
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 
 #include "fp8lin.h"
@@ -18,6 +19,36 @@ namespace fp8lin {
 bool make_tmap_2d(CUtensorMap_st* map, const void* base, int elem_bytes, int64_t inner,
                   int64_t rows, int box_inner, int box_rows, bool swizzle128);
 int num_sms();      // of the current device
+
+// Programmatic dependent launch: every kernel of the library lets the next kernel in its
+// stream start launching as soon as all of its own CTAs are running, and waits for the kernel
+// before it (griddepcontrol.wait) before its first global memory access. The next kernel's
+// launch and prologue (barrier setup, TMEM allocation) then overlap this one's tail.
+// Environment FP8LIN_PDL=0 turns the launch attribute off (read once per process).
+bool pdl_enabled();
+
+// cudaLaunchKernelEx with the programmatic-serialisation attribute (when enabled) plus up to
+// one extra attribute (a cluster shape).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t st, const cudaLaunchAttribute* extra, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  if (extra != nullptr) attr[n++] = *extra;
+  if (pdl_enabled()) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Run set() (a per-device, idempotent setup such as cudaFuncSetAttribute) the first time a
 // device reaches this flag word; later calls on that device skip it. Thread-safe: concurrent

@@ -91,6 +91,8 @@ __device__ __forceinline__ uint32_t block_max_256(uint32_t v, uint32_t* red) {
 
 template <int MODE>
 __global__ void __launch_bounds__(256) quantize_master_kernel(const MasterParams p) {
+  pdl_launch_dependents();
+  pdl_wait();
   extern __shared__ float4 msm_raw[];
   float* tile = reinterpret_cast<float*>(msm_raw);
   __shared__ uint32_t red[8];
@@ -201,6 +203,8 @@ __global__ void __launch_bounds__(256) quantize_master_kernel(const MasterParams
 __global__ void __launch_bounds__(512) amax_partial_f32_kernel(const float* __restrict__ x,
                                                                int64_t n_vec,
                                                                uint32_t* __restrict__ part) {
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ uint32_t red[16];
   uint32_t m = 0;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
@@ -222,6 +226,8 @@ __global__ void __launch_bounds__(512) amax_partial_f32_kernel(const float* __re
 // Delayed: reduce the per-tile 31-bit maxima into the tensor's amax.
 __global__ void __launch_bounds__(1024) amax_finalize_f32_kernel(const uint32_t* __restrict__ part,
                                                                  int n, float* __restrict__ amax) {
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ uint32_t red[32];
   uint32_t m = 0;
   for (int i = threadIdx.x; i < n; i += blockDim.x) m = max(m, part[i]);
@@ -237,6 +243,8 @@ __global__ void __launch_bounds__(1024) amax_finalize_f32_kernel(const uint32_t*
 }
 
 __global__ void master_empty_kernel(float* amax, float* scale, float* scale_inv, int margin) {
+  pdl_launch_dependents();
+  pdl_wait();
   if (amax) *amax = 0.0f;
   if (scale) {
     float si;
@@ -255,8 +263,8 @@ static cudaError_t launch_master(MasterParams p, cudaStream_t st) {
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(kMasterSmem));
   });
   if (ae != cudaSuccess) return ae;
-  quantize_master_kernel<MODE><<<p.tiles_r * p.tiles_c, 256, kMasterSmem, st>>>(p);
-  return cudaGetLastError();
+  return launch_kernel(quantize_master_kernel<MODE>, dim3(unsigned(p.tiles_r * p.tiles_c)),
+                       dim3(256), kMasterSmem, st, nullptr, p);
 }
 
 cudaError_t quantize_master_launch(int kind, int margin, const float* x, int64_t R, int64_t C,
@@ -264,10 +272,9 @@ cudaError_t quantize_master_launch(int kind, int margin, const float* x, int64_t
                                    void* workspace, cudaStream_t st) {
   if (R == 0 || C == 0) {
     if (kind == FP8_RECIPE_TENSORWISE || kind == FP8_RECIPE_DELAYED) {
-      master_empty_kernel<<<1, 1, 0, st>>>(out->amax,
-                                           kind == FP8_RECIPE_TENSORWISE ? out->scale : nullptr,
-                                           out->scale_inv, margin);
-      return cudaGetLastError();
+      return launch_kernel(master_empty_kernel, dim3(1), dim3(1), 0, st, nullptr, out->amax,
+                           kind == FP8_RECIPE_TENSORWISE ? out->scale : nullptr, out->scale_inv,
+                           margin);
     }
     return cudaSuccess;
   }
@@ -287,8 +294,8 @@ cudaError_t quantize_master_launch(int kind, int margin, const float* x, int64_t
       // as many partials as the bf16 path uses, so fp8_workspace_bytes covers both
       const int ctas = amax_partial_ctas(R * C / 8);
       uint32_t* part = reinterpret_cast<uint32_t*>(workspace);
-      amax_partial_f32_kernel<<<ctas, 512, 0, st>>>(x, R * C / 4, part);
-      cudaError_t e = cudaGetLastError();
+      const cudaError_t e = launch_kernel(amax_partial_f32_kernel, dim3(ctas), dim3(512), 0, st,
+                                          nullptr, x, R * C / 4, part);
       if (e != cudaSuccess) return e;
       p.part_in = part;
       p.n_part_in = ctas;
@@ -302,8 +309,9 @@ cudaError_t quantize_master_launch(int kind, int margin, const float* x, int64_t
       p.part_out = reinterpret_cast<uint32_t*>(workspace);
       cudaError_t e = launch_master<M_TENSOR>(p, st);
       if (e != cudaSuccess) return e;
-      amax_finalize_f32_kernel<<<1, 1024, 0, st>>>(p.part_out, p.tiles_r * p.tiles_c, out->amax);
-      return cudaGetLastError();
+      return launch_kernel(amax_finalize_f32_kernel, dim3(1), dim3(1024), 0, st, nullptr,
+                           static_cast<const uint32_t*>(p.part_out), p.tiles_r * p.tiles_c,
+                           out->amax);
     }
     case FP8_RECIPE_MXFP8:
       return launch_master<M_MX>(p, st);

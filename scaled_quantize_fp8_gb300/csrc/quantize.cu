@@ -496,12 +496,14 @@ __global__ void __launch_bounds__(256, quant_ctas_per_sm<MODE, EPI>())
   const int tiles_r = int((p.R + 127) >> 7);
   const int n_tiles = tiles_r * p.tiles_c;
 
+  pdl_launch_dependents();
   if (t == 0) {
     for (int b = 0; b < kQBufs; ++b) ptx::mbar_init(&S.bar[b], 1);
     S.abort_flag = 0;
     ptx::fence_mbar_init();
   }
   __syncthreads();
+  pdl_wait();                      // the previous kernel's writes are visible from here on
 
   // per-tensor scale once per CTA: tensorwise from the amax partials, delayed from memory
   float s_tensor = 1.0f;
@@ -566,6 +568,8 @@ __global__ void __launch_bounds__(256, quant_ctas_per_sm<MODE, EPI>())
 __global__ void __launch_bounds__(512) amax_partial_kernel(const uint16_t* __restrict__ x,
                                                            int64_t n_vec,
                                                            uint32_t* __restrict__ part) {
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ uint32_t red[16];
   uint32_t m = 0;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
@@ -590,6 +594,8 @@ __global__ void __launch_bounds__(512) amax_partial_kernel(const uint16_t* __res
 // Delayed recipe: reduce the per-tile partials written by the cast into the tensor's amax.
 __global__ void __launch_bounds__(1024) amax_finalize_kernel(const uint32_t* __restrict__ part,
                                                              int n, float* __restrict__ amax) {
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ uint32_t red[32];
   uint32_t m = 0;
   for (int i = threadIdx.x; i < n; i += blockDim.x) m = max(m, part[i]);
@@ -607,6 +613,8 @@ __global__ void __launch_bounds__(1024) amax_finalize_kernel(const uint32_t* __r
 // Empty tensor: amax 0; tensorwise also writes scale/scale_inv for amax 0.
 __global__ void empty_scalars_kernel(float* amax, float* scale, float* scale_inv, int margin,
                                      float fmax) {
+  pdl_launch_dependents();
+  pdl_wait();
   if (amax) *amax = 0.0f;
   if (scale) {
     float si;
@@ -622,6 +630,8 @@ __global__ void __launch_bounds__(1024) amax_history_update_kernel(
     float* __restrict__ hist, int32_t* __restrict__ head, int len,
     const float* __restrict__ amax_new, float* __restrict__ scale,
     float* __restrict__ scale_inv, int margin, float fmax, int algo) {
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ float red[32];
   __shared__ int nan_seen;
   const int h = *head;
@@ -686,8 +696,8 @@ static cudaError_t launch_tiles(QuantParams p, cudaStream_t st) {
   });
   if (ae != cudaSuccess) return ae;
   const int grid = std::max(1, std::min(n, num_sms() * quant_ctas_per_sm<MODE, EPI>()));
-  quantize_tile_kernel<MODE, EPI, F8><<<grid, 256, smem, st>>>(map, p);
-  return cudaGetLastError();
+  return launch_kernel(quantize_tile_kernel<MODE, EPI, F8>, dim3(grid), dim3(256), smem, st,
+                       nullptr, map, p);
 }
 
 cudaError_t quantize_launch(int kind, int role, int fmt, bool pow2, int margin,
@@ -710,11 +720,9 @@ cudaError_t quantize_launch(int kind, int role, int fmt, bool pow2, int margin,
   p.margin = margin;
   if (R == 0 || C == 0) {
     if (kind == FP8_RECIPE_TENSORWISE || kind == FP8_RECIPE_DELAYED) {
-      empty_scalars_kernel<<<1, 1, 0, st>>>(out->amax,
-                                            kind == FP8_RECIPE_TENSORWISE ? out->scale : nullptr,
-                                            out->scale_inv, margin,
-                                            e5 ? fp8_max<F8_E5M2>() : fp8_max<F8_E4M3>());
-      return cudaGetLastError();
+      return launch_kernel(empty_scalars_kernel, dim3(1), dim3(1), 0, st, nullptr, out->amax,
+                           kind == FP8_RECIPE_TENSORWISE ? out->scale : nullptr, out->scale_inv,
+                           margin, e5 ? fp8_max<F8_E5M2>() : fp8_max<F8_E4M3>());
     }
     return cudaSuccess;
   }
@@ -723,8 +731,8 @@ cudaError_t quantize_launch(int kind, int role, int fmt, bool pow2, int margin,
       const int64_t n_vec = R * C / 8;
       const int ctas = amax_partial_ctas(n_vec);
       uint32_t* part = reinterpret_cast<uint32_t*>(workspace);
-      amax_partial_kernel<<<ctas, 512, 0, st>>>(x, n_vec, part);
-      cudaError_t e = cudaGetLastError();
+      const cudaError_t e = launch_kernel(amax_partial_kernel, dim3(ctas), dim3(512), 0, st,
+                                          nullptr, x, n_vec, part);
       if (e != cudaSuccess) return e;
       p.part_in = part;
       p.n_part_in = ctas;
@@ -741,8 +749,8 @@ cudaError_t quantize_launch(int kind, int role, int fmt, bool pow2, int margin,
                          : launch_tiles<Q_TENSOR, EPI_NONE>(p, st);
       if (e != cudaSuccess) return e;
       const int n = int((R + 127) / 128) * p.tiles_c;
-      amax_finalize_kernel<<<1, 1024, 0, st>>>(p.part_out, n, out->amax);
-      return cudaGetLastError();
+      return launch_kernel(amax_finalize_kernel, dim3(1), dim3(1024), 0, st, nullptr,
+                           static_cast<const uint32_t*>(p.part_out), n, out->amax);
     }
     case FP8_RECIPE_MXFP8:
       if (e5) return cudaErrorInvalidValue;
@@ -800,9 +808,8 @@ cudaError_t dgelu_quantize_launch(const uint16_t* da, const fp8_tensor* h_q, int
 cudaError_t amax_update_launch(float* hist, int32_t* head, int len, const float* amax_new,
                                float* scale, float* scale_inv, int margin, float fmax,
                                int algo, cudaStream_t st) {
-  amax_history_update_kernel<<<1, 1024, 0, st>>>(hist, head, len, amax_new, scale, scale_inv,
-                                                 margin, fmax, algo);
-  return cudaGetLastError();
+  return launch_kernel(amax_history_update_kernel, dim3(1), dim3(1024), 0, st, nullptr, hist,
+                       head, len, amax_new, scale, scale_inv, margin, fmax, algo);
 }
 
 }  // namespace fp8lin

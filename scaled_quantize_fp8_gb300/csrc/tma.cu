@@ -1,5 +1,6 @@
 // Host-side TMA tensor-map construction (the driver entry point is fetched through the
 // runtime, so the library does not link libcuda directly).
+#include <cstdlib>
 #include <cuda.h>
 
 #include "internal.cuh"
@@ -42,6 +43,14 @@ bool make_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, int64_t in
                          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("FP8LIN_PDL");
+    return !(v != nullptr && v[0] == '0' && v[1] == '\0');
+  }();
+  return on;
 }
 
 int num_sms() {
