@@ -54,6 +54,9 @@ _SIG = {
                                _P, _P, _P]),
     "fp8_linear_fwd": (_I32, [ctypes.POINTER(Recipe), ctypes.POINTER(Tensor),
                               ctypes.POINTER(Tensor), _P, _I32, _P, _P]),
+    "fp8_test_quantize_stalled": (_I32, [ctypes.POINTER(Recipe), _P, _I64, _I64, _I32, _I32,
+                                         _I32, ctypes.POINTER(Tensor), _P, ctypes.c_size_t,
+                                         _P, _P]),
     "fp8_test_linear_fwd_stalled": (_I32, [ctypes.POINTER(Recipe), ctypes.POINTER(Tensor),
                                            ctypes.POINTER(Tensor), _P, _P, _P]),
     "fp8_linear_bwd": (_I32, [ctypes.POINTER(Recipe), ctypes.POINTER(Tensor),

@@ -226,6 +226,24 @@ def linear_fwd(recipe: Recipe, x: QTensor, w: QTensor, y: Optional[torch.Tensor]
     return y
 
 
+def quantize_stalled(recipe: Recipe, x: torch.Tensor, role: str, out: QTensor,
+                     status: torch.Tensor, stream=None):
+    """Test hook (fp8_test_quantize_stalled): fp8_quantize with CTA 0's first tile never
+    arriving, so its bounded wait runs out (about two seconds) and it records
+    FP8_ERR_TIMEOUT in `status` (an int32 device word, zeroed by the caller)."""
+    lib = L.load()
+    rows, cols = x.shape
+    rc = recipe.c()
+    need = int(lib.fp8_workspace_bytes(ctypes.byref(rc), rows, cols))
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    ct = out.c()
+    st = lib.fp8_test_quantize_stalled(ctypes.byref(rc), _ptr(x), rows, cols, ROLES[role], 1, 1,
+                                       ctypes.byref(ct), _ptr(ws), ws.numel(), _ptr(status),
+                                       _stream(stream))
+    L.check(st, "fp8_test_quantize_stalled")
+    return out
+
+
 def linear_fwd_stalled(recipe: Recipe, x: QTensor, w: QTensor, y: torch.Tensor,
                        status: torch.Tensor, stream=None):
     """Test hook (fp8_test_linear_fwd_stalled): fp8_linear_fwd with a pipeline stage that

@@ -105,10 +105,11 @@ size_t fp8_workspace_bytes(const fp8_recipe* recipe, int64_t rows, int64_t cols)
   return quantize_workspace_bytes(recipe->kind, rows, cols);
 }
 
-fp8_status fp8_quantize(const fp8_recipe* recipe, const void* x_bf16, int64_t rows, int64_t cols,
-                        int32_t role, int32_t want_row, int32_t want_col, fp8_tensor* out,
-                        void* workspace, size_t ws_bytes, int32_t* dev_status,
-                        cudaStream_t stream) {
+namespace {
+fp8_status quantize_impl(const fp8_recipe* recipe, const void* x_bf16, int64_t rows,
+                         int64_t cols, int32_t role, int32_t want_row, int32_t want_col,
+                         fp8_tensor* out, void* workspace, size_t ws_bytes, int32_t* dev_status,
+                         cudaStream_t stream, uint32_t stall_tx) {
   FP8_TRY(check_recipe(recipe));
   if (out == nullptr) return FP8_ERR_NULL;
   if (role < FP8_ROLE_ACTIVATION || role > FP8_ROLE_GRAD) return FP8_ERR_UNSUPPORTED;
@@ -140,7 +141,25 @@ fp8_status fp8_quantize(const fp8_recipe* recipe, const void* x_bf16, int64_t ro
                                      recipe->power_2_scales != 0, recipe->margin,
                                      reinterpret_cast<const uint16_t*>(x_bf16), rows, cols,
                                      want_row != 0, want_col != 0, col_bf16, out, workspace,
-                                     dev_status, stream));
+                                     dev_status, stream, stall_tx));
+}
+}  // namespace
+
+fp8_status fp8_quantize(const fp8_recipe* recipe, const void* x_bf16, int64_t rows, int64_t cols,
+                        int32_t role, int32_t want_row, int32_t want_col, fp8_tensor* out,
+                        void* workspace, size_t ws_bytes, int32_t* dev_status,
+                        cudaStream_t stream) {
+  return quantize_impl(recipe, x_bf16, rows, cols, role, want_row, want_col, out, workspace,
+                       ws_bytes, dev_status, stream, 0u);
+}
+
+fp8_status fp8_test_quantize_stalled(const fp8_recipe* recipe, const void* x_bf16, int64_t rows,
+                                     int64_t cols, int32_t role, int32_t want_row,
+                                     int32_t want_col, fp8_tensor* out, void* workspace,
+                                     size_t ws_bytes, int32_t* dev_status, cudaStream_t stream) {
+  if (dev_status == nullptr) return FP8_ERR_NULL;     // the outcome is only visible there
+  return quantize_impl(recipe, x_bf16, rows, cols, role, want_row, want_col, out, workspace,
+                       ws_bytes, dev_status, stream, 16u);
 }
 
 fp8_status fp8_quantize_master(const fp8_recipe* recipe, const float* w_f32, int64_t rows,

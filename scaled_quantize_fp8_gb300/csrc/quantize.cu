@@ -51,6 +51,9 @@ struct QuantParams {
   uint16_t* y_bf16;           // GELU: a = gelu(h) in bf16; DGELU: dh in bf16 (optional)
   uint8_t* aux_row;           // GELU: h row codes; DGELU: h row codes (read)
   uint8_t* aux_scale;         // GELU: h row E8M0 (written); DGELU: h row E8M0 (read)
+  // Failure-detection test hook (0 otherwise): extra bytes CTA 0's first tile expects, so its
+  // barrier never completes and the bounded wait runs out (fp8_test_quantize_stalled).
+  uint32_t stall_tx;
 };
 
 // Max of the 15-bit magnitudes of the eight bf16 in a vector.
@@ -529,7 +532,7 @@ __global__ void __launch_bounds__(256, quant_ctas_per_sm<MODE, EPI>())
   auto issue = [&](int tile_id, int b) {
     const int tr = tile_id / p.tiles_c, tc = tile_id % p.tiles_c;
     uint8_t* dst = tiles + b * kQTileBytes;
-    ptx::mbar_arrive_expect_tx(&S.bar[b], kQTileBytes);
+    ptx::mbar_arrive_expect_tx(&S.bar[b], kQTileBytes + (tile_id == 0 ? p.stall_tx : 0u));
     ptx::tma_load_2d(dst, &tmX, tc * kTile, tr * kTile, &S.bar[b]);
     ptx::tma_load_2d(dst + 16384, &tmX, tc * kTile + 64, tr * kTile, &S.bar[b]);
   };
@@ -703,11 +706,12 @@ static cudaError_t launch_tiles(QuantParams p, cudaStream_t st) {
 cudaError_t quantize_launch(int kind, int role, int fmt, bool pow2, int margin,
                             const uint16_t* x, int64_t R, int64_t C, bool want_row,
                             bool want_col, bool col_bf16, fp8_tensor* out, void* workspace,
-                            int32_t* status, cudaStream_t st) {
+                            int32_t* status, cudaStream_t st, uint32_t stall_tx) {
   const bool e5 = fmt == F8_E5M2;
   QuantParams p{};
   p.pow2 = pow2 && kind == FP8_RECIPE_BLOCKWISE;
   p.status = status;
+  p.stall_tx = stall_tx;
   p.col_bf16 = col_bf16;
   p.x = x;
   p.R = R;

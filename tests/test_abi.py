@@ -138,6 +138,17 @@ def test_stalled_fwd_hook_checks(lib):
     assert hook(ctypes.byref(r), ctypes.byref(x), ctypes.byref(w), 0, 0x9000, None) == 1
 
 
+def test_stalled_quantize_hook_checks(lib):
+    """The quantize hook validates like fp8_quantize and needs a status word."""
+    r = _rec(kind=L.RECIPE_MXFP8)
+    out = _tensor()
+    hook = lib.fp8_test_quantize_stalled
+    assert hook(ctypes.byref(r), 0x1000, 256, 256, 0, 1, 1, ctypes.byref(out), None, 0, None,
+                None) == 1
+    assert hook(ctypes.byref(r), 0x1000, 200, 256, 0, 1, 1, ctypes.byref(out), None, 0, 0x9000,
+                None) == 3                                     # rows not a multiple of 128
+
+
 def test_linear_bwd_checks(lib):
     r = _rec(kind=L.RECIPE_TENSORWISE)
     dy = _qt(L.RECIPE_TENSORWISE, 256, 384)

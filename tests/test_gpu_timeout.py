@@ -1,10 +1,12 @@
-"""Failure detection on the GPU without a fault: a GEMM whose first pipeline stage never becomes
-ready (the test hook plants 16 bytes that no copy delivers) must come back on its own with
-FP8_ERR_TIMEOUT in the caller's status word. After it, the context is still usable: the next
-GEMMs on the same stream give the oracle's results.
+"""Failure detection on the GPU without a fault. A GEMM whose first pipeline stage never becomes
+ready, or a quantize whose first tile never arrives, must come back on its own with
+FP8_ERR_TIMEOUT in the caller's status word. The test hooks plant 16 bytes that no copy
+delivers. After it, the context is still usable: the next calls on the same stream give the
+oracle's results.
 
 Each stalled launch takes about two seconds, the kernel's wait budget. The hook stalls only
 the first CTA (pair); the other CTAs, and every later launch, run normally."""
+import numpy as np
 import pytest
 import torch
 
@@ -16,7 +18,7 @@ pytestmark = pytest.mark.gpu
 
 if cuda_ok():
     import scaled_quantize_fp8_gb300 as F
-    from scaled_quantize_fp8_gb300.binding import linear_fwd_stalled
+    from scaled_quantize_fp8_gb300.binding import linear_fwd_stalled, quantize_stalled
 
 FP8_ERR_TIMEOUT = 6
 
@@ -77,3 +79,32 @@ def test_timeout_keeps_the_first_status():
     linear_fwd_stalled(rec, xq, wq, y, status)
     torch.cuda.synchronize()
     assert int(status.item()) == 5
+
+
+@pytest.mark.parametrize("kind", ["mxfp8", "tensorwise", "delayed", "blockwise"])
+def test_stalled_quantize_reports_timeout_and_context_survives(kind):
+    rec = F.Recipe(kind=kind)
+    R, C = 1024, 512
+    xb = bf16_bits_normal(R, C, seed=122)
+    x = to_dev_bf16(xb)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q = F.empty_qtensor(rec, R, C, "activation")
+    quantize_stalled(rec, x, "activation", q, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == FP8_ERR_TIMEOUT
+
+    # the next quantize on the same stream is bit-exact
+    status2 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q2 = F.quantize(rec, x, "activation", status=status2)
+    torch.cuda.synchronize()
+    assert int(status2.item()) == 0
+    if kind == "mxfp8":
+        ref = O.quantize_mxfp8(xb)
+    elif kind == "tensorwise":
+        ref = O.quantize_tensorwise(xb)
+    elif kind == "delayed":
+        ref = O.DelayedScaling(16).quantize(xb)          # scale 1 from a fresh history
+    else:
+        ref = O.quantize_blockwise_1x128(xb)
+    assert np.array_equal(q2.row.cpu().numpy(), ref["row"])
+    assert np.array_equal(q2.col.cpu().numpy(), ref["col"])
