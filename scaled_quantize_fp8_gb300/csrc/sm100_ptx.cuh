@@ -202,9 +202,12 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
                ::: "memory");
 }
+// Arrive on an mbarrier of another CTA of the cluster with the default (CTA-scope release)
+// semantics. The callers signal that their tcgen05 reads have completed (tcgen05.wait::ld,
+// then tcgen05.fence::before_thread_sync), which needs no cluster-wide memory fence; a
+// .release.cluster arrive would add one to every call.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 // TMA load into this CTA's shared memory, completion counted on an mbarrier that may live in
 // either CTA of the pair (cluster address).

@@ -46,21 +46,20 @@ def _oracle_fprop(kind, xb, wb):
                          O.dequant_128x128(qw["row"], qw["row_scale_inv"]))
 
 
-# mxfp8: CTA pair with the scale-factor warp; tensorwise: CTA pair, two accumulators;
-# blockwise: single CTA with the per-chunk promotion
-@pytest.mark.parametrize("kind,M,N,K", [("mxfp8", 256, 256, 512), ("tensorwise", 512, 512, 256),
-                                         ("blockwise", 256, 512, 512)])
-def test_stalled_gemm_reports_timeout_and_context_survives(kind, M, N, K):
+# mxfp8: CTA pair with the scale-factor warp (256 x 256 tiles); tensorwise: CTA pair, two
+# accumulators; blockwise: single CTA with the per-chunk promotion (128 x 256 tiles)
+@pytest.mark.parametrize("kind,M,N,K,tile", [("mxfp8", 256, 256, 512, (256, 256)),
+                                              ("tensorwise", 512, 512, 256, (256, 256)),
+                                              ("blockwise", 256, 512, 512, (128, 256))])
+def test_stalled_gemm_reports_timeout_and_context_survives(kind, M, N, K, tile):
     rec, xb, wb, xq, wq = _operands(kind, M, N, K, seed=120)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     y = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
     linear_fwd_stalled(rec, xq, wq, y, status)
     torch.cuda.synchronize()                     # returns: the kernel gave up on its own
     assert int(status.item()) == FP8_ERR_TIMEOUT
-    # the stalled pair's tile is left unwritten; with one tile per CTA (pair) here, the
-    # first 128 (single CTA) or 256 (pair) rows x 256 columns stay zero
-    rows = 128 if kind == "blockwise" else 256
-    assert not torch.any(y[:rows, :256].view(torch.int16) != 0)
+    # the stalled CTA (pair) has one tile here, its first, which stays zero
+    assert not torch.any(y[:tile[0], :tile[1]].view(torch.int16) != 0)
 
     # the same stream and context still work: a normal GEMM matches the oracle
     status2 = torch.zeros(1, dtype=torch.int32, device="cuda")
