@@ -557,7 +557,10 @@ __global__ void __launch_bounds__(256, quant_ctas_per_sm<MODE, EPI>())
     if (!quant_wait(S, b, uint32_t(i / kQBufs) & 1u, p.status)) break;
     uint8_t* buf = tiles + b * kQTileBytes;
     quantize_one_tile<MODE, EPI, F8>(p, S, buf, buf, table, tile, s_tensor, tensor_nan);
-    __syncthreads();                                 // buffer b is refilled next iteration
+    // buffer b is refilled by TMA next iteration: per-tensor and 128x128 scales wrote their
+    // row codes into it with ordinary stores, which must be ordered before the async copy
+    if constexpr (uses_code_tile<MODE>()) ptx::fence_proxy_async_smem();
+    __syncthreads();
   }
   if (*reinterpret_cast<volatile int*>(&S.abort_flag)) {
     const uint64_t t0 = ptx::clock64_();             // let the outstanding copies land
