@@ -28,6 +28,11 @@ static_assert(kDgeluEntries * 4 <= int(kDgeluTableBytes), "gelu' table size");
 __device__ __forceinline__ uint32_t bf16_rn_bits(float f) {
   return uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(f)));
 }
+// Two floats rounded to bf16 in one conversion (low half = a), the same rounding as above.
+__device__ __forceinline__ uint32_t bf16x2_rn_bits(float a, float b) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
 
 // E4M3 code pair -> two floats (exact, through the hardware f16x2 conversion).
 __device__ __forceinline__ float2 e4m3x2_to_f2(uint16_t codes) {
@@ -158,7 +163,7 @@ __device__ __forceinline__ uint32_t dgelu_bf16x2(const void* table, uint32_t da,
                              dgelu_table_lookup(table, __fmul_rn(hv.x, hs)));
   const float d1 = __fmul_rn(__uint_as_float(da & 0xFFFF0000u),
                              dgelu_table_lookup(table, __fmul_rn(hv.y, hs)));
-  return bf16_rn_bits(d0) | (bf16_rn_bits(d1) << 16);
+  return bf16x2_rn_bits(d0, d1);
 }
 
 // gelu'(h) as the standalone kernels define it: 1/2 at h = +-0, gelu_grad_f32 elsewhere (the
@@ -192,7 +197,7 @@ static __device__ __noinline__ uint32_t dgelu_bf16x2_direct(uint32_t da, uint32_
   const float d0 = __fmul_rn(__uint_as_float(da << 16), gelu_grad_value(__fmul_rn(hv.x, hs)));
   const float d1 =
       __fmul_rn(__uint_as_float(da & 0xFFFF0000u), gelu_grad_value(__fmul_rn(hv.y, hs)));
-  return bf16_rn_bits(d0) | (bf16_rn_bits(d1) << 16);
+  return bf16x2_rn_bits(d0, d1);
 }
 
 }  // namespace fp8lin

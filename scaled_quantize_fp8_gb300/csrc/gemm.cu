@@ -261,7 +261,7 @@ __device__ __forceinline__ void mlp_epilogue(const GemmParams& p, const uint32_t
           const uint32_t c = hw[k >> 1] >> (16 * (k & 1));
           const float d0 = __fmul_rn(bf16_lo(w[k]), row[c & 0xFFu]);
           const float d1 = __fmul_rn(bf16_hi(w[k]), row[(c >> 8) & 0xFFu]);
-          w[k] = bf16_rn_bits(d0) | (bf16_rn_bits(d1) << 16);
+          w[k] = bf16x2_rn_bits(d0, d1);
         }
       } else {
         const float hs = sb == 0xFFu ? __uint_as_float(0x7FC00000u) : exp2i(int(sb) - 127);
