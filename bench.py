@@ -15,6 +15,11 @@ from pinned host memory and every result (y, dX, dW1, dW2) copied back inside th
 uploads and downloads on their own streams overlapping the neighbouring steps' compute.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload mlp|mxfp8_fprop|blockwise_fwd_bwd|delayed_step|tensorwise_256]
+
+`--workload` times one of the smaller configurations instead (MXFP8 quantize + fprop;
+blockwise quantize + fprop, dgrad and wgrad at 4096^3; a delayed-scaling step with its amax
+history; a 256^3 tensorwise step replayed as a CUDA graph), with the same JSON contract.
 
 `--impl reference` times the CPU oracle (a deliberately slow, plain implementation) on a
 bounded sample of the same workload and reports the same metric.
@@ -46,7 +51,7 @@ FP8_OVER_BF16 = 2.0                                   # nominal dense fp8 / bf16
 # step's four such launches in one capture of `ncu --metrics dram__bytes_read.sum,
 # dram__bytes_write.sum -k regex:gemm_tn_kernel -s 4 -c 4 python bench.py --profile
 # gemm_mx_mlp --steps 2`. Reset to None whenever that kernel changes.
-GEMM_TRAFFIC_BYTES = 578.8e6
+GEMM_TRAFFIC_BYTES = 581.8e6
 
 
 def peaks():
