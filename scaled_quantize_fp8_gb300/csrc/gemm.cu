@@ -1,28 +1,43 @@
 // Scaled FP8 GEMMs of the FP8 linear layer on the sm_103a tensor core (tcgen05 + TMEM + TMA).
 //
 // Every GEMM of the layer is "TN": D[M][N] = sum_k A[M][K] * B[N][K] with both operands
-// K-major, because the column-wise FP8 copies are physically transposed (fprop X.W^T from
-// the row copies, dgrad dY.(W^T)^T from dY's row copy and W's column copy, wgrad
-// (dY^T).(X^T)^T from the two column copies). Scaling, per recipe of the Megatron Core
-// "Low-Precision Training Guide" (Recipe Reference):
+// K-major, because the column-wise FP8 copies are physically transposed:
+//   fprop   X.W^T from the row copies;
+//   dgrad   dY.(W^T)^T from dY's row copy and W's column copy;
+//   wgrad   (dY^T).(X^T)^T from the two column copies.
+// A per-tensor or 128x128 operand whose column copy was not made is read MN-major from its
+// row copy instead.
+//
+// Scaling, per recipe of the Megatron Core "Low-Precision Training Guide" (Recipe Reference):
 //   G_TENSOR  delayed / tensorwise: fp32 accumulation of the raw codes, times
 //             s_inv(A) * s_inv(B) in the epilogue.
-//   G_MX      mxfp8: the tensor core applies the E8M0 scale of every 32-wide K block of A
-//             and B during accumulation (tcgen05.mma kind::mxf8f6f4.block_scale).
-//   G_BLOCK   blockwise: each 128-wide K chunk is accumulated alone into TMEM; epilogue
+//   G_MX      mxfp8 (and power-of-two blockwise): the tensor core applies the E8M0 scale of
+//             every 32-wide K block of A and B during accumulation
+//             (tcgen05.mma kind::mxf8f6f4.block_scale).
+//   G_BLOCK   blockwise: each 128-wide K chunk is accumulated alone into TMEM. Epilogue
 //             warps promote it into fp32 registers times s_inv(A row, chunk) * s_inv(B, chunk)
-//             (B: 128x128 tile scale, or per-row 1x128 scale for wgrad).
+//             (B: the 128x128 tile scale, or the per-row 1x128 scale for wgrad).
 //   G_BF16    bf16 x bf16 (wgrad with --fp8-wgrad off).
 //
-// Structure: a persistent kernel, one CTA per SM, 128 x 256 output tiles handed out
-// round-robin. Warp 0 streams A/B (and MX scale) tiles with TMA into a 4-stage shared-memory
-// ring; warp 1 allocates TMEM and issues the MMAs (one thread); warps 2..9 drain TMEM,
-// scale, round to bf16 and store. Accumulators are double-buffered in TMEM (512 columns) so
-// a tile's epilogue overlaps the next tile's main loop (MX keeps one accumulator buffer and
-// uses the remaining columns for the scale factors; its epilogue frees TMEM as soon as it
-// has read it). Every barrier wait has a clock budget; on expiry the kernel records
-// FP8_ERR_TIMEOUT in the caller's status word, lets in-flight copies land, frees TMEM and
-// returns.
+// Structure: a persistent kernel. One CTA pair (cluster of two, cta_group::2) per two SMs
+// runs 256 x 256 tiles; blockwise, and problems with one 128-row half, use one CTA per SM on
+// 128 x 256 tiles. Tiles come in a grouped order (16 M tiles per N step).
+//   warp 0        streams A/B tiles (and MX scale atoms) with TMA into a 4-6 stage ring.
+//   warp 1        allocates TMEM; one thread of the leader CTA issues the MMAs.
+//   epilogue      warps 2.. drain TMEM, scale, round to bf16 and store. There are 8 of them,
+//                 or 16 for blockwise and the fused MLP epilogues (GeLU / dGeLU with MXFP8
+//                 quantisation of their outputs).
+//   MXFP8 adds    a warp that copies each stage's scale factors into TMEM.
+// Accumulators are double-buffered in TMEM (512 columns), so a tile's epilogue overlaps the
+// next tile's main loop. MXFP8 keeps one accumulator buffer, because its scale factors take
+// the other columns; its epilogue frees TMEM as soon as it has read it.
+//
+// Every barrier wait has a clock budget. On expiry the kernel:
+//   - records FP8_ERR_TIMEOUT in the caller's status word;
+//   - lets in-flight copies land;
+//   - frees TMEM and returns.
+// Each kernel launches with programmatic dependent launch: it waits for the previous kernel
+// only before its first global memory access.
 #include <algorithm>
 #include <cstdio>
 
