@@ -3,13 +3,19 @@
 // "Low-Precision Training Guide" (Recipe Reference: delayed, tensorwise, mxfp8, blockwise),
 // plus the MLP activation variants that keep the GeLU input in FP8.
 //
-// One CTA (256 threads) owns a 128 x 128 source tile. It reads the tile once from HBM with
-// 16-byte non-allocating loads, writes the row-wise codes straight from registers (a
-// half-warp covers one 128-byte row segment), parks the bf16 tile in shared memory, and
-// writes the column-wise codes from there (each thread emits 32 consecutive bytes of two
-// transposed rows, i.e. whole 32-byte sectors). Scales are staged in shared memory and
-// written as one coalesced block per tile. HBM traffic per element: 2 bytes read, 1 byte
-// per copy written, plus the scales.
+// A persistent kernel: two CTAs of 256 threads per SM, each walking 128 x 128 source tiles
+// (blockIdx.x, then + gridDim.x, ...). Thread 0 streams the tiles with TMA (two 64-column
+// boxes, 128-byte swizzle) into a ring of three shared-memory buffers, so two tiles are in
+// flight while one is converted.
+//   Row-wise codes   written straight from registers (a half-warp covers one 128-byte row
+//                    segment).
+//   Column-wise      written from the shared-memory tile: each thread emits 32 consecutive
+//   codes            bytes of two transposed rows, i.e. whole 32-byte sectors, with one
+//                    256-bit store.
+//   Scales           staged in shared memory and written as one coalesced block per tile.
+// HBM traffic per element: 2 bytes read, 1 byte per copy written, plus the scales. Each
+// launch uses programmatic dependent launch: the next kernel may start launching at once, and
+// this one waits for the previous kernel before its first global memory access.
 #include <algorithm>
 
 #include "common.cuh"
