@@ -319,8 +319,7 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
   constexpr int kEpiWarps = epi_warps<MODE, EPI>();
   static_assert(EPI == EPI_NONE || MODE == G_MX, "fused MLP epilogues are MXFP8 only");
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+  uint8_t* smem = ptx::align_smem<1024>(smem_raw);
   uint8_t* sA = smem;
   uint8_t* sB = smem + G::kStages * kTileABytes;
   uint8_t* sSF = sB + G::kStages * G::kTileBBytes;

@@ -495,8 +495,7 @@ __global__ void __launch_bounds__(256, quant_ctas_per_sm<MODE, EPI>())
     quantize_tile_kernel(const __grid_constant__ CUtensorMap tmX, const QuantParams p) {
   static_assert(F8 == F8_E4M3 || (MODE != Q_MX && EPI == EPI_NONE), "E5M2: per-tensor / blockwise");
   extern __shared__ uint8_t qsm_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(qsm_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* base = ptx::align_smem<1024>(qsm_raw);
   QuantCtl& S = *reinterpret_cast<QuantCtl*>(base);
   constexpr int kQBufs = quant_bufs<EPI>();
   uint8_t* tiles = base + quant_tiles_off<EPI>();

@@ -12,6 +12,14 @@ namespace ptx {
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+// The dynamic shared-memory base rounded up to a multiple of `align` bytes by pointer
+// arithmetic on the shared array itself, so the compiler still knows that the result (and
+// everything derived from it) is shared memory and emits shared loads and stores for it.
+// A round trip through an integer would turn every access into a generic one.
+template <uint32_t align>
+__device__ __forceinline__ uint8_t* align_smem(uint8_t* raw) {
+  return raw + ((align - (smem_u32(raw) & (align - 1))) & (align - 1));
+}
 
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
