@@ -51,7 +51,7 @@ FP8_OVER_BF16 = 2.0                                   # nominal dense fp8 / bf16
 # step's four such launches in one capture of `ncu --metrics dram__bytes_read.sum,
 # dram__bytes_write.sum -k regex:gemm_tn_kernel -s 4 -c 4 python bench.py --profile
 # gemm_mx_mlp --steps 2`. Reset to None whenever that kernel changes.
-GEMM_TRAFFIC_BYTES = 581.8e6
+GEMM_TRAFFIC_BYTES = 582.4e6
 
 
 def peaks():
