@@ -39,7 +39,11 @@
  * Ownership and ordering: the caller owns every buffer. No entry point allocates or frees
  * device memory, synchronises the device or the stream, or keeps state between calls; all
  * work is enqueued on the caller's stream in stream order. Every entry point is safe to call
- * from several host threads on different streams.
+ * from several host threads on different streams. The kernels are launched with programmatic
+ * dependent launch: a kernel may start its setup while the preceding kernel in the stream
+ * finishes. It waits for that kernel's completion, and for the visibility of its writes,
+ * before its first global memory access, so stream order holds for every buffer. Setting the
+ * environment variable FP8LIN_PDL=0 launches without the attribute.
  *
  * Errors: argument errors are found on the host before anything is enqueued and returned as
  * a status (nothing is launched then). Conditions seen on the device (a pipeline wait that
