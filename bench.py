@@ -298,6 +298,98 @@ def whole_job_tflops(world, ms_total, steps):
     return world * GEMM_FLOPS / (ms_total / steps * 1e-3) / 1e12
 
 
+def _event_ms(torch, stream, fn, reps, warm=5):
+    """Mean device time (ms) of fn over `reps` back-to-back calls on `stream` (CUDA events,
+    after `warm` untimed calls)."""
+    for _ in range(warm):
+        fn(0)
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for i in range(reps):
+        fn(i)
+    e.record(stream)
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / reps
+
+
+def measure_gemm_4096(torch, F, dev, fp8_peak, reps=30):
+    """The MXFP8 GEMM 4096 x 4096 x 4096 alone (fprop of seeded X N(0,1), W N(0,0.02)): mean of
+    `reps` back-to-back launches timed with CUDA events."""
+    from workloads import bf16_bits_normal
+    rec = F.Recipe(kind="mxfp8")
+    n = 4096
+    to_dev = lambda b: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).to(dev)  # noqa: E731
+    xq = F.quantize(rec, to_dev(bf16_bits_normal(n, n, seed=0, stream=0)), "activation")
+    wq = F.quantize(rec, to_dev(bf16_bits_normal(n, n, seed=0, stream=1, sigma=0.02)), "weight")
+    y = torch.empty((n, n), dtype=torch.bfloat16, device=dev)
+    ms = _event_ms(torch, torch.cuda.current_stream(dev),
+                   lambda i: F.linear_fwd(rec, xq, wq, y=y), reps)
+    tf = 2.0 * n ** 3 / (ms * 1e-3) / 1e12
+    return {"kernel": "gemm_tn_kernel<G_MX> (CTA pair)", "M": n, "N": n, "K": n,
+            "launches": reps, "avg_launch_ms": round(ms, 4), "tflops": round(tf, 1),
+            "peak": fp8_peak, "frac": round(tf / fp8_peak, 4), "target_frac": 0.60,
+            "operands": "16 MB FP8 each, L2-resident across launches (compute-bound)"}
+
+
+def measure_quantize_by_recipe(torch, F, dev, hbm, reps=20):
+    """Every recipe's quantize of an 8192 x 4096 tensor (row + column copies) alone: mean of
+    `reps` launches, the input rotating over enough distinct buffers (> 2 x L2) that each
+    launch reads it from DRAM. GB/s are algorithmic bytes (bf16 or fp32 read, one byte per
+    code written, the scales) over the CUDA-event time."""
+    R, C = 8192, 4096
+    n_in = 5                                             # 5 x 64 MiB bf16 > 2 x 129 MB L2
+    g = torch.Generator(device=dev).manual_seed(0)
+    xs = [torch.randn((R, C), device=dev, generator=g).to(torch.bfloat16) for _ in range(n_in)]
+    stream = torch.cuda.current_stream(dev)
+    cases = [("tensorwise", "activation", 4.0), ("delayed", "activation", 4.0),
+             ("mxfp8", "activation", 4.0 + 2 / 32.0),
+             ("blockwise_1x128", "activation", 4.0 + 2 * 4 / 128.0),
+             ("blockwise_128x128", "weight", 4.0 + 2 * 4 / (128.0 * 128.0))]
+    out = {}
+    for name, role, per_elt in cases:
+        rec = F.Recipe(kind=name.split("_")[0])
+        q = F.empty_qtensor(rec, R, C, role, device=dev)
+        ws = torch.empty(max(16, F.workspace_bytes(rec, R, C)), dtype=torch.uint8, device=dev)
+        ms = _event_ms(torch, stream,
+                       lambda i: F.quantize(rec, xs[i % n_in], role, out=q, workspace=ws), reps)
+        gbs = R * C * per_elt / (ms * 1e-3) / 1e9
+        out[name] = {"ms": round(ms, 4), "gbs": round(gbs, 1), "frac": round(gbs / hbm, 4),
+                     "bytes_per_elt": round(per_elt, 5)}
+    del xs
+    # fp32 master weight -> MXFP8 row + column copies: 4 B in, 2 x (1 + 1/32) B out
+    w32 = [torch.randn((R, C), device=dev, generator=g) * 0.02 for _ in range(3)]  # 3 x 128 MiB
+    rec = F.Recipe(kind="mxfp8")
+    q = F.empty_qtensor(rec, R, C, "weight", device=dev)
+    ms = _event_ms(torch, stream, lambda i: F.quantize_master(rec, w32[i % 3], out=q), reps)
+    per_elt = 4.0 + 2 + 2 / 32.0
+    gbs = R * C * per_elt / (ms * 1e-3) / 1e9
+    out["master_mxfp8"] = {"ms": round(ms, 4), "gbs": round(gbs, 1), "frac": round(gbs / hbm, 4),
+                           "bytes_per_elt": per_elt}
+    return {"shape": [R, C], "copies": "row + column", "launches": reps, "peak_gbs": hbm,
+            "target_frac": 0.70, "recipes": out}
+
+
+def measure_sustained(torch, st, ms_step, local, seconds=3.0):
+    """The step back to back for about `seconds` (long enough to reach the power cap), with its
+    own clock samples: the figure a long training run sees, next to the short timed region."""
+    n = max(10, int(seconds * 1e3 / max(ms_step, 1e-3)))
+    st.events = None
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(st.stream)
+    for _ in range(n):
+        st.run()
+    t1.record(st.stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1)
+    return {"steps": n, "seconds": round(ms / 1e3, 2), "ms_per_step": round(ms / n, 4),
+            "tflops": round(GEMM_FLOPS / (ms / n * 1e-3) / 1e12, 1), "clocks": clk}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -355,9 +447,15 @@ def run_ours(args):
     barrier()
 
     ms_step = ms_total / args.steps
+    hbm, fp8_peak, src = peaks()
+    # ---- the benchmark spec's two named targets and the power-capped figure, measured apart
+    # from the timed region above
+    gemm4096 = measure_gemm_4096(torch, F, dev, fp8_peak)
+    quant_recipes = measure_quantize_by_recipe(torch, F, dev, hbm)
+    sustained = measure_sustained(torch, st, ms_step, local)
+    barrier()
     value = whole_job_tflops(world, ms_total, args.steps)
     e2e_value = whole_job_tflops(world, ms_e2e, args.steps)
-    hbm, fp8_peak, src = peaks()
     # the roofline kernel: the plain-store MXFP8 GEMM (four of the six GEMM launches when the
     # MLP epilogues are fused, all six otherwise); every GEMM of the step has the same flops
     gemm_ms = statistics.mean(ks["gemm"])
@@ -398,6 +496,9 @@ def run_ours(args):
                     "h2d_bytes_per_step": st.h2d_bytes(), "d2h_bytes_per_step": st.d2h_bytes(),
                     "copies": "pinned host, own streams, overlapped with the adjacent steps"},
             "kernels_ms": per_kernel,
+            "gemm_4096_mxfp8": gemm4096,
+            "quantize_by_recipe": quant_recipes,
+            "sustained": sustained,
             "gpu_launches": st.kernels_per_step * args.steps,
             "clocks": clk,
             "cpu_baseline": cpu,
@@ -798,7 +899,46 @@ def _oracle_setup():
     return _ORACLE_SETUP
 
 
-def cpu_baseline(m_sample=128, w_frac=16):
+def _oracle_warm(_):
+    """Pool worker start-up: import the oracle and the generators (not timed)."""
+    from oracle import fp8_oracle  # noqa: F401
+    from workloads import bf16_bits_normal  # noqa: F401
+    time.sleep(0.5)
+    return os.getpid()
+
+
+def _oracle_quantize_chunk(task):
+    """Pool worker: the oracle's MXFP8 quantiser (row + column copies) on one seeded
+    rows x 4096 bf16 chunk; returns the wall-clock start and end of the quantisation."""
+    seed, rows = task
+    from oracle import fp8_oracle as O
+    from workloads import bf16_bits_normal
+    x = bf16_bits_normal(rows, 4096, seed=seed, stream=0)
+    t0 = time.time()
+    O.quantize_mxfp8(x)
+    return t0, time.time()
+
+
+def oracle_quantize_rates(rows=512):
+    """The oracle's MXFP8 quantize in algorithmic GB/s (2 B read, 2 x (1 + 1/32) B written per
+    element) on one core, and on every core of the host with one chunk per core in a spawned
+    process pool (wall clock from the first chunk's start to the last one's end)."""
+    import multiprocessing as mp
+    per_chunk = rows * 4096 * (2 + 2 + 2 / 32.0)
+    t0, t1 = _oracle_quantize_chunk((0, rows))
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    with mp.get_context("spawn").Pool(cores) as pool:
+        pool.map(_oracle_warm, range(cores), chunksize=1)
+        spans = pool.map(_oracle_quantize_chunk, [(i + 1, rows) for i in range(cores)],
+                         chunksize=1)
+    wall = max(e for _, e in spans) - min(b for b, _ in spans)
+    return {"gbs_1_core": round(per_chunk / (t1 - t0) / 1e9, 4),
+            "gbs_all_cores": round(cores * per_chunk / wall / 1e9, 4), "cores": cores,
+            "sample": f"MXFP8 quantize (row + column copies) of a {rows} x 4096 bf16 chunk, "
+                      f"one chunk per core"}
+
+
+def cpu_baseline(m_sample=128, w_frac=16, quantize_rates=True):
     """The oracle, as it stands, on a bounded sample of the same step: the token-proportional
     work on m_sample of the 8192 tokens (scaled up by 8192/m_sample) plus the per-step weight
     quantisation on 1/w_frac of the weight rows (scaled up by w_frac)."""
@@ -825,11 +965,14 @@ def cpu_baseline(m_sample=128, w_frac=16):
     t_tok = (time.perf_counter() - t0) * (TOKENS // m_sample)
     step_s = t_w + t_tok
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    return {"value": round(GEMM_FLOPS / step_s / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
-            "kind": "oracle", "step_seconds_estimate": round(step_s, 2),
-            "sample": (f"oracle MLP step on {m_sample} of {TOKENS} tokens (x{TOKENS // m_sample})"
-                       f" plus weight quantisation of 1/{w_frac} of the rows (x{w_frac}); "
-                       "numpy: elementwise work on one core, fp64 matmuls on the BLAS threads")}
+    out = {"value": round(GEMM_FLOPS / step_s / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
+           "kind": "oracle", "step_seconds_estimate": round(step_s, 2),
+           "sample": (f"oracle MLP step on {m_sample} of {TOKENS} tokens (x{TOKENS // m_sample})"
+                      f" plus weight quantisation of 1/{w_frac} of the rows (x{w_frac}); "
+                      "numpy: elementwise work on one core, fp64 matmuls on the BLAS threads")}
+    if quantize_rates:
+        out["quantize"] = oracle_quantize_rates()
+    return out
 
 
 def run_reference(args):
@@ -840,7 +983,7 @@ def run_reference(args):
     vals = []
     if args.workload == "mlp":
         def one():
-            return cpu_baseline(m_sample=32, w_frac=64)
+            return cpu_baseline(m_sample=32, w_frac=64, quantize_rates=False)
         workload = WORKLOAD
     else:
         def one():
@@ -861,6 +1004,8 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(statistics.median(x["step_seconds_estimate"] for x in vals) * 1e3, 1),
+        "ms_per_step_kind": "extrapolated: each step times the oracle on a bounded sample of the "
+                            "workload and scales the time to the whole step",
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64 (oracle)", "data": "synthetic",
         "config": {"workload": workload, "recipe": {"mlp": "mxfp8"}.get(

@@ -37,8 +37,10 @@
  *       column copy [C/128][R/128] (the transposed grid). col = byte transpose of row.
  *
  * Ownership and ordering: the caller owns every buffer. No entry point allocates or frees
- * device memory, synchronises the device or the stream, or keeps state between calls; all
- * work is enqueued on the caller's stream in stream order. Every entry point is safe to call
+ * device memory, synchronises the device or the stream, or keeps state between calls (the
+ * one exception is fp8_quantize_static_scratch, whose scratch array in the library image
+ * keeps the last call's amax partials: see its "Sharing" note); all work is enqueued on the
+ * caller's stream in stream order. Every entry point is safe to call
  * from several host threads on different streams. The kernels are launched with programmatic
  * dependent launch: a kernel may start its setup while the preceding kernel in the stream
  * finishes. It waits for that kernel's completion, and for the visibility of its writes,
@@ -272,9 +274,10 @@ fp8_status fp8_linear_dgrad_dgelu(const fp8_recipe *recipe, const fp8_tensor *dy
  * nothing.
  *   Limit: tensors needing more than 65536 partials (delayed: more than 65536 128x128 tiles)
  *   return FP8_ERR_WORKSPACE; MXFP8 and blockwise need no scratch.
- *   Set-up: the first call on each device looks up the array's device address
- *   (cudaGetSymbolAddress) with that device current; make that first call before any stream
- *   capture.
+ *   Set-up: the first call in each CUDA context looks up the array's device address
+ *   (cudaGetSymbolAddress) with that context's device current; make that first call before
+ *   any stream capture. A new context on a device (after cudaDeviceReset, or a context the
+ *   caller made current) gets its own lookup on its first call.
  *   Sharing: every call on a device uses the same array, which keeps the last call's
  *   contents (nothing in it needs to start at zero); calls whose work overlaps on the GPU
  *   (different streams, or several host threads) race on it and must be serialised by the

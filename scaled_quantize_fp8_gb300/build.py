@@ -16,7 +16,7 @@ OBJDIR = os.path.join(ROOT, "_build", "fp8lin")
 LIB = os.path.join(PKG, "libfp8lin.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE,
+NVCC_FLAGS = ["-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE,
               "-Xptxas", "-v"]
 
 

@@ -11,6 +11,16 @@
 using namespace fp8lin;
 
 namespace {
+thread_local const char* g_last_cuda_error = "";
+}  // namespace
+
+fp8_status fp8lin::cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return FP8_OK;
+  g_last_cuda_error = cudaGetErrorString(e);
+  return FP8_ERR_CUDA;
+}
+
+namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -56,14 +66,6 @@ int gemm_kind(const fp8_recipe* r) {
 // Row/column multiple a recipe needs: 128 for the block recipes, 16 for per-tensor scales.
 int64_t shape_quantum(int kind) {
   return (kind == FP8_RECIPE_MXFP8 || kind == FP8_RECIPE_BLOCKWISE) ? 128 : 16;
-}
-
-thread_local const char* g_last_cuda_error = "";
-
-fp8_status cuda_status(cudaError_t e) {
-  if (e == cudaSuccess) return FP8_OK;
-  g_last_cuda_error = cudaGetErrorString(e);
-  return FP8_ERR_CUDA;
 }
 
 // Scale pointers a recipe needs for one copy.

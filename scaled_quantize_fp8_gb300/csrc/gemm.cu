@@ -850,8 +850,8 @@ static cudaError_t launch_mode(const GemmLaunch& g, cudaStream_t st) {
     else if constexpr (MODE == G_BLOCK) return gemm_wide_kernel<MODE, B128, CTA2>;
     else return gemm_tn_kernel<MODE, B128, CTA2>;
   }();
-  static std::atomic<uint64_t> attr_done{0};
-  cudaError_t ae = once_per_device(attr_done, [&] {
+  static ContextOnce attr_done{};
+  cudaError_t ae = once_per_context(attr_done, [&] {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(G::kSmemBytes));
     if (e == cudaSuccess && CTA2)

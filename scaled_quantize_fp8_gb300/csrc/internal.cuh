@@ -50,19 +50,42 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
-// Run set() (a per-device, idempotent setup such as cudaFuncSetAttribute) the first time a
-// device reaches this flag word; later calls on that device skip it. Thread-safe: concurrent
-// first calls may both run set(), which is harmless. Devices beyond 63 run it every time.
+// Unique id of the calling thread's current CUDA context (cuCtxGetId), or 0 when no context
+// is current or the driver cannot say. Ids are never reused within a process, so a setup
+// keyed on them is redone in a new context: after cudaDeviceReset, or when the caller makes
+// its own context current.
+unsigned long long current_context_id();
+
+// Errors of a CUDA call as a status; FP8_ERR_CUDA also records the error's text for
+// fp8_last_cuda_error() (per host thread).
+fp8_status cuda_status(cudaError_t e);
+
+constexpr int kMaxDevices = 64;
+
+// The contexts in which a per-context setup has run: one slot per device, holding the id of
+// the context it last ran in.
+struct ContextOnce {
+  std::atomic<unsigned long long> ctx[kMaxDevices];
+};
+
+// Run set() (an idempotent per-context setup such as cudaFuncSetAttribute) the first time the
+// current context reaches this flag; later calls in the same context skip it. A different
+// context on the device (after cudaDeviceReset, or another context made current) runs it
+// again. Thread-safe: concurrent first calls may both run set(), which is harmless. Devices
+// beyond kMaxDevices, or a context whose id is unknown, run it every time.
 template <class Set>
-cudaError_t once_per_device(std::atomic<uint64_t>& done, Set set) {
+cudaError_t once_per_context(ContextOnce& done, Set set) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
-  if (bit != 0 && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  const bool slot = dev >= 0 && dev < kMaxDevices;
+  unsigned long long id = current_context_id();
+  if (slot && id != 0 && done.ctx[dev].load(std::memory_order_acquire) == id) return cudaSuccess;
   e = set();
-  if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_acq_rel);
-  return e;
+  if (e != cudaSuccess) return e;
+  if (id == 0) id = current_context_id();          // set() may have made the context current
+  if (slot && id != 0) done.ctx[dev].store(id, std::memory_order_release);
+  return cudaSuccess;
 }
 
 // ---- quantize.cu

@@ -257,8 +257,8 @@ template <int MODE>
 static cudaError_t launch_master(MasterParams p, cudaStream_t st) {
   auto a32 = [](const void* q) { return q == nullptr || reinterpret_cast<uintptr_t>(q) % 32 == 0; };
   p.v8 = a32(p.row) && a32(p.col) && p.C % 32 == 0 && p.R % 32 == 0;
-  static std::atomic<uint64_t> attr_done{0};
-  const cudaError_t ae = once_per_device(attr_done, [] {
+  static ContextOnce attr_done{};
+  const cudaError_t ae = once_per_context(attr_done, [] {
     return cudaFuncSetAttribute(quantize_master_kernel<MODE>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(kMasterSmem));
   });

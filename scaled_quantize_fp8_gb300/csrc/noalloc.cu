@@ -17,24 +17,34 @@ constexpr size_t kStaticScratchWords = 65536;
 static __device__ __align__(256) uint32_t g_static_scratch[kStaticScratchWords];
 
 namespace {
-constexpr int kMaxDevices = 64;
+// The array's device address in the context where it was last looked up, per device. A
+// cudaDeviceReset, or a context of the caller's own made current, gives the device a new
+// context (with a new id) in which the library image, and the array, may sit elsewhere.
+struct ScratchSlot {
+  unsigned long long ctx;
+  void* ptr;
+};
 std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
+ScratchSlot g_slot[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device (looked up once per device).
+// Device address of the scratch array in the current context (looked up once per context).
 cudaError_t scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  unsigned long long id = current_context_id();
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_static_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = p;
+  if (id != 0 && g_slot[dev].ctx == id) {
+    *out = g_slot[dev].ptr;
+    return cudaSuccess;
   }
-  *out = g_scratch_ptr[dev];
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_static_scratch);
+  if (e != cudaSuccess) return e;
+  if (id == 0) id = current_context_id();   // the lookup may have made the context current
+  g_slot[dev] = ScratchSlot{id, p};          // id 0 (unknown) never matches: looked up again
+  *out = p;
   return cudaSuccess;
 }
 }  // namespace
@@ -53,7 +63,8 @@ extern "C" fp8_status fp8_quantize_static_scratch(const fp8_recipe* recipe, cons
   if (need > kStaticScratchWords * sizeof(uint32_t)) return FP8_ERR_WORKSPACE;
   void* scratch = nullptr;
   if (need > 0) {
-    if (scratch_address(&scratch) != cudaSuccess) return FP8_ERR_CUDA;
+    const fp8_status st = cuda_status(scratch_address(&scratch));
+    if (st != FP8_OK) return st;
   }
   return fp8_quantize(recipe, x_bf16, rows, cols, role, want_row, want_col, out, scratch,
                       need, dev_status, stream);

@@ -700,8 +700,8 @@ static cudaError_t launch_tiles(QuantParams p, cudaStream_t st) {
   CUtensorMap map;
   if (!make_tmap_2d(&map, p.x, 2, p.C, p.R, 64, kTile, true)) return cudaErrorInvalidValue;
   constexpr int smem = int(quant_smem_bytes<MODE, EPI>());
-  static std::atomic<uint64_t> attr_done{0};
-  const cudaError_t ae = once_per_device(attr_done, [&] {
+  static ContextOnce attr_done{};
+  const cudaError_t ae = once_per_context(attr_done, [&] {
     return cudaFuncSetAttribute(quantize_tile_kernel<MODE, EPI, F8>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   });

@@ -45,6 +45,30 @@ bool make_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, int64_t in
   return r == CUDA_SUCCESS;
 }
 
+// A driver entry point fetched through the runtime (null when the driver lacks it).
+template <class Fn>
+static Fn driver_entry(const char* name) {
+  void* ptr = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    return reinterpret_cast<Fn>(ptr);
+  return nullptr;
+}
+
+unsigned long long current_context_id() {
+  using GetCurrentFn = CUresult (*)(CUcontext*);
+  using GetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+  static const GetCurrentFn get_current = driver_entry<GetCurrentFn>("cuCtxGetCurrent");
+  static const GetIdFn get_id = driver_entry<GetIdFn>("cuCtxGetId");
+  if (get_current == nullptr || get_id == nullptr) return 0;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  unsigned long long id = 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
 bool pdl_enabled() {
   static const bool on = [] {
     const char* v = std::getenv("FP8LIN_PDL");

@@ -35,3 +35,9 @@ def test_reference_arm_prints_the_contract(workload):
         assert key in line, key
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
     assert line["config"]["workload"] == bench.CONFIGS[workload]
+
+
+def test_oracle_quantize_rates_one_and_all_cores():
+    """The CPU baseline's quantize leg: the oracle on one core and, in a spawned pool, on all."""
+    r = bench.oracle_quantize_rates(rows=64)
+    assert r["cores"] >= 1 and r["gbs_1_core"] > 0 and r["gbs_all_cores"] > 0

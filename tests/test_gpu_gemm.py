@@ -199,7 +199,8 @@ def test_wgrad_bf16_with_fp8_dgrad():
 
 def test_full_size_blockwise_fwd_dgrad_wgrad_sampled():
     """Blockwise fwd + dgrad + wgrad at 4096 x 4096 x 4096 (X 1x128, W 128x128, dY N(0,1e-3)),
-    in the benchmark's launch configuration; the oracle sums sampled output rows."""
+    in the benchmark's launch configuration, in bf16 and fp32 output mode; the oracle sums
+    sampled output rows."""
     rec = F.Recipe(kind="blockwise")
     xb = bf16_bits_normal(4096, 4096, seed=0, stream=0)
     wb = bf16_bits_normal(4096, 4096, seed=0, stream=1, sigma=0.02)
@@ -208,13 +209,21 @@ def test_full_size_blockwise_fwd_dgrad_wgrad_sampled():
                    for b, r in ((xb, "activation"), (wb, "weight"), (dyb, "grad")))
     y = F.linear_fwd(rec, xq, wq)
     dx, dw = F.linear_bwd(rec, dyq, xq, wq)
+    y32 = F.linear_fwd(rec, xq, wq, fp32=True)
+    dx32, dw32 = F.linear_bwd(rec, dyq, xq, wq, fp32=True)
     torch.cuda.synchronize()
     rows = _sample_rows(4096)
     qx, qw, qd = (O.quantize_blockwise_1x128(xb), O.quantize_blockwise_128x128(wb),
                   O.quantize_blockwise_1x128(dyb))
     d1 = lambda q, c: O.dequant_1x128(q[c], q[c + "_scale_inv"])  # noqa: E731
     d2 = lambda q, c: O.dequant_128x128(q[c], q[c + "_scale_inv"])  # noqa: E731
-    for got, a, b in ((y, d1(qx, "row"), d2(qw, "row")), (dx, d1(qd, "row"), d2(qw, "col")),
-                      (dw, d1(qd, "col"), d1(qx, "col"))):
-        ok, err = gemm_bf16_close(from_dev_bf16(got)[rows], O.gemm_tn_f64(a[rows], b))
+    for got, got32, a, b in ((y, y32, d1(qx, "row"), d2(qw, "row")),
+                             (dx, dx32, d1(qd, "row"), d2(qw, "col")),
+                             (dw, dw32, d1(qd, "col"), d1(qx, "col"))):
+        ref = O.gemm_tn_f64(a[rows], b)
+        ok, err = gemm_bf16_close(from_dev_bf16(got)[rows], ref)
         assert ok, err
+        # the promoted fp32 sum (per 128-wide K chunk, times both block scales) agrees with
+        # the fp64 sum on the same FP8 operands
+        ok, err = gemm_f32_normwise(got32.cpu().numpy()[rows], ref)
+        assert ok, ("fp32", err)

@@ -8,6 +8,9 @@ first one left behind). This file sorts last so a run that stops at the first fa
 already run every other test; it also passes when run alone in a fresh process.
 """
 import ctypes
+import os
+import subprocess
+import sys
 
 import pytest
 import torch
@@ -57,3 +60,14 @@ def test_static_scratch_rejects_oversized():
     st = lib.fp8_quantize_static_scratch(ctypes.byref(rc), ctypes.c_void_p(x.data_ptr()),
                                          128 * 65537, 128, 0, 1, 1, ctypes.byref(t), None, None)
     assert st == 7                                   # FP8_ERR_WORKSPACE
+
+
+def test_static_scratch_after_device_reset():
+    """A cudaDeviceReset gives the device a new context, in which the scratch array may sit at
+    another address: the entry point must look it up again rather than reuse the old one (and
+    the kernels' shared-memory attributes must be set again). Run in a child process without
+    torch, whose allocator would otherwise hold pointers the reset invalidates; the child
+    compares the entry point with fp8_quantize before and after the reset."""
+    child = os.path.join(os.path.dirname(os.path.abspath(__file__)), "noalloc_reset_child.py")
+    r = subprocess.run([sys.executable, child], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, (r.returncode, r.stdout[-2000:], r.stderr[-2000:])
