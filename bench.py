@@ -1017,7 +1017,8 @@ def run_reference(args):
 
 def run_profile_case(args):
     """Launch one kernel kind a few times on its own (for ncu captures; prints no JSON line).
-    quant_mx / quant_tensorwise / quant_blockwise: X 16384 x 8192 bf16 (256 MiB, above L2).
+    quant_mx / quant_tensorwise / quant_blockwise: X --rows x --cols bf16 (default 16384 x 8192,
+    256 MiB, above L2).
     gemm_mx / gemm_tensorwise / gemm_blockwise: fprop 8192 x 4096 x 4096.
     gemm_wgrad_blockwise: blockwise wgrad 4096 x 4096 x 8192 (1x128 scales on both operands).
     gelu_mx / dgelu_mx: the standalone GeLU / dGeLU + MXFP8 quantize on h 8192 x 16384.
@@ -1082,8 +1083,9 @@ def run_profile_case(args):
         for _ in range(args.steps):
             F.linear_bwd(rec, dyq, xq, None, want_dx=False, dw=dw)
     elif case.startswith("quant"):
-        x = torch.randn((16384, 8192), device="cuda", generator=g).to(torch.bfloat16)
-        q = F.empty_qtensor(rec, 16384, 8192, "activation")
+        R, C = args.rows, args.cols
+        x = torch.randn((R, C), device="cuda", generator=g).to(torch.bfloat16)
+        q = F.empty_qtensor(rec, R, C, "activation")
         for _ in range(args.steps):
             F.quantize(rec, x, "activation", out=q)
     else:
@@ -1179,6 +1181,8 @@ def main():
                              "gemm_tensorwise", "gemm_blockwise", "gelu_mx", "dgelu_mx",
                              "gemm_gelu_mx", "gemm_dgelu_mx", "gemm_mx_mlp",
                              "gemm_wgrad_blockwise"])
+    ap.add_argument("--rows", type=int, default=16384, help="--profile quant_*: tensor rows")
+    ap.add_argument("--cols", type=int, default=8192, help="--profile quant_*: tensor columns")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)

@@ -215,6 +215,15 @@ __device__ __forceinline__ void store_seg32(void* p, uint4 a, uint4 b, bool lo_o
   }
 }
 
+// 16-byte read-only load with an L2 cache policy (see ptx::l2_evict_last_policy).
+__device__ __forceinline__ uint4 ldg_nc_v4_policy(const void* p, uint64_t policy) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(policy));
+  return v;
+}
+
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"

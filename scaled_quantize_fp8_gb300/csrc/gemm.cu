@@ -121,6 +121,17 @@ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, 
   *nt = r / gm;
 }
 
+// K order of a tile: a CTA (pair) walks the K blocks of its tiles alternately forwards and
+// backwards. All units run about in step, so the tiles of one round end on the K blocks that
+// the next round's tiles (which share their A panels: consecutive rounds move along N within a
+// group of M tiles) start on, while those are still in L2. Blockwise keeps the forward order
+// (its epilogue promotes the chunks in order).
+template <int MODE>
+__device__ __forceinline__ int k_block(int tile, int unit, int n_units, int kk, int nk) {
+  if constexpr (MODE == G_BLOCK) return kk;
+  return (((tile - unit) / n_units) & 1) ? nk - 1 - kk : kk;
+}
+
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, SharedCtl* ctl,
                                          int32_t* status) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
@@ -387,9 +398,10 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
         tile_coords(tile, tiles_m, tiles_n, &mt, &nt);
         const int m0 = mt * G::kTileM + int(rank) * kBM;
         const int n0 = nt * kBN + int(rank) * int(kBRows);
-        for (int kb = 0; kb < nk; ++kb) {
+        for (int kk = 0; kk < nk; ++kk) {
+          const int kb = k_block<MODE>(tile, unit, n_units, kk, nk);
           if (!wait_bar(&ctl->empty[s], ph ^ 1u, ctl, p.status)) goto producer_done;
-          const uint32_t stall = (unit == 0 && tile == 0 && kb == 0) ? p.stall_tx : 0u;
+          const uint32_t stall = (unit == 0 && tile == 0 && kk == 0) ? p.stall_tx : 0u;
           uint8_t* a_dst = sA + s * kTileABytes;
           uint8_t* b_dst = sB + s * G::kTileBBytes;
           if constexpr (CTA2) {
@@ -475,7 +487,7 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
           ptx::tc_fence_after();
           d_t = tmem + b * kBN;
         }
-        for (int kb = 0; kb < nk; ++kb) {
+        for (int kk = 0; kk < nk; ++kk) {
           uint32_t b = 0;
           if constexpr (MODE == G_BLOCK) {
             b = u & 1u;
@@ -502,7 +514,7 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
             const uint64_t bd =
                 p.b_mn ? ptx::smem_desc(b_addr + 4096 * k, 16384, 1024, ptx::kSwizzle128B)
                        : ptx::smem_desc(b_addr + 32 * k, 16, 1024, ptx::kSwizzle128B);
-            const uint32_t acc_on = MODE == G_BLOCK ? uint32_t(k != 0) : uint32_t((kb | k) != 0);
+            const uint32_t acc_on = MODE == G_BLOCK ? uint32_t(k != 0) : uint32_t((kk | k) != 0);
             if constexpr (CTA2) {
               if constexpr (MODE == G_BF16) {
                 ptx::mma_f16_pair(d_t, ad, bd, idesc, acc_on);
@@ -737,7 +749,7 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
       int s = 0;
       uint32_t ph = 0;
       for (int tile = unit; tile < n_tiles; tile += n_units) {
-        for (int kb = 0; kb < nk; ++kb) {
+        for (int kk = 0; kk < nk; ++kk) {
           if (!wait_bar(&ctl->full[s], ph, ctl, p.status)) goto sf_done;
           ptx::tc_fence_after();
           const uint32_t sfa_t = sf_base + kSfCols * uint32_t(s), sfb_t = sfa_t + 4;

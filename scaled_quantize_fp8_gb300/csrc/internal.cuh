@@ -19,6 +19,7 @@ namespace fp8lin {
 bool make_tmap_2d(CUtensorMap_st* map, const void* base, int elem_bytes, int64_t inner,
                   int64_t rows, int box_inner, int box_rows, bool swizzle128);
 int num_sms();      // of the current device
+int64_t l2_bytes(); // L2 cache size of the current device
 
 // Programmatic dependent launch: every kernel of the library lets the next kernel in its
 // stream start launching as soon as all of its own CTAs are running, and waits for the kernel

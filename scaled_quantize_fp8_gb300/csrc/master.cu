@@ -15,6 +15,7 @@
 
 #include "common.cuh"
 #include "internal.cuh"
+#include "sm100_ptx.cuh"
 
 namespace fp8lin {
 
@@ -100,15 +101,17 @@ __global__ void __launch_bounds__(256) quantize_master_kernel(const MasterParams
   const int tr = int(blockIdx.x) / p.tiles_c, tc = int(blockIdx.x) % p.tiles_c;
   const int64_t r0 = int64_t(tr) * 128, c0 = int64_t(tc) * 128;
 
-  // ---- stage the fp32 tile (zeros outside the tensor)
-#pragma unroll 4
+  // ---- stage the fp32 tile (zeros outside the tensor): all 16 of a thread's 16-byte copies
+  // in flight at once, global -> shared without passing through registers
+#pragma unroll
   for (int i = 0; i < 16; ++i) {
     const int idx = i * 256 + t, r = idx >> 5, c4 = idx & 31;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (r0 + r < p.R && c0 + 4 * c4 < p.C)
-      v = __ldg(reinterpret_cast<const float4*>(p.x + (r0 + r) * p.C + c0 + 4 * c4));
-    *reinterpret_cast<float4*>(tile + r * kMLd + 4 * c4) = v;
+    const bool in = r0 + r < p.R && c0 + 4 * c4 < p.C;
+    const float* src = in ? p.x + (r0 + r) * p.C + c0 + 4 * c4 : p.x;
+    ptx::cp_async_16_zfill(tile + r * kMLd + 4 * c4, src, in ? 16u : 0u);
   }
+  ptx::cp_async_commit();
+  ptx::cp_async_wait<0>();
   __syncthreads();
 
   const int r = t >> 1, h = t & 1;          // row pass: row r, columns 64h .. 64h+63
@@ -208,10 +211,17 @@ __global__ void __launch_bounds__(512) amax_partial_f32_kernel(const float* __re
   __shared__ uint32_t red[16];
   uint32_t m = 0;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n_vec; i += stride) {
-    const float4 v = __ldg(reinterpret_cast<const float4*>(x) + i);
-    m = max(max(m, max(mag31(v.x), mag31(v.y))), max(mag31(v.z), mag31(v.w)));
+  const float4* x4 = reinterpret_cast<const float4*>(x);
+  auto fold = [](uint32_t acc, float4 v) {
+    return max(max(acc, max(mag31(v.x), mag31(v.y))), max(mag31(v.z), mag31(v.w)));
+  };
+  int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < n_vec; i += 4 * stride) {       // four loads in flight per thread
+    const float4 a = __ldg(x4 + i), b = __ldg(x4 + i + stride);
+    const float4 c = __ldg(x4 + i + 2 * stride), d = __ldg(x4 + i + 3 * stride);
+    m = fold(fold(fold(fold(m, a), b), c), d);
   }
+  for (; i < n_vec; i += stride) m = fold(m, __ldg(x4 + i));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;

@@ -60,6 +60,10 @@ struct QuantParams {
   // Failure-detection test hook (0 otherwise): extra bytes CTA 0's first tile expects, so its
   // barrier never completes and the bounded wait runs out (fp8_test_quantize_stalled).
   uint32_t stall_tx;
+  // Tensorwise cast pass: the amax pass has just read the input with an L2 evict_last policy.
+  // Walk the tiles in reverse (the most recently read first) and read them with evict_first,
+  // so the second read is served from L2 and leaves it.
+  bool l2_reread;
 };
 
 // Max of the 15-bit magnitudes of the eight bf16 in a vector.
@@ -534,12 +538,22 @@ __global__ void __launch_bounds__(256, quant_ctas_per_sm<MODE, EPI>())
     }
   }
 
-  auto issue = [&](int tile_id, int b) {
+  // the i-th tile of the walk: in order, or last first for the tensorwise re-read
+  auto tile_at = [&](int seq) { return p.l2_reread ? n_tiles - 1 - seq : seq; };
+  uint64_t policy = 0;
+  if (p.l2_reread && t == 0) policy = ptx::l2_evict_first_policy();
+  auto issue = [&](int seq, int b) {
+    const int tile_id = tile_at(seq);
     const int tr = tile_id / p.tiles_c, tc = tile_id % p.tiles_c;
     uint8_t* dst = tiles + b * kQTileBytes;
-    ptx::mbar_arrive_expect_tx(&S.bar[b], kQTileBytes + (tile_id == 0 ? p.stall_tx : 0u));
-    ptx::tma_load_2d(dst, &tmX, tc * kTile, tr * kTile, &S.bar[b]);
-    ptx::tma_load_2d(dst + 16384, &tmX, tc * kTile + 64, tr * kTile, &S.bar[b]);
+    ptx::mbar_arrive_expect_tx(&S.bar[b], kQTileBytes + (seq == 0 ? p.stall_tx : 0u));
+    if (p.l2_reread) {
+      ptx::tma_load_2d_hint(dst, &tmX, tc * kTile, tr * kTile, &S.bar[b], policy);
+      ptx::tma_load_2d_hint(dst + 16384, &tmX, tc * kTile + 64, tr * kTile, &S.bar[b], policy);
+    } else {
+      ptx::tma_load_2d(dst, &tmX, tc * kTile, tr * kTile, &S.bar[b]);
+      ptx::tma_load_2d(dst + 16384, &tmX, tc * kTile + 64, tr * kTile, &S.bar[b]);
+    }
   };
 
   // prologue: the first kQBufs - 1 tiles in flight
@@ -561,7 +575,8 @@ __global__ void __launch_bounds__(256, quant_ctas_per_sm<MODE, EPI>())
     if (t == 0 && ahead < n_tiles) issue(ahead, (i + kQBufs - 1) % kQBufs);
     if (!quant_wait(S, b, uint32_t(i / kQBufs) & 1u, p.status)) break;
     uint8_t* buf = tiles + b * kQTileBytes;
-    quantize_one_tile<MODE, EPI, F8>(p, S, buf, buf, table, tile, s_tensor, tensor_nan);
+    quantize_one_tile<MODE, EPI, F8>(p, S, buf, buf, table, tile_at(tile), s_tensor,
+                                     tensor_nan);
     // buffer b is refilled by TMA next iteration: per-tensor and 128x128 scales wrote their
     // row codes into it with ordinary stores, which must be ordered before the async copy
     if constexpr (uses_code_tile<MODE>()) ptx::fence_proxy_async_smem();
@@ -575,22 +590,35 @@ __global__ void __launch_bounds__(256, quant_ctas_per_sm<MODE, EPI>())
 }
 
 // Tensorwise first pass: per-CTA max of the 15-bit bf16 magnitudes over a grid-strided
-// sweep of 16-byte vectors (four independent loads in flight per thread).
+// sweep of 16-byte vectors (four independent loads in flight per thread). With l2_keep the
+// input is read with an L2 evict_last policy, so the cast pass that follows finds it in L2.
 __global__ void __launch_bounds__(512) amax_partial_kernel(const uint16_t* __restrict__ x,
                                                            int64_t n_vec,
-                                                           uint32_t* __restrict__ part) {
+                                                           uint32_t* __restrict__ part,
+                                                           int l2_keep) {
   pdl_launch_dependents();
   pdl_wait();
   __shared__ uint32_t red[16];
   uint32_t m = 0;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
   int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  for (; i + 3 * stride < n_vec; i += 4 * stride) {
-    uint4 a = ldg_nc_v4(x + 8 * i), b = ldg_nc_v4(x + 8 * (i + stride));
-    uint4 c = ldg_nc_v4(x + 8 * (i + 2 * stride)), d = ldg_nc_v4(x + 8 * (i + 3 * stride));
-    m = max(m, max(max(vec_amax_bits(a), vec_amax_bits(b)), max(vec_amax_bits(c), vec_amax_bits(d))));
+  if (l2_keep) {
+    const uint64_t pol = ptx::l2_evict_last_policy();
+    for (; i + 3 * stride < n_vec; i += 4 * stride) {
+      uint4 a = ldg_nc_v4_policy(x + 8 * i, pol), b = ldg_nc_v4_policy(x + 8 * (i + stride), pol);
+      uint4 c = ldg_nc_v4_policy(x + 8 * (i + 2 * stride), pol);
+      uint4 d = ldg_nc_v4_policy(x + 8 * (i + 3 * stride), pol);
+      m = max(m, max(max(vec_amax_bits(a), vec_amax_bits(b)), max(vec_amax_bits(c), vec_amax_bits(d))));
+    }
+    for (; i < n_vec; i += stride) m = max(m, vec_amax_bits(ldg_nc_v4_policy(x + 8 * i, pol)));
+  } else {
+    for (; i + 3 * stride < n_vec; i += 4 * stride) {
+      uint4 a = ldg_nc_v4(x + 8 * i), b = ldg_nc_v4(x + 8 * (i + stride));
+      uint4 c = ldg_nc_v4(x + 8 * (i + 2 * stride)), d = ldg_nc_v4(x + 8 * (i + 3 * stride));
+      m = max(m, max(max(vec_amax_bits(a), vec_amax_bits(b)), max(vec_amax_bits(c), vec_amax_bits(d))));
+    }
+    for (; i < n_vec; i += stride) m = max(m, vec_amax_bits(ldg_nc_v4(x + 8 * i)));
   }
-  for (; i < n_vec; i += stride) m = max(m, vec_amax_bits(ldg_nc_v4(x + 8 * i)));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
@@ -743,9 +771,13 @@ cudaError_t quantize_launch(int kind, int role, int fmt, bool pow2, int margin,
       const int64_t n_vec = R * C / 8;
       const int ctas = amax_partial_ctas(n_vec);
       uint32_t* part = reinterpret_cast<uint32_t*>(workspace);
+      // Keep the input in L2 between the two passes when it fits in well under half of L2
+      // (the codes written by the cast pass share the cache).
+      const bool keep = R * C * 2 <= l2_bytes() / 2;
       const cudaError_t e = launch_kernel(amax_partial_kernel, dim3(ctas), dim3(512), 0, st,
-                                          nullptr, x, n_vec, part);
+                                          nullptr, x, n_vec, part, keep ? 1 : 0);
       if (e != cudaSuccess) return e;
+      p.l2_reread = keep;
       p.part_in = part;
       p.n_part_in = ctas;
       p.amax_out = out->amax;

@@ -92,4 +92,18 @@ int num_sms() {
   return v;
 }
 
+int64_t l2_bytes() {
+  static std::atomic<int64_t> l2[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev < 64) {
+    const int64_t v = l2[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+  }
+  int v = 0;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) != cudaSuccess || v <= 0) return 0;
+  if (dev < 64) l2[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
+
 }  // namespace fp8lin
