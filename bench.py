@@ -1099,6 +1099,133 @@ def run_profile_case(args):
     print(f"profile case {case}: {args.steps} launches done")
 
 
+def run_profile_suite(args):
+    """Every kernel of the library that has no capture of its own, twice each (the second call
+    inside an NVTX range "capture"), one case after another, for one ncu capture; prints the
+    case order, no JSON line. Tensors are 16384 x
+    8192 bf16 (256 MiB, above L2) for the quantizers, 8192 x 16384 for GeLU / dGeLU, and
+    8192 x 4096 x 4096 for the GEMMs; each case frees its memory before the next."""
+    import torch
+    import scaled_quantize_fp8_gb300 as F
+    from scaled_quantize_fp8_gb300 import build as B
+    B.build()
+    g = torch.Generator(device="cuda").manual_seed(0)
+    bf = torch.bfloat16
+    R, C = 16384, 8192
+
+    def randn(r, c, sigma=1.0, dtype=bf):
+        return (torch.randn((r, c), device="cuda", generator=g) * sigma).to(dtype)
+
+    def case(name, fn, prep=None):
+        # the second call runs inside an NVTX range named "capture", which an ncu capture
+        # selects with --nvtx --nvtx-include capture/
+        state = prep() if prep else None
+        torch.cuda.synchronize()
+        print(f"case {name}", flush=True)
+        fn(state)
+        torch.cuda.nvtx.range_push("capture")
+        fn(state)
+        torch.cuda.nvtx.range_pop()
+        torch.cuda.synchronize()
+        del state
+        torch.cuda.empty_cache()
+
+    def quant(kind, role="activation", fmt="e4m3"):
+        rec = F.Recipe(kind=kind, format=fmt)
+
+        def prep():
+            x = randn(R, C)
+            q = F.empty_qtensor(rec, R, C, role)
+            if kind == "delayed":
+                q.scale.fill_(448.0 / 5.0)
+                q.scale_inv.fill_(5.0 / 448.0)
+            ws = torch.empty(max(16, F.workspace_bytes(rec, R, C)), dtype=torch.uint8,
+                             device="cuda")
+            return x, q, ws
+        return lambda st: F.quantize(rec, st[0], role, out=st[1], workspace=st[2]), prep
+
+    for kind, role, fmt in (("tensorwise", "activation", "e4m3"),
+                            ("delayed", "activation", "e4m3"),
+                            ("blockwise", "activation", "e4m3"),
+                            ("blockwise", "weight", "e4m3"),
+                            ("tensorwise", "grad", "hybrid"),
+                            ("blockwise", "grad", "hybrid")):
+        fn, prep = quant(kind, role, fmt)
+        case(f"quantize {kind} {role} {fmt}", fn, prep)
+
+    rec_d = F.Recipe(kind="delayed", amax_history_len=1024)
+
+    def prep_hist():
+        st = F.DelayedState(rec_d)
+        return st, torch.full((1,), 3.0, device="cuda")
+    case("amax_history_update L=1024", lambda st: F.amax_update(rec_d, st[0], st[1]), prep_hist)
+
+    for kind in ("mxfp8", "tensorwise", "blockwise"):
+        rec = F.Recipe(kind=kind)
+
+        def prep_master(rec=rec):
+            w = torch.randn((R, C // 2), device="cuda", generator=g) * 0.02
+            q = F.empty_qtensor(rec, R, C // 2, "weight")
+            ws = torch.empty(max(16, F.workspace_bytes(rec, R, C // 2)), dtype=torch.uint8,
+                             device="cuda")
+            return w, q, ws
+        case(f"quantize_master {kind} fp32 {R}x{C // 2}",
+             lambda st, rec=rec: F.quantize_master(rec, st[0], out=st[1], workspace=st[2]),
+             prep_master)
+
+    rec = F.Recipe(kind="mxfp8")
+
+    def prep_gelu():
+        h = randn(8192, 16384, 2.0)
+        a_q, h_q, _ = F.gelu_quantize(rec, h)
+        return h, a_q, h_q
+    case("gelu_quantize 8192x16384", lambda st: F.gelu_quantize(rec, st[0], a_q=st[1], h_q=st[2]),
+         prep_gelu)
+
+    def prep_dgelu():
+        h = randn(8192, 16384, 2.0)
+        _, h_q, _ = F.gelu_quantize(rec, h)
+        da = randn(8192, 16384, 1e-3)
+        dh_q, _ = F.dgelu_quantize(rec, da, h_q)
+        return da, h_q, dh_q
+    case("dgelu_quantize 8192x16384",
+         lambda st: F.dgelu_quantize(rec, st[0], st[1], dh_q=st[2]), prep_dgelu)
+
+    rec_t = F.Recipe(kind="tensorwise")
+
+    def prep_gemm_t():
+        xq = F.quantize(rec_t, randn(8192, 4096), "activation")
+        wq = F.quantize(rec_t, randn(4096, 4096, 0.02), "weight")
+        return xq, wq, torch.empty((8192, 4096), dtype=bf, device="cuda")
+    case("gemm tensorwise 8192x4096x4096",
+         lambda st: F.linear_fwd(rec_t, st[0], st[1], y=st[2]), prep_gemm_t)
+
+    rec_b = F.Recipe(kind="mxfp8", fp8_wgrad=False)
+
+    def prep_gemm_bf16():
+        xq = F.quantize(rec_b, randn(8192, 4096), "activation", want_row=False)
+        dyq = F.quantize(rec_b, randn(8192, 4096, 1e-3), "grad", want_row=False)
+        return xq, dyq, torch.empty((4096, 4096), dtype=bf, device="cuda")
+    case("gemm bf16 wgrad 4096x4096x8192",
+         lambda st: F.linear_bwd(rec_b, st[1], st[0], None, want_dx=False, dw=st[2]),
+         prep_gemm_bf16)
+    print("profile suite done", flush=True)
+
+
+def run_targets(args):
+    """The benchmark spec's two named targets alone (prints one JSON object, not the benchmark
+    line): the 4096^3 MXFP8 GEMM and every recipe's quantize at 8192 x 4096."""
+    import torch
+    import scaled_quantize_fp8_gb300 as F
+    from scaled_quantize_fp8_gb300 import build as B
+    B.build()
+    dev = torch.device("cuda", 0)
+    hbm, fp8_peak, _ = peaks()
+    print(json.dumps({"gemm_4096_mxfp8": measure_gemm_4096(torch, F, dev, fp8_peak),
+                      "quantize_by_recipe": measure_quantize_by_recipe(torch, F, dev, hbm)}),
+          flush=True)
+
+
 def run_kernels(args):
     """Per-recipe kernel timings (prints one JSON object; not the benchmark line): quantize of an
     8192 x 4096 bf16 activation (row + column copies) and the fprop GEMM 8192 x 4096 x 4096 and
@@ -1180,7 +1307,7 @@ def main():
                     choices=["quant_mx", "quant_tensorwise", "quant_blockwise", "gemm_mx",
                              "gemm_tensorwise", "gemm_blockwise", "gelu_mx", "dgelu_mx",
                              "gemm_gelu_mx", "gemm_dgelu_mx", "gemm_mx_mlp",
-                             "gemm_wgrad_blockwise"])
+                             "gemm_wgrad_blockwise", "suite"])
     ap.add_argument("--rows", type=int, default=16384, help="--profile quant_*: tensor rows")
     ap.add_argument("--cols", type=int, default=8192, help="--profile quant_*: tensor columns")
     ap.add_argument("--gpus", type=int, default=1)
@@ -1189,6 +1316,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="mlp", choices=["mlp"] + sorted(CONFIGS),
                     help="the MXFP8 MLP step (default) or one of the smaller configurations")
+    ap.add_argument("--targets", action="store_true",
+                    help="the 4096^3 MXFP8 GEMM and per-recipe quantize rates only")
     ap.add_argument("--kernels", action="store_true",
                     help="per-recipe quantize and GEMM timings instead of the benchmark step")
     ap.add_argument("--unfused", action="store_true",
@@ -1196,8 +1325,12 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.profile:
+    if args.profile == "suite":
+        run_profile_suite(args)
+    elif args.profile:
         run_profile_case(args)
+    elif args.targets:
+        run_targets(args)
     elif args.kernels:
         run_kernels(args)
     elif args.workload != "mlp" and args.impl != "reference":

@@ -89,6 +89,26 @@ __device__ __forceinline__ float exp2i(int k) {
                    : __uint_as_float(1u << (k + 149));
 }
 
+// The scale alone (the first half of scale_from_amax below, for callers that do not store
+// s_inv).
+__device__ __forceinline__ float scale_only_from_amax(float amax, int margin,
+                                                      float fmax = 448.0f, bool pow2 = false) {
+  float s;
+  if (!(amax > 0.0f) || !(amax <= 3.402823466e38f)) {
+    s = 1.0f;
+  } else {
+    s = __fdiv_rn(fmax, amax);
+  }
+  if (margin != 0) s = __fmul_rn(s, exp2i(-margin));
+  if (s > 3.402823466e38f) s = 3.402823466e38f;
+  if (pow2) {
+    const uint32_t b = __float_as_uint(s);
+    s = __uint_as_float(b >= 0x00800000u ? (b & 0xFF800000u)
+                                         : (b == 0u ? 0u : (0x80000000u >> __clz(b))));
+  }
+  return s;
+}
+
 // Per-tensor / per-block scale from an amax: s = fp32(fmax/amax) * 2^-margin (fmax = 448 for
 // E4M3, 57344 for E5M2), rounded down to a power of two when pow2 is set, s = 1 for
 // amax 0 / Inf / NaN, an infinite s becomes FLT_MAX. Returns s; *s_inv = fp32(1/s).
@@ -215,12 +235,21 @@ __device__ __forceinline__ void store_seg32(void* p, uint4 a, uint4 b, bool lo_o
   }
 }
 
-// 16-byte read-only load with an L2 cache policy (see ptx::l2_evict_last_policy).
+// 16-byte read-only load with an L2 cache policy (see ptx::l2_evict_last_policy). Not
+// volatile: the compiler may batch several of them ahead of their uses (read-only data).
 __device__ __forceinline__ uint4 ldg_nc_v4_policy(const void* p, uint64_t policy) {
   uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p), "l"(policy));
+  asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p), "l"(policy));
+  return v;
+}
+// The same without a policy, also free to be scheduled ahead of its uses.
+__device__ __forceinline__ uint4 ldg_nc_v4_sched(const void* p) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
   return v;
 }
 

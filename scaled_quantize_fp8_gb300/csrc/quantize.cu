@@ -272,29 +272,50 @@ __device__ __forceinline__ void quantize_one_tile(const QuantParams& p, QuantCtl
   // ---- row-wise copy (and the code tile for the transposed copy)
   const bool code_tile = uses_code_tile<MODE>() && !p.col_bf16;
   if (code_tile && p.col != nullptr) __syncthreads();   // every lane holds its bf16 in registers
+  // 1x128 blocks: a row's block spans the 8 lanes with this lane's rr (both h, all cc). Each of
+  // the four rows i of a lane gets its amax from those lanes; lane cc = i then computes that
+  // row's scale (one division pair a lane instead of four) and hands it to the other seven.
+  float s_bw[4] = {1.0f, 1.0f, 1.0f, 1.0f};
+  uint32_t m_bw[4] = {0u, 0u, 0u, 0u};
+  if constexpr (MODE == Q_BW1x128) {
+    if (p.row != nullptr) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint32_t m = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m = absmax_bf16x2(m, w[i][k]);
+        m = fold_bf16x2(m);
+        m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        m_bw[i] = max(m, __shfl_xor_sync(0xffffffffu, m, 16));
+      }
+      const uint32_t mine = cc == 0 ? m_bw[0] : cc == 1 ? m_bw[1] : cc == 2 ? m_bw[2] : m_bw[3];
+      float sinv;
+      const float s_mine = scale_from_amax(amax_from_bits(mine), p.margin, &sinv, fp8_max<F8>(),
+                                           p.pow2);
+      if (h == 0) S.scf_row[32u * cc + 4u * warp + rr] = sinv;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) s_bw[i] = __shfl_sync(0xffffffffu, s_mine, (lane & ~3) | i);
+    }
+  }
   if (p.row != nullptr || code_tile) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint32_t r = 32u * i + 4u * warp + rr;
       float s = s_tile;
       bool nan = tile_nan;
-      if constexpr (MODE == Q_MX || MODE == Q_BW1x128) {
+      if constexpr (MODE == Q_MX) {
         uint32_t m = 0;
 #pragma unroll
         for (int k = 0; k < 8; ++k) m = absmax_bf16x2(m, w[i][k]);
         m = fold_bf16x2(m);
         m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-        if constexpr (MODE == Q_MX) {
-          const uint32_t sb = mx_scale_byte(m, &s);
-          if ((cc & 1) == 0) S.sc_row[(r & 31) * 16 + (r >> 5) * 4 + 2 * h + (cc >> 1)] = uint8_t(sb);
-        } else {
-          m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
-          m = max(m, __shfl_xor_sync(0xffffffffu, m, 16));
-          float sinv;
-          s = scale_from_amax(amax_from_bits(m), p.margin, &sinv, fp8_max<F8>(), p.pow2);
-          if (h == 0 && cc == 0) S.scf_row[r] = sinv;
-        }
+        const uint32_t sb = mx_scale_byte(m, &s);
+        if ((cc & 1) == 0) S.sc_row[(r & 31) * 16 + (r >> 5) * 4 + 2 * h + (cc >> 1)] = uint8_t(sb);
         nan = m > 0x7F80u;
+      } else if constexpr (MODE == Q_BW1x128) {
+        s = s_bw[i];
+        nan = m_bw[i] > 0x7F80u;
       }
       uint4 q4 = make_uint4(encode4<F8>(w[i][0], w[i][1], s), encode4<F8>(w[i][2], w[i][3], s),
                             encode4<F8>(w[i][4], w[i][5], s), encode4<F8>(w[i][6], w[i][7], s));
@@ -395,12 +416,15 @@ __device__ __forceinline__ void quantize_one_tile(const QuantParams& p, QuantCtl
                                 max(S.red_col[2][2 * pp], S.red_col[3][2 * pp]));
         const uint32_t fb = max(max(S.red_col[0][2 * pp + 1], S.red_col[1][2 * pp + 1]),
                                 max(S.red_col[2][2 * pp + 1], S.red_col[3][2 * pp + 1]));
-        float ia, ib;
-        sa = scale_from_amax(amax_from_bits(fa), p.margin, &ia, fp8_max<F8>(), p.pow2);
-        sb = scale_from_amax(amax_from_bits(fb), p.margin, &ib, fp8_max<F8>(), p.pow2);
-        if (q == 0) {
+        if (q == 0) {                  // the threads that store the dequantisation factors
+          float ia, ib;
+          sa = scale_from_amax(amax_from_bits(fa), p.margin, &ia, fp8_max<F8>(), p.pow2);
+          sb = scale_from_amax(amax_from_bits(fb), p.margin, &ib, fp8_max<F8>(), p.pow2);
           S.scf_col[2 * pp] = ia;
           S.scf_col[2 * pp + 1] = ib;
+        } else {
+          sa = scale_only_from_amax(amax_from_bits(fa), p.margin, fp8_max<F8>(), p.pow2);
+          sb = scale_only_from_amax(amax_from_bits(fb), p.margin, fp8_max<F8>(), p.pow2);
         }
       }
       // codes of column 2pp (low halves) and 2pp+1 (high halves), 32 rows each
@@ -590,34 +614,39 @@ __global__ void __launch_bounds__(256, quant_ctas_per_sm<MODE, EPI>())
 }
 
 // Tensorwise first pass: per-CTA max of the 15-bit bf16 magnitudes over a grid-strided
-// sweep of 16-byte vectors (four independent loads in flight per thread). With l2_keep the
-// input is read with an L2 evict_last policy, so the cast pass that follows finds it in L2.
-__global__ void __launch_bounds__(512) amax_partial_kernel(const uint16_t* __restrict__ x,
-                                                           int64_t n_vec,
-                                                           uint32_t* __restrict__ part,
-                                                           int l2_keep) {
+// sweep of 16-byte vectors. Each thread keeps a batch of sixteen independent loads in flight
+// (out-of-range ones read nothing), so a 64 MB tensor takes two round trips to DRAM with
+// tens of MB in flight across the GPU. With KEEP the input is read with an L2 evict_last
+// policy, so the cast pass that follows finds it in L2.
+constexpr int kAmaxThreads = 256;
+constexpr int kAmaxBatch = 16;
+constexpr int kAmaxCtasPerSm = 4;             // 64 registers a thread (the batch is 64 of them)
+template <bool KEEP>
+__device__ __forceinline__ uint4 amax_load(const uint16_t* x, int64_t v, uint64_t pol) {
+  if constexpr (KEEP) return ldg_nc_v4_policy(x + 8 * v, pol);
+  else return ldg_nc_v4_sched(x + 8 * v);
+}
+template <bool KEEP>
+__global__ void __launch_bounds__(kAmaxThreads, kAmaxCtasPerSm)
+    amax_partial_kernel(const uint16_t* __restrict__ x, int64_t n_vec,
+                        uint32_t* __restrict__ part) {
   pdl_launch_dependents();
   pdl_wait();
-  __shared__ uint32_t red[16];
+  __shared__ uint32_t red[kAmaxThreads / 32];
+  uint64_t pol = 0;
+  if constexpr (KEEP) pol = ptx::l2_evict_last_policy();
   uint32_t m = 0;
-  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-  int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (l2_keep) {
-    const uint64_t pol = ptx::l2_evict_last_policy();
-    for (; i + 3 * stride < n_vec; i += 4 * stride) {
-      uint4 a = ldg_nc_v4_policy(x + 8 * i, pol), b = ldg_nc_v4_policy(x + 8 * (i + stride), pol);
-      uint4 c = ldg_nc_v4_policy(x + 8 * (i + 2 * stride), pol);
-      uint4 d = ldg_nc_v4_policy(x + 8 * (i + 3 * stride), pol);
-      m = max(m, max(max(vec_amax_bits(a), vec_amax_bits(b)), max(vec_amax_bits(c), vec_amax_bits(d))));
+  const int64_t stride = int64_t(gridDim.x) * kAmaxThreads;
+  for (int64_t i = int64_t(blockIdx.x) * kAmaxThreads + threadIdx.x; i < n_vec;
+       i += kAmaxBatch * stride) {
+    uint4 v[kAmaxBatch];
+#pragma unroll
+    for (int k = 0; k < kAmaxBatch; ++k) {
+      const int64_t j = i + k * stride;
+      v[k] = j < n_vec ? amax_load<KEEP>(x, j, pol) : make_uint4(0u, 0u, 0u, 0u);
     }
-    for (; i < n_vec; i += stride) m = max(m, vec_amax_bits(ldg_nc_v4_policy(x + 8 * i, pol)));
-  } else {
-    for (; i + 3 * stride < n_vec; i += 4 * stride) {
-      uint4 a = ldg_nc_v4(x + 8 * i), b = ldg_nc_v4(x + 8 * (i + stride));
-      uint4 c = ldg_nc_v4(x + 8 * (i + 2 * stride)), d = ldg_nc_v4(x + 8 * (i + 3 * stride));
-      m = max(m, max(max(vec_amax_bits(a), vec_amax_bits(b)), max(vec_amax_bits(c), vec_amax_bits(d))));
-    }
-    for (; i < n_vec; i += stride) m = max(m, vec_amax_bits(ldg_nc_v4(x + 8 * i)));
+#pragma unroll
+    for (int k = 0; k < kAmaxBatch; ++k) m = max(m, vec_amax_bits(v[k]));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -625,7 +654,7 @@ __global__ void __launch_bounds__(512) amax_partial_kernel(const uint16_t* __res
   __syncthreads();
   if (threadIdx.x == 0) {
     uint32_t r = 0;
-    for (int k = 0; k < int(blockDim.x >> 5); ++k) r = max(r, red[k]);
+    for (int k = 0; k < kAmaxThreads / 32; ++k) r = max(r, red[k]);
     part[blockIdx.x] = r;
   }
 }
@@ -706,8 +735,9 @@ __global__ void __launch_bounds__(1024) amax_history_update_kernel(
 
 int amax_partial_ctas(int64_t n_vec) {
   const int sms = num_sms();
-  int64_t want = (n_vec + 2047) / 2048;                    // >= 4 vectors per thread
-  return int(std::max<int64_t>(1, std::min<int64_t>(want, int64_t(sms) * 4)));
+  // one batch of sixteen vectors per thread, up to one wave of resident CTAs
+  int64_t want = (n_vec + kAmaxThreads * kAmaxBatch - 1) / (kAmaxThreads * kAmaxBatch);
+  return int(std::max<int64_t>(1, std::min<int64_t>(want, int64_t(sms) * kAmaxCtasPerSm)));
 }
 
 size_t quantize_workspace_bytes(int kind, int64_t R, int64_t C) {
@@ -774,8 +804,11 @@ cudaError_t quantize_launch(int kind, int role, int fmt, bool pow2, int margin,
       // Keep the input in L2 between the two passes when it fits in well under half of L2
       // (the codes written by the cast pass share the cache).
       const bool keep = R * C * 2 <= l2_bytes() / 2;
-      const cudaError_t e = launch_kernel(amax_partial_kernel, dim3(ctas), dim3(512), 0, st,
-                                          nullptr, x, n_vec, part, keep ? 1 : 0);
+      const cudaError_t e =
+          keep ? launch_kernel(amax_partial_kernel<true>, dim3(ctas), dim3(kAmaxThreads), 0, st,
+                               nullptr, x, n_vec, part)
+               : launch_kernel(amax_partial_kernel<false>, dim3(ctas), dim3(kAmaxThreads), 0, st,
+                               nullptr, x, n_vec, part);
       if (e != cudaSuccess) return e;
       p.l2_reread = keep;
       p.part_in = part;
