@@ -193,6 +193,10 @@ fp8_status fp8_amax_update(const fp8_recipe *recipe, fp8_amax_history *hist, int
 
 /*
  * fp8_linear_fwd — fprop Y[M,N] = deq(X)[M,K] . deq(W)[N,K]^T (fp32 accumulation).
+ * Source: the Megatron Core "Low-Precision Training Guide", section "When to Use Low
+ * Precision" (the linear layers' GEMMs run on FP8 tensor cores) and section "Recipe
+ * Reference" (what each recipe scales by: one scale per tensor, one E8M0 scale per 1x32
+ * block, 1x128 / 128x128 blocks).
  * Uses x->row and w->row. x and w must come from the same recipe. Tensor scales are applied
  * after accumulation, MXFP8 block scales by the tensor core during accumulation, blockwise
  * scales per 128-wide K chunk. y is bf16 [M][N] (y_fp32 = 0) or fp32 [M][N] (y_fp32 = 1,
@@ -208,10 +212,16 @@ fp8_status fp8_linear_fwd(const fp8_recipe *recipe, const fp8_tensor *x, const f
  * copies cached in the forward pass). Where both copies hold the same codes — per-tensor
  * scales (DELAYED, TENSORWISE) and 128x128 weight tiles (BLOCKWISE, role WEIGHT) — a tensor
  * whose col is NULL is read from its row copy instead, as an MN-major (transposed) tensor-core
- * operand, so those tensors can be quantised with want_col = 0. With recipe->fp8_wgrad == 0 (--fp8-wgrad off) those two
- * column copies are bf16 transposes (see fp8_quantize) and the wgrad GEMM runs in bf16 with
- * fp32 accumulation. dx or dw may be NULL to skip that GEMM. Outputs are bf16 (out_fp32 = 0)
+ * operand, so those tensors can be quantised with want_col = 0. With recipe->fp8_wgrad == 0
+ * (--fp8-wgrad off) those two column copies are bf16 transposes (see fp8_quantize) and the
+ * wgrad GEMM runs in bf16 with fp32 accumulation. dx or dw may be NULL to skip that GEMM. Outputs are bf16 (out_fp32 = 0)
  * or fp32 (out_fp32 = 1).
+ * Source: the MegaDLMs summary "Benefits of Using FP8 Precision with MegaDLMs and Required
+ * Hardware", section "Training Speed Improvements" (the backward pass's GEMMs in FP8), the
+ * TransformerEngine issue "How to reduce cuda memory usage of fp8?" (the backward pass reads
+ * the FP8 copies cached in the forward pass: the transpose on Hopper, the data itself on
+ * Blackwell), and the "Low-Precision Training Guide" section "Numerical Stability Knobs"
+ * (--fp8-wgrad: wgrad in FP8 or in bf16).
  */
 fp8_status fp8_linear_bwd(const fp8_recipe *recipe, const fp8_tensor *dy,
                           const fp8_tensor *x_saved, const fp8_tensor *w, void *dx, void *dw,

@@ -105,8 +105,11 @@ struct QuantCtl {
   int abort_flag;
 };
 constexpr uint32_t kQCtlBytes = 5120;
-template <int EPI>
-__host__ __device__ constexpr int quant_bufs() { return 3; }
+// Per-tensor scales (tensorwise, delayed) convert a tile with fewer registers, so they run
+// three CTAs per SM with two buffers each (one tile in flight while one is converted); the
+// other recipes run two CTAs per SM with three buffers.
+template <int MODE, int EPI>
+__host__ __device__ constexpr int quant_bufs() { return (MODE == Q_TENSOR && EPI == EPI_NONE) ? 2 : 3; }
 template <int EPI>
 __host__ __device__ constexpr uint32_t quant_tiles_off() {
   return kQCtlBytes + quant_table_bytes<EPI>();
@@ -119,10 +122,12 @@ template <int MODE>
 __host__ __device__ constexpr bool uses_code_tile() { return MODE == Q_TENSOR || MODE == Q_BW128; }
 template <int MODE, int EPI>
 __host__ __device__ constexpr uint32_t quant_smem_bytes() {
-  return 1024 + quant_tiles_off<EPI>() + quant_bufs<EPI>() * kQTileBytes;
+  return 1024 + quant_tiles_off<EPI>() + quant_bufs<MODE, EPI>() * kQTileBytes;
 }
 template <int MODE, int EPI>
-__host__ __device__ constexpr int quant_ctas_per_sm() { return 2; }
+__host__ __device__ constexpr int quant_ctas_per_sm() {
+  return (MODE == Q_TENSOR && EPI == EPI_NONE) ? 3 : 2;
+}
 
 // Byte offset of logical 16-byte chunk c (0..7) of row r in a 128-byte-swizzled 128-row block.
 __device__ __forceinline__ uint32_t swz(uint32_t r, uint32_t c) {
@@ -525,7 +530,7 @@ __global__ void __launch_bounds__(256, quant_ctas_per_sm<MODE, EPI>())
   extern __shared__ uint8_t qsm_raw[];
   uint8_t* base = ptx::align_smem<1024>(qsm_raw);
   QuantCtl& S = *reinterpret_cast<QuantCtl*>(base);
-  constexpr int kQBufs = quant_bufs<EPI>();
+  constexpr int kQBufs = quant_bufs<MODE, EPI>();
   uint8_t* tiles = base + quant_tiles_off<EPI>();
   void* table = base + kQCtlBytes;
   const int t = threadIdx.x;
