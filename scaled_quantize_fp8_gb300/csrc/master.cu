@@ -240,7 +240,17 @@ __global__ void __launch_bounds__(1024) amax_finalize_f32_kernel(const uint32_t*
   pdl_wait();
   __shared__ uint32_t red[32];
   uint32_t m = 0;
-  for (int i = threadIdx.x; i < n; i += blockDim.x) m = max(m, part[i]);
+  // eight independent loads in flight per thread
+  for (int base = threadIdx.x; base < n; base += 8 * int(blockDim.x)) {
+    uint32_t v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int j = base + k * int(blockDim.x);
+      v[k] = j < n ? __ldg(part + j) : 0u;
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) m = max(m, v[k]);
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;

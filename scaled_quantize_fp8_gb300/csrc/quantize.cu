@@ -105,11 +105,11 @@ struct QuantCtl {
   int abort_flag;
 };
 constexpr uint32_t kQCtlBytes = 5120;
-// Per-tensor scales (tensorwise, delayed) convert a tile with fewer registers, so they run
-// three CTAs per SM with two buffers each (one tile in flight while one is converted); the
-// other recipes run two CTAs per SM with three buffers.
+// Three tile buffers per CTA (two tiles in flight while one is converted), two CTAs per SM.
+// (Three CTAs of two buffers each, which the per-tensor casts' register count would allow,
+// measured 4-5% slower for tensorwise and delayed at 8192 x 4096.)
 template <int MODE, int EPI>
-__host__ __device__ constexpr int quant_bufs() { return (MODE == Q_TENSOR && EPI == EPI_NONE) ? 2 : 3; }
+__host__ __device__ constexpr int quant_bufs() { return 3; }
 template <int EPI>
 __host__ __device__ constexpr uint32_t quant_tiles_off() {
   return kQCtlBytes + quant_table_bytes<EPI>();
@@ -119,15 +119,13 @@ static_assert(sizeof(QuantCtl) <= kQCtlBytes, "control block too large");
 constexpr uint64_t kQuantWaitBudget = 4000000000ull;   // ~2 s at 2 GHz
 
 template <int MODE>
-__host__ __device__ constexpr bool uses_code_tile() { return MODE == Q_TENSOR || MODE == Q_BW128; }
+__host__ __device__ constexpr bool uses_code_tile() { return false; }
 template <int MODE, int EPI>
 __host__ __device__ constexpr uint32_t quant_smem_bytes() {
   return 1024 + quant_tiles_off<EPI>() + quant_bufs<MODE, EPI>() * kQTileBytes;
 }
 template <int MODE, int EPI>
-__host__ __device__ constexpr int quant_ctas_per_sm() {
-  return (MODE == Q_TENSOR && EPI == EPI_NONE) ? 3 : 2;
-}
+__host__ __device__ constexpr int quant_ctas_per_sm() { return 2; }
 
 // Byte offset of logical 16-byte chunk c (0..7) of row r in a 128-byte-swizzled 128-row block.
 __device__ __forceinline__ uint32_t swz(uint32_t r, uint32_t c) {
@@ -403,11 +401,18 @@ __device__ __forceinline__ void quantize_one_tile(const QuantParams& p, QuantCtl
         const uint32_t r = 32u * q + j;
         x[j] = *reinterpret_cast<const uint32_t*>(hb + swz(r, chunk) + wofs);
       }
+      float sa, sb;
+      bool nan_here;
+      if constexpr (MODE == Q_TENSOR || MODE == Q_BW128) {
+        // one scale for the whole tile: the same codes as the row copy, transposed
+        sa = sb = s_tile;
+        nan_here = tile_nan;
+      } else {
       uint32_t mw = 0;
 #pragma unroll
       for (int j = 0; j < 32; ++j) mw = absmax_bf16x2(mw, x[j]);
       const uint32_t ma = mw & 0x7FFFu, mb = (mw >> 16) & 0x7FFFu;   // columns 2pp and 2pp+1
-      float sa, sb;
+      nan_here = ma > 0x7F80u || mb > 0x7F80u;
       if constexpr (MODE == Q_MX) {
         const uint32_t ba = mx_scale_byte(ma, &sa), bb = mx_scale_byte(mb, &sb);
         const int ca = 2 * pp, cb = 2 * pp + 1;
@@ -432,6 +437,7 @@ __device__ __forceinline__ void quantize_one_tile(const QuantParams& p, QuantCtl
           sb = scale_only_from_amax(amax_from_bits(fb), p.margin, fp8_max<F8>(), p.pow2);
         }
       }
+      }
       // codes of column 2pp (low halves) and 2pp+1 (high halves), 32 rows each
       uint32_t ca[8], cb[8];
       const float2 sab = make_float2(sa, sb);
@@ -445,7 +451,7 @@ __device__ __forceinline__ void quantize_one_tile(const QuantParams& p, QuantCtl
         ca[j] = cvt_fp8x4<F8>(y[0].x, y[1].x, y[2].x, y[3].x);
         cb[j] = cvt_fp8x4<F8>(y[0].y, y[1].y, y[2].y, y[3].y);
       }
-      if ((mw & 0x7FFFu) > 0x7F80u || ((mw >> 16) & 0x7FFFu) > 0x7F80u) {   // NaN present
+      if (nan_here) {                                                   // NaN present
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const uint32_t lo01 = (x[4 * j] & 0xFFFFu) | (x[4 * j + 1] << 16);
@@ -546,27 +552,6 @@ __global__ void __launch_bounds__(256, quant_ctas_per_sm<MODE, EPI>())
   __syncthreads();
   pdl_wait();                      // the previous kernel's writes are visible from here on
 
-  // per-tensor scale once per CTA: tensorwise from the amax partials, delayed from memory
-  float s_tensor = 1.0f;
-  bool tensor_nan = false;
-  if constexpr (MODE == Q_TENSOR) {
-    if (p.scale_in != nullptr) {
-      s_tensor = *p.scale_in;
-    } else {
-      uint32_t m = 0;
-      for (int i = t; i < p.n_part_in; i += 256) m = max(m, p.part_in[i]);
-      m = block_max_u32(m, S.red);
-      tensor_nan = m > 0x7F80u;
-      float sinv;
-      s_tensor = scale_from_amax(amax_from_bits(m), p.margin, &sinv, fp8_max<F8>(), p.pow2);
-      if (blockIdx.x == 0 && t == 0) {
-        *p.amax_out = amax_from_bits(m);
-        *p.scale_out = s_tensor;
-        *p.scale_inv_out = sinv;
-      }
-    }
-  }
-
   // the i-th tile of the walk: in order, or last first for the tensorwise re-read
   auto tile_at = [&](int seq) { return p.l2_reread ? n_tiles - 1 - seq : seq; };
   uint64_t policy = 0;
@@ -592,6 +577,36 @@ __global__ void __launch_bounds__(256, quant_ctas_per_sm<MODE, EPI>())
       if (tl < n_tiles) issue(tl, j);
     }
   }
+  // per-tensor scale once per CTA (the first tiles are already in flight): tensorwise from the
+  // amax partials, delayed from memory
+  float s_tensor = 1.0f;
+  bool tensor_nan = false;
+  if constexpr (MODE == Q_TENSOR) {
+    if (p.scale_in != nullptr) {
+      s_tensor = *p.scale_in;
+    } else {
+      uint32_t m = 0;
+      for (int base = t; base < p.n_part_in; base += 4 * 256) {   // four loads in flight
+        uint32_t v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int j = base + 256 * k;
+          v[k] = j < p.n_part_in ? __ldg(p.part_in + j) : 0u;
+        }
+        m = max(max(m, max(v[0], v[1])), max(v[2], v[3]));
+      }
+      m = block_max_u32(m, S.red);
+      tensor_nan = m > 0x7F80u;
+      float sinv;
+      s_tensor = scale_from_amax(amax_from_bits(m), p.margin, &sinv, fp8_max<F8>(), p.pow2);
+      if (blockIdx.x == 0 && t == 0) {
+        *p.amax_out = amax_from_bits(m);
+        *p.scale_out = s_tensor;
+        *p.scale_inv_out = sinv;
+      }
+    }
+  }
+
   // MLP kernels: fill the GeLU table while the first tiles are in flight
   if constexpr (EPI == EPI_GELU) gelu_table_fill(table, t, 256);
   else if constexpr (EPI == EPI_DGELU) dgelu_table_fill(table, t, 256);
@@ -671,7 +686,17 @@ __global__ void __launch_bounds__(1024) amax_finalize_kernel(const uint32_t* __r
   pdl_wait();
   __shared__ uint32_t red[32];
   uint32_t m = 0;
-  for (int i = threadIdx.x; i < n; i += blockDim.x) m = max(m, part[i]);
+  // eight independent loads in flight per thread
+  for (int base = threadIdx.x; base < n; base += 8 * int(blockDim.x)) {
+    uint32_t v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int j = base + k * int(blockDim.x);
+      v[k] = j < n ? __ldg(part + j) : 0u;
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) m = max(m, v[k]);
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
