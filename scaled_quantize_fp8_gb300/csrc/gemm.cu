@@ -490,11 +490,10 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
         for (int kk = 0; kk < nk; ++kk) {
           uint32_t b = 0;
           if constexpr (MODE == G_BLOCK) {
-            // one partial-sum buffer: the epilogue frees it as soon as it has read a chunk
-            b = 0;
-            if (!wait_bar(&ctl->acce[0], (u & 1u) ^ 1u, ctl, p.status)) goto mma_done;
+            b = u & 1u;
+            if (!wait_bar(&ctl->acce[b], ((u >> 1) & 1u) ^ 1u, ctl, p.status)) goto mma_done;
             ptx::tc_fence_after();
-            d_t = tmem;
+            d_t = tmem + b * kBN;
           }
           // MX: the scale-factor warp signals once the stage's operands have landed and its
           // scales are in TMEM; other modes wait for the operands themselves
@@ -630,21 +629,19 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
           for (int j = 0; j < kCols; ++j) acc[j] = __fmul_rn(acc[j], alpha);
         }
       } else {
-        // Blockwise promotion. TMEM holds the MMA's partial sum P of one 128-wide K chunk in
-        // columns [0, 256) and the running sum S of the chunks so far in [256, 512). For
-        // chunk kb each thread reads its 64 columns of P, frees the buffer (the MMAs of chunk
-        // kb + 1 start at once), and then adds S += P * (s_inv(A row, kb) * s_inv(B, kb)) in
-        // 16-column pieces (read S, two columns per packed FMA, write S back) while those MMAs
-        // run. The last chunk leaves the result in registers for the store. Chunk kb + 1's
-        // scales are fetched while chunk kb is promoted. With per-row B scales (1x128, wgrad)
-        // the warp's 64 column scales of a chunk go from global to the warp's slice of the
-        // (otherwise unused) scale-factor region of shared memory with cp.async, two chunk
-        // buffers a warp, and are read back as broadcasts.
+        // Blockwise promotion: chunk kb's partial sum P (fp32 in TMEM) is added into the
+        // register accumulator as acc += P * (s_inv(A row, kb) * s_inv(B, kb)), two columns
+        // per packed FMA. Chunk kb + 1's scales are fetched while chunk kb is promoted. With
+        // per-row B scales (1x128, wgrad) the warp's 64 column scales of a chunk go straight
+        // from global to the warp's slice of the (otherwise unused) scale-factor region of
+        // shared memory with cp.async, two chunk buffers a warp, and are read back as
+        // broadcasts, so no registers hold them in flight.
         static_assert(MODE != G_BLOCK || B128 || kEpiWarps * kCols * 8 <= G::kStages * kSfStageBytes,
                       "per-warp B-scale buffers fit in the scale-factor region");
-        static_assert(MODE != G_BLOCK || kCols == 64, "promotion works on 64 columns a thread");
         const int kblocks = p.K / 128;
-        const uint32_t t_sum = t_lane + kBN;              // this thread's columns of S
+        float2 acc2[kCols / 2];
+#pragma unroll
+        for (int j = 0; j < kCols / 2; ++j) acc2[j] = make_float2(0.0f, 0.0f);
         auto load_sa = [&](int kb) { return m < p.M ? __ldg(p.a_bs + int64_t(kb) * p.M + m) : 0.0f; };
         auto load_sb = [&](int kb) {
           float v = 0.0f;
@@ -668,7 +665,6 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
           fetch_sb(0);
         }
         bool ok = true;
-        uint32_t pr[kCols];               // this chunk's partials, then (last chunk) the result
         for (int kb = 0; kb < kblocks; ++kb) {
           const float sa = sa_nx;
           const float sb = sb_nx;
@@ -686,68 +682,60 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
             }
             __syncwarp();
           }
-          if (!wait_bar(&ctl->accf[0], u & 1u, ctl, p.status)) {
+          const uint32_t b = u & 1u;
+          if (!wait_bar(&ctl->accf[b], (u >> 1) & 1u, ctl, p.status)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
-          {
-            uint32_t (&lo)[32] = *reinterpret_cast<uint32_t (*)[32]>(pr);
-            uint32_t (&hi)[32] = *reinterpret_cast<uint32_t (*)[32]>(pr + 32);
-            ptx::tmem_ld_32x32b_x32(t_lane, lo);
-            ptx::tmem_ld_32x32b_x32(t_lane + 32, hi);
-          }
-          ptx::tmem_wait_ld();
-          release_acc(0);
-          ++u;
-          const bool first = kb == 0, last = kb + 1 == kblocks;
-          if (!first) ptx::tmem_wait_st();   // the previous chunk's S writes have landed
           const float f = __fmul_rn(sa, sb);
           const float2 f2 = make_float2(f, f), sa2 = make_float2(sa, sa);
-          const float4* sb4 = reinterpret_cast<const float4*>(sbw + (kb & 1) * (kCols / 2));
+          if constexpr (B128 != 0) {
 #pragma unroll
-          for (int c = 0; c < kCols / 16; ++c) {
-            uint32_t sm[16];
-            if (!first) {
-              ptx::tmem_ld_32x32b_x16(t_sum + 16 * c, sm);
+            for (int c = 0; c < kCols / 16; ++c) {
+              uint32_t r[16];
+              ptx::tmem_ld_32x32b_x16(t_lane + b * kBN + 16 * c, r);
               ptx::tmem_wait_ld();
-            }
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              float2 pv = make_float2(__uint_as_float(pr[16 * c + 2 * j]),
-                                      __uint_as_float(pr[16 * c + 2 * j + 1]));
-              const float2 sv = first ? make_float2(0.0f, 0.0f)
-                                      : make_float2(__uint_as_float(sm[2 * j]),
-                                                    __uint_as_float(sm[2 * j + 1]));
-              float2 r;
-              if constexpr (B128 != 0) {
-                r = __ffma2_rn(pv, f2, sv);
-              } else {
-                // (P * s_inv(B column)) * s_inv(A row) + S
-                const float4 q = sb4[(16 * c + 2 * j) >> 2];
-                pv = __fmul2_rn(pv, (j & 1) ? make_float2(q.z, q.w) : make_float2(q.x, q.y));
-                r = __ffma2_rn(pv, sa2, sv);
+              for (int j = 0; j < 8; ++j) {
+                const float2 pr = make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+                acc2[8 * c + j] = __ffma2_rn(pr, f2, acc2[8 * c + j]);
               }
-              pr[16 * c + 2 * j] = __float_as_uint(r.x);
-              pr[16 * c + 2 * j + 1] = __float_as_uint(r.y);
             }
-            if (!last) {
-              uint32_t (&piece)[16] = *reinterpret_cast<uint32_t (*)[16]>(pr + 16 * c);
-              ptx::tmem_st_32x32b_x16(t_sum + 16 * c, piece);
+          } else {
+            // 8 columns a load: the per-column path has fewer registers to spare
+            const float4* sb4 = reinterpret_cast<const float4*>(sbw + (kb & 1) * (kCols / 2));
+#pragma unroll
+            for (int c = 0; c < kCols / 8; ++c) {
+              uint32_t r[8];
+              ptx::tmem_ld_32x32b_x8(t_lane + b * kBN + 8 * c, r);
+              ptx::tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 4; j += 2) {
+                // (P * s_inv(B column)) * s_inv(A row): the partials take the column scale in
+                // place, so no product registers are needed
+                const float4 q = sb4[2 * c + j / 2];
+                float2 p0 = make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+                float2 p1 = make_float2(__uint_as_float(r[2 * j + 2]), __uint_as_float(r[2 * j + 3]));
+                p0 = __fmul2_rn(p0, make_float2(q.x, q.y));
+                p1 = __fmul2_rn(p1, make_float2(q.z, q.w));
+                acc2[4 * c + j] = __ffma2_rn(p0, sa2, acc2[4 * c + j]);
+                acc2[4 * c + j + 1] = __ffma2_rn(p1, sa2, acc2[4 * c + j + 1]);
+              }
             }
           }
+          release_acc(b);
+          ++u;
         }
         if constexpr (B128 == 0) ptx::cp_async_wait<0>();   // nothing left in flight on exit
-        if (!ok) break;
 #pragma unroll
-        for (int j = 0; j < kCols; ++j) acc[j] = __uint_as_float(pr[j]);
+        for (int j = 0; j < kCols / 2; ++j) {
+          acc[2 * j] = acc2[j].x;
+          acc[2 * j + 1] = acc2[j].y;
+        }
+        if (!ok) break;
       }
       store_row<kCols>(p, m, n, acc);
-    }
-    if constexpr (MODE == G_BLOCK) {
-      // no running-sum write may be in flight when TMEM is released
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
     }
     }
   } else if constexpr (MODE == G_MX) {
