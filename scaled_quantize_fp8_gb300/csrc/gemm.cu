@@ -59,11 +59,22 @@ template <int MODE, int EPI>
 __host__ __device__ constexpr int epi_warps() {
   return (EPI != EPI_NONE || MODE == G_BLOCK) ? 16 : 8;
 }
+// First epilogue warp. Blockwise kernels give warpgroup 0 (TMA producer, MMA issuer and two
+// idle warps) the first four warps, so the sixteen promoting epilogue warps form warpgroups of
+// their own and can take registers from warpgroup 0 (setmaxnreg).
+template <int MODE, int EPI>
+__host__ __device__ constexpr int epi_first_warp() { return MODE == G_BLOCK ? 4 : 2; }
+// Register split of the blockwise kernel: launched at kBlockLaunchRegs a thread (20 warps),
+// warpgroup 0 drops to kBlockWg0Regs and the four epilogue warpgroups rise to kBlockEpiRegs.
+// 128 x 32 + 512 x 112 = 640 x 96: the pool the CTA was launched with, exactly.
+constexpr int kBlockLaunchRegs = 96, kBlockWg0Regs = 32, kBlockEpiRegs = 112;
+static_assert(128 * kBlockWg0Regs + 512 * kBlockEpiRegs <= 640 * kBlockLaunchRegs,
+              "register split within the launch pool");
 // MXFP8 kernels add one warp that copies each stage's scale factors into TMEM, so the MMA
 // issuer's instruction stream holds nothing but MMAs.
 template <int MODE, int EPI>
 __host__ __device__ constexpr int gemm_threads() {
-  return 64 + 32 * epi_warps<MODE, EPI>() + (MODE == G_MX ? 32 : 0);
+  return 32 * epi_first_warp<MODE, EPI>() + 32 * epi_warps<MODE, EPI>() + (MODE == G_MX ? 32 : 0);
 }
 constexpr uint32_t kTileABytes = kBM * kBKBytes;      // 16 KiB
 constexpr uint32_t kSfStageBytes = 2048;              // SFA 512 B at 0, SFB 2 x 512 B at 512
@@ -380,179 +391,186 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
   ptx::tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
   pdl_wait();                      // the previous kernel's writes are visible from here on
+  constexpr int kEpiBase = epi_first_warp<MODE, EPI>();
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      ptx::prefetch_tmap(&tmA);
-      ptx::prefetch_tmap(&tmB);
-      if constexpr (MODE == G_MX && CTA2) {
-        ptx::prefetch_tmap(&tmSFA);
-        ptx::prefetch_tmap(&tmSFB);
-      }
-      int s = 0;
-      uint32_t ph = 0;
-      const int kblocks128 = p.K / 128;       // MX scale atoms per operand row tile
-      for (int tile = unit; tile < n_tiles; tile += n_units) {
-        int mt, nt;
-        tile_coords(tile, tiles_m, tiles_n, &mt, &nt);
-        const int m0 = mt * G::kTileM + int(rank) * kBM;
-        const int n0 = nt * kBN + int(rank) * int(kBRows);
-        for (int kk = 0; kk < nk; ++kk) {
-          const int kb = k_block<MODE>(tile, unit, n_units, kk, nk);
-          if (!wait_bar(&ctl->empty[s], ph ^ 1u, ctl, p.status)) goto producer_done;
-          const uint32_t stall = (unit == 0 && tile == 0 && kk == 0) ? p.stall_tx : 0u;
-          uint8_t* a_dst = sA + s * kTileABytes;
-          uint8_t* b_dst = sB + s * G::kTileBBytes;
-          if constexpr (CTA2) {
-            // Both CTAs' loads complete on the leader's barrier, which expects all of them.
-            // MXFP8: each CTA also brings its own 512-byte A-scale atom and both B-scale atoms
-            // of the pair's 256 B rows (the scale-factor arrays are viewed as rows of 256 B).
-            const uint32_t bar = ptx::map_to_rank(&ctl->full[s], 0);
-            constexpr uint32_t sf_bytes = MODE == G_MX ? 512u + 1024u : 0u;
-            if (leader)
-              ptx::mbar_arrive_expect_tx(&ctl->full[s],
-                                         2 * (kTileABytes + G::kTileBBytes + sf_bytes) + stall);
-            // a K-major tile is 128 bytes of K x rows; an MN-major one 128 of M (N) x 128 K rows
-            if (p.a_mn) ptx::tma_load_2d_pair(a_dst, &tmA, m0, kb * kBKElems, bar);
-            else ptx::tma_load_2d_pair(a_dst, &tmA, kb * kBKElems, m0, bar);
-            if (p.b_mn) ptx::tma_load_2d_pair(b_dst, &tmB, n0, kb * kBKElems, bar);
-            else ptx::tma_load_2d_pair(b_dst, &tmB, kb * kBKElems, n0, bar);
-            if constexpr (MODE == G_MX) {
-              uint8_t* sf = sSF + s * kSfStageBytes;
-              const int nb_pair = nt * kBN;                        // first B row of the pair
-              ptx::tma_load_2d_pair(sf, &tmSFA, 0, 2 * ((m0 >> 7) * kblocks128 + kb), bar);
-              ptx::tma_load_2d_pair(sf + 512, &tmSFB, 0,
-                                    2 * ((nb_pair >> 7) * kblocks128 + kb), bar);
-              ptx::tma_load_2d_pair(sf + 1024, &tmSFB, 0,
-                                    2 * (((nb_pair >> 7) + 1) * kblocks128 + kb), bar);
-            }
-          } else {
-            uint32_t bytes = kTileABytes + G::kTileBBytes + stall;
-            const bool sfb_hi = (n0 + 128) < p.N;
-            if constexpr (MODE == G_MX) bytes += 512u + (sfb_hi ? 1024u : 512u);
-            ptx::mbar_arrive_expect_tx(&ctl->full[s], bytes);
-            if (p.a_mn) ptx::tma_load_2d(a_dst, &tmA, m0, kb * kBKElems, &ctl->full[s]);
-            else ptx::tma_load_2d(a_dst, &tmA, kb * kBKElems, m0, &ctl->full[s]);
-            if (p.b_mn) {
-              // the 256-wide B tile as two 128-column boxes, 16 KiB apart
-              ptx::tma_load_2d(b_dst, &tmB, n0, kb * kBKElems, &ctl->full[s]);
-              ptx::tma_load_2d(b_dst + 16384, &tmB, n0 + 128, kb * kBKElems, &ctl->full[s]);
+  if (warp < kEpiBase) {
+    // Warpgroup 0 of the blockwise kernel hands registers to the promoting epilogue warps,
+    // which hold a 64-column accumulator and a 32-column partial-sum piece.
+    if constexpr (MODE == G_BLOCK) ptx::setmaxnreg_dec<kBlockWg0Regs>();
+    if (warp == 0) {
+      // ------------------------------------------------------------ TMA producer
+      if (lane == 0) {
+        ptx::prefetch_tmap(&tmA);
+        ptx::prefetch_tmap(&tmB);
+        if constexpr (MODE == G_MX && CTA2) {
+          ptx::prefetch_tmap(&tmSFA);
+          ptx::prefetch_tmap(&tmSFB);
+        }
+        int s = 0;
+        uint32_t ph = 0;
+        const int kblocks128 = p.K / 128;       // MX scale atoms per operand row tile
+        for (int tile = unit; tile < n_tiles; tile += n_units) {
+          int mt, nt;
+          tile_coords(tile, tiles_m, tiles_n, &mt, &nt);
+          const int m0 = mt * G::kTileM + int(rank) * kBM;
+          const int n0 = nt * kBN + int(rank) * int(kBRows);
+          for (int kk = 0; kk < nk; ++kk) {
+            const int kb = k_block<MODE>(tile, unit, n_units, kk, nk);
+            if (!wait_bar(&ctl->empty[s], ph ^ 1u, ctl, p.status)) goto producer_done;
+            const uint32_t stall = (unit == 0 && tile == 0 && kk == 0) ? p.stall_tx : 0u;
+            uint8_t* a_dst = sA + s * kTileABytes;
+            uint8_t* b_dst = sB + s * G::kTileBBytes;
+            if constexpr (CTA2) {
+              // Both CTAs' loads complete on the leader's barrier, which expects all of them.
+              // MXFP8: each CTA also brings its own 512-byte A-scale atom and both B-scale atoms
+              // of the pair's 256 B rows (the scale-factor arrays are viewed as rows of 256 B).
+              const uint32_t bar = ptx::map_to_rank(&ctl->full[s], 0);
+              constexpr uint32_t sf_bytes = MODE == G_MX ? 512u + 1024u : 0u;
+              if (leader)
+                ptx::mbar_arrive_expect_tx(&ctl->full[s],
+                                           2 * (kTileABytes + G::kTileBBytes + sf_bytes) + stall);
+              // a K-major tile is 128 bytes of K x rows; an MN-major one 128 of M (N) x 128 K rows
+              if (p.a_mn) ptx::tma_load_2d_pair(a_dst, &tmA, m0, kb * kBKElems, bar);
+              else ptx::tma_load_2d_pair(a_dst, &tmA, kb * kBKElems, m0, bar);
+              if (p.b_mn) ptx::tma_load_2d_pair(b_dst, &tmB, n0, kb * kBKElems, bar);
+              else ptx::tma_load_2d_pair(b_dst, &tmB, kb * kBKElems, n0, bar);
+              if constexpr (MODE == G_MX) {
+                uint8_t* sf = sSF + s * kSfStageBytes;
+                const int nb_pair = nt * kBN;                        // first B row of the pair
+                ptx::tma_load_2d_pair(sf, &tmSFA, 0, 2 * ((m0 >> 7) * kblocks128 + kb), bar);
+                ptx::tma_load_2d_pair(sf + 512, &tmSFB, 0,
+                                      2 * ((nb_pair >> 7) * kblocks128 + kb), bar);
+                ptx::tma_load_2d_pair(sf + 1024, &tmSFB, 0,
+                                      2 * (((nb_pair >> 7) + 1) * kblocks128 + kb), bar);
+              }
             } else {
-              ptx::tma_load_2d(b_dst, &tmB, kb * kBKElems, n0, &ctl->full[s]);
-            }
-            if constexpr (MODE == G_MX) {
-              uint8_t* sf = sSF + s * kSfStageBytes;
-              ptx::bulk_load(sf, p.sfa + (int64_t(m0 >> 7) * kblocks128 + kb) * 512, 512,
-                             &ctl->full[s]);
-              ptx::bulk_load(sf + 512, p.sfb + (int64_t(n0 >> 7) * kblocks128 + kb) * 512, 512,
-                             &ctl->full[s]);
-              if (sfb_hi)
-                ptx::bulk_load(sf + 1024,
-                               p.sfb + (int64_t((n0 >> 7) + 1) * kblocks128 + kb) * 512, 512,
+              uint32_t bytes = kTileABytes + G::kTileBBytes + stall;
+              const bool sfb_hi = (n0 + 128) < p.N;
+              if constexpr (MODE == G_MX) bytes += 512u + (sfb_hi ? 1024u : 512u);
+              ptx::mbar_arrive_expect_tx(&ctl->full[s], bytes);
+              if (p.a_mn) ptx::tma_load_2d(a_dst, &tmA, m0, kb * kBKElems, &ctl->full[s]);
+              else ptx::tma_load_2d(a_dst, &tmA, kb * kBKElems, m0, &ctl->full[s]);
+              if (p.b_mn) {
+                // the 256-wide B tile as two 128-column boxes, 16 KiB apart
+                ptx::tma_load_2d(b_dst, &tmB, n0, kb * kBKElems, &ctl->full[s]);
+                ptx::tma_load_2d(b_dst + 16384, &tmB, n0 + 128, kb * kBKElems, &ctl->full[s]);
+              } else {
+                ptx::tma_load_2d(b_dst, &tmB, kb * kBKElems, n0, &ctl->full[s]);
+              }
+              if constexpr (MODE == G_MX) {
+                uint8_t* sf = sSF + s * kSfStageBytes;
+                ptx::bulk_load(sf, p.sfa + (int64_t(m0 >> 7) * kblocks128 + kb) * 512, 512,
                                &ctl->full[s]);
+                ptx::bulk_load(sf + 512, p.sfb + (int64_t(n0 >> 7) * kblocks128 + kb) * 512, 512,
+                               &ctl->full[s]);
+                if (sfb_hi)
+                  ptx::bulk_load(sf + 1024,
+                                 p.sfb + (int64_t((n0 >> 7) + 1) * kblocks128 + kb) * 512, 512,
+                                 &ctl->full[s]);
+              }
+            }
+            if (++s == G::kStages) {
+              s = 0;
+              ph ^= 1u;
             }
           }
-          if (++s == G::kStages) {
-            s = 0;
-            ph ^= 1u;
-          }
         }
+      producer_done:;
       }
-    producer_done:;
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer (leader)
-    if (lane == 0 && leader) {
-      // operand formats (E4M3 = 0, E5M2 = 1) in descriptor bits 7-9 (A) and 10-12 (B)
-      uint32_t idesc = instr_desc<MODE, CTA2>();
-      if constexpr (MODE == G_TENSOR || MODE == G_BLOCK)
-        idesc |= (uint32_t(p.a_fmt) << 7) | (uint32_t(p.b_fmt) << 10) |
-                 (uint32_t(p.a_mn) << 15) | (uint32_t(p.b_mn) << 16);   // operand majorness
-      if constexpr (MODE == G_MX)      // E5M2 gradients of power-of-two blockwise under hybrid
-        idesc |= (uint32_t(p.a_fmt) << 7) | (uint32_t(p.b_fmt) << 10);
-      const uint32_t sf_base = tmem + 256;      // MX scale factors: kSfCols columns a stage
-      int s = 0;
-      uint32_t ph = 0;
-      uint32_t u = 0;
-      auto commit = [&](uint64_t* bar) {
-        if constexpr (CTA2) ptx::mma_commit_pair(bar, 0x3);
-        else ptx::mma_commit(bar);
-      };
-      for (int tile = unit; tile < n_tiles; tile += n_units) {
-        uint32_t d_t = tmem;
-        if constexpr (MODE != G_BLOCK) {
-          const uint32_t b = u % kNumAcc;
-          if (!wait_bar(&ctl->acce[b], ((u / kNumAcc) & 1u) ^ 1u, ctl, p.status)) goto mma_done;
-          ptx::tc_fence_after();
-          d_t = tmem + b * kBN;
-        }
-        for (int kk = 0; kk < nk; ++kk) {
-          uint32_t b = 0;
-          if constexpr (MODE == G_BLOCK) {
-            b = u & 1u;
-            if (!wait_bar(&ctl->acce[b], ((u >> 1) & 1u) ^ 1u, ctl, p.status)) goto mma_done;
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA issuer (leader)
+      if (lane == 0 && leader) {
+        // operand formats (E4M3 = 0, E5M2 = 1) in descriptor bits 7-9 (A) and 10-12 (B)
+        uint32_t idesc = instr_desc<MODE, CTA2>();
+        if constexpr (MODE == G_TENSOR || MODE == G_BLOCK)
+          idesc |= (uint32_t(p.a_fmt) << 7) | (uint32_t(p.b_fmt) << 10) |
+                   (uint32_t(p.a_mn) << 15) | (uint32_t(p.b_mn) << 16);   // operand majorness
+        if constexpr (MODE == G_MX)      // E5M2 gradients of power-of-two blockwise under hybrid
+          idesc |= (uint32_t(p.a_fmt) << 7) | (uint32_t(p.b_fmt) << 10);
+        const uint32_t sf_base = tmem + 256;      // MX scale factors: kSfCols columns a stage
+        int s = 0;
+        uint32_t ph = 0;
+        uint32_t u = 0;
+        auto commit = [&](uint64_t* bar) {
+          if constexpr (CTA2) ptx::mma_commit_pair(bar, 0x3);
+          else ptx::mma_commit(bar);
+        };
+        for (int tile = unit; tile < n_tiles; tile += n_units) {
+          uint32_t d_t = tmem;
+          if constexpr (MODE != G_BLOCK) {
+            const uint32_t b = u % kNumAcc;
+            if (!wait_bar(&ctl->acce[b], ((u / kNumAcc) & 1u) ^ 1u, ctl, p.status)) goto mma_done;
             ptx::tc_fence_after();
             d_t = tmem + b * kBN;
           }
-          // MX: the scale-factor warp signals once the stage's operands have landed and its
-          // scales are in TMEM; other modes wait for the operands themselves
-          uint64_t* ready = MODE == G_MX ? &ctl->sfr[s] : &ctl->full[s];
-          if (!wait_bar(ready, ph, ctl, p.status)) goto mma_done;
-          ptx::tc_fence_after();
-          const uint32_t a_addr = ptx::smem_u32(sA + s * kTileABytes);
-          const uint32_t b_addr = ptx::smem_u32(sB + s * G::kTileBBytes);
-          const uint32_t sfa_t = sf_base + kSfCols * uint32_t(s), sfb_t = sfa_t + 4;
-#pragma unroll
-          for (int k = 0; k < kBKBytes / 32; ++k) {
-            // K-major: rows of 128 bytes of K, the k-th K=32 slice 32 bytes in. MN-major: rows
-            // of 128 MN elements, one per K, the slice 32 rows = 4 KiB in; 8-row swizzle atoms
-            // 1 KiB apart (SBO), 128-column chunks 16 KiB apart (LBO).
-            const uint64_t ad =
-                p.a_mn ? ptx::smem_desc(a_addr + 4096 * k, 16384, 1024, ptx::kSwizzle128B)
-                       : ptx::smem_desc(a_addr + 32 * k, 16, 1024, ptx::kSwizzle128B);
-            const uint64_t bd =
-                p.b_mn ? ptx::smem_desc(b_addr + 4096 * k, 16384, 1024, ptx::kSwizzle128B)
-                       : ptx::smem_desc(b_addr + 32 * k, 16, 1024, ptx::kSwizzle128B);
-            const uint32_t acc_on = MODE == G_BLOCK ? uint32_t(k != 0) : uint32_t((kk | k) != 0);
-            if constexpr (CTA2) {
-              if constexpr (MODE == G_BF16) {
-                ptx::mma_f16_pair(d_t, ad, bd, idesc, acc_on);
+          for (int kk = 0; kk < nk; ++kk) {
+            uint32_t b = 0;
+            if constexpr (MODE == G_BLOCK) {
+              b = u & 1u;
+              if (!wait_bar(&ctl->acce[b], ((u >> 1) & 1u) ^ 1u, ctl, p.status)) goto mma_done;
+              ptx::tc_fence_after();
+              d_t = tmem + b * kBN;
+            }
+            // MX: the scale-factor warp signals once the stage's operands have landed and its
+            // scales are in TMEM; other modes wait for the operands themselves
+            uint64_t* ready = MODE == G_MX ? &ctl->sfr[s] : &ctl->full[s];
+            if (!wait_bar(ready, ph, ctl, p.status)) goto mma_done;
+            ptx::tc_fence_after();
+            const uint32_t a_addr = ptx::smem_u32(sA + s * kTileABytes);
+            const uint32_t b_addr = ptx::smem_u32(sB + s * G::kTileBBytes);
+            const uint32_t sfa_t = sf_base + kSfCols * uint32_t(s), sfb_t = sfa_t + 4;
+  #pragma unroll
+            for (int k = 0; k < kBKBytes / 32; ++k) {
+              // K-major: rows of 128 bytes of K, the k-th K=32 slice 32 bytes in. MN-major: rows
+              // of 128 MN elements, one per K, the slice 32 rows = 4 KiB in; 8-row swizzle atoms
+              // 1 KiB apart (SBO), 128-column chunks 16 KiB apart (LBO).
+              const uint64_t ad =
+                  p.a_mn ? ptx::smem_desc(a_addr + 4096 * k, 16384, 1024, ptx::kSwizzle128B)
+                         : ptx::smem_desc(a_addr + 32 * k, 16, 1024, ptx::kSwizzle128B);
+              const uint64_t bd =
+                  p.b_mn ? ptx::smem_desc(b_addr + 4096 * k, 16384, 1024, ptx::kSwizzle128B)
+                         : ptx::smem_desc(b_addr + 32 * k, 16, 1024, ptx::kSwizzle128B);
+              const uint32_t acc_on = MODE == G_BLOCK ? uint32_t(k != 0) : uint32_t((kk | k) != 0);
+              if constexpr (CTA2) {
+                if constexpr (MODE == G_BF16) {
+                  ptx::mma_f16_pair(d_t, ad, bd, idesc, acc_on);
+                } else if constexpr (MODE == G_MX) {
+                  const uint32_t id = idesc | (uint32_t(k) << 29) | (uint32_t(k) << 4);
+                  ptx::mma_mxf8f6f4_pair(d_t, ad, bd, id, sfa_t, sfb_t, acc_on);
+                } else {
+                  ptx::mma_f8f6f4_pair(d_t, ad, bd, idesc, acc_on);
+                }
               } else if constexpr (MODE == G_MX) {
                 const uint32_t id = idesc | (uint32_t(k) << 29) | (uint32_t(k) << 4);
-                ptx::mma_mxf8f6f4_pair(d_t, ad, bd, id, sfa_t, sfb_t, acc_on);
+                ptx::mma_mxf8f6f4(d_t, ad, bd, id, sfa_t, sfb_t, acc_on);
+              } else if constexpr (MODE == G_BF16) {
+                ptx::mma_f16(d_t, ad, bd, idesc, acc_on);
               } else {
-                ptx::mma_f8f6f4_pair(d_t, ad, bd, idesc, acc_on);
+                ptx::mma_f8f6f4(d_t, ad, bd, idesc, acc_on);
               }
-            } else if constexpr (MODE == G_MX) {
-              const uint32_t id = idesc | (uint32_t(k) << 29) | (uint32_t(k) << 4);
-              ptx::mma_mxf8f6f4(d_t, ad, bd, id, sfa_t, sfb_t, acc_on);
-            } else if constexpr (MODE == G_BF16) {
-              ptx::mma_f16(d_t, ad, bd, idesc, acc_on);
-            } else {
-              ptx::mma_f8f6f4(d_t, ad, bd, idesc, acc_on);
+            }
+            commit(&ctl->empty[s]);
+            if constexpr (MODE == G_BLOCK) {
+              commit(&ctl->accf[b]);
+              ++u;
+            }
+            if (++s == G::kStages) {
+              s = 0;
+              ph ^= 1u;
             }
           }
-          commit(&ctl->empty[s]);
-          if constexpr (MODE == G_BLOCK) {
-            commit(&ctl->accf[b]);
+          if constexpr (MODE != G_BLOCK) {
+            commit(&ctl->accf[u % kNumAcc]);
             ++u;
           }
-          if (++s == G::kStages) {
-            s = 0;
-            ph ^= 1u;
-          }
         }
-        if constexpr (MODE != G_BLOCK) {
-          commit(&ctl->accf[u % kNumAcc]);
-          ++u;
-        }
+      mma_done:;
       }
-    mma_done:;
     }
-  } else if (warp < 2 + kEpiWarps) {
+  } else if (warp < kEpiBase + kEpiWarps) {
     // ------------------------------------------------------------ epilogue warps
-    const int ew = warp - 2;
+    if constexpr (MODE == G_BLOCK) ptx::setmaxnreg_inc<kBlockEpiRegs>();
+    const int ew = warp - kEpiBase;
     const int quad = warp & 3;            // TMEM lane quadrant this warp may access
     constexpr int kCols = 4 * kBN / kEpiWarps;              // accumulator columns per warp
 
@@ -690,37 +708,25 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
           ptx::tc_fence_after();
           const float f = __fmul_rn(sa, sb);
           const float2 f2 = make_float2(f, f), sa2 = make_float2(sa, sa);
-          if constexpr (B128 != 0) {
+          // 32 columns a TMEM load (two round trips a chunk): the epilogue warpgroups run with
+          // kBlockEpiRegs registers, room for the 64-column accumulator and a 32-column piece
+          const float4* sb4 = reinterpret_cast<const float4*>(sbw + (kb & 1) * (kCols / 2));
 #pragma unroll
-            for (int c = 0; c < kCols / 16; ++c) {
-              uint32_t r[16];
-              ptx::tmem_ld_32x32b_x16(t_lane + b * kBN + 16 * c, r);
-              ptx::tmem_wait_ld();
+          for (int c = 0; c < kCols / 32; ++c) {
+            uint32_t r[32];
+            ptx::tmem_ld_32x32b_x32(t_lane + b * kBN + 32 * c, r);
+            ptx::tmem_wait_ld();
 #pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const float2 pr = make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-                acc2[8 * c + j] = __ffma2_rn(pr, f2, acc2[8 * c + j]);
-              }
-            }
-          } else {
-            // 8 columns a load: the per-column path has fewer registers to spare
-            const float4* sb4 = reinterpret_cast<const float4*>(sbw + (kb & 1) * (kCols / 2));
-#pragma unroll
-            for (int c = 0; c < kCols / 8; ++c) {
-              uint32_t r[8];
-              ptx::tmem_ld_32x32b_x8(t_lane + b * kBN + 8 * c, r);
-              ptx::tmem_wait_ld();
-#pragma unroll
-              for (int j = 0; j < 4; j += 2) {
+            for (int j = 0; j < 16; ++j) {
+              float2 pr = make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+              if constexpr (B128 != 0) {
+                acc2[16 * c + j] = __ffma2_rn(pr, f2, acc2[16 * c + j]);
+              } else {
                 // (P * s_inv(B column)) * s_inv(A row): the partials take the column scale in
                 // place, so no product registers are needed
-                const float4 q = sb4[2 * c + j / 2];
-                float2 p0 = make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-                float2 p1 = make_float2(__uint_as_float(r[2 * j + 2]), __uint_as_float(r[2 * j + 3]));
-                p0 = __fmul2_rn(p0, make_float2(q.x, q.y));
-                p1 = __fmul2_rn(p1, make_float2(q.z, q.w));
-                acc2[4 * c + j] = __ffma2_rn(p0, sa2, acc2[4 * c + j]);
-                acc2[4 * c + j + 1] = __ffma2_rn(p1, sa2, acc2[4 * c + j + 1]);
+                const float4 q = sb4[8 * c + (j >> 1)];
+                pr = __fmul2_rn(pr, (j & 1) ? make_float2(q.z, q.w) : make_float2(q.x, q.y));
+                acc2[16 * c + j] = __ffma2_rn(pr, sa2, acc2[16 * c + j]);
               }
             }
           }
@@ -814,10 +820,12 @@ __global__ void __maxnreg__(96)
   gemm_tn_body<G_MX, 1, CTA2, EPI>(tmA, tmB, tmSFA, tmSFB, p);
 }
 
-// Blockwise GEMMs: 16 promoting epilogue warps (18 warps, five on two of the sub-partitions):
-// 96 registers.
+// Blockwise GEMMs: 20 warps (warpgroup 0: TMA producer, MMA issuer and two idle warps; four
+// warpgroups of promoting epilogue warps), launched at kBlockLaunchRegs registers a thread;
+// setmaxnreg then moves registers from warpgroup 0 (kBlockWg0Regs) to the epilogue warpgroups
+// (kBlockEpiRegs).
 template <int MODE, int B128, int CTA2>
-__global__ void __maxnreg__(96)
+__global__ void __maxnreg__(kBlockLaunchRegs)
     gemm_wide_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmSFA,
@@ -868,6 +876,13 @@ static cudaError_t launch_mode(const GemmLaunch& g, cudaStream_t st) {
                                          int(G::kSmemBytes));
     if (e == cudaSuccess && CTA2)
       (void)cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+    if (e == cudaSuccess && MODE == G_BLOCK) {
+      // The blockwise kernel's register split (setmaxnreg) is sized for a launch at exactly
+      // kBlockLaunchRegs a thread; with fewer its epilogue warps could never get theirs.
+      cudaFuncAttributes fa{};
+      e = cudaFuncGetAttributes(&fa, kern);
+      if (e == cudaSuccess && fa.numRegs != kBlockLaunchRegs) e = cudaErrorInvalidConfiguration;
+    }
     return e;
   });
   if (ae != cudaSuccess) return ae;

@@ -190,6 +190,19 @@ __device__ __forceinline__ void tmem_ld_32x32b_x8(uint32_t taddr, uint32_t (&r)[
                  "=r"(r[6]), "=r"(r[7])
                : "r"(taddr));
 }
+// Move registers between the warpgroups of a CTA (all four warps of a warpgroup execute the
+// same instruction): dec gives registers back to the CTA's pool, inc waits until the pool can
+// grant the new count. The counts must add up to at most the registers the CTA was launched
+// with, or an inc waits forever; the host checks the launch count before such a kernel runs.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
