@@ -59,22 +59,28 @@ template <int MODE, int EPI>
 __host__ __device__ constexpr int epi_warps() {
   return (EPI != EPI_NONE || MODE == G_BLOCK) ? 16 : 8;
 }
-// First epilogue warp. Blockwise kernels give warpgroup 0 (TMA producer, MMA issuer and two
-// idle warps) the first four warps, so the sixteen promoting epilogue warps form warpgroups of
-// their own and can take registers from warpgroup 0 (setmaxnreg).
+// Kernels with sixteen epilogue warps (blockwise promotion, fused MLP epilogues) split the
+// register file between warpgroups: warpgroup 0 (warps 0-3: TMA producer, MMA issuer, the
+// MXFP8 scale-factor copier or an idle warp, an idle warp) gives registers to the four
+// epilogue warpgroups (warps 4-19) with setmaxnreg.
 template <int MODE, int EPI>
-__host__ __device__ constexpr int epi_first_warp() { return MODE == G_BLOCK ? 4 : 2; }
-// Register split of the blockwise kernel: launched at kBlockLaunchRegs a thread (20 warps),
-// warpgroup 0 drops to kBlockWg0Regs and the four epilogue warpgroups rise to kBlockEpiRegs.
+__host__ __device__ constexpr bool reg_split() { return MODE == G_BLOCK || EPI != EPI_NONE; }
+// First epilogue warp.
+template <int MODE, int EPI>
+__host__ __device__ constexpr int epi_first_warp() { return reg_split<MODE, EPI>() ? 4 : 2; }
+// The split: launched at kSplitLaunchRegs a thread (20 warps), warpgroup 0 drops to
+// kSplitWg0Regs and the epilogue warpgroups rise to kSplitEpiRegs.
 // 128 x 32 + 512 x 112 = 640 x 96: the pool the CTA was launched with, exactly.
-constexpr int kBlockLaunchRegs = 96, kBlockWg0Regs = 32, kBlockEpiRegs = 112;
-static_assert(128 * kBlockWg0Regs + 512 * kBlockEpiRegs <= 640 * kBlockLaunchRegs,
+constexpr int kSplitLaunchRegs = 96, kSplitWg0Regs = 32, kSplitEpiRegs = 112;
+static_assert(128 * kSplitWg0Regs + 512 * kSplitEpiRegs <= 640 * kSplitLaunchRegs,
               "register split within the launch pool");
 // MXFP8 kernels add one warp that copies each stage's scale factors into TMEM, so the MMA
-// issuer's instruction stream holds nothing but MMAs.
+// issuer's instruction stream holds nothing but MMAs (warp 2 with the register split, else
+// the warp after the epilogue warps).
 template <int MODE, int EPI>
 __host__ __device__ constexpr int gemm_threads() {
-  return 32 * epi_first_warp<MODE, EPI>() + 32 * epi_warps<MODE, EPI>() + (MODE == G_MX ? 32 : 0);
+  return 32 * epi_first_warp<MODE, EPI>() + 32 * epi_warps<MODE, EPI>() +
+         ((MODE == G_MX && !reg_split<MODE, EPI>()) ? 32 : 0);
 }
 constexpr uint32_t kTileABytes = kBM * kBKBytes;      // 16 KiB
 constexpr uint32_t kSfStageBytes = 2048;              // SFA 512 B at 0, SFB 2 x 512 B at 512
@@ -393,10 +399,50 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
   pdl_wait();                      // the previous kernel's writes are visible from here on
   constexpr int kEpiBase = epi_first_warp<MODE, EPI>();
 
+  // ------------------------------------------------------------ scale-factor copier (MXFP8)
+  auto sf_copier = [&]() {
+    // (leader) Once a stage's loads have landed, copy its E8M0 atoms from shared memory into
+    // that stage's TMEM columns (A's own atom, then the pair's two B atoms) and signal the MMA
+    // issuer through sfr. A stage's columns are rewritten only after its smem slot has been
+    // released by the MMAs that read them and refilled.
+    if (lane == 0 && leader) {
+      const uint32_t sf_base = tmem + 256;
+      int s = 0;
+      uint32_t ph = 0;
+      for (int tile = unit; tile < n_tiles; tile += n_units) {
+        for (int kk = 0; kk < nk; ++kk) {
+          if (!wait_bar(&ctl->full[s], ph, ctl, p.status)) goto sf_done;
+          ptx::tc_fence_after();
+          const uint32_t sfa_t = sf_base + kSfCols * uint32_t(s), sfb_t = sfa_t + 4;
+          const uint32_t sf = ptx::smem_u32(sSF + s * kSfStageBytes);
+          const uint64_t d0 = ptx::smem_desc(sf, 0, 128, ptx::kSwizzleNone);
+          const uint64_t d1 = ptx::smem_desc(sf + 512, 0, 128, ptx::kSwizzleNone);
+          const uint64_t d2 = ptx::smem_desc(sf + 1024, 0, 128, ptx::kSwizzleNone);
+          if constexpr (CTA2) {
+            ptx::tmem_cp_32x128b_warpx4_pair(sfa_t, d0);
+            ptx::tmem_cp_32x128b_warpx4_pair(sfb_t, d1);
+            ptx::tmem_cp_32x128b_warpx4_pair(sfb_t + 4, d2);
+            ptx::mma_commit_pair(&ctl->sfr[s], 0x1);     // the leader's barrier only
+          } else {
+            ptx::tmem_cp_32x128b_warpx4(sfa_t, d0);
+            ptx::tmem_cp_32x128b_warpx4(sfb_t, d1);
+            ptx::tmem_cp_32x128b_warpx4(sfb_t + 4, d2);
+            ptx::mma_commit(&ctl->sfr[s]);
+          }
+          if (++s == G::kStages) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+    sf_done:;
+    }
+  };
+
   if (warp < kEpiBase) {
-    // Warpgroup 0 of the blockwise kernel hands registers to the promoting epilogue warps,
-    // which hold a 64-column accumulator and a 32-column partial-sum piece.
-    if constexpr (MODE == G_BLOCK) ptx::setmaxnreg_dec<kBlockWg0Regs>();
+    // With the register split warpgroup 0 hands registers to the epilogue warps (the
+    // blockwise promotion holds a 64-column accumulator and a 32-column partial-sum piece).
+    if constexpr (reg_split<MODE, EPI>()) ptx::setmaxnreg_dec<kSplitWg0Regs>();
     if (warp == 0) {
       // ------------------------------------------------------------ TMA producer
       if (lane == 0) {
@@ -566,10 +612,12 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
         }
       mma_done:;
       }
+    } else if (warp == 2) {
+      if constexpr (MODE == G_MX && reg_split<MODE, EPI>()) sf_copier();
     }
   } else if (warp < kEpiBase + kEpiWarps) {
     // ------------------------------------------------------------ epilogue warps
-    if constexpr (MODE == G_BLOCK) ptx::setmaxnreg_inc<kBlockEpiRegs>();
+    if constexpr (reg_split<MODE, EPI>()) ptx::setmaxnreg_inc<kSplitEpiRegs>();
     const int ew = warp - kEpiBase;
     const int quad = warp & 3;            // TMEM lane quadrant this warp may access
     constexpr int kCols = 4 * kBN / kEpiWarps;              // accumulator columns per warp
@@ -590,8 +638,9 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
       // ---- fused MLP epilogue (MXFP8, single accumulator)
       uint8_t* stage = sEpi + ew * kEpiStageBytes;
       void* table = sEpi + kEpiWarps * kEpiStageBytes;
-      if constexpr (EPI == EPI_GELU) gelu_table_fill(table, int(threadIdx.x) - 64, 32 * kEpiWarps);
-      else dgelu_code_table_fill(table, int(threadIdx.x) - 64, 32 * kEpiWarps);
+      const int et = int(threadIdx.x) - 32 * kEpiBase;       // thread index among them
+      if constexpr (EPI == EPI_GELU) gelu_table_fill(table, et, 32 * kEpiWarps);
+      else dgelu_code_table_fill(table, et, 32 * kEpiWarps);
       asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");   // epilogue warps only
       uint32_t u = 0;
       for (int tile = unit; tile < n_tiles; tile += n_units) {
@@ -709,7 +758,7 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
           const float f = __fmul_rn(sa, sb);
           const float2 f2 = make_float2(f, f), sa2 = make_float2(sa, sa);
           // 32 columns a TMEM load (two round trips a chunk): the epilogue warpgroups run with
-          // kBlockEpiRegs registers, room for the 64-column accumulator and a 32-column piece
+          // kSplitEpiRegs registers, room for the 64-column accumulator and a 32-column piece
           const float4* sb4 = reinterpret_cast<const float4*>(sbw + (kb & 1) * (kCols / 2));
 #pragma unroll
           for (int c = 0; c < kCols / 32; ++c) {
@@ -744,44 +793,8 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
       store_row<kCols>(p, m, n, acc);
     }
     }
-  } else if constexpr (MODE == G_MX) {
-    // ------------------------------------------------------------ scale-factor copier
-    // (leader) Once a stage's loads have landed, copy its E8M0 atoms from shared memory into
-    // that stage's TMEM columns (A's own atom, then the pair's two B atoms) and signal the MMA
-    // issuer through sfr. A stage's columns are rewritten only after its smem slot has been
-    // released by the MMAs that read them and refilled.
-    if (lane == 0 && leader) {
-      const uint32_t sf_base = tmem + 256;
-      int s = 0;
-      uint32_t ph = 0;
-      for (int tile = unit; tile < n_tiles; tile += n_units) {
-        for (int kk = 0; kk < nk; ++kk) {
-          if (!wait_bar(&ctl->full[s], ph, ctl, p.status)) goto sf_done;
-          ptx::tc_fence_after();
-          const uint32_t sfa_t = sf_base + kSfCols * uint32_t(s), sfb_t = sfa_t + 4;
-          const uint32_t sf = ptx::smem_u32(sSF + s * kSfStageBytes);
-          const uint64_t d0 = ptx::smem_desc(sf, 0, 128, ptx::kSwizzleNone);
-          const uint64_t d1 = ptx::smem_desc(sf + 512, 0, 128, ptx::kSwizzleNone);
-          const uint64_t d2 = ptx::smem_desc(sf + 1024, 0, 128, ptx::kSwizzleNone);
-          if constexpr (CTA2) {
-            ptx::tmem_cp_32x128b_warpx4_pair(sfa_t, d0);
-            ptx::tmem_cp_32x128b_warpx4_pair(sfb_t, d1);
-            ptx::tmem_cp_32x128b_warpx4_pair(sfb_t + 4, d2);
-            ptx::mma_commit_pair(&ctl->sfr[s], 0x1);     // the leader's barrier only
-          } else {
-            ptx::tmem_cp_32x128b_warpx4(sfa_t, d0);
-            ptx::tmem_cp_32x128b_warpx4(sfb_t, d1);
-            ptx::tmem_cp_32x128b_warpx4(sfb_t + 4, d2);
-            ptx::mma_commit(&ctl->sfr[s]);
-          }
-          if (++s == G::kStages) {
-            s = 0;
-            ph ^= 1u;
-          }
-        }
-      }
-    sf_done:;
-    }
+  } else if constexpr (MODE == G_MX && !reg_split<MODE, EPI>()) {
+    sf_copier();
   }
 
   __syncthreads();
@@ -810,9 +823,11 @@ __global__ void __maxnreg__(168)
   gemm_tn_body<MODE, B128, CTA2, EPI_NONE>(tmA, tmB, tmSFA, tmSFB, p);
 }
 
-// Fused MLP GEMMs: 19 warps, five on three of the sub-partitions, so at most 96 registers.
+// Fused MLP GEMMs: 20 warps (warpgroup 0: TMA producer, MMA issuer, scale-factor copier, one
+// idle warp; four warpgroups of epilogue warps), launched at kSplitLaunchRegs registers a
+// thread, with the epilogue warpgroups raised to kSplitEpiRegs by setmaxnreg.
 template <int CTA2, int EPI>
-__global__ void __maxnreg__(96)
+__global__ void __maxnreg__(kSplitLaunchRegs)
     gemm_mlp_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmSFA,
@@ -821,11 +836,11 @@ __global__ void __maxnreg__(96)
 }
 
 // Blockwise GEMMs: 20 warps (warpgroup 0: TMA producer, MMA issuer and two idle warps; four
-// warpgroups of promoting epilogue warps), launched at kBlockLaunchRegs registers a thread;
-// setmaxnreg then moves registers from warpgroup 0 (kBlockWg0Regs) to the epilogue warpgroups
-// (kBlockEpiRegs).
+// warpgroups of promoting epilogue warps), launched at kSplitLaunchRegs registers a thread;
+// setmaxnreg then moves registers from warpgroup 0 (kSplitWg0Regs) to the epilogue warpgroups
+// (kSplitEpiRegs).
 template <int MODE, int B128, int CTA2>
-__global__ void __maxnreg__(kBlockLaunchRegs)
+__global__ void __maxnreg__(kSplitLaunchRegs)
     gemm_wide_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmSFA,
@@ -876,12 +891,12 @@ static cudaError_t launch_mode(const GemmLaunch& g, cudaStream_t st) {
                                          int(G::kSmemBytes));
     if (e == cudaSuccess && CTA2)
       (void)cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
-    if (e == cudaSuccess && MODE == G_BLOCK) {
-      // The blockwise kernel's register split (setmaxnreg) is sized for a launch at exactly
-      // kBlockLaunchRegs a thread; with fewer its epilogue warps could never get theirs.
+    if (e == cudaSuccess && reg_split<MODE, EPI>()) {
+      // The register split (setmaxnreg) is sized for a launch at exactly kSplitLaunchRegs a
+      // thread; with fewer the epilogue warps could never get theirs.
       cudaFuncAttributes fa{};
       e = cudaFuncGetAttributes(&fa, kern);
-      if (e == cudaSuccess && fa.numRegs != kBlockLaunchRegs) e = cudaErrorInvalidConfiguration;
+      if (e == cudaSuccess && fa.numRegs != kSplitLaunchRegs) e = cudaErrorInvalidConfiguration;
     }
     return e;
   });
