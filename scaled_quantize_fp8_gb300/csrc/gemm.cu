@@ -59,12 +59,12 @@ template <int MODE, int EPI>
 __host__ __device__ constexpr int epi_warps() {
   return (EPI != EPI_NONE || MODE == G_BLOCK) ? 16 : 8;
 }
-// Kernels with sixteen epilogue warps (blockwise promotion, fused MLP epilogues) split the
-// register file between warpgroups: warpgroup 0 (warps 0-3: TMA producer, MMA issuer, the
-// MXFP8 scale-factor copier or an idle warp, an idle warp) gives registers to the four
-// epilogue warpgroups (warps 4-19) with setmaxnreg.
+// The blockwise kernel splits the register file between warpgroups: warpgroup 0 (warps 0-3:
+// TMA producer, MMA issuer, two idle warps) gives registers to the four promoting epilogue
+// warpgroups (warps 4-19) with setmaxnreg. (The fused MLP epilogues measured 3% slower on
+// dGeLU with the same split, so they keep 19 warps at 96 registers.)
 template <int MODE, int EPI>
-__host__ __device__ constexpr bool reg_split() { return MODE == G_BLOCK || EPI != EPI_NONE; }
+__host__ __device__ constexpr bool reg_split() { return MODE == G_BLOCK; }
 // First epilogue warp.
 template <int MODE, int EPI>
 __host__ __device__ constexpr int epi_first_warp() { return reg_split<MODE, EPI>() ? 4 : 2; }
@@ -823,11 +823,10 @@ __global__ void __maxnreg__(168)
   gemm_tn_body<MODE, B128, CTA2, EPI_NONE>(tmA, tmB, tmSFA, tmSFB, p);
 }
 
-// Fused MLP GEMMs: 20 warps (warpgroup 0: TMA producer, MMA issuer, scale-factor copier, one
-// idle warp; four warpgroups of epilogue warps), launched at kSplitLaunchRegs registers a
-// thread, with the epilogue warpgroups raised to kSplitEpiRegs by setmaxnreg.
+// Fused MLP GEMMs: 19 warps (TMA producer, MMA issuer, 16 epilogue warps, scale-factor
+// copier), five on three of the sub-partitions, so at most 96 registers.
 template <int CTA2, int EPI>
-__global__ void __maxnreg__(kSplitLaunchRegs)
+__global__ void __maxnreg__(96)
     gemm_mlp_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmSFA,

@@ -333,7 +333,10 @@ __device__ __forceinline__ void quantize_one_tile(const QuantParams& p, QuantCtl
   }
 
   if (p.col != nullptr) {
-    __syncthreads();                                   // write-backs / code tile visible
+    // The MLP epilogues wrote their transformed tile back into the buffer (and a code tile
+    // would be read transposed): wait for every lane's writes. Otherwise the column pass reads
+    // the tile as TMA delivered it, which every thread has already seen complete.
+    if constexpr (EPI != EPI_NONE || uses_code_tile<MODE>()) __syncthreads();
     if (p.col_bf16) {
       // ---- column-wise copy in bf16 (wgrad kept in bf16): the plain transpose. Thread
       // (pp, q) owns source columns 2pp, 2pp+1 over rows 32q .. 32q+31 (64 bytes each).
@@ -621,9 +624,9 @@ __global__ void __launch_bounds__(256, quant_ctas_per_sm<MODE, EPI>())
     uint8_t* buf = tiles + b * kQTileBytes;
     quantize_one_tile<MODE, EPI, F8>(p, S, buf, buf, table, tile_at(tile), s_tensor,
                                      tensor_nan);
-    // buffer b is refilled by TMA next iteration: per-tensor and 128x128 scales wrote their
-    // row codes into it with ordinary stores, which must be ordered before the async copy
-    if constexpr (uses_code_tile<MODE>()) ptx::fence_proxy_async_smem();
+    // buffer b is refilled by TMA next iteration: the MLP epilogues wrote their transformed
+    // tile into it with ordinary stores, which must be ordered before the async copy
+    if constexpr (EPI != EPI_NONE || uses_code_tile<MODE>()) ptx::fence_proxy_async_smem();
     __syncthreads();
   }
   if (*reinterpret_cast<volatile int*>(&S.abort_flag)) {
