@@ -253,6 +253,11 @@ __device__ __forceinline__ uint4 ldg_nc_v4_sched(const void* p) {
   return v;
 }
 
+// Bring the L2 line holding p in from DRAM ahead of its use (no register holds anything).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"

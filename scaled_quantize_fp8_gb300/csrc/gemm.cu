@@ -655,13 +655,25 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
         uint4 hc[4];
         uint32_t hsc = 0;
         if constexpr (EPI == EPI_DGELU) {
-          // h's codes and scales do not depend on the accumulator: fetch them first
+          // h's codes and scales do not depend on the accumulator: fetch them first, and ask
+          // L2 for the next tile's (its loads then wait on L2, not on DRAM)
           if (live) {
             const uint8_t* src = p.h_row + int64_t(m) * p.N + n;
 #pragma unroll
             for (int i = 0; i < 4; ++i) hc[i] = ldg_nc_v4(src + 16 * i);
             hsc = __ldg(reinterpret_cast<const uint16_t*>(p.h_scale +
                                                           mx_scale_offset(m, n >> 5, p.N)));
+          }
+          const int nx = tile + n_units;
+          if (nx < n_tiles) {
+            int mt2, nt2;
+            tile_coords(nx, tiles_m, tiles_n, &mt2, &nt2);
+            const int m2 = mt2 * G::kTileM + int(rank) * kBM + row, n2 = nt2 * kBN + slice * kCols;
+            if (m2 < p.M && n2 < p.N) {
+              prefetch_l2(p.h_row + int64_t(m2) * p.N + n2);          // 64 bytes, one line
+              if ((lane & 7) == 0)
+                prefetch_l2(p.h_scale + mx_scale_offset(m2, n2 >> 5, p.N));
+            }
           }
         }
         if (!wait_bar(&ctl->accf[0], u & 1u, ctl, p.status)) break;
