@@ -620,6 +620,21 @@ __global__ void __launch_bounds__(256, quant_ctas_per_sm<MODE, EPI>())
     const int b = i % kQBufs;
     const int ahead = tile + (kQBufs - 1) * int(gridDim.x);
     if (t == 0 && ahead < n_tiles) issue(ahead, (i + kQBufs - 1) % kQBufs);
+    if constexpr (EPI == EPI_DGELU) {
+      // the h codes this lane will read for that tile: into L2 while it is in flight
+      if (ahead < n_tiles) {
+        const int tid = tile_at(ahead);
+        const uint32_t ar0 = uint32_t(tid / p.tiles_c) * kTile, ac0 = uint32_t(tid % p.tiles_c) * kTile;
+        const int lane = t & 31, h = lane >> 4, rr = (lane >> 2) & 3, cc = lane & 3;
+        const uint32_t col = ac0 + 64u * h + 16u * cc;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t r = ar0 + 32u * k + 4u * (t >> 5) + rr;
+          if (r < uint32_t(p.R) && col < uint32_t(p.C))
+            prefetch_l2(p.aux_row + r * uint32_t(p.C) + col);
+        }
+      }
+    }
     if (!quant_wait(S, b, uint32_t(i / kQBufs) & 1u, p.status)) break;
     uint8_t* buf = tiles + b * kQTileBytes;
     quantize_one_tile<MODE, EPI, F8>(p, S, buf, buf, table, tile_at(tile), s_tensor,
