@@ -102,15 +102,10 @@ __host__ __device__ constexpr uint32_t epi_smem_bytes() {
                          : epi_warps<G_MX, EPI>() * kEpiStageBytes +
                                (EPI == EPI_GELU ? kGeluTableBytes : kDgeluCodeTableBytes);
 }
-// Accumulator columns of a tile: 256; blockwise uses 128-column tiles, so that TMEM holds four
-// partial-sum buffers and its promotion reads two K chunks per TMEM round trip.
-template <int MODE>
-__host__ __device__ constexpr int tile_n() { return MODE == G_BLOCK ? 128 : kBN; }
-template <int CTA2, int EPI = EPI_NONE, int TN = kBN>
+template <int CTA2, int EPI = EPI_NONE>
 struct Geo {
-  static constexpr int kStages =
-      CTA2 ? (EPI == EPI_NONE ? 6 : 5) : (EPI == EPI_NONE ? (TN == 128 ? 6 : 4) : 3);
-  static constexpr uint32_t kTileBBytes = (CTA2 ? TN / 2 : TN) * kBKBytes;
+  static constexpr int kStages = CTA2 ? (EPI == EPI_NONE ? 6 : 5) : (EPI == EPI_NONE ? 4 : 3);
+  static constexpr uint32_t kTileBBytes = (CTA2 ? kBN / 2 : kBN) * kBKBytes;
   static constexpr uint32_t kStageBytes = kTileABytes + kTileBBytes + kSfStageBytes;
   static constexpr uint32_t kSmemBytes =
       1024 + kStages * kStageBytes + 512 + epi_smem_bytes<EPI>();
@@ -122,8 +117,8 @@ struct SharedCtl {
   uint64_t full[6];
   uint64_t empty[6];
   uint64_t sfr[6];                  // MX: stage's scale factors are in TMEM
-  uint64_t accf[4];
-  uint64_t acce[4];
+  uint64_t accf[2];
+  uint64_t acce[2];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -174,7 +169,7 @@ __device__ __forceinline__ uint32_t instr_desc() {
   // [4,6) D format (1 = f32) | [7,10) A fmt | [10,13) B fmt | [15] A major | [16] B major
   // | [17,23) N >> 3 | [24,29) M >> 4. E4M3 = 0, bf16 = 1. The pair's MMA has M = 256.
   const uint32_t M = CTA2 ? 2 * kBM : kBM;
-  uint32_t d = (uint32_t(tile_n<MODE>() >> 3) << 17) | ((M >> 4) << 24);
+  uint32_t d = (uint32_t(kBN >> 3) << 17) | ((M >> 4) << 24);
   if constexpr (MODE == G_MX) {
     d |= (1u << 23);                          // scale factors are E8M0
   } else if constexpr (MODE == G_BF16) {
@@ -348,8 +343,7 @@ template <int MODE, int B128, int CTA2, int EPI>
 __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUtensorMap& tmB,
                                              const CUtensorMap& tmSFA, const CUtensorMap& tmSFB,
                                              const GemmParams& p) {
-  constexpr int kTN = tile_n<MODE>();
-  using G = Geo<CTA2, EPI, kTN>;
+  using G = Geo<CTA2, EPI>;
   constexpr int kEpiWarps = epi_warps<MODE, EPI>();
   static_assert(EPI == EPI_NONE || MODE == G_MX, "fused MLP epilogues are MXFP8 only");
   extern __shared__ uint8_t smem_raw[];
@@ -360,10 +354,10 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
   SharedCtl* ctl = reinterpret_cast<SharedCtl*>(sSF + G::kStages * kSfStageBytes);
   uint8_t* sEpi = reinterpret_cast<uint8_t*>(ctl) + 512;   // fused epilogues only
 
-  constexpr int kNumAcc = (MODE == G_MX) ? 1 : (MODE == G_BLOCK ? 4 : 2);
+  constexpr int kNumAcc = (MODE == G_MX) ? 1 : 2;
   constexpr int kElem = (MODE == G_BF16) ? 2 : 1;
   constexpr int kBKElems = kBKBytes / kElem;
-  constexpr uint32_t kBRows = CTA2 ? kTN / 2 : kTN;     // B rows this CTA loads per stage
+  constexpr uint32_t kBRows = CTA2 ? kBN / 2 : kBN;     // B rows this CTA loads per stage
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = CTA2 ? ptx::cluster_rank() : 0u;
@@ -371,7 +365,7 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
   const int unit = CTA2 ? int(blockIdx.x >> 1) : int(blockIdx.x);       // CTA or CTA pair
   const int n_units = CTA2 ? int(gridDim.x >> 1) : int(gridDim.x);
   const int tiles_m = (p.M + G::kTileM - 1) / G::kTileM;
-  const int tiles_n = (p.N + kTN - 1) / kTN;
+  const int tiles_n = (p.N + kBN - 1) / kBN;
   const int n_tiles = tiles_m * tiles_n;
   const int nk = (p.K + kBKElems - 1) / kBKElems;
 
@@ -382,7 +376,7 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
       ptx::mbar_init(&ctl->empty[s], 1);
       ptx::mbar_init(&ctl->sfr[s], 1);
     }
-    for (int b = 0; b < 4; ++b) {
+    for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&ctl->accf[b], 1);
       ptx::mbar_init(&ctl->acce[b], CTA2 ? 2 * kEpiWarps : kEpiWarps);
     }
@@ -465,7 +459,7 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
           int mt, nt;
           tile_coords(tile, tiles_m, tiles_n, &mt, &nt);
           const int m0 = mt * G::kTileM + int(rank) * kBM;
-          const int n0 = nt * kTN + int(rank) * int(kBRows);
+          const int n0 = nt * kBN + int(rank) * int(kBRows);
           for (int kk = 0; kk < nk; ++kk) {
             const int kb = k_block<MODE>(tile, unit, n_units, kk, nk);
             if (!wait_bar(&ctl->empty[s], ph ^ 1u, ctl, p.status)) goto producer_done;
@@ -488,7 +482,7 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
               else ptx::tma_load_2d_pair(b_dst, &tmB, kb * kBKElems, n0, bar);
               if constexpr (MODE == G_MX) {
                 uint8_t* sf = sSF + s * kSfStageBytes;
-                const int nb_pair = nt * kTN;                        // first B row of the pair
+                const int nb_pair = nt * kBN;                        // first B row of the pair
                 ptx::tma_load_2d_pair(sf, &tmSFA, 0, 2 * ((m0 >> 7) * kblocks128 + kb), bar);
                 ptx::tma_load_2d_pair(sf + 512, &tmSFB, 0,
                                       2 * ((nb_pair >> 7) * kblocks128 + kb), bar);
@@ -503,10 +497,9 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
               if (p.a_mn) ptx::tma_load_2d(a_dst, &tmA, m0, kb * kBKElems, &ctl->full[s]);
               else ptx::tma_load_2d(a_dst, &tmA, kb * kBKElems, m0, &ctl->full[s]);
               if (p.b_mn) {
-                // the B tile as 128-column boxes, 16 KiB apart
+                // the 256-wide B tile as two 128-column boxes, 16 KiB apart
                 ptx::tma_load_2d(b_dst, &tmB, n0, kb * kBKElems, &ctl->full[s]);
-                if constexpr (kTN > 128)
-                  ptx::tma_load_2d(b_dst + 16384, &tmB, n0 + 128, kb * kBKElems, &ctl->full[s]);
+                ptx::tma_load_2d(b_dst + 16384, &tmB, n0 + 128, kb * kBKElems, &ctl->full[s]);
               } else {
                 ptx::tma_load_2d(b_dst, &tmB, kb * kBKElems, n0, &ctl->full[s]);
               }
@@ -554,16 +547,15 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
             const uint32_t b = u % kNumAcc;
             if (!wait_bar(&ctl->acce[b], ((u / kNumAcc) & 1u) ^ 1u, ctl, p.status)) goto mma_done;
             ptx::tc_fence_after();
-            d_t = tmem + b * kTN;
+            d_t = tmem + b * kBN;
           }
           for (int kk = 0; kk < nk; ++kk) {
             uint32_t b = 0;
             if constexpr (MODE == G_BLOCK) {
-              // each K chunk into the next of the four partial-sum buffers
-              b = u % kNumAcc;
-              if (!wait_bar(&ctl->acce[b], ((u / kNumAcc) & 1u) ^ 1u, ctl, p.status)) goto mma_done;
+              b = u & 1u;
+              if (!wait_bar(&ctl->acce[b], ((u >> 1) & 1u) ^ 1u, ctl, p.status)) goto mma_done;
               ptx::tc_fence_after();
-              d_t = tmem + b * kTN;
+              d_t = tmem + b * kBN;
             }
             // MX: the scale-factor warp signals once the stage's operands have landed and its
             // scales are in TMEM; other modes wait for the operands themselves
@@ -628,7 +620,7 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
     if constexpr (reg_split<MODE, EPI>()) ptx::setmaxnreg_inc<kSplitEpiRegs>();
     const int ew = warp - kEpiBase;
     const int quad = warp & 3;            // TMEM lane quadrant this warp may access
-    constexpr int kCols = 4 * kTN / kEpiWarps;              // accumulator columns per warp
+    constexpr int kCols = 4 * kBN / kEpiWarps;              // accumulator columns per warp
 
     const int slice = ew >> 2;            // which kCols columns of the 256-wide tile
     const int row = 32 * quad + lane;
@@ -655,7 +647,7 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
         int mt, nt;
         tile_coords(tile, tiles_m, tiles_n, &mt, &nt);
         const int m0 = mt * G::kTileM + int(rank) * kBM;
-        const int n0 = nt * kTN;
+        const int n0 = nt * kBN;
         const int m = m0 + row, n = n0 + slice * kCols;
         const int mrow0 = m0 + 32 * quad;
         // M and N are multiples of 128, so a warp's 32 rows x 64 columns are all in or all out
@@ -676,7 +668,7 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
           if (nx < n_tiles) {
             int mt2, nt2;
             tile_coords(nx, tiles_m, tiles_n, &mt2, &nt2);
-            const int m2 = mt2 * G::kTileM + int(rank) * kBM + row, n2 = nt2 * kTN + slice * kCols;
+            const int m2 = mt2 * G::kTileM + int(rank) * kBM + row, n2 = nt2 * kBN + slice * kCols;
             if (m2 < p.M && n2 < p.N) {
               prefetch_l2(p.h_row + int64_t(m2) * p.N + n2);          // 64 bytes, one line
               if ((lane & 7) == 0)
@@ -701,13 +693,13 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
       int mt, nt;
       tile_coords(tile, tiles_m, tiles_n, &mt, &nt);
       const int m0 = mt * G::kTileM + int(rank) * kBM;
-      const int n0 = nt * kTN;
+      const int n0 = nt * kBN;
       const int m = m0 + row, n = n0 + slice * kCols;
       if constexpr (MODE != G_BLOCK) {
         const uint32_t b = u % kNumAcc;
         if (!wait_bar(&ctl->accf[b], (u / kNumAcc) & 1u, ctl, p.status)) break;
         ptx::tc_fence_after();
-        tmem_load_cols<kCols>(t_lane + b * kTN, acc);
+        tmem_load_cols<kCols>(t_lane + b * kBN, acc);
         ptx::tmem_wait_ld();
         release_acc(b);
         ++u;
@@ -716,118 +708,91 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
           for (int j = 0; j < kCols; ++j) acc[j] = __fmul_rn(acc[j], alpha);
         }
       } else {
-        // Blockwise promotion (128 x 128 tiles, 32 columns a thread): chunk kb's partial sum P
-        // (fp32, in the next of four 128-column TMEM buffers) is added into the register
-        // accumulator as acc += P * (s_inv(A row, kb) * s_inv(B, kb)), two columns per packed
-        // FMA, chunks in order. Two chunks are read per TMEM round trip (both loads in flight,
-        // one wait), which halves the promotion's round trips; the MMA issuer runs up to three
-        // chunks ahead. The next pair's scales are fetched while a pair is promoted. With
-        // per-row B scales (1x128, wgrad) the warp's 32 column scales of a chunk go straight
+        // Blockwise promotion: chunk kb's partial sum P (fp32 in TMEM) is added into the
+        // register accumulator as acc += P * (s_inv(A row, kb) * s_inv(B, kb)), two columns
+        // per packed FMA. Chunk kb + 1's scales are fetched while chunk kb is promoted. With
+        // per-row B scales (1x128, wgrad) the warp's 64 column scales of a chunk go straight
         // from global to the warp's slice of the (otherwise unused) scale-factor region of
-        // shared memory with cp.async (four chunk buffers a warp: the pair being promoted and
-        // the next) and are read back as broadcasts.
-        static_assert(MODE != G_BLOCK || kCols == 32, "promotion works on 32 columns a thread");
-        static_assert(MODE != G_BLOCK || B128 ||
-                          kEpiWarps * 4 * (kCols / 2) * 8 <= G::kStages * kSfStageBytes,
+        // shared memory with cp.async, two chunk buffers a warp, and are read back as
+        // broadcasts, so no registers hold them in flight.
+        static_assert(MODE != G_BLOCK || B128 || kEpiWarps * kCols * 8 <= G::kStages * kSfStageBytes,
                       "per-warp B-scale buffers fit in the scale-factor region");
         const int kblocks = p.K / 128;
         float2 acc2[kCols / 2];
 #pragma unroll
         for (int j = 0; j < kCols / 2; ++j) acc2[j] = make_float2(0.0f, 0.0f);
-        auto load_sa = [&](int kb) {
-          return (m < p.M && kb < kblocks) ? __ldg(p.a_bs + int64_t(kb) * p.M + m) : 0.0f;
-        };
+        auto load_sa = [&](int kb) { return m < p.M ? __ldg(p.a_bs + int64_t(kb) * p.M + m) : 0.0f; };
         auto load_sb = [&](int kb) {
           float v = 0.0f;
-          if (n < p.N && kb < kblocks)
+          if (n < p.N)
             v = p.b_mn ? __ldg(p.b_bs + int64_t(kb) * (p.N >> 7) + (n >> 7))   // grid [K][N]
                        : __ldg(p.b_bs + int64_t(n >> 7) * kblocks + kb);        // grid [N][K]
           return v;
         };
-        float2* sbw = reinterpret_cast<float2*>(sSF) + ew * (4 * (kCols / 2));  // 4 x 16 float2
-        auto fetch_pair = [&](int kb) {              // chunks kb, kb + 1: one cp.async group
-          if (lane < kCols / 2) {
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              const int k = kb + c;
-              float2* dst = sbw + (k & 3) * (kCols / 2) + lane;
-              if (k < kblocks && n < p.N)
-                ptx::cp_async_8(dst, p.b_bs + int64_t(k) * p.N + n + 2 * lane);
-              else
-                *dst = make_float2(0.0f, 0.0f);
-            }
-          }
+        float2* sbw = reinterpret_cast<float2*>(sSF) + ew * kCols;      // 2 x 32 float2
+        auto fetch_sb = [&](int kb) {
+          float2* dst = sbw + (kb & 1) * (kCols / 2) + lane;
+          if (n < p.N) ptx::cp_async_8(dst, p.b_bs + int64_t(kb) * p.N + n + 2 * lane);
+          else *dst = make_float2(0.0f, 0.0f);
           ptx::cp_async_commit();
         };
-        auto promote = [&](const uint32_t (&r)[32], float sa, float sb, int buf) {
-          if constexpr (B128 != 0) {
-            const float f = __fmul_rn(sa, sb);
-            const float2 f2 = make_float2(f, f);
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              acc2[j] = __ffma2_rn(make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])),
-                                   f2, acc2[j]);
-          } else {
-            // (P * s_inv(B column)) * s_inv(A row): the partials take the column scale in
-            // place, so no product registers are needed
-            const float2 sa2 = make_float2(sa, sa);
-            const float4* sb4 = reinterpret_cast<const float4*>(sbw + buf * (kCols / 2));
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float4 q = sb4[j >> 1];
-              float2 pr = make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-              pr = __fmul2_rn(pr, (j & 1) ? make_float2(q.z, q.w) : make_float2(q.x, q.y));
-              acc2[j] = __ffma2_rn(pr, sa2, acc2[j]);
-            }
-          }
-        };
-        float sa_nx0 = load_sa(0), sa_nx1 = load_sa(1);
-        float sb_nx0 = 0.0f, sb_nx1 = 0.0f;
-        if constexpr (B128 != 0) {
-          sb_nx0 = load_sb(0);
-          sb_nx1 = load_sb(1);
-        } else {
-          __syncwarp();                    // the previous tile's reads of these buffers are done
-          fetch_pair(0);
+        float sa_nx = load_sa(0);
+        float sb_nx = 0.0f;
+        if constexpr (B128 != 0) sb_nx = load_sb(0);
+        else {
+          __syncwarp();                    // the previous tile's reads of buffer 0 are done
+          fetch_sb(0);
         }
         bool ok = true;
-        for (int kb = 0; kb < kblocks; kb += 2) {
-          const bool two = kb + 1 < kblocks;
-          const float sa0 = sa_nx0, sa1 = sa_nx1, sb0 = sb_nx0, sb1 = sb_nx1;
-          if (kb + 2 < kblocks) {
-            sa_nx0 = load_sa(kb + 2);
-            sa_nx1 = load_sa(kb + 3);
-            if constexpr (B128 != 0) {
-              sb_nx0 = load_sb(kb + 2);
-              sb_nx1 = load_sb(kb + 3);
-            }
+        for (int kb = 0; kb < kblocks; ++kb) {
+          const float sa = sa_nx;
+          const float sb = sb_nx;
+          if (kb + 1 < kblocks) {
+            sa_nx = load_sa(kb + 1);
+            if constexpr (B128 != 0) sb_nx = load_sb(kb + 1);
           }
           if constexpr (B128 == 0) {
-            __syncwarp();                  // the pair before is done with the other buffers
-            if (kb + 2 < kblocks) {
-              fetch_pair(kb + 2);
-              ptx::cp_async_wait<1>();     // this pair's group has landed
+            __syncwarp();                  // chunk kb - 1's reads of the other buffer are done
+            if (kb + 1 < kblocks) {
+              fetch_sb(kb + 1);
+              ptx::cp_async_wait<1>();     // chunk kb's group has landed
             } else {
               ptx::cp_async_wait<0>();
             }
             __syncwarp();
           }
-          const uint32_t b0 = u % kNumAcc, b1 = (u + 1) % kNumAcc;
-          if (!wait_bar(&ctl->accf[b0], (u / kNumAcc) & 1u, ctl, p.status) ||
-              (two && !wait_bar(&ctl->accf[b1], ((u + 1) / kNumAcc) & 1u, ctl, p.status))) {
+          const uint32_t b = u & 1u;
+          if (!wait_bar(&ctl->accf[b], (u >> 1) & 1u, ctl, p.status)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
-          uint32_t r0[32], r1[32];
-          ptx::tmem_ld_32x32b_x32(t_lane + b0 * kTN, r0);
-          if (two) ptx::tmem_ld_32x32b_x32(t_lane + b1 * kTN, r1);
-          ptx::tmem_wait_ld();
-          release_acc(b0);
-          if (two) release_acc(b1);
-          u += two ? 2u : 1u;
-          promote(r0, sa0, sb0, kb & 3);
-          if (two) promote(r1, sa1, sb1, (kb + 1) & 3);
+          const float f = __fmul_rn(sa, sb);
+          const float2 f2 = make_float2(f, f), sa2 = make_float2(sa, sa);
+          // 32 columns a TMEM load (two round trips a chunk): the epilogue warpgroups run with
+          // kSplitEpiRegs registers, room for the 64-column accumulator and a 32-column piece
+          const float4* sb4 = reinterpret_cast<const float4*>(sbw + (kb & 1) * (kCols / 2));
+#pragma unroll
+          for (int c = 0; c < kCols / 32; ++c) {
+            uint32_t r[32];
+            ptx::tmem_ld_32x32b_x32(t_lane + b * kBN + 32 * c, r);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              float2 pr = make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+              if constexpr (B128 != 0) {
+                acc2[16 * c + j] = __ffma2_rn(pr, f2, acc2[16 * c + j]);
+              } else {
+                // (P * s_inv(B column)) * s_inv(A row): the partials take the column scale in
+                // place, so no product registers are needed
+                const float4 q = sb4[8 * c + (j >> 1)];
+                pr = __fmul2_rn(pr, (j & 1) ? make_float2(q.z, q.w) : make_float2(q.x, q.y));
+                acc2[16 * c + j] = __ffma2_rn(pr, sa2, acc2[16 * c + j]);
+              }
+            }
+          }
+          release_acc(b);
+          ++u;
         }
         if constexpr (B128 == 0) ptx::cp_async_wait<0>();   // nothing left in flight on exit
 #pragma unroll
@@ -906,8 +871,7 @@ static bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, i
 
 template <int MODE, int B128, int CTA2, int EPI = EPI_NONE>
 static cudaError_t launch_mode(const GemmLaunch& g, cudaStream_t st) {
-  constexpr int kTN = tile_n<MODE>();
-  using G = Geo<CTA2, EPI, kTN>;
+  using G = Geo<CTA2, EPI>;
   static_assert(EPI == EPI_NONE || (MODE == G_MX && B128 == 1), "fused: MXFP8 only");
   CUtensorMap ma, mb;
   const int eb = MODE == G_BF16 ? 2 : 1;
@@ -916,7 +880,7 @@ static cudaError_t launch_mode(const GemmLaunch& g, cudaStream_t st) {
   const bool okA = g.p.a_mn ? make_tmap_2d(&ma, g.A, 1, g.p.M, g.p.K, 128, kBKBytes, true)
                             : make_operand_map(&ma, g.A, g.p.M, g.p.K, eb, kBM);
   const bool okB = g.p.b_mn ? make_tmap_2d(&mb, g.B, 1, g.p.N, g.p.K, 128, kBKBytes, true)
-                            : make_operand_map(&mb, g.B, g.p.N, g.p.K, eb, CTA2 ? kTN / 2 : kTN);
+                            : make_operand_map(&mb, g.B, g.p.N, g.p.K, eb, CTA2 ? kBN / 2 : kBN);
   if (!okA || !okB) return cudaErrorInvalidValue;
   // MXFP8 scale arrays viewed as rows of 256 bytes (two rows per 512-byte atom) for TMA.
   CUtensorMap msfa = ma, msfb = mb;
@@ -949,7 +913,7 @@ static cudaError_t launch_mode(const GemmLaunch& g, cudaStream_t st) {
   });
   if (ae != cudaSuccess) return ae;
   const int sms = num_sms();
-  const int tiles = ((g.p.M + G::kTileM - 1) / G::kTileM) * ((g.p.N + kTN - 1) / kTN);
+  const int tiles = ((g.p.M + G::kTileM - 1) / G::kTileM) * ((g.p.N + kBN - 1) / kBN);
   const int units = std::max(1, std::min(tiles, CTA2 ? sms / 2 : sms));
   cudaLaunchAttribute cluster;
   cluster.id = cudaLaunchAttributeClusterDimension;

@@ -47,10 +47,10 @@ def _oracle_fprop(kind, xb, wb):
 
 
 # mxfp8: CTA pair with the scale-factor warp (256 x 256 tiles); tensorwise: CTA pair, two
-# accumulators; blockwise: single CTA with the per-chunk promotion (128 x 128 tiles)
+# accumulators; blockwise: single CTA with the per-chunk promotion (128 x 256 tiles)
 @pytest.mark.parametrize("kind,M,N,K,tile", [("mxfp8", 256, 256, 512, (256, 256)),
                                               ("tensorwise", 512, 512, 256, (256, 256)),
-                                              ("blockwise", 256, 512, 512, (128, 128))])
+                                              ("blockwise", 256, 512, 512, (128, 256))])
 def test_stalled_gemm_reports_timeout_and_context_survives(kind, M, N, K, tile):
     rec, xb, wb, xq, wq = _operands(kind, M, N, K, seed=120)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
