@@ -152,6 +152,9 @@ struct GemmParams {
   // (pair) expects, so that stage's barrier never completes and the kernel's bounded waits
   // run out (fp8_test_linear_fwd_stalled).
   uint32_t stall_tx;
+  // Tile order: 0 walks a group of M tiles first (A's panels are reused from L2 across the
+  // rounds of tiles), 1 a group of N tiles (B's panels are). The host picks the smaller operand.
+  int group_n;
 };
 
 struct GemmLaunch {
