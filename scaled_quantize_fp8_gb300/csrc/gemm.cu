@@ -542,9 +542,28 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
         if constexpr (MODE == G_MX)      // E5M2 gradients of power-of-two blockwise under hybrid
           idesc |= (uint32_t(p.a_fmt) << 7) | (uint32_t(p.b_fmt) << 10);
         const uint32_t sf_base = tmem + 256;      // MX scale factors: kSfCols columns a stage
+        // Operand descriptors of stage 0's first K = 32 slice. Between stages and slices only the
+        // start-address field (bits 0-13, 16-byte units) changes, and an address inside shared
+        // memory never carries out of it, so the loop steps the descriptors by plain adds.
+        // K-major: rows of 128 bytes of K, the k-th slice 32 bytes in. MN-major: rows of 128 MN
+        // elements, one per K, the slice 32 rows = 4 KiB in; 8-row swizzle atoms 1 KiB apart
+        // (SBO), 128-column chunks 16 KiB apart (LBO).
+        const uint64_t adesc0 =
+            ptx::smem_desc(ptx::smem_u32(sA), p.a_mn ? 16384 : 16, 1024, ptx::kSwizzle128B);
+        const uint64_t bdesc0 =
+            ptx::smem_desc(ptx::smem_u32(sB), p.b_mn ? 16384 : 16, 1024, ptx::kSwizzle128B);
+        const uint32_t astep = p.a_mn ? 4096 / 16 : 32 / 16, bstep = p.b_mn ? 4096 / 16 : 32 / 16;
+        // MX: the instruction descriptor of K slice k also selects the slice's scale factors
+        uint32_t idk[kBKBytes / 32];
+  #pragma unroll
+        for (int k = 0; k < kBKBytes / 32; ++k)
+          idk[k] = MODE == G_MX ? idesc | (uint32_t(k) << 29) | (uint32_t(k) << 4) : idesc;
         int s = 0;
         uint32_t ph = 0;
         uint32_t u = 0;
+        // stage s's operand descriptors and scale-factor columns, stepped with s
+        uint64_t ad_s = adesc0, bd_s = bdesc0;
+        uint32_t sfa_t = sf_base;
         auto commit = [&](uint64_t* bar) {
           if constexpr (CTA2) ptx::mma_commit_pair(bar, 0x3);
           else ptx::mma_commit(bar);
@@ -570,33 +589,22 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
             uint64_t* ready = MODE == G_MX ? &ctl->sfr[s] : &ctl->full[s];
             if (!wait_bar(ready, ph, ctl, p.status)) goto mma_done;
             ptx::tc_fence_after();
-            const uint32_t a_addr = ptx::smem_u32(sA + s * kTileABytes);
-            const uint32_t b_addr = ptx::smem_u32(sB + s * G::kTileBBytes);
-            const uint32_t sfa_t = sf_base + kSfCols * uint32_t(s), sfb_t = sfa_t + 4;
+            const uint32_t sfb_t = sfa_t + 4;
   #pragma unroll
             for (int k = 0; k < kBKBytes / 32; ++k) {
-              // K-major: rows of 128 bytes of K, the k-th K=32 slice 32 bytes in. MN-major: rows
-              // of 128 MN elements, one per K, the slice 32 rows = 4 KiB in; 8-row swizzle atoms
-              // 1 KiB apart (SBO), 128-column chunks 16 KiB apart (LBO).
-              const uint64_t ad =
-                  p.a_mn ? ptx::smem_desc(a_addr + 4096 * k, 16384, 1024, ptx::kSwizzle128B)
-                         : ptx::smem_desc(a_addr + 32 * k, 16, 1024, ptx::kSwizzle128B);
-              const uint64_t bd =
-                  p.b_mn ? ptx::smem_desc(b_addr + 4096 * k, 16384, 1024, ptx::kSwizzle128B)
-                         : ptx::smem_desc(b_addr + 32 * k, 16, 1024, ptx::kSwizzle128B);
+              const uint64_t ad = ad_s + astep * uint32_t(k);
+              const uint64_t bd = bd_s + bstep * uint32_t(k);
               const uint32_t acc_on = MODE == G_BLOCK ? uint32_t(k != 0) : uint32_t((kk | k) != 0);
               if constexpr (CTA2) {
                 if constexpr (MODE == G_BF16) {
                   ptx::mma_f16_pair(d_t, ad, bd, idesc, acc_on);
                 } else if constexpr (MODE == G_MX) {
-                  const uint32_t id = idesc | (uint32_t(k) << 29) | (uint32_t(k) << 4);
-                  ptx::mma_mxf8f6f4_pair(d_t, ad, bd, id, sfa_t, sfb_t, acc_on);
+                  ptx::mma_mxf8f6f4_pair(d_t, ad, bd, idk[k], sfa_t, sfb_t, acc_on);
                 } else {
                   ptx::mma_f8f6f4_pair(d_t, ad, bd, idesc, acc_on);
                 }
               } else if constexpr (MODE == G_MX) {
-                const uint32_t id = idesc | (uint32_t(k) << 29) | (uint32_t(k) << 4);
-                ptx::mma_mxf8f6f4(d_t, ad, bd, id, sfa_t, sfb_t, acc_on);
+                ptx::mma_mxf8f6f4(d_t, ad, bd, idk[k], sfa_t, sfb_t, acc_on);
               } else if constexpr (MODE == G_BF16) {
                 ptx::mma_f16(d_t, ad, bd, idesc, acc_on);
               } else {
@@ -611,6 +619,13 @@ __device__ __forceinline__ void gemm_tn_body(const CUtensorMap& tmA, const CUten
             if (++s == G::kStages) {
               s = 0;
               ph ^= 1u;
+              ad_s = adesc0;
+              bd_s = bdesc0;
+              sfa_t = sf_base;
+            } else {
+              ad_s += kTileABytes >> 4;
+              bd_s += G::kTileBBytes >> 4;
+              sfa_t += kSfCols;
             }
           }
           if constexpr (MODE != G_BLOCK) {
