@@ -50,10 +50,10 @@ FP8_OVER_BF16 = 2.0                                   # nominal dense fp8 / bf16
 # DRAM bytes (read + write) per launch of the plain-store MXFP8 GEMM: the average over the
 # step's four such launches in one capture of `ncu --metrics dram__bytes_read.sum,
 # dram__bytes_write.sum,gpu__time_duration.sum --clock-control none -k regex:gemm_tn_kernel
-# -s 4 -c 4 python bench.py --profile gemm_mx_mlp --steps 2` (481.6, 341.8, 478.9 and 345.7
+# -s 4 -c 4 python bench.py --profile gemm_mx_mlp --steps 2` (475.3, 332.6, 471.9 and 338.8
 # MB for fc2 fprop, fc2 wgrad, fc1 dgrad and fc1 wgrad). Reset to None whenever that kernel
 # changes.
-GEMM_TRAFFIC_BYTES = 412.0e6
+GEMM_TRAFFIC_BYTES = 404.7e6
 
 
 def peaks():
