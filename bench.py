@@ -44,6 +44,7 @@ GEMM_FLOPS = 6 * 2.0 * TOKENS * HIDDEN * FFN          # fc1, fc2 fwd; dgrad + wg
 WORKLOAD = "mxfp8_mlp_fwd_bwd tokens=8192 hidden=4096 ffn=16384"
 KERNELS_PER_STEP = 10                                 # 4 quantize, 6 GEMMs (2 fused)
 KERNELS_PER_STEP_UNFUSED = 12                         # plus standalone gelu and dgelu
+E2E_SETS = 3                                          # buffer sets the end-to-end leg rotates
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FP8_OVER_BF16 = 2.0                                   # nominal dense fp8 / bf16 rate
@@ -165,14 +166,15 @@ class MlpStep:
             self.hbuf = torch.empty((M, Fd), dtype=bf, device=dev)
             self.da = torch.empty((M, Fd), dtype=bf, device=dev)
         shapes = {"y": (M, H), "dx": (M, H), "dw1": (Fd, H), "dw2": (H, Fd)}
-        # two sets of device inputs / outputs and pinned host outputs, so the end-to-end leg
-        # can copy one step's data while the next step computes
+        # E2E_SETS sets of device inputs / outputs and pinned host outputs, so the end-to-end
+        # leg can copy the data of the steps around the one that computes
         self.out_sets = [{k: torch.empty(v, dtype=bf, device=dev) for k, v in shapes.items()}
-                         for _ in range(2)]
+                         for _ in range(E2E_SETS)]
         self.outs = self.out_sets[0]
-        self.d_sets = [self.d, {k: torch.empty_like(v) for k, v in self.d.items()}]
+        self.d_sets = [self.d] + [{k: torch.empty_like(v) for k, v in self.d.items()}
+                                  for _ in range(E2E_SETS - 1)]
         self.h_out = [{k: torch.empty(v, dtype=bf).pin_memory() for k, v in shapes.items()}
-                      for _ in range(2)]
+                      for _ in range(E2E_SETS)]
         # algorithmic bytes of the quantize kernels per step
         mx = lambda r, c, copies: r * c * (2 + copies + copies / 32.0)  # noqa: E731
         self.quant_bytes = mx(M, H, 2) + mx(Fd, H, 2) + mx(H, Fd, 2) + mx(M, H, 2)
@@ -229,31 +231,32 @@ class MlpStep:
     def run_e2e(self, steps):
         """`steps` steps whose inputs are copied from pinned host memory and whose results
         (y, dX, dW1, dW2) are copied back to pinned host memory, pipelined the way a training
-        loop overlaps its data movement: step i's inputs are uploaded on one stream while step
-        i-1 computes, and its results are downloaded on a third stream while step i+1 computes
-        (two buffer sets alternate). Returns the elapsed ms from the first upload to the last
+        loop overlaps its data movement: step i's inputs are uploaded on one stream while the
+        steps before it compute, and its results are downloaded on a third stream while the
+        steps after it compute (E2E_SETS buffer sets rotate, so a copy has more than one step's
+        compute to hide behind). Returns the elapsed ms from the first upload to the last
         download, measured on the compute stream."""
         torch = self.torch
         comp = self.stream
         s_in, s_out = torch.cuda.Stream(self.dev), torch.cuda.Stream(self.dev)
-        ev_in = [torch.cuda.Event() for _ in range(2)]
-        ev_comp = [torch.cuda.Event() for _ in range(2)]
-        ev_out = [torch.cuda.Event() for _ in range(2)]
+        ev_in = [torch.cuda.Event() for _ in range(E2E_SETS)]
+        ev_comp = [torch.cuda.Event() for _ in range(E2E_SETS)]
+        ev_out = [torch.cuda.Event() for _ in range(E2E_SETS)]
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0.record(comp)
         s_in.wait_stream(comp)
         s_out.wait_stream(comp)
         for i in range(steps):
-            b = i % 2
-            if i >= 2:
-                s_in.wait_event(ev_comp[b])               # step i-2 is done with these inputs
+            b = i % E2E_SETS
+            if i >= E2E_SETS:
+                s_in.wait_event(ev_comp[b])               # the set's last step is done with them
             with torch.cuda.stream(s_in):
                 for k, v in self.h.items():
                     self.d_sets[b][k].copy_(v, non_blocking=True)
                 ev_in[b].record(s_in)
             comp.wait_event(ev_in[b])
-            if i >= 2:
-                comp.wait_event(ev_out[b])                # step i-2's results are downloaded
+            if i >= E2E_SETS:
+                comp.wait_event(ev_out[b])                # the set's last results are downloaded
             with torch.cuda.stream(comp):
                 self.run(self.d_sets[b], self.out_sets[b])
                 ev_comp[b].record(comp)
@@ -496,7 +499,8 @@ def run_ours(args):
                          "algorithmic_bytes_per_step": st.quant_bytes, "peak_source": src},
             "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s",
                     "h2d_bytes_per_step": st.h2d_bytes(), "d2h_bytes_per_step": st.d2h_bytes(),
-                    "copies": "pinned host, own streams, overlapped with the adjacent steps"},
+                    "copies": "pinned host, own streams, overlapped with the neighbouring "
+                              f"steps ({E2E_SETS} buffer sets)"},
             "kernels_ms": per_kernel,
             "gemm_4096_mxfp8": gemm4096,
             "quantize_by_recipe": quant_recipes,
