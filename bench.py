@@ -2,10 +2,10 @@
 
 One step = one forward + backward pass of an MXFP8 transformer MLP block (8192 tokens,
 hidden 4096, ffn 16384), everything through the library's C ABI:
-    quantize X, W1, W2 (row + column copies) -> fc1 GEMM whose epilogue applies GeLU, keeps
-    its input h in FP8 and writes the MXFP8 copies of the activation -> fc2 GEMM -> quantize
-    dY -> fc2 dgrad (epilogue: dGeLU and the MXFP8 copies of dh) + fc2 wgrad -> fc1 dgrad +
-    wgrad.
+    quantize X, W1, W2 (row + column copies, one grouped launch) -> fc1 GEMM whose epilogue
+    applies GeLU, keeps its input h in FP8 and writes the MXFP8 copies of the activation ->
+    fc2 GEMM -> quantize dY -> fc2 dgrad (epilogue: dGeLU and the MXFP8 copies of dh) + fc2
+    wgrad -> fc1 dgrad + wgrad.
 `--unfused` runs the same step with the GEMMs storing h and da in bf16 and the standalone
 GeLU / dGeLU quantize kernels in between.
 Metric: GEMM TFLOP/s of the whole step (quantize time included), plus the quantize kernels'
@@ -42,8 +42,8 @@ METRIC = "FP8 linear fwd+bwd TFLOPS (incl. quantize) vs FP8 peak; quantize HBM G
 TOKENS, HIDDEN, FFN = 8192, 4096, 16384
 GEMM_FLOPS = 6 * 2.0 * TOKENS * HIDDEN * FFN          # fc1, fc2 fwd; dgrad + wgrad of both
 WORKLOAD = "mxfp8_mlp_fwd_bwd tokens=8192 hidden=4096 ffn=16384"
-KERNELS_PER_STEP = 10                                 # 4 quantize, 6 GEMMs (2 fused)
-KERNELS_PER_STEP_UNFUSED = 12                         # plus standalone gelu and dgelu
+KERNELS_PER_STEP = 8                                  # 2 quantize, 6 GEMMs (2 fused)
+KERNELS_PER_STEP_UNFUSED = 10                         # plus standalone gelu and dgelu
 E2E_SETS = 3                                          # buffer sets the end-to-end leg rotates
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -200,9 +200,10 @@ class MlpStep:
         F, rec, T = self.F, self.rec, self._timed
         d = src or self.d
         o = outs or self.outs
-        T("quant", lambda: F.quantize(rec, d["x"], "activation", out=self.xq), "quantize_x")
-        T("quant", lambda: F.quantize(rec, d["w1"], "weight", out=self.w1q), "quantize_w1")
-        T("quant", lambda: F.quantize(rec, d["w2"], "weight", out=self.w2q), "quantize_w2")
+        # X, W1 and W2 in one launch (fp8_quantize_group)
+        T("quant", lambda: F.quantize_group(rec, [d["x"], d["w1"], d["w2"]],
+                                            ["activation", "weight", "weight"],
+                                            outs=[self.xq, self.w1q, self.w2q]), "quantize_x_w1_w2")
         if self.fused:
             T("gemm_fused", lambda: F.linear_fwd_gelu(rec, self.xq, self.w1q, a_q=self.aq,
                                                       h_q=self.hq), "fc1_fprop_gelu")

@@ -180,6 +180,39 @@ fp8_status fp8_quantize_master(const fp8_recipe *recipe, const float *w_f32, int
                                int32_t *dev_status, cudaStream_t stream);
 
 /*
+ * fp8_quantize_group — fp8_quantize of up to FP8_QUANTIZE_GROUP_MAX bf16 tensors under the
+ * MXFP8 recipe in one launch. One persistent grid walks the tiles of all the tensors, so a
+ * layer's activation and weights are quantised at the rate of one large tensor instead of
+ * each paying a launch's ramp-up and tail. Source: the Megatron Core "Low-Precision Training
+ * Guide", section "Recipe Reference", entry mxfp8 (an E8M0 scale per 1x32 block); the codes
+ * and scale bytes are exactly those fp8_quantize writes for each tensor on its own.
+ *   recipe     kind FP8_RECIPE_MXFP8; other kinds return FP8_ERR_UNSUPPORTED.
+ *   n          number of items, 1 .. FP8_QUANTIZE_GROUP_MAX (else FP8_ERR_SHAPE).
+ *   items      n descriptions in host memory, read during the call only. Each field means
+ *              what the same-named argument of fp8_quantize means (x_bf16, rows, cols, role,
+ *              want_row, want_col, out), with the same shape, alignment and layout rules and
+ *              the same --fp8-wgrad handling of the column copy. No output may overlap
+ *              another item's output or any input.
+ * Every item is checked before anything is launched: on the first failing item its status is
+ * returned and nothing runs. out->rows/cols/role/kind/col_bf16 are set as by fp8_quantize.
+ * Needs no workspace.
+ */
+#define FP8_QUANTIZE_GROUP_MAX 4
+typedef struct fp8_quantize_item {
+  const void *x_bf16;
+  int64_t rows;
+  int64_t cols;
+  int32_t role;
+  int32_t want_row;
+  int32_t want_col;
+  fp8_tensor *out;
+} fp8_quantize_item;
+
+fp8_status fp8_quantize_group(const fp8_recipe *recipe, int32_t n,
+                              const fp8_quantize_item *items, int32_t *dev_status,
+                              cudaStream_t stream);
+
+/*
  * fp8_amax_update — delayed scaling: push *amax_new into the history (the oldest of `len`
  * entries drops out) and write scale = f(max(history)), scale_inv = 1/scale with f the
  * per-tensor rule above (--fp8-amax-history-len, --fp8-margin), or with

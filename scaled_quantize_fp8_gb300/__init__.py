@@ -4,6 +4,6 @@ blockwise) and scaled FP8 GEMMs on the sm_103a tensor core, behind a C ABI
 from . import _lib  # noqa: F401
 from .binding import (  # noqa: F401
     DelayedState, QTensor, Recipe, amax_update, dgelu_quantize, empty_qtensor, gelu_quantize,
-    linear_bwd, linear_dgrad_dgelu, linear_fwd, linear_fwd_gelu, quantize, quantize_master,
-    quantize_static_scratch, workspace_bytes,
+    linear_bwd, linear_dgrad_dgelu, linear_fwd, linear_fwd_gelu, quantize, quantize_group,
+    quantize_master, quantize_static_scratch, workspace_bytes,
 )

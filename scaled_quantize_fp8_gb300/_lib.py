@@ -37,6 +37,15 @@ class Tensor(ctypes.Structure):
                 ("col_bf16", ctypes.c_int32)]
 
 
+QUANTIZE_GROUP_MAX = 4
+
+
+class QuantizeItem(ctypes.Structure):
+    _fields_ = [("x_bf16", ctypes.c_void_p), ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
+                ("role", ctypes.c_int32), ("want_row", ctypes.c_int32),
+                ("want_col", ctypes.c_int32), ("out", ctypes.POINTER(Tensor))]
+
+
 class AmaxHistory(ctypes.Structure):
     _fields_ = [("history", ctypes.c_void_p), ("head", ctypes.c_void_p), ("len", ctypes.c_int32)]
 
@@ -48,6 +57,8 @@ _SIG = {
     "fp8_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(Recipe), _I64, _I64]),
     "fp8_quantize": (_I32, [ctypes.POINTER(Recipe), _P, _I64, _I64, _I32, _I32, _I32,
                             ctypes.POINTER(Tensor), _P, ctypes.c_size_t, _P, _P]),
+    "fp8_quantize_group": (_I32, [ctypes.POINTER(Recipe), _I32, ctypes.POINTER(QuantizeItem),
+                                  _P, _P]),
     "fp8_quantize_master": (_I32, [ctypes.POINTER(Recipe), _P, _I64, _I64, _I32, _I32,
                                    ctypes.POINTER(Tensor), _P, ctypes.c_size_t, _P, _P]),
     "fp8_amax_update": (_I32, [ctypes.POINTER(Recipe), ctypes.POINTER(AmaxHistory), _I32, _P,

@@ -140,6 +140,30 @@ def quantize(recipe: Recipe, x: torch.Tensor, role="activation", want_row=True, 
     return out
 
 
+def quantize_group(recipe: Recipe, xs, roles, outs=None, want_row=True, want_col=True,
+                   status: Optional[torch.Tensor] = None, stream=None):
+    """fp8_quantize_group: up to four bf16 [rows, cols] tensors quantised by one MXFP8 launch.
+    `roles` and `outs` (QTensors, or None to allocate) run parallel to `xs`."""
+    lib = L.load()
+    n = len(xs)
+    if outs is None:
+        outs = [None] * n
+    outs = [o if o is not None else
+            empty_qtensor(recipe, x.shape[0], x.shape[1], r, want_row, want_col, device=x.device)
+            for x, r, o in zip(xs, roles, outs)]
+    rc = recipe.c()
+    cts = [o.c() for o in outs]
+    items = (L.QuantizeItem * max(1, n))()
+    for i, (x, r) in enumerate(zip(xs, roles)):
+        items[i] = L.QuantizeItem(_ptr(x), x.shape[0], x.shape[1], ROLES[r], int(want_row),
+                                  int(want_col), ctypes.pointer(cts[i]))
+    st = lib.fp8_quantize_group(ctypes.byref(rc), n, items, _ptr(status), _stream(stream))
+    L.check(st, "fp8_quantize_group")
+    for o, ct in zip(outs, cts):
+        o.rows, o.cols, o.kind, o.role, o.col_bf16 = ct.rows, ct.cols, ct.kind, ct.role, ct.col_bf16
+    return outs
+
+
 def quantize_master(recipe: Recipe, w: torch.Tensor, want_row=True, want_col=True,
                     out: Optional[QTensor] = None, workspace: Optional[torch.Tensor] = None,
                     status: Optional[torch.Tensor] = None, stream=None):

@@ -108,11 +108,11 @@ size_t fp8_workspace_bytes(const fp8_recipe* recipe, int64_t rows, int64_t cols)
 }
 
 namespace {
-fp8_status quantize_impl(const fp8_recipe* recipe, const void* x_bf16, int64_t rows,
-                         int64_t cols, int32_t role, int32_t want_row, int32_t want_col,
-                         fp8_tensor* out, void* workspace, size_t ws_bytes, int32_t* dev_status,
-                         cudaStream_t stream, uint32_t stall_tx) {
-  FP8_TRY(check_recipe(recipe));
+// The checks fp8_quantize makes on one tensor's arguments (the recipe already checked), apart
+// from the workspace. Sets *col_bf16: the column copy is the bf16 transpose.
+fp8_status check_quantize_args(const fp8_recipe* recipe, const void* x_bf16, int64_t rows,
+                               int64_t cols, int32_t role, int32_t want_row, int32_t want_col,
+                               const fp8_tensor* out, bool* col_bf16) {
   if (out == nullptr) return FP8_ERR_NULL;
   if (role < FP8_ROLE_ACTIVATION || role > FP8_ROLE_GRAD) return FP8_ERR_UNSUPPORTED;
   if (!want_row && !want_col) return FP8_ERR_SHAPE;
@@ -121,15 +121,29 @@ fp8_status quantize_impl(const fp8_recipe* recipe, const void* x_bf16, int64_t r
   if (rows < 0 || cols < 0 || rows % q != 0 || cols % q != 0) return FP8_ERR_SHAPE;
   if (rows * cols >= (int64_t(1) << 31)) return FP8_ERR_SHAPE;   // 32-bit element offsets
   FP8_TRY(check_scalars(kind, out));
-  const bool empty = rows == 0 || cols == 0;
-  const bool col_bf16 = recipe->fp8_wgrad == 0 && role != FP8_ROLE_WEIGHT;
-  if (!empty) {
+  *col_bf16 = recipe->fp8_wgrad == 0 && role != FP8_ROLE_WEIGHT;
+  if (rows != 0 && cols != 0) {
     FP8_TRY(check_ptr(x_bf16));
     if (want_row) FP8_TRY(check_copy(kind, out->row, out->row_scale));
     if (want_col) {
-      if (col_bf16) FP8_TRY(check_ptr(out->col));
+      if (*col_bf16) FP8_TRY(check_ptr(out->col));
       else FP8_TRY(check_copy(kind, out->col, out->col_scale));
     }
+  }
+  return FP8_OK;
+}
+
+fp8_status quantize_impl(const fp8_recipe* recipe, const void* x_bf16, int64_t rows,
+                         int64_t cols, int32_t role, int32_t want_row, int32_t want_col,
+                         fp8_tensor* out, void* workspace, size_t ws_bytes, int32_t* dev_status,
+                         cudaStream_t stream, uint32_t stall_tx) {
+  FP8_TRY(check_recipe(recipe));
+  bool col_bf16 = false;
+  FP8_TRY(check_quantize_args(recipe, x_bf16, rows, cols, role, want_row, want_col, out,
+                              &col_bf16));
+  const int kind = recipe->kind;
+  const bool empty = rows == 0 || cols == 0;
+  if (!empty) {
     const size_t need = quantize_workspace_bytes(kind, rows, cols);
     if (need > 0 && (workspace == nullptr || ws_bytes < need)) return FP8_ERR_WORKSPACE;
     if (need > 0 && !aligned16(workspace)) return FP8_ERR_ALIGN;
@@ -162,6 +176,33 @@ fp8_status fp8_test_quantize_stalled(const fp8_recipe* recipe, const void* x_bf1
   if (dev_status == nullptr) return FP8_ERR_NULL;     // the outcome is only visible there
   return quantize_impl(recipe, x_bf16, rows, cols, role, want_row, want_col, out, workspace,
                        ws_bytes, dev_status, stream, 16u);
+}
+
+fp8_status fp8_quantize_group(const fp8_recipe* recipe, int32_t n,
+                              const fp8_quantize_item* items, int32_t* dev_status,
+                              cudaStream_t stream) {
+  FP8_TRY(check_recipe(recipe));
+  if (recipe->kind != FP8_RECIPE_MXFP8) return FP8_ERR_UNSUPPORTED;
+  if (items == nullptr) return FP8_ERR_NULL;
+  if (n < 1 || n > FP8_QUANTIZE_GROUP_MAX) return FP8_ERR_SHAPE;
+  fp8lin::QuantGroupItem q[FP8_QUANTIZE_GROUP_MAX];
+  for (int i = 0; i < n; ++i) {
+    const fp8_quantize_item& it = items[i];
+    bool col_bf16 = false;
+    FP8_TRY(check_quantize_args(recipe, it.x_bf16, it.rows, it.cols, it.role, it.want_row,
+                                it.want_col, it.out, &col_bf16));
+    q[i] = {reinterpret_cast<const uint16_t*>(it.x_bf16), it.rows, it.cols, it.want_row != 0,
+            it.want_col != 0, col_bf16, it.out};
+  }
+  for (int i = 0; i < n; ++i) {
+    fp8_tensor* out = items[i].out;
+    out->rows = items[i].rows;
+    out->cols = items[i].cols;
+    out->role = items[i].role;
+    out->kind = recipe->kind;
+    out->col_bf16 = q[i].col_bf16 ? 1 : 0;
+  }
+  return cuda_status(fp8lin::quantize_group_launch(n, q, dev_status, stream));
 }
 
 fp8_status fp8_quantize_master(const fp8_recipe* recipe, const float* w_f32, int64_t rows,

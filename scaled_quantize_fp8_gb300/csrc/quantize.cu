@@ -651,6 +651,79 @@ __global__ void __launch_bounds__(256, quant_ctas_per_sm<MODE, EPI>())
   }
 }
 
+// Several MXFP8 tensors in one launch: one persistent grid walks the tiles of all of them
+// (tensor 0's first, then tensor 1's, ...), so a set of small tensors runs at the rate of one
+// large one instead of paying a launch's ramp and tail each. Every tile is quantised exactly
+// as the single-tensor kernel quantises it.
+constexpr int kQuantGroupMax = 4;
+struct QuantGroup {
+  CUtensorMap map[kQuantGroupMax];
+  QuantParams p[kQuantGroupMax];
+  int first[kQuantGroupMax + 1];    // first global tile of each tensor; first[n] = all tiles
+  int n;
+};
+
+__global__ void __launch_bounds__(256, quant_ctas_per_sm<Q_MX, EPI_NONE>())
+    quantize_group_kernel(const __grid_constant__ QuantGroup g) {
+  extern __shared__ uint8_t qsm_raw[];
+  uint8_t* base = ptx::align_smem<1024>(qsm_raw);
+  QuantCtl& S = *reinterpret_cast<QuantCtl*>(base);
+  constexpr int kQBufs = quant_bufs<Q_MX, EPI_NONE>();
+  uint8_t* tiles = base + quant_tiles_off<EPI_NONE>();
+  const int t = threadIdx.x;
+  const int n_tiles = g.first[g.n];
+  int32_t* status = g.p[0].status;
+
+  pdl_launch_dependents();
+  if (t == 0) {
+    for (int b = 0; b < kQBufs; ++b) ptx::mbar_init(&S.bar[b], 1);
+    S.abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_wait();
+
+  auto tensor_of = [&](int tile) {
+    int k = 0;
+    while (k + 1 < g.n && tile >= g.first[k + 1]) ++k;
+    return k;
+  };
+  auto issue = [&](int tile, int b) {
+    const int k = tensor_of(tile);
+    const int local = tile - g.first[k];
+    const int tc_n = g.p[k].tiles_c;
+    const int tr = local / tc_n, tc = local % tc_n;
+    uint8_t* dst = tiles + b * kQTileBytes;
+    ptx::mbar_arrive_expect_tx(&S.bar[b], kQTileBytes);
+    ptx::tma_load_2d(dst, &g.map[k], tc * kTile, tr * kTile, &S.bar[b]);
+    ptx::tma_load_2d(dst + 16384, &g.map[k], tc * kTile + 64, tr * kTile, &S.bar[b]);
+  };
+
+  if (t == 0) {
+    for (int j = 0; j < kQBufs - 1; ++j) {
+      const int tl = int(blockIdx.x) + j * int(gridDim.x);
+      if (tl < n_tiles) issue(tl, j);
+    }
+  }
+  int tile = blockIdx.x;
+  for (int i = 0; tile < n_tiles; ++i, tile += gridDim.x) {
+    const int b = i % kQBufs;
+    const int ahead = tile + (kQBufs - 1) * int(gridDim.x);
+    if (t == 0 && ahead < n_tiles) issue(ahead, (i + kQBufs - 1) % kQBufs);
+    if (!quant_wait(S, b, uint32_t(i / kQBufs) & 1u, status)) break;
+    uint8_t* buf = tiles + b * kQTileBytes;
+    const int k = tensor_of(tile);
+    quantize_one_tile<Q_MX, EPI_NONE, F8_E4M3>(g.p[k], S, buf, buf, nullptr, tile - g.first[k],
+                                                1.0f, false);
+    __syncthreads();
+  }
+  if (*reinterpret_cast<volatile int*>(&S.abort_flag)) {
+    const uint64_t t0 = ptx::clock64_();             // let the outstanding copies land
+    while (ptx::clock64_() - t0 < 20000000ull) {
+    }
+  }
+}
+
 // Tensorwise first pass: per-CTA max of the 15-bit bf16 magnitudes over a grid-strided
 // sweep of 16-byte vectors. Each thread keeps a batch of sixteen independent loads in flight
 // (out-of-range ones read nothing), so a 64 MB tensor takes two round trips to DRAM with
@@ -888,6 +961,48 @@ cudaError_t quantize_launch(int kind, int role, int fmt, bool pow2, int margin,
                 : launch_tiles<Q_BW1x128, EPI_NONE>(p, st);
   }
   return cudaErrorInvalidValue;
+}
+
+cudaError_t quantize_group_launch(int n, const QuantGroupItem* items, int32_t* status,
+                                  cudaStream_t st) {
+  if (n < 1 || n > kQuantGroupMax) return cudaErrorInvalidValue;
+  QuantGroup g{};
+  int total = 0, k = 0;
+  for (int i = 0; i < n; ++i) {
+    const QuantGroupItem& it = items[i];
+    if (it.R == 0 || it.C == 0) continue;                 // nothing to write for it
+    QuantParams& p = g.p[k];
+    p.status = status;
+    p.col_bf16 = it.col_bf16;
+    p.x = it.x;
+    p.R = it.R;
+    p.C = it.C;
+    p.tiles_c = int((it.C + 127) / 128);
+    p.row = it.want_row ? it.out->row : nullptr;
+    p.col = it.want_col ? it.out->col : nullptr;
+    p.row_scale = it.want_row ? it.out->row_scale : nullptr;
+    p.col_scale = it.want_col ? it.out->col_scale : nullptr;
+    const int64_t col_row_bytes = p.R * (p.col_bf16 ? 2 : 1);
+    p.col_v8 = p.col != nullptr && (reinterpret_cast<uintptr_t>(p.col) % 32 == 0) &&
+               (col_row_bytes % 32 == 0);
+    if (!make_tmap_2d(&g.map[k], p.x, 2, p.C, p.R, 64, kTile, true))
+      return cudaErrorInvalidValue;
+    g.first[k] = total;
+    total += int((p.R + 127) / 128) * p.tiles_c;
+    ++k;
+  }
+  g.n = k;
+  g.first[k] = total;
+  if (total == 0) return cudaSuccess;
+  constexpr int smem = int(quant_smem_bytes<Q_MX, EPI_NONE>());
+  static ContextOnce attr_done{};
+  const cudaError_t ae = once_per_context(attr_done, [&] {
+    return cudaFuncSetAttribute(quantize_group_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                smem);
+  });
+  if (ae != cudaSuccess) return ae;
+  const int grid = std::max(1, std::min(total, num_sms() * quant_ctas_per_sm<Q_MX, EPI_NONE>()));
+  return launch_kernel(quantize_group_kernel, dim3(grid), dim3(256), smem, st, nullptr, g);
 }
 
 cudaError_t gelu_quantize_launch(const uint16_t* h, int64_t R, int64_t C, uint16_t* a_bf16,

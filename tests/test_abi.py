@@ -51,6 +51,37 @@ def _q(lib, rec, x=0x8000, rows=256, cols=256, role=0, wr=1, wc=1, t=None, ws=0x
                             ws_bytes, None, None)
 
 
+def _group(lib, rec, items, n=None):
+    arr = (L.QuantizeItem * max(1, len(items)))(*items)
+    return lib.fp8_quantize_group(ctypes.byref(rec), len(items) if n is None else n, arr, None,
+                                  None)
+
+
+def _item(t, x=0x8000, rows=256, cols=256, role=0, wr=1, wc=1):
+    return L.QuantizeItem(x, rows, cols, role, wr, wc, ctypes.pointer(t))
+
+
+def test_quantize_group_rejects_bad_arguments(lib):
+    mx = _rec(kind=L.RECIPE_MXFP8)
+    t0, t1 = _tensor(), _tensor(row=0x11000, col=0x12000, rs=0x13000, cs=0x14000)
+    assert lib.fp8_quantize_group(None, 1, None, None, None) == 1
+    assert _group(lib, _rec(), [_item(t0)]) == 4                 # MXFP8 only
+    assert _group(lib, _rec(kind=L.RECIPE_BLOCKWISE), [_item(t0)]) == 4
+    assert lib.fp8_quantize_group(ctypes.byref(mx), 1, None, None, None) == 1
+    assert _group(lib, mx, [_item(t0)], n=0) == 3
+    assert _group(lib, mx, [_item(t0)] * 5) == 3               # at most FP8_QUANTIZE_GROUP_MAX
+    assert _group(lib, mx, [_item(t0), _item(t1, rows=192)]) == 3    # item 1: not a 128 multiple
+    assert _group(lib, mx, [_item(t0), _item(t1, x=0)]) == 1
+    assert _group(lib, mx, [_item(t0, x=0x8008), _item(t1)]) == 2
+    assert _group(lib, mx, [_item(t0), _item(t1, role=7)]) == 4
+    assert _group(lib, mx, [_item(t0), _item(t1, wr=0, wc=0)]) == 3
+    assert _group(lib, mx, [_item(t0), _item(_tensor(rs=0))]) == 1
+    bad = L.QuantizeItem(0x8000, 256, 256, 0, 1, 1, None)     # no output tensor
+    assert _group(lib, mx, [_item(t0), bad]) == 1
+    # nothing launched and no output touched when any item fails
+    assert t0.rows == 0 and t0.cols == 0 and t0.kind == 0
+
+
 def test_quantize_rejects_bad_arguments(lib):
     r = _rec()
     assert lib.fp8_quantize(None, 0x8000, 16, 16, 0, 1, 1, ctypes.byref(_tensor()), None, 0, None,

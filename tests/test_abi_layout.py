@@ -1,6 +1,7 @@
 """The binding's ctypes structures have the C structs' layout: a small C program compiled
-against include/fp8lin.h prints sizeof and every field's offset of fp8_recipe, fp8_tensor and
-fp8_amax_history, and the ctypes Structure classes must agree field by field."""
+against include/fp8lin.h prints sizeof and every field's offset of fp8_recipe, fp8_tensor,
+fp8_amax_history and fp8_quantize_item, and the ctypes Structure classes must agree field by
+field."""
 import ctypes
 import os
 import shutil
@@ -10,7 +11,8 @@ import pytest
 
 from scaled_quantize_fp8_gb300 import _lib as L
 
-STRUCTS = {"fp8_recipe": L.Recipe, "fp8_tensor": L.Tensor, "fp8_amax_history": L.AmaxHistory}
+STRUCTS = {"fp8_recipe": L.Recipe, "fp8_tensor": L.Tensor, "fp8_amax_history": L.AmaxHistory,
+           "fp8_quantize_item": L.QuantizeItem}
 
 
 def _cuda_include():

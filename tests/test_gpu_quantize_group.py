@@ -1,0 +1,102 @@
+"""GPU parity of fp8_quantize_group (several MXFP8 tensors in one launch).
+
+The grouped call must write exactly the bytes that fp8_quantize writes for each tensor on its
+own: codes and E8M0 scales of both copies, or the bf16 column transpose with --fp8-wgrad off.
+Checked on groups of mixed shapes and roles (different tile counts, so one CTA's walk crosses
+from one tensor into the next), on an empty member, on four members, on the MLP step's own
+X 8192 x 4096, W1 16384 x 4096 and W2 4096 x 16384 at full size, and on a small group against
+the oracle directly.
+"""
+import numpy as np
+import pytest
+import torch
+
+from helpers import cuda_ok, mx_untile, to_dev_bf16
+from oracle import fp8_oracle as O
+from workloads import bf16_bits_normal
+
+pytestmark = pytest.mark.gpu
+
+if cuda_ok():
+    import scaled_quantize_fp8_gb300 as F
+
+FIELDS = ("row", "row_scale", "col", "col_scale")
+
+
+def _bytes(t):
+    return None if t is None else t.view(torch.uint8).cpu().numpy()
+
+
+def _group_vs_single(shapes, roles, fp8_wgrad=True, sigmas=None, streams=None):
+    rec = F.Recipe(kind="mxfp8", fp8_wgrad=fp8_wgrad)
+    sigmas = sigmas or [1.0] * len(shapes)
+    streams = streams or list(range(10, 10 + len(shapes)))
+    xs = [to_dev_bf16(bf16_bits_normal(r, c, sigma=s, seed=3, stream=st))
+          for (r, c), s, st in zip(shapes, sigmas, streams)]
+    got = F.quantize_group(rec, xs, roles)
+    want = [F.quantize(rec, x, r) for x, r in zip(xs, roles)]
+    torch.cuda.synchronize()
+    for i, (g, w) in enumerate(zip(got, want)):
+        assert (g.rows, g.cols, g.kind, g.role, g.col_bf16) == \
+            (w.rows, w.cols, w.kind, w.role, w.col_bf16), i
+        for f in FIELDS:
+            a, b = _bytes(getattr(g, f)), _bytes(getattr(w, f))
+            assert (a is None) == (b is None), (i, f)
+            if a is not None:
+                assert np.array_equal(a, b), (i, f, int(np.count_nonzero(a != b)))
+    return got
+
+
+def test_group_mixed_shapes_and_roles():
+    _group_vs_single([(384, 512), (1024, 256), (128, 128)], ["activation", "weight", "grad"],
+                     sigmas=[1.0, 0.02, 1e-3])
+
+
+def test_group_four_members():
+    _group_vs_single([(256, 384), (128, 1024), (640, 128), (256, 256)],
+                     ["activation", "weight", "weight", "grad"])
+
+
+def test_group_bf16_column_copies():
+    # --fp8-wgrad off: activation and gradient column copies are bf16 transposes, the weight's
+    # stays FP8
+    got = _group_vs_single([(256, 512), (512, 256), (384, 384)], ["activation", "weight", "grad"],
+                           fp8_wgrad=False)
+    assert [g.col_bf16 for g in got] == [1, 0, 1]
+
+
+def test_group_with_empty_member():
+    rec = F.Recipe(kind="mxfp8")
+    x0 = to_dev_bf16(bf16_bits_normal(256, 256, seed=4, stream=20))
+    e = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
+    x2 = to_dev_bf16(bf16_bits_normal(128, 512, seed=4, stream=21))
+    got = F.quantize_group(rec, [x0, e, x2], ["activation", "activation", "weight"])
+    want = [F.quantize(rec, x0, "activation"), F.quantize(rec, x2, "weight")]
+    torch.cuda.synchronize()
+    assert (got[1].rows, got[1].cols) == (0, 256)
+    for g, w in zip((got[0], got[2]), want):
+        for f in FIELDS:
+            assert np.array_equal(_bytes(getattr(g, f)), _bytes(getattr(w, f))), f
+
+
+def test_group_against_oracle():
+    shapes = [(256, 384), (128, 256)]
+    bits = [bf16_bits_normal(r, c, seed=5, stream=30 + i, outlier_p=0.01)
+            for i, (r, c) in enumerate(shapes)]
+    rec = F.Recipe(kind="mxfp8")
+    got = F.quantize_group(rec, [to_dev_bf16(b) for b in bits], ["activation", "weight"])
+    torch.cuda.synchronize()
+    for g, b in zip(got, bits):
+        R, C = b.shape
+        ref = O.quantize_mxfp8(b)
+        assert np.array_equal(g.row.cpu().numpy(), ref["row"])
+        assert np.array_equal(mx_untile(g.row_scale.cpu().numpy(), R, C), ref["row_scale"])
+        assert np.array_equal(g.col.cpu().numpy(), ref["col"])
+        assert np.array_equal(mx_untile(g.col_scale.cpu().numpy(), C, R), ref["col_scale"])
+
+
+def test_group_mlp_step_tensors_full_size():
+    # the benchmark's grouped launch: X 8192 x 4096, W1 16384 x 4096, W2 4096 x 16384
+    _group_vs_single([(8192, 4096), (16384, 4096), (4096, 16384)],
+                     ["activation", "weight", "weight"], sigmas=[1.0, 0.02, 0.02],
+                     streams=[0, 1, 3])
