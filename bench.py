@@ -564,7 +564,7 @@ class ConfigStep:
             self.outs = {"y": torch.empty((M, N), dtype=bf, device=dev)}
             self.flops = 2.0 * M * N * K
             self.quant_bytes = (M * K + N * K) * (2 + 2 + 2 / 32.0)
-            self.launches = 3
+            self.launches = 2                    # X and W in one grouped launch, GEMM
         elif name == "blockwise_fwd_bwd":
             self.rec = F.Recipe(kind="blockwise")
             n = 4096
@@ -624,8 +624,8 @@ class ConfigStep:
               "quantize_w")
             T("gemm", lambda: F.linear_fwd(rec, q["x"], q["w"], y=o["y"]), "fprop")
         elif self.name == "mxfp8_fprop":
-            T("quant", lambda: F.quantize(rec, d["x"], "activation", out=q["x"]), "quantize_x")
-            T("quant", lambda: F.quantize(rec, d["w"], "weight", out=q["w"]), "quantize_w")
+            T("quant", lambda: F.quantize_group(rec, [d["x"], d["w"]], ["activation", "weight"],
+                                                outs=[q["x"], q["w"]]), "quantize_x_w")
             T("gemm", lambda: F.linear_fwd(rec, q["x"], q["w"], y=o["y"]), "fprop")
         elif self.name == "blockwise_fwd_bwd":
             T("quant", lambda: F.quantize(rec, d["x"], "activation", out=q["x"]), "quantize_x")
