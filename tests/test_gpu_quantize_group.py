@@ -100,3 +100,18 @@ def test_group_mlp_step_tensors_full_size():
     _group_vs_single([(8192, 4096), (16384, 4096), (4096, 16384)],
                      ["activation", "weight", "weight"], sigmas=[1.0, 0.02, 0.02],
                      streams=[0, 1, 3])
+
+
+def test_group_one_copy_only():
+    # want_row = 0: only the column copies (and their scales) are written
+    rec = F.Recipe(kind="mxfp8")
+    xs = [to_dev_bf16(bf16_bits_normal(r, c, seed=6, stream=40 + i))
+          for i, (r, c) in enumerate([(256, 512), (384, 128)])]
+    roles = ["activation", "grad"]
+    got = F.quantize_group(rec, xs, roles, want_row=False)
+    want = [F.quantize(rec, x, r, want_row=False) for x, r in zip(xs, roles)]
+    torch.cuda.synchronize()
+    for g, w in zip(got, want):
+        assert g.row is None and w.row is None
+        assert np.array_equal(_bytes(g.col), _bytes(w.col))
+        assert np.array_equal(_bytes(g.col_scale), _bytes(w.col_scale))
