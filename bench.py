@@ -45,6 +45,7 @@ WORKLOAD = "mxfp8_mlp_fwd_bwd tokens=8192 hidden=4096 ffn=16384"
 KERNELS_PER_STEP = 8                                  # 2 quantize, 6 GEMMs (2 fused)
 KERNELS_PER_STEP_UNFUSED = 10                         # plus standalone gelu and dgelu
 E2E_SETS = 3                                          # buffer sets the end-to-end leg rotates
+DELAYED_STEPS = 64                                    # distinct inputs of the delayed-scaling config
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FP8_OVER_BF16 = 2.0                                   # nominal dense fp8 / bf16 rate
@@ -581,11 +582,15 @@ class ConfigStep:
         else:
             self.rec = F.Recipe(kind="delayed", amax_history_len=1024)
             M, N, K = 8192, 4096, 4096
-            sig = sigma_schedule(8)
-            # eight inputs of drifting scale, cycled through the timed steps
-            self.xs_host = [host(bf16_bits_normal(M, K, seed=0, stream=STREAM_STEP0 + t,
-                                                  sigma=sig[t])) for t in range(8)]
-            self.xs = [x.to(dev) for x in self.xs_host]
+            sig = sigma_schedule(DELAYED_STEPS)
+            # 64 distinct inputs of drifting scale (x_t ~ N(0, sigma_t), 64 MB each), drawn on
+            # the device from one seeded generator per step (a host draw takes seconds per
+            # tensor); the timed steps walk through them in order
+            def draw(t):
+                gt = torch.Generator(device=dev).manual_seed(STREAM_STEP0 + t)
+                return (torch.randn((M, K), device=dev, generator=gt) * float(sig[t])).to(bf)
+            self.xs = [draw(t) for t in range(DELAYED_STEPS)]
+            self.xs_host = [x.cpu().pin_memory() for x in self.xs]
             self.h = {"x": self.xs_host[0]}
             self.state = F.DelayedState(self.rec, device=dev)
             wstate = F.DelayedState(self.rec, device=dev, role="weight")
@@ -637,7 +642,7 @@ class ConfigStep:
             T("gemm", lambda: F.linear_bwd(rec, q["dy"], q["x"], q["w"], want_dx=False,
                                            dw=o["dw"]), "wgrad")
         else:
-            x = self.xs[self.t % 8] if resident else d["x"]
+            x = self.xs[self.t % DELAYED_STEPS] if resident else d["x"]
             self.t += 1
             T("quant", lambda: F.quantize(rec, x, "activation", out=q["x"], workspace=self.ws),
               "quantize_x")
@@ -666,7 +671,8 @@ class ConfigStep:
         s_out.wait_stream(comp)
         for i in range(steps):
             b = i % 2
-            src = {"x": self.xs_host[i % 8]} if self.name == "delayed_step" else self.h
+            src = ({"x": self.xs_host[i % DELAYED_STEPS]} if self.name == "delayed_step"
+                   else self.h)
             if i >= 2:
                 s_in.wait_event(ev_comp[b])               # step i-2 is done with these inputs
             with torch.cuda.stream(s_in):
@@ -860,7 +866,7 @@ def run_config(args):
                               if args.workload == "tensorwise_256" else
                               "not flushed: each step touches more than L2 (129 MB): "
                               "0.26-0.3 GB of inputs, codes and outputs; the delayed step "
-                              "also cycles eight 64 MB X_t"),
+                              f"walks through {DELAYED_STEPS} distinct 64 MB X_t"),
                        "gemm_flops_per_step": st.flops},
             "roofline": {"bound": "tensor", "kernel": f"gemm_tn_kernel ({st.rec.kind})",
                          "achieved": round(achieved, 1), "peak": fp8_peak, "unit": "TFLOP/s",
