@@ -1,7 +1,7 @@
 """The library launches only on the caller's stream, never allocates and never synchronises,
-so whole steps can be captured in a CUDA graph. A captured MXFP8 MLP step (fused epilogues) and
-a delayed-scaling step (quantize, fprop, history update) replayed from the graph must give the
-same bytes as the same calls run eagerly."""
+so whole steps can be captured in a CUDA graph. A captured MXFP8 MLP step (grouped quantize of
+X, W1 and W2, fused epilogues) and a delayed-scaling step (quantize, fprop, history update)
+replayed from the graph must give the same bytes as the same calls run eagerly."""
 import pytest
 import torch
 
@@ -53,9 +53,9 @@ def test_graph_mxfp8_mlp_step():
     dw1, dw2 = torch.empty_like(w1), torch.empty_like(w2)
 
     def step():
-        F.quantize(rec, x, "activation", out=xq)
-        F.quantize(rec, w1, "weight", out=w1q)
-        F.quantize(rec, w2, "weight", out=w2q)
+        # X, W1 and W2 in one grouped launch, as the benchmark step does
+        F.quantize_group(rec, [x, w1, w2], ["activation", "weight", "weight"],
+                         outs=[xq, w1q, w2q])
         F.linear_fwd_gelu(rec, xq, w1q, a_q=aq, h_q=hq)
         F.linear_fwd(rec, aq, w2q, y=y)
         F.quantize(rec, dy, "grad", out=dyq)
@@ -63,7 +63,8 @@ def test_graph_mxfp8_mlp_step():
         F.linear_bwd(rec, dyq, aq, None, want_dx=False, dw=dw2)
         F.linear_bwd(rec, dhq, xq, w1q, dx=dx, dw=dw1)
 
-    _capture_and_compare(step, [y, dx, dw1, dw2, aq.row, aq.col, dhq.row, dhq.col])
+    _capture_and_compare(step, [y, dx, dw1, dw2, aq.row, aq.col, dhq.row, dhq.col, xq.row,
+                                xq.col, w1q.col, w2q.row])
 
 
 def test_graph_delayed_step_with_history():
