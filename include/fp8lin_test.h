@@ -10,7 +10,7 @@
  *   - frees its tensor memory and returns.
  * The CUDA context stays usable. The hooks below make such a wait run out on purpose,
  * without faulting, trapping or hanging the GPU, so tests can check that path. There is one
- * hook for the GEMM pipeline and one for the quantize kernels.
+ * hook for the GEMM pipeline, one for the quantize kernels and one for the grouped quantize.
  */
 #ifndef FP8LIN_TEST_H
 #define FP8LIN_TEST_H
@@ -57,6 +57,24 @@ fp8_status fp8_test_quantize_stalled(const fp8_recipe *recipe, const void *x_bf1
                                      int64_t cols, int32_t role, int32_t want_row,
                                      int32_t want_col, fp8_tensor *out, void *workspace,
                                      size_t ws_bytes, int32_t *dev_status, cudaStream_t stream);
+
+/*
+ * fp8_quantize_group with a stall planted in the grouped kernel's TMA pipeline. The group's
+ * first tile (the first item's, loaded by CTA 0) expects 16 more bytes than its TMA loads
+ * deliver.
+ *
+ * Arguments are as for fp8_quantize_group; dev_status is required.
+ *
+ * On the device, CTA 0's wait runs out after its budget. *dev_status then becomes
+ * FP8_ERR_TIMEOUT, unless it already held a nonzero status. CTA 0's tiles are left unwritten;
+ * the other CTAs finish theirs.
+ *
+ * Host-side errors are those of fp8_quantize_group, plus FP8_ERR_NULL when dev_status is
+ * NULL. Takes about two seconds of GPU time.
+ */
+fp8_status fp8_test_quantize_group_stalled(const fp8_recipe *recipe, int32_t n,
+                                           const fp8_quantize_item *items, int32_t *dev_status,
+                                           cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -59,6 +59,8 @@ _SIG = {
                             ctypes.POINTER(Tensor), _P, ctypes.c_size_t, _P, _P]),
     "fp8_quantize_group": (_I32, [ctypes.POINTER(Recipe), _I32, ctypes.POINTER(QuantizeItem),
                                   _P, _P]),
+    "fp8_test_quantize_group_stalled": (_I32, [ctypes.POINTER(Recipe), _I32,
+                                               ctypes.POINTER(QuantizeItem), _P, _P]),
     "fp8_quantize_master": (_I32, [ctypes.POINTER(Recipe), _P, _I64, _I64, _I32, _I32,
                                    ctypes.POINTER(Tensor), _P, ctypes.c_size_t, _P, _P]),
     "fp8_amax_update": (_I32, [ctypes.POINTER(Recipe), ctypes.POINTER(AmaxHistory), _I32, _P,

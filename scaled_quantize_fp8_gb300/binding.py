@@ -141,9 +141,11 @@ def quantize(recipe: Recipe, x: torch.Tensor, role="activation", want_row=True, 
 
 
 def quantize_group(recipe: Recipe, xs, roles, outs=None, want_row=True, want_col=True,
-                   status: Optional[torch.Tensor] = None, stream=None):
+                   status: Optional[torch.Tensor] = None, stream=None, _stalled=False):
     """fp8_quantize_group: up to four bf16 [rows, cols] tensors quantised by one MXFP8 launch.
-    `roles` and `outs` (QTensors, or None to allocate) run parallel to `xs`."""
+    `roles` and `outs` (QTensors, or None to allocate) run parallel to `xs`. `_stalled` calls
+    the test hook fp8_test_quantize_group_stalled instead (the group's first tile never
+    arrives, so CTA 0's bounded wait runs out and records FP8_ERR_TIMEOUT in `status`)."""
     lib = L.load()
     n = len(xs)
     if outs is None:
@@ -157,7 +159,8 @@ def quantize_group(recipe: Recipe, xs, roles, outs=None, want_row=True, want_col
     for i, (x, r) in enumerate(zip(xs, roles)):
         items[i] = L.QuantizeItem(_ptr(x), x.shape[0], x.shape[1], ROLES[r], int(want_row),
                                   int(want_col), ctypes.pointer(cts[i]))
-    st = lib.fp8_quantize_group(ctypes.byref(rc), n, items, _ptr(status), _stream(stream))
+    fn = lib.fp8_test_quantize_group_stalled if _stalled else lib.fp8_quantize_group
+    st = fn(ctypes.byref(rc), n, items, _ptr(status), _stream(stream))
     L.check(st, "fp8_quantize_group")
     for o, ct in zip(outs, cts):
         o.rows, o.cols, o.kind, o.role, o.col_bf16 = ct.rows, ct.cols, ct.kind, ct.role, ct.col_bf16

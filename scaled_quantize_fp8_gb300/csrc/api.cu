@@ -178,9 +178,10 @@ fp8_status fp8_test_quantize_stalled(const fp8_recipe* recipe, const void* x_bf1
                        ws_bytes, dev_status, stream, 16u);
 }
 
-fp8_status fp8_quantize_group(const fp8_recipe* recipe, int32_t n,
-                              const fp8_quantize_item* items, int32_t* dev_status,
-                              cudaStream_t stream) {
+namespace {
+fp8_status quantize_group_impl(const fp8_recipe* recipe, int32_t n,
+                               const fp8_quantize_item* items, int32_t* dev_status,
+                               cudaStream_t stream, uint32_t stall_tx) {
   FP8_TRY(check_recipe(recipe));
   if (recipe->kind != FP8_RECIPE_MXFP8) return FP8_ERR_UNSUPPORTED;
   if (items == nullptr) return FP8_ERR_NULL;
@@ -202,7 +203,21 @@ fp8_status fp8_quantize_group(const fp8_recipe* recipe, int32_t n,
     out->kind = recipe->kind;
     out->col_bf16 = q[i].col_bf16 ? 1 : 0;
   }
-  return cuda_status(fp8lin::quantize_group_launch(n, q, dev_status, stream));
+  return cuda_status(fp8lin::quantize_group_launch(n, q, dev_status, stream, stall_tx));
+}
+}  // namespace
+
+fp8_status fp8_quantize_group(const fp8_recipe* recipe, int32_t n,
+                              const fp8_quantize_item* items, int32_t* dev_status,
+                              cudaStream_t stream) {
+  return quantize_group_impl(recipe, n, items, dev_status, stream, 0u);
+}
+
+fp8_status fp8_test_quantize_group_stalled(const fp8_recipe* recipe, int32_t n,
+                                           const fp8_quantize_item* items, int32_t* dev_status,
+                                           cudaStream_t stream) {
+  if (dev_status == nullptr) return FP8_ERR_NULL;     // the outcome is only visible there
+  return quantize_group_impl(recipe, n, items, dev_status, stream, 16u);
 }
 
 fp8_status fp8_quantize_master(const fp8_recipe* recipe, const float* w_f32, int64_t rows,

@@ -106,7 +106,7 @@ struct QuantGroupItem {
   fp8_tensor* out;
 };
 cudaError_t quantize_group_launch(int n, const QuantGroupItem* items, int32_t* status,
-                                  cudaStream_t st);
+                                  cudaStream_t st, uint32_t stall_tx = 0);
 cudaError_t gelu_quantize_launch(const uint16_t* h, int64_t R, int64_t C, uint16_t* a_bf16,
                                  fp8_tensor* a_q, fp8_tensor* h_q, int32_t* status,
                                  cudaStream_t st);

@@ -661,6 +661,7 @@ struct QuantGroup {
   QuantParams p[kQuantGroupMax];
   int first[kQuantGroupMax + 1];    // first global tile of each tensor; first[n] = all tiles
   int n;
+  uint32_t stall_tx;                // test hook (0 otherwise): extra bytes tile 0 expects
 };
 
 __global__ void __launch_bounds__(256, quant_ctas_per_sm<Q_MX, EPI_NONE>())
@@ -694,7 +695,7 @@ __global__ void __launch_bounds__(256, quant_ctas_per_sm<Q_MX, EPI_NONE>())
     const int tc_n = g.p[k].tiles_c;
     const int tr = local / tc_n, tc = local % tc_n;
     uint8_t* dst = tiles + b * kQTileBytes;
-    ptx::mbar_arrive_expect_tx(&S.bar[b], kQTileBytes);
+    ptx::mbar_arrive_expect_tx(&S.bar[b], kQTileBytes + (tile == 0 ? g.stall_tx : 0u));
     ptx::tma_load_2d(dst, &g.map[k], tc * kTile, tr * kTile, &S.bar[b]);
     ptx::tma_load_2d(dst + 16384, &g.map[k], tc * kTile + 64, tr * kTile, &S.bar[b]);
   };
@@ -964,9 +965,10 @@ cudaError_t quantize_launch(int kind, int role, int fmt, bool pow2, int margin,
 }
 
 cudaError_t quantize_group_launch(int n, const QuantGroupItem* items, int32_t* status,
-                                  cudaStream_t st) {
+                                  cudaStream_t st, uint32_t stall_tx) {
   if (n < 1 || n > kQuantGroupMax) return cudaErrorInvalidValue;
   QuantGroup g{};
+  g.stall_tx = stall_tx;
   int total = 0, k = 0;
   for (int i = 0; i < n; ++i) {
     const QuantGroupItem& it = items[i];

@@ -1,8 +1,8 @@
 """Failure detection on the GPU without a fault. A GEMM whose first pipeline stage never becomes
-ready, or a quantize whose first tile never arrives, must come back on its own with
-FP8_ERR_TIMEOUT in the caller's status word. The test hooks plant 16 bytes that no copy
-delivers. After it, the context is still usable: the next calls on the same stream give the
-oracle's results.
+ready, or a quantize (single or grouped) whose first tile never arrives, must come back on its
+own with FP8_ERR_TIMEOUT in the caller's status word. The test hooks plant 16 bytes that no
+copy delivers. After it, the context is still usable: the next calls on the same stream give
+the oracle's results.
 
 Each stalled launch takes about two seconds, the kernel's wait budget. The hook stalls only
 the first CTA (pair); the other CTAs, and every later launch, run normally."""
@@ -107,3 +107,24 @@ def test_stalled_quantize_reports_timeout_and_context_survives(kind):
         ref = O.quantize_blockwise_1x128(xb)
     assert np.array_equal(q2.row.cpu().numpy(), ref["row"])
     assert np.array_equal(q2.col.cpu().numpy(), ref["col"])
+
+
+def test_stalled_quantize_group_reports_timeout_and_context_survives():
+    rec = F.Recipe(kind="mxfp8")
+    bits = [bf16_bits_normal(1024, 512, seed=123), bf16_bits_normal(512, 256, seed=124)]
+    xs = [to_dev_bf16(b) for b in bits]
+    roles = ["activation", "weight"]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    F.quantize_group(rec, xs, roles, status=status, _stalled=True)
+    torch.cuda.synchronize()
+    assert int(status.item()) == FP8_ERR_TIMEOUT
+
+    # the next grouped call on the same stream is bit-exact
+    status2 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = F.quantize_group(rec, xs, roles, status=status2)
+    torch.cuda.synchronize()
+    assert int(status2.item()) == 0
+    for g, b in zip(got, bits):
+        ref = O.quantize_mxfp8(b)
+        assert np.array_equal(g.row.cpu().numpy(), ref["row"])
+        assert np.array_equal(g.col.cpu().numpy(), ref["col"])
