@@ -1,9 +1,9 @@
 """Out-of-bounds writes and tile-corner addressing, checked without a sanitizer.
 
 1. Canaries. Every output buffer of a call (codes, scales, the per-tensor scalars, GEMM
-   results, the fused MLP epilogues' copies) sits inside a larger allocation with 4 KiB of
-   canary bytes on either side. After the call the canaries are unchanged, and the outputs
-   equal those of the same call on plain buffers.
+   results, the fused MLP epilogues' copies, a grouped quantize's tensors) sits inside a
+   larger allocation with 4 KiB of canary bytes on either side. After the call the canaries
+   are unchanged, and the outputs equal those of the same call on plain buffers.
 2. Tile corners. A tensor that is zero but for one value at a corner of a 128 x 128 tile
    (including the corners of the ragged last tile) quantises bit-exactly like the oracle,
    and its GEMM matches the oracle. An index slip at a tile edge moves or drops that value.
@@ -127,6 +127,23 @@ def test_quantize_writes_stay_inside(kind, fmt, role, shape, extra):
     torch.cuda.synchronize()
     assert g.intact()
     assert same_qtensor(q, ref)
+
+
+@pytest.mark.parametrize("fp8_wgrad", [True, False])
+def test_quantize_group_writes_stay_inside(fp8_wgrad):
+    # one grouped MXFP8 launch over three tensors of different tile counts
+    rec = F.Recipe(kind="mxfp8", fp8_wgrad=fp8_wgrad)
+    shapes, roles = [(256, 384), (384, 128), (128, 512)], ["activation", "weight", "grad"]
+    xs = [to_dev_bf16(bf16_bits_normal(r, c, seed=140 + i, outlier_p=1e-2, outlier_factor=30.0))
+          for i, (r, c) in enumerate(shapes)]
+    g = Guards()
+    qs = [guarded_qtensor(g, rec, r, c, role) for (r, c), role in zip(shapes, roles)]
+    F.quantize_group(rec, xs, roles, outs=qs)
+    refs = [F.quantize(rec, x, role) for x, role in zip(xs, roles)]
+    torch.cuda.synchronize()
+    assert g.intact()
+    for q, ref in zip(qs, refs):
+        assert same_qtensor(q, ref)
 
 
 @pytest.mark.parametrize("kind", ["tensorwise", "mxfp8", "blockwise"])
