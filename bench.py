@@ -522,7 +522,8 @@ CONFIGS = {
     "tensorwise_256": "tensorwise quantize X, W 256x256 (N(0,1)) + fprop 256^3, one CUDA graph "
                       "a step",
     "mxfp8_fprop": "mxfp8 quantize X 8192x4096 (0.1% outliers x50) + W 4096x4096 + fprop",
-    "blockwise_fwd_bwd": "blockwise quantize X, W, dY 4096x4096 + fprop + dgrad + wgrad",
+    "blockwise_fwd_bwd": "blockwise quantize X, W (one grouped launch), dY 4096x4096 + fprop + "
+                         "dgrad + wgrad",
     "delayed_step": "delayed quantize X_t 8192x4096 (log-uniform sigma) + fprop (W 4096x4096) "
                     "+ amax history update (length 1024)",
 }
@@ -578,7 +579,7 @@ class ConfigStep:
             self.outs = {k: torch.empty((n, n), dtype=bf, device=dev) for k in ("y", "dx", "dw")}
             self.flops = 3 * 2.0 * n ** 3
             self.quant_bytes = 2 * n * n * (2 + 2 + 2 * 4 / 128.0) + n * n * (2 + 2)
-            self.launches = 6
+            self.launches = 5                    # X and W grouped, dY, three GEMMs
         else:
             self.rec = F.Recipe(kind="delayed", amax_history_len=1024)
             M, N, K = 8192, 4096, 4096
@@ -633,8 +634,8 @@ class ConfigStep:
                                                 outs=[q["x"], q["w"]]), "quantize_x_w")
             T("gemm", lambda: F.linear_fwd(rec, q["x"], q["w"], y=o["y"]), "fprop")
         elif self.name == "blockwise_fwd_bwd":
-            T("quant", lambda: F.quantize(rec, d["x"], "activation", out=q["x"]), "quantize_x")
-            T("quant", lambda: F.quantize(rec, d["w"], "weight", out=q["w"]), "quantize_w")
+            T("quant", lambda: F.quantize_group(rec, [d["x"], d["w"]], ["activation", "weight"],
+                                                outs=[q["x"], q["w"]]), "quantize_x_w")
             T("gemm", lambda: F.linear_fwd(rec, q["x"], q["w"], y=o["y"]), "fprop")
             T("quant", lambda: F.quantize(rec, d["dy"], "grad", out=q["dy"]), "quantize_dy")
             T("gemm", lambda: F.linear_bwd(rec, q["dy"], q["x"], q["w"], want_dw=False,

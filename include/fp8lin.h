@@ -180,13 +180,16 @@ fp8_status fp8_quantize_master(const fp8_recipe *recipe, const float *w_f32, int
                                int32_t *dev_status, cudaStream_t stream);
 
 /*
- * fp8_quantize_group — fp8_quantize of up to FP8_QUANTIZE_GROUP_MAX bf16 tensors under the
- * MXFP8 recipe in one launch. One persistent grid walks the tiles of all the tensors, so a
- * layer's activation and weights are quantised at the rate of one large tensor instead of
- * each paying a launch's ramp-up and tail. Source: the Megatron Core "Low-Precision Training
- * Guide", section "Recipe Reference", entry mxfp8 (an E8M0 scale per 1x32 block); the codes
- * and scale bytes are exactly those fp8_quantize writes for each tensor on its own.
- *   recipe     kind FP8_RECIPE_MXFP8; other kinds return FP8_ERR_UNSUPPORTED.
+ * fp8_quantize_group — fp8_quantize of up to FP8_QUANTIZE_GROUP_MAX bf16 tensors under one
+ * block-scaled recipe in one launch. One persistent grid walks the tiles of all the tensors,
+ * so a layer's activation and weights are quantised at the rate of one large tensor instead
+ * of each paying a launch's ramp-up and tail. Source: the Megatron Core "Low-Precision
+ * Training Guide", section "Recipe Reference", entries mxfp8 (an E8M0 scale per 1x32 block)
+ * and blockwise (1x128 activation / gradient blocks, 128x128 weight blocks); the codes and
+ * scales are exactly those fp8_quantize writes for each tensor on its own, the hybrid format
+ * and power-of-two block scales included.
+ *   recipe     kind FP8_RECIPE_MXFP8 or FP8_RECIPE_BLOCKWISE; the per-tensor recipes
+ *              (tensorwise, delayed) return FP8_ERR_UNSUPPORTED.
  *   n          number of items, 1 .. FP8_QUANTIZE_GROUP_MAX (else FP8_ERR_SHAPE).
  *   items      n descriptions in host memory, read during the call only. Each field means
  *              what the same-named argument of fp8_quantize means (x_bf16, rows, cols, role,

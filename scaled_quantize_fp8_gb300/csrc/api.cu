@@ -183,7 +183,8 @@ fp8_status quantize_group_impl(const fp8_recipe* recipe, int32_t n,
                                const fp8_quantize_item* items, int32_t* dev_status,
                                cudaStream_t stream, uint32_t stall_tx) {
   FP8_TRY(check_recipe(recipe));
-  if (recipe->kind != FP8_RECIPE_MXFP8) return FP8_ERR_UNSUPPORTED;
+  if (recipe->kind != FP8_RECIPE_MXFP8 && recipe->kind != FP8_RECIPE_BLOCKWISE)
+    return FP8_ERR_UNSUPPORTED;
   if (items == nullptr) return FP8_ERR_NULL;
   if (n < 1 || n > FP8_QUANTIZE_GROUP_MAX) return FP8_ERR_SHAPE;
   fp8lin::QuantGroupItem q[FP8_QUANTIZE_GROUP_MAX];
@@ -192,8 +193,8 @@ fp8_status quantize_group_impl(const fp8_recipe* recipe, int32_t n,
     bool col_bf16 = false;
     FP8_TRY(check_quantize_args(recipe, it.x_bf16, it.rows, it.cols, it.role, it.want_row,
                                 it.want_col, it.out, &col_bf16));
-    q[i] = {reinterpret_cast<const uint16_t*>(it.x_bf16), it.rows, it.cols, it.want_row != 0,
-            it.want_col != 0, col_bf16, it.out};
+    q[i] = {reinterpret_cast<const uint16_t*>(it.x_bf16), it.rows, it.cols, it.role,
+            it.want_row != 0, it.want_col != 0, col_bf16, fmt_of(recipe, it.role) == 1, it.out};
   }
   for (int i = 0; i < n; ++i) {
     fp8_tensor* out = items[i].out;
@@ -203,7 +204,9 @@ fp8_status quantize_group_impl(const fp8_recipe* recipe, int32_t n,
     out->kind = recipe->kind;
     out->col_bf16 = q[i].col_bf16 ? 1 : 0;
   }
-  return cuda_status(fp8lin::quantize_group_launch(n, q, dev_status, stream, stall_tx));
+  return cuda_status(fp8lin::quantize_group_launch(recipe->kind, recipe->power_2_scales != 0,
+                                                   recipe->margin, n, q, dev_status, stream,
+                                                   stall_tx));
 }
 }  // namespace
 

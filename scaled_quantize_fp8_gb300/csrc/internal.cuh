@@ -98,15 +98,19 @@ cudaError_t quantize_launch(int kind, int role, int fmt, bool pow2, int margin,
                             const uint16_t* x, int64_t R, int64_t C, bool want_row,
                             bool want_col, bool col_bf16, fp8_tensor* out, void* workspace,
                             int32_t* status, cudaStream_t st, uint32_t stall_tx = 0);
-// One tensor of a grouped MXFP8 quantize (fp8_quantize_group), checked by the caller.
+// One tensor of a grouped quantize (fp8_quantize_group), checked by the caller.
 struct QuantGroupItem {
   const uint16_t* x;
   int64_t R, C;
+  int role;
   bool want_row, want_col, col_bf16;
+  bool e5;                  // blockwise, hybrid format, role GRAD: E5M2 codes
   fp8_tensor* out;
 };
-cudaError_t quantize_group_launch(int n, const QuantGroupItem* items, int32_t* status,
-                                  cudaStream_t st, uint32_t stall_tx = 0);
+// kind: FP8_RECIPE_MXFP8 or FP8_RECIPE_BLOCKWISE (pow2 and margin apply to blockwise).
+cudaError_t quantize_group_launch(int kind, bool pow2, int margin, int n,
+                                  const QuantGroupItem* items, int32_t* status, cudaStream_t st,
+                                  uint32_t stall_tx = 0);
 cudaError_t gelu_quantize_launch(const uint16_t* h, int64_t R, int64_t C, uint16_t* a_bf16,
                                  fp8_tensor* a_q, fp8_tensor* h_q, int32_t* status,
                                  cudaStream_t st);

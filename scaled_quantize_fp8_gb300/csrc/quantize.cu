@@ -651,19 +651,24 @@ __global__ void __launch_bounds__(256, quant_ctas_per_sm<MODE, EPI>())
   }
 }
 
-// Several MXFP8 tensors in one launch: one persistent grid walks the tiles of all of them
-// (tensor 0's first, then tensor 1's, ...), so a set of small tensors runs at the rate of one
-// large one instead of paying a launch's ramp and tail each. Every tile is quantised exactly
-// as the single-tensor kernel quantises it.
+// Several tensors of one block-scaled recipe in one launch: one persistent grid walks the
+// tiles of all of them (tensor 0's first, then tensor 1's, ...), so a set of small tensors runs
+// at the rate of one large one instead of paying a launch's ramp and tail each. Every tile is
+// quantised exactly as the single-tensor kernel quantises it. FAM 0 is MXFP8; FAM 1 is
+// blockwise, where each tensor has its own mode (1x128 or 128x128 blocks by role, E4M3 or, for
+// a hybrid-format gradient, E5M2).
 constexpr int kQuantGroupMax = 4;
+enum GroupMode : int { GM_MX = 0, GM_BW1x128 = 1, GM_BW128 = 2, GM_BW1x128_E5 = 3, GM_BW128_E5 = 4 };
 struct QuantGroup {
   CUtensorMap map[kQuantGroupMax];
   QuantParams p[kQuantGroupMax];
   int first[kQuantGroupMax + 1];    // first global tile of each tensor; first[n] = all tiles
+  int mode[kQuantGroupMax];         // GroupMode of each tensor
   int n;
   uint32_t stall_tx;                // test hook (0 otherwise): extra bytes tile 0 expects
 };
 
+template <int FAM>
 __global__ void __launch_bounds__(256, quant_ctas_per_sm<Q_MX, EPI_NONE>())
     quantize_group_kernel(const __grid_constant__ QuantGroup g) {
   extern __shared__ uint8_t qsm_raw[];
@@ -714,8 +719,30 @@ __global__ void __launch_bounds__(256, quant_ctas_per_sm<Q_MX, EPI_NONE>())
     if (!quant_wait(S, b, uint32_t(i / kQBufs) & 1u, status)) break;
     uint8_t* buf = tiles + b * kQTileBytes;
     const int k = tensor_of(tile);
-    quantize_one_tile<Q_MX, EPI_NONE, F8_E4M3>(g.p[k], S, buf, buf, nullptr, tile - g.first[k],
-                                                1.0f, false);
+    const int local = tile - g.first[k];
+    if constexpr (FAM == 0) {
+      quantize_one_tile<Q_MX, EPI_NONE, F8_E4M3>(g.p[k], S, buf, buf, nullptr, local, 1.0f,
+                                                  false);
+    } else {
+      switch (g.mode[k]) {
+        case GM_BW128:
+          quantize_one_tile<Q_BW128, EPI_NONE, F8_E4M3>(g.p[k], S, buf, buf, nullptr, local,
+                                                         1.0f, false);
+          break;
+        case GM_BW1x128_E5:
+          quantize_one_tile<Q_BW1x128, EPI_NONE, F8_E5M2>(g.p[k], S, buf, buf, nullptr, local,
+                                                           1.0f, false);
+          break;
+        case GM_BW128_E5:
+          quantize_one_tile<Q_BW128, EPI_NONE, F8_E5M2>(g.p[k], S, buf, buf, nullptr, local,
+                                                         1.0f, false);
+          break;
+        default:
+          quantize_one_tile<Q_BW1x128, EPI_NONE, F8_E4M3>(g.p[k], S, buf, buf, nullptr, local,
+                                                           1.0f, false);
+          break;
+      }
+    }
     __syncthreads();
   }
   if (*reinterpret_cast<volatile int*>(&S.abort_flag)) {
@@ -964,9 +991,12 @@ cudaError_t quantize_launch(int kind, int role, int fmt, bool pow2, int margin,
   return cudaErrorInvalidValue;
 }
 
-cudaError_t quantize_group_launch(int n, const QuantGroupItem* items, int32_t* status,
-                                  cudaStream_t st, uint32_t stall_tx) {
+cudaError_t quantize_group_launch(int kind, bool pow2, int margin, int n,
+                                  const QuantGroupItem* items, int32_t* status, cudaStream_t st,
+                                  uint32_t stall_tx) {
   if (n < 1 || n > kQuantGroupMax) return cudaErrorInvalidValue;
+  if (kind != FP8_RECIPE_MXFP8 && kind != FP8_RECIPE_BLOCKWISE) return cudaErrorInvalidValue;
+  const bool bw = kind == FP8_RECIPE_BLOCKWISE;
   QuantGroup g{};
   g.stall_tx = stall_tx;
   int total = 0, k = 0;
@@ -975,6 +1005,11 @@ cudaError_t quantize_group_launch(int n, const QuantGroupItem* items, int32_t* s
     if (it.R == 0 || it.C == 0) continue;                 // nothing to write for it
     QuantParams& p = g.p[k];
     p.status = status;
+    p.pow2 = bw && pow2;
+    p.margin = margin;
+    g.mode[k] = !bw ? GM_MX
+                    : it.role == FP8_ROLE_WEIGHT ? (it.e5 ? GM_BW128_E5 : GM_BW128)
+                                                 : (it.e5 ? GM_BW1x128_E5 : GM_BW1x128);
     p.col_bf16 = it.col_bf16;
     p.x = it.x;
     p.R = it.R;
@@ -997,14 +1032,17 @@ cudaError_t quantize_group_launch(int n, const QuantGroupItem* items, int32_t* s
   g.first[k] = total;
   if (total == 0) return cudaSuccess;
   constexpr int smem = int(quant_smem_bytes<Q_MX, EPI_NONE>());
-  static ContextOnce attr_done{};
-  const cudaError_t ae = once_per_context(attr_done, [&] {
-    return cudaFuncSetAttribute(quantize_group_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                smem);
+  static_assert(quant_smem_bytes<Q_MX, EPI_NONE>() == quant_smem_bytes<Q_BW128, EPI_NONE>() &&
+                    quant_smem_bytes<Q_MX, EPI_NONE>() == quant_smem_bytes<Q_BW1x128, EPI_NONE>(),
+                "the group kernels size shared memory like the single-tensor ones");
+  static ContextOnce attr_mx{}, attr_bw{};
+  auto kern = bw ? quantize_group_kernel<1> : quantize_group_kernel<0>;
+  const cudaError_t ae = once_per_context(bw ? attr_bw : attr_mx, [&] {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   });
   if (ae != cudaSuccess) return ae;
   const int grid = std::max(1, std::min(total, num_sms() * quant_ctas_per_sm<Q_MX, EPI_NONE>()));
-  return launch_kernel(quantize_group_kernel, dim3(grid), dim3(256), smem, st, nullptr, g);
+  return launch_kernel(kern, dim3(grid), dim3(256), smem, st, nullptr, g);
 }
 
 cudaError_t gelu_quantize_launch(const uint16_t* h, int64_t R, int64_t C, uint16_t* a_bf16,

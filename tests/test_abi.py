@@ -65,8 +65,10 @@ def test_quantize_group_rejects_bad_arguments(lib):
     mx = _rec(kind=L.RECIPE_MXFP8)
     t0, t1 = _tensor(), _tensor(row=0x11000, col=0x12000, rs=0x13000, cs=0x14000)
     assert lib.fp8_quantize_group(None, 1, None, None, None) == 1
-    assert _group(lib, _rec(), [_item(t0)]) == 4                 # MXFP8 only
-    assert _group(lib, _rec(kind=L.RECIPE_BLOCKWISE), [_item(t0)]) == 4
+    assert _group(lib, _rec(), [_item(t0)]) == 4                 # MXFP8 and blockwise only
+    assert _group(lib, _rec(kind=L.RECIPE_DELAYED), [_item(t0)]) == 4
+    assert _group(lib, _rec(kind=L.RECIPE_BLOCKWISE), [_item(t0, cols=64)]) == 3
+    assert _group(lib, _rec(kind=L.RECIPE_MXFP8, fmt=L.FORMAT_HYBRID), [_item(t0)]) == 4
     assert lib.fp8_quantize_group(ctypes.byref(mx), 1, None, None, None) == 1
     assert _group(lib, mx, [_item(t0)], n=0) == 3
     assert _group(lib, mx, [_item(t0)] * 5) == 3               # at most FP8_QUANTIZE_GROUP_MAX

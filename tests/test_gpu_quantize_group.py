@@ -1,17 +1,18 @@
-"""GPU parity of fp8_quantize_group (several MXFP8 tensors in one launch).
+"""GPU parity of fp8_quantize_group (several MXFP8 or blockwise tensors in one launch).
 
 The grouped call must write exactly the bytes that fp8_quantize writes for each tensor on its
 own: codes and E8M0 scales of both copies, or the bf16 column transpose with --fp8-wgrad off.
 Checked on groups of mixed shapes and roles (different tile counts, so one CTA's walk crosses
 from one tensor into the next), on an empty member, on four members, on the MLP step's own
 X 8192 x 4096, W1 16384 x 4096 and W2 4096 x 16384 at full size, and on a small group against
-the oracle directly.
+the oracle directly; blockwise groups mix 1x128 and 128x128 members, under the hybrid format,
+power-of-two scales, --fp8-wgrad off and a margin.
 """
 import numpy as np
 import pytest
 import torch
 
-from helpers import cuda_ok, mx_untile, to_dev_bf16
+from helpers import bw_untile, cuda_ok, mx_untile, to_dev_bf16
 from oracle import fp8_oracle as O
 from workloads import bf16_bits_normal
 
@@ -115,3 +116,41 @@ def test_group_one_copy_only():
         assert g.row is None and w.row is None
         assert np.array_equal(_bytes(g.col), _bytes(w.col))
         assert np.array_equal(_bytes(g.col_scale), _bytes(w.col_scale))
+
+
+@pytest.mark.parametrize("extra", [{}, {"format": "hybrid"}, {"power_2_scales": True},
+                                   {"fp8_wgrad": False}, {"margin": 2}])
+def test_group_blockwise(extra):
+    # 1x128 activation and gradient blocks, 128x128 weight blocks, in one launch; under the
+    # hybrid format the gradient's codes are E5M2
+    rec = F.Recipe(kind="blockwise", **extra)
+    shapes, roles = [(384, 512), (512, 256), (256, 384)], ["activation", "weight", "grad"]
+    xs = [to_dev_bf16(bf16_bits_normal(r, c, seed=7, stream=50 + i, sigma=s, outlier_p=1e-2))
+          for i, ((r, c), s) in enumerate(zip(shapes, [1.0, 0.02, 1e-3]))]
+    got = F.quantize_group(rec, xs, roles)
+    want = [F.quantize(rec, x, r) for x, r in zip(xs, roles)]
+    torch.cuda.synchronize()
+    for i, (g, w) in enumerate(zip(got, want)):
+        assert (g.kind, g.role, g.col_bf16) == (w.kind, w.role, w.col_bf16), i
+        for f in FIELDS:
+            a, b = _bytes(getattr(g, f)), _bytes(getattr(w, f))
+            assert (a is None) == (b is None), (i, f)
+            if a is not None:
+                assert np.array_equal(a, b), (i, f, int(np.count_nonzero(a != b)))
+
+
+def test_group_blockwise_against_oracle():
+    rec = F.Recipe(kind="blockwise")
+    xb, wb = bf16_bits_normal(256, 384, seed=8, stream=60), bf16_bits_normal(384, 256, seed=8,
+                                                                             stream=61, sigma=0.02)
+    gx, gw = F.quantize_group(rec, [to_dev_bf16(xb), to_dev_bf16(wb)], ["activation", "weight"])
+    torch.cuda.synchronize()
+    rx, rw = O.quantize_blockwise_1x128(xb), O.quantize_blockwise_128x128(wb)
+    assert np.array_equal(gx.row.cpu().numpy(), rx["row"])
+    assert np.array_equal(gx.col.cpu().numpy(), rx["col"])
+    assert np.array_equal(bw_untile(gx.row_scale.cpu().numpy(), 256, 384), rx["row_scale_inv"])
+    assert np.array_equal(bw_untile(gx.col_scale.cpu().numpy(), 384, 256), rx["col_scale_inv"])
+    assert np.array_equal(gw.row.cpu().numpy(), rw["row"])
+    assert np.array_equal(gw.col.cpu().numpy(), rw["col"])
+    assert np.array_equal(gw.row_scale.cpu().numpy(), rw["row_scale_inv"])
+    assert np.array_equal(gw.col_scale.cpu().numpy(), rw["col_scale_inv"])
