@@ -157,12 +157,16 @@ __device__ __forceinline__ int k_block(int tile, int unit, int n_units, int kk, 
   return (((tile - unit) / n_units) & 1) ? nk - 1 - kk : kk;
 }
 
+// After a first test, the polls suspend the waiting thread (up to kSleepHintNs each; it resumes
+// as soon as the phase completes) instead of spinning: a warp that waits for a whole main loop
+// (the epilogue warps) then takes no issue slots from the MMA and scale-factor warps beside it.
+constexpr uint32_t kSleepHintNs = 20000;
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, SharedCtl* ctl,
                                          int32_t* status) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::clock64_();
   while (true) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (ptx::mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
     if (*reinterpret_cast<volatile int*>(&ctl->abort_flag)) return false;
     if (ptx::clock64_() - t0 > kWaitBudgetCycles) {
       *reinterpret_cast<volatile int*>(&ctl->abort_flag) = 1;
