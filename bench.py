@@ -52,10 +52,10 @@ FP8_OVER_BF16 = 2.0                                   # nominal dense fp8 / bf16
 # DRAM bytes (read + write) per launch of the plain-store MXFP8 GEMM: the average over the
 # step's four such launches in one capture of `ncu --metrics dram__bytes_read.sum,
 # dram__bytes_write.sum,gpu__time_duration.sum --clock-control none -k regex:gemm_tn_kernel
-# -s 4 -c 4 python bench.py --profile gemm_mx_mlp --steps 2` (475.3, 332.6, 471.9 and 338.8
+# -s 4 -c 4 python bench.py --profile gemm_mx_mlp --steps 2` (480.0, 340.9, 476.4 and 345.6
 # MB for fc2 fprop, fc2 wgrad, fc1 dgrad and fc1 wgrad). Reset to None whenever that kernel
 # changes.
-GEMM_TRAFFIC_BYTES = 404.7e6
+GEMM_TRAFFIC_BYTES = 410.7e6
 
 
 def peaks():
