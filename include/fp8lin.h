@@ -158,6 +158,11 @@ size_t fp8_workspace_bytes(const fp8_recipe *recipe, int64_t rows, int64_t cols)
  *              are set by this call.
  *   workspace  device scratch of at least fp8_workspace_bytes() (may be NULL when that is 0).
  * Returns FP8_OK or a host-detected error (nothing launched on error).
+ * Source: the Megatron Core "Low-Precision Training Guide", section "Recipe Reference"
+ * (entries delayed, tensorwise, mxfp8 and blockwise: what each recipe scales by) and section
+ * "Hardware and Recipe Compatibility" (E4M3 / hybrid formats); the two copies are the cached
+ * FP8 data and FP8 transpose of the TransformerEngine issue "How to reduce cuda memory usage
+ * of fp8?".
  */
 fp8_status fp8_quantize(const fp8_recipe *recipe, const void *x_bf16, int64_t rows,
                         int64_t cols, int32_t role, int32_t want_row, int32_t want_col,
@@ -173,6 +178,10 @@ fp8_status fp8_quantize(const fp8_recipe *recipe, const void *x_bf16, int64_t ro
  * always FP8. Arguments, layouts, workspace (fp8_workspace_bytes of the same shape) and
  * errors as for fp8_quantize; w_f32 is [rows][cols] fp32, 16-byte aligned.
  * power_2_scales is not supported here (FP8_ERR_UNSUPPORTED).
+ * Source: the TransformerEngine issue "How to reduce cuda memory usage of fp8?" (with
+ * --fp8-param-gather the distributed optimizer casts the fp32 master weight straight into the
+ * FP8 weight) and the Megatron Core "Low-Precision Training Guide", section "Recipe
+ * Reference" (the weight's scaling under each recipe).
  */
 fp8_status fp8_quantize_master(const fp8_recipe *recipe, const float *w_f32, int64_t rows,
                                int64_t cols, int32_t want_row, int32_t want_col,
@@ -222,6 +231,9 @@ fp8_status fp8_quantize_group(const fp8_recipe *recipe, int32_t n,
  * --fp8-amax-compute-algo most_recent scale = f(*amax_new) (the history is still recorded).
  * role: fp8_role of the tensor this history belongs to (under the hybrid format a gradient's
  * scale uses the E5M2 maximum 57344). One CTA; reads and writes device memory only.
+ * Source: the Megatron Core "Low-Precision Training Guide", section "Recipe Reference" entry
+ * delayed (the scale comes from a rolling amax history) and section "Numerical Stability
+ * Knobs" (--fp8-amax-history-len, --fp8-amax-compute-algo max / most_recent, --fp8-margin).
  */
 fp8_status fp8_amax_update(const fp8_recipe *recipe, fp8_amax_history *hist, int32_t role,
                            const float *amax_new, float *scale, float *scale_inv,
@@ -268,6 +280,11 @@ fp8_status fp8_linear_bwd(const fp8_recipe *recipe, const fp8_tensor *dy,
  * (activation_func_fp8_input_store): a = bf16(gelu(h)) with gelu(h) = h * Phi(h) in fp32,
  * quantised (row and column copies) into a_q, and h itself quantised (row copy) into h_q.
  * a_bf16 may be NULL (only needed for bf16 wgrad or inspection). MXFP8 recipe only.
+ * Source: the MegaDLMs summary "Benefits of Using FP8 Precision with MegaDLMs and Required
+ * Hardware", section "Python API Configuration" (activation_func_fp8_input_store: the
+ * activation's input is stored in FP8 for the backward pass) and section "Memory and Storage
+ * Optimization"; the quantisation is the "Low-Precision Training Guide" Recipe Reference
+ * entry mxfp8.
  */
 fp8_status fp8_gelu_quantize(const fp8_recipe *recipe, const void *h_bf16, int64_t rows,
                              int64_t cols, void *a_bf16, fp8_tensor *a_q, fp8_tensor *h_q,
@@ -277,6 +294,8 @@ fp8_status fp8_gelu_quantize(const fp8_recipe *recipe, const void *h_bf16, int64
  * fp8_dgelu_quantize — dh = bf16(da * gelu'(deq(h_q))) in fp32, gelu'(h) = Phi(h) + h phi(h),
  * reading h back from its FP8 row copy, then quantised (row and column copies) into dh_q.
  * dh_bf16 may be NULL. MXFP8 recipe only.
+ * Source: as fp8_gelu_quantize (the backward of the activation whose input was stored in
+ * FP8).
  */
 fp8_status fp8_dgelu_quantize(const fp8_recipe *recipe, const void *da_bf16,
                               const fp8_tensor *h_q, void *dh_bf16, fp8_tensor *dh_q,
@@ -292,6 +311,8 @@ fp8_status fp8_dgelu_quantize(const fp8_recipe *recipe, const void *da_bf16,
  * both scale arrays, h_q needs row and row_scale, all 16-byte aligned (32-byte aligned code
  * arrays get 256-bit stores). M = x->rows and N = w->rows multiples of 128. On return a_q and
  * h_q describe [M][N] MXFP8 activations.
+ * Source: as fp8_linear_fwd and fp8_gelu_quantize (the quantisation fused into the producing
+ * GEMM is this library's design, not a step of the pages).
  */
 fp8_status fp8_linear_fwd_gelu(const fp8_recipe *recipe, const fp8_tensor *x,
                                const fp8_tensor *w, fp8_tensor *a_q, fp8_tensor *h_q,
@@ -304,6 +325,7 @@ fp8_status fp8_linear_fwd_gelu(const fp8_recipe *recipe, const fp8_tensor *x,
  * (written by fp8_linear_fwd_gelu or fp8_gelu_quantize), quantised as MXFP8 row and column
  * copies into dh_q. Byte-identical to fp8_linear_bwd (dx only) followed by fp8_dgelu_quantize.
  * h_q must be [dy->rows][w->cols]; dh_q needs row, col and both scale arrays.
+ * Source: as fp8_linear_bwd and fp8_dgelu_quantize.
  */
 fp8_status fp8_linear_dgrad_dgelu(const fp8_recipe *recipe, const fp8_tensor *dy,
                                   const fp8_tensor *w, const fp8_tensor *h_q, fp8_tensor *dh_q,
