@@ -129,10 +129,13 @@ def test_quantize_writes_stay_inside(kind, fmt, role, shape, extra):
     assert same_qtensor(q, ref)
 
 
+@pytest.mark.parametrize("kind,extra", [("mxfp8", {}), ("blockwise", {}),
+                                         ("blockwise", {"format": "hybrid", "power_2_scales": True})])
 @pytest.mark.parametrize("fp8_wgrad", [True, False])
-def test_quantize_group_writes_stay_inside(fp8_wgrad):
-    # one grouped MXFP8 launch over three tensors of different tile counts
-    rec = F.Recipe(kind="mxfp8", fp8_wgrad=fp8_wgrad)
+def test_quantize_group_writes_stay_inside(kind, extra, fp8_wgrad):
+    # one grouped launch over three tensors of different tile counts (blockwise: 1x128, 128x128
+    # and a 1x128 gradient, E5M2 under the hybrid format)
+    rec = F.Recipe(kind=kind, fp8_wgrad=fp8_wgrad, **extra)
     shapes, roles = [(256, 384), (384, 128), (128, 512)], ["activation", "weight", "grad"]
     xs = [to_dev_bf16(bf16_bits_normal(r, c, seed=140 + i, outlier_p=1e-2, outlier_factor=30.0))
           for i, (r, c) in enumerate(shapes)]

@@ -109,8 +109,11 @@ def test_stalled_quantize_reports_timeout_and_context_survives(kind):
     assert np.array_equal(q2.col.cpu().numpy(), ref["col"])
 
 
-def test_stalled_quantize_group_reports_timeout_and_context_survives():
-    rec = F.Recipe(kind="mxfp8")
+@pytest.mark.parametrize("kind", ["mxfp8", "blockwise"])
+def test_stalled_quantize_group_reports_timeout_and_context_survives(kind):
+    # both instantiations of the grouped kernel: MXFP8, and blockwise (1x128 activation and
+    # 128x128 weight in one launch)
+    rec = F.Recipe(kind=kind)
     bits = [bf16_bits_normal(1024, 512, seed=123), bf16_bits_normal(512, 256, seed=124)]
     xs = [to_dev_bf16(b) for b in bits]
     roles = ["activation", "weight"]
@@ -124,7 +127,8 @@ def test_stalled_quantize_group_reports_timeout_and_context_survives():
     got = F.quantize_group(rec, xs, roles, status=status2)
     torch.cuda.synchronize()
     assert int(status2.item()) == 0
-    for g, b in zip(got, bits):
-        ref = O.quantize_mxfp8(b)
+    refs = ([O.quantize_mxfp8(b) for b in bits] if kind == "mxfp8" else
+            [O.quantize_blockwise_1x128(bits[0]), O.quantize_blockwise_128x128(bits[1])])
+    for g, ref in zip(got, refs):
         assert np.array_equal(g.row.cpu().numpy(), ref["row"])
         assert np.array_equal(g.col.cpu().numpy(), ref["col"])
