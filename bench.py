@@ -455,8 +455,8 @@ def run_ours(args):
 
     ms_step = ms_total / args.steps
     hbm, fp8_peak, src = peaks()
-    # ---- the benchmark spec's two named targets and the power-capped figure, measured apart
-    # from the timed region above
+    # ---- the two named performance targets (4096^3 MXFP8 GEMM, quantize bandwidth per
+    # recipe) and the power-capped figure, measured apart from the timed region above
     gemm4096 = measure_gemm_4096(torch, F, dev, fp8_peak)
     quant_recipes = measure_quantize_by_recipe(torch, F, dev, hbm)
     sustained = measure_sustained(torch, st, ms_step, local)
@@ -1237,7 +1237,7 @@ def run_profile_suite(args):
 
 
 def run_targets(args):
-    """The benchmark spec's two named targets alone (prints one JSON object, not the benchmark
+    """The two named performance targets alone (prints one JSON object, not the benchmark
     line): the 4096^3 MXFP8 GEMM and every recipe's quantize at 8192 x 4096."""
     import torch
     import scaled_quantize_fp8_gb300 as F

@@ -69,7 +69,7 @@ typedef enum {
   FP8_ERR_ALIGN = 2,        /* a pointer is not 16-byte aligned */
   FP8_ERR_SHAPE = 3,        /* sizes negative, not multiples of the required block, or
                                inconsistent between operands */
-  FP8_ERR_UNSUPPORTED = 4,  /* a recipe option this build does not implement */
+  FP8_ERR_UNSUPPORTED = 4,  /* a recipe option this library does not implement */
   FP8_ERR_CUDA = 5,         /* a CUDA launch or query failed */
   FP8_ERR_TIMEOUT = 6,      /* device-side only: a pipeline wait exceeded its budget */
   FP8_ERR_WORKSPACE = 7     /* workspace missing or smaller than fp8_workspace_bytes() */
@@ -84,7 +84,7 @@ typedef enum {
 } fp8_recipe_kind;
 
 /* --fp8-format values ("Hardware and Recipe Compatibility": e4m3 for every recipe, hybrid for
- * delayed, tensorwise and blockwise). The pages do not define hybrid; this build reads it as
+ * delayed, tensorwise and blockwise). The pages do not define hybrid; this library reads it as
  * E4M3 for activations and weights and E5M2 for gradients (role FP8_ROLE_GRAD): OCP E5M2, bias
  * 15, 2 mantissa bits, largest finite value 57344, encoded like E4M3 (round to nearest even,
  * finite overflow and infinities saturate to +-57344, NaN -> 0x7F with its sign) with 57344 in
