@@ -1041,7 +1041,8 @@ def run_profile_case(args):
     gemm_mx_mlp: the MLP step's four plain-store MXFP8 GEMMs (fc2 fprop, fc2 wgrad, fc1
     dgrad, fc1 wgrad) at full size, in that order.
     quant_group_mx: the MLP step's grouped MXFP8 quantize of X 8192 x 4096, W1 16384 x 4096
-    and W2 4096 x 16384 (one launch)."""
+    and W2 4096 x 16384 (one launch); quant_group_blockwise: the same three tensors under the
+    blockwise recipe (X in 1x128 blocks, W1 and W2 in 128x128 tiles)."""
     import torch
     import scaled_quantize_fp8_gb300 as F
     from scaled_quantize_fp8_gb300 import build as B
@@ -1091,7 +1092,7 @@ def run_profile_case(args):
                 F.gelu_quantize(rec, h, a_q=a_q, h_q=h_q)
             else:
                 F.dgelu_quantize(rec, h, h_q, dh_q=a_q)
-    elif case == "quant_group_mx":
+    elif case in ("quant_group_mx", "quant_group_blockwise"):
         shapes = ((8192, 4096, 1.0), (16384, 4096, 0.02), (4096, 16384, 0.02))
         xs = [(torch.randn((r, c), device="cuda", generator=g) * sg).to(torch.bfloat16)
               for r, c, sg in shapes]
@@ -1328,7 +1329,8 @@ def run_kernels(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--profile", default=None,
-                    choices=["quant_mx", "quant_group_mx", "quant_tensorwise", "quant_blockwise",
+                    choices=["quant_mx", "quant_group_mx", "quant_group_blockwise",
+                             "quant_tensorwise", "quant_blockwise",
                              "gemm_mx",
                              "gemm_tensorwise", "gemm_blockwise", "gelu_mx", "dgelu_mx",
                              "gemm_gelu_mx", "gemm_dgelu_mx", "gemm_mx_mlp",
