@@ -90,8 +90,10 @@ def _fc1(M, N, K, seed):
     return rec, xb, wb, xq, wq
 
 
+# the last shape runs 160 pair tiles on the 76 pairs of a full GPU (a partial last round),
+# grouped along M (M < N)
 @pytest.mark.parametrize("M,N,K", [(128, 256, 128), (256, 256, 256), (384, 512, 256),
-                                   (512, 384, 512), (256, 128, 384)])
+                                   (512, 384, 512), (256, 128, 384), (2560, 4096, 256)])
 def test_fc1_gelu_fused(M, N, K):
     rec, xb, wb, xq, wq = _fc1(M, N, K, seed=M + N)
     a_q, h_q = F.linear_fwd_gelu(rec, xq, wq)
@@ -113,8 +115,9 @@ def test_fc1_gelu_fused(M, N, K):
     _check_copies(a_q, a_g, M, N)
 
 
+# the last shape runs 96 pair tiles (two rounds) in the exchanged tile order (M > N)
 @pytest.mark.parametrize("M,Fd,H", [(128, 256, 128), (256, 256, 256), (384, 512, 256),
-                                    (512, 384, 128)])
+                                    (512, 384, 128), (4096, 1536, 256)])
 def test_fc2_dgrad_dgelu_fused(M, Fd, H):
     rec = F.Recipe(kind="mxfp8")
     seed = M + Fd
