@@ -89,6 +89,28 @@ def test_dgrad_wgrad(kind, M, N, K, fp32):
     _check(dw, ref_dw, fp32)
 
 
+# More tiles than the persistent grid runs at once: 160 pair tiles on 76 pairs (tensorwise,
+# MXFP8) or 320 single-CTA tiles on 152 SMs (blockwise), so the last round is partial; with
+# M > N the tile groups run along N (the exchanged order), with M < N along M. Every element
+# is compared, in bf16 and in fp32 output mode.
+@pytest.mark.parametrize("kind", ["tensorwise", "mxfp8", "blockwise"])
+@pytest.mark.parametrize("M,N", [(4096, 2560), (2560, 4096)])
+def test_fprop_multi_round_full_compare(kind, M, N):
+    K = 256
+    rec = F.Recipe(kind=kind)
+    xb = bf16_bits_normal(M, K, seed=17, outlier_p=1e-3 if kind == "mxfp8" else 0.0)
+    wb = bf16_bits_normal(N, K, seed=18, sigma=0.02)
+    xq = _quant_gpu(rec, xb, "activation")
+    wq = _quant_gpu(rec, wb, "weight")
+    y = F.linear_fwd(rec, xq, wq)
+    y32 = F.linear_fwd(rec, xq, wq, fp32=True)
+    torch.cuda.synchronize()
+    ref = O.gemm_tn_f64(_oracle_deq(kind, xb, "activation", "row"),
+                        _oracle_deq(kind, wb, "weight", "row"))
+    _check(y, ref, False)
+    _check(y32, ref, True)
+
+
 @pytest.mark.parametrize("M,N,K", [(272, 208, 144), (16, 16, 16), (400, 528, 48)])
 def test_tensorwise_ragged(M, N, K):
     rec = F.Recipe(kind="tensorwise")
