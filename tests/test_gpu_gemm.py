@@ -69,7 +69,10 @@ def test_fprop(kind, M, N, K, fp32):
 
 
 @pytest.mark.parametrize("kind", ["tensorwise", "mxfp8", "blockwise"])
-@pytest.mark.parametrize("M,N,K", [(256, 384, 512), (512, 256, 128)])
+# the last two shapes give dgrad (dX 2560 x 4096) and wgrad (dW 4096 x 2560) more tiles than
+# the grid runs at once
+@pytest.mark.parametrize("M,N,K", [(256, 384, 512), (512, 256, 128), (2560, 256, 4096),
+                                   (256, 4096, 2560)])
 @pytest.mark.parametrize("fp32", [False, True])
 def test_dgrad_wgrad(kind, M, N, K, fp32):
     rec = F.Recipe(kind=kind)
