@@ -187,7 +187,9 @@ def test_full_size_mxfp8_fprop_sampled():
 # ------------------------------------------------------------------ --fp8-wgrad off
 
 @pytest.mark.parametrize("kind", ["tensorwise", "delayed", "mxfp8", "blockwise"])
-@pytest.mark.parametrize("M,N,K", [(256, 384, 512), (512, 256, 128), (640, 512, 384), (256, 128, 256)])
+# the last shape's dW (4096 x 2560) has more tiles than the grid runs at once
+@pytest.mark.parametrize("M,N,K", [(256, 384, 512), (512, 256, 128), (640, 512, 384), (256, 128, 256),
+                                   (256, 4096, 2560)])
 @pytest.mark.parametrize("fp32", [False, True])
 def test_wgrad_bf16(kind, M, N, K, fp32):
     """With fp8_wgrad off the column copies of X and dY are bf16 transposes and wgrad is a

@@ -46,7 +46,10 @@ def _oracle_pair(kind, b, role, fmt, scale):
 
 @pytest.mark.parametrize("kind,fmt", [("tensorwise", "e4m3"), ("delayed", "e4m3"),
                                       ("tensorwise", "hybrid"), ("blockwise", "e4m3")])
-@pytest.mark.parametrize("M,N,K", [(256, 384, 512), (128, 256, 384), (384, 256, 128)])
+# the last two shapes give dgrad (dX 2560 x 4096) and wgrad (dW 4096 x 2560), each reading
+# MN-major operands, more tiles than the grid runs at once
+@pytest.mark.parametrize("M,N,K", [(256, 384, 512), (128, 256, 384), (384, 256, 128),
+                                   (2560, 256, 4096), (256, 4096, 2560)])
 @pytest.mark.parametrize("fp32", [False, True])
 def test_bwd_without_column_copies(kind, fmt, M, N, K, fp32):
     rec = F.Recipe(kind=kind, format=fmt)
