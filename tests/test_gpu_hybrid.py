@@ -117,10 +117,12 @@ def _oracle_q(kind, b, role, delayed_scale=None):
 
 @pytest.mark.parametrize("kind", ["tensorwise", "delayed", "blockwise"])
 @pytest.mark.parametrize("fp32", [False, True])
-def test_hybrid_dgrad_wgrad(kind, fp32):
+# the last two shapes give dX (2560 x 4096) and dW (4096 x 2560) more tiles than the grid runs
+# at once
+@pytest.mark.parametrize("M,N,K", [(256, 384, 512), (2560, 256, 4096), (256, 4096, 2560)])
+def test_hybrid_dgrad_wgrad(kind, fp32, M, N, K):
     """dX = dY . W and dW = dY^T . X with dY in E5M2, W and X in E4M3, against the oracle's
     GEMMs over its own quantisation of the same seeded inputs."""
-    M, N, K = 256, 384, 512
     rec = F.Recipe(kind=kind, format="hybrid")
     xb = bf16_bits_normal(M, K, seed=91)
     wb = bf16_bits_normal(N, K, seed=92, sigma=0.02)
